@@ -1,0 +1,127 @@
+"""ORACLE — test infrastructure only (tests, the package smoke check and the
+bench's CPU-baseline leg).  Python face of the fp64 C oracle plus the integer
+parts of the method (grouping tokens by adapter, walking the page table).
+
+The GPU product path never imports this module.
+
+Sources, by page and section:
+  * "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels
+    work": SGMV sorts or groups tokens so each contiguous segment shares an
+    adapter; engines precompute per step an index mapping tokens to adapters.
+  * "S-LoRA: Serving Thousands of Concurrent Adapters in 2026", "The Three Core
+    Pillars": the fused kernel groups token slices by target adapter id.
+  * "S-LoRA: Serving Thousands of Concurrent LoRA Adapters": adapters are gathered
+    from non-contiguous pages of the unified pool.
+Readings (the pages fix no order): groups are listed by ascending adapter id;
+inside a group tokens keep their batch order; base-only tokens (-1) are in no group.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SO = os.path.join(_HERE, "liboracle.so")
+SRC = os.path.join(_HERE, "lora_oracle.c")
+
+ERRORS = {1: "adapter id out of range", 2: "rank out of range",
+          3: "page-table block out of range", 4: "page id out of range"}
+
+
+def build_cmd() -> list[str]:
+    return ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-std=c11",
+            "-o", SO, SRC]
+
+
+def build() -> None:
+    subprocess.check_call(build_cmd())
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(SO) or os.path.getmtime(SO) < os.path.getmtime(SRC):
+            build()
+        lib = ctypes.CDLL(SO)
+        p = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        lib.oracle_lora_delta.argtypes = [p, i64, i32, p, i64, p, p, p, i32, i32, i32, i32,
+                                          i32, i32, p, i64, p, i64, p, i32, p, i64, p, p]
+        lib.oracle_lora_delta.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def lora_delta(pool: np.ndarray, pt: np.ndarray, pt_off: np.ndarray, ranks: np.ndarray,
+               scales: np.ndarray, num_layers: int, num_proj: int, layer: int, proj: int,
+               x: np.ndarray, y0: np.ndarray, token_adapter: np.ndarray,
+               want_t: bool = False):
+    """y_ref = y0 + delta for one (layer, proj) problem, in float64.
+
+    pool: uint16 [num_pages, h] raw bf16 bits;  x: uint16 [T, h] raw bf16 bits;
+    y0: float64 [T, h] (bf16 inputs widened by the caller); token_adapter int32 [T].
+    Returns (y_ref [T, h] float64, t [T, r_max] float64 or None, multiply-adds).
+    """
+    pool = np.ascontiguousarray(pool, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    y0 = np.ascontiguousarray(y0, dtype=np.float64)
+    pt = np.ascontiguousarray(pt, dtype=np.int32)
+    pt_off = np.ascontiguousarray(pt_off, dtype=np.int64)
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    ids = np.ascontiguousarray(token_adapter, dtype=np.int32)
+    T = ids.size
+    h = pool.shape[1]
+    assert x.shape == (T, h) and y0.shape == (T, h)
+    r_max = int(ranks.max()) if ranks.size else 1
+    y = np.empty((T, h), dtype=np.float64)
+    t = np.empty((T, r_max), dtype=np.float64) if want_t else None
+    madds = ctypes.c_int64(0)
+    err = _load().oracle_lora_delta(
+        pool.ctypes.data, pool.shape[0], h, pt.ctypes.data, pt.size, pt_off.ctypes.data,
+        ranks.ctypes.data, scales.ctypes.data, ranks.size, num_layers, num_proj, r_max,
+        layer, proj, x.ctypes.data, h, y0.ctypes.data, h, ids.ctypes.data, T,
+        y.ctypes.data, h, t.ctypes.data if t is not None else None, ctypes.byref(madds))
+    if err:
+        raise OracleError(ERRORS.get(err, str(err)))
+    return y, t, int(madds.value)
+
+
+def group_tokens(token_adapter: np.ndarray):
+    """Stable grouping of the adapted tokens by adapter id.
+
+    Returns perm (token indices, ascending adapter id, batch order inside a group),
+    grp_start [G+1] (offsets into perm) and grp_adapter [G]."""
+    ids = np.asarray(token_adapter, dtype=np.int64)
+    adapted = np.nonzero(ids >= 0)[0]
+    perm = adapted[np.argsort(ids[adapted], kind="stable")]
+    sid = ids[perm]
+    if perm.size == 0:
+        return perm.astype(np.int32), np.zeros(1, np.int32), np.zeros(0, np.int32)
+    starts = np.concatenate([[0], np.nonzero(np.diff(sid))[0] + 1])
+    grp_start = np.concatenate([starts, [perm.size]]).astype(np.int32)
+    return perm.astype(np.int32), grp_start, sid[starts].astype(np.int32)
+
+
+def page_list(pt: np.ndarray, pt_off: np.ndarray, ranks: np.ndarray, num_proj: int,
+              layer: int, proj: int, grp_adapter: np.ndarray) -> np.ndarray:
+    """Gathered page ids of one problem, group by group: the r_a A-row pages then the
+    r_a B-column pages of each group's adapter (page-table walk)."""
+    out = []
+    for a in np.asarray(grp_adapter, dtype=np.int64):
+        r = int(ranks[a])
+        for ab in (0, 1):
+            base = int(pt_off[a]) + ((layer * num_proj + proj) * 2 + ab) * r
+            out.append(np.asarray(pt[base:base + r], dtype=np.int32))
+    return np.concatenate(out) if out else np.zeros(0, np.int32)
+

@@ -1,0 +1,344 @@
+"""Pins of the fp64 CPU oracle against what the pages and the mathematics fix.
+
+Each test targets a mistake the oracle could plausibly contain (a transposed
+operand, a wrong page-table index, a dropped or duplicated term, a wrong scale,
+touching base-only rows) and checks it against something other than the
+oracle's own formula: the merge identity (a dense library matmul of the merged
+weight), the gathered-bmm form printed on the pofe.ai page (a library bmm),
+exact invariances, and the pages' flop count.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import spec, valuegen as vg
+from workloads.materialize import a_param, host_inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def dense_adapter(wl, a, layer, proj):
+    """Dense A (r x h) and B (h x r) of adapter a for (layer, proj), generated straight
+    from the generator keys of the layout convention -- never through the page table."""
+    pool = wl.pool
+    r = int(pool.ranks[a])
+    h = pool.h
+    P = pool.num_proj
+    out = []
+    for ab, dist, param in ((0, vg.DIST_UNIFORM, a_param(h)),
+                            (1, vg.DIST_NORMAL, vg.normal_param(spec.SIGMA_B))):
+        local = ((layer * P + proj) * 2 + ab) * r + np.arange(r)
+        rows = np.zeros((r, h), np.uint16)
+        vg.fill_rows_host(rows, np.arange(r), spec.page_key(a, local), wl.seed, dist, param)
+        out.append(vg.bf16_bits_to_f64(rows))
+    A, Bcols = out
+    return A, Bcols.T  # B is d_out x r: column j is page j
+
+
+def run_oracle(wl, hi, layer, proj, y0=None, ids=None, want_t=False):
+    pool = wl.pool
+    x = hi.x[(layer, proj)]
+    if y0 is None:
+        y0 = vg.bf16_bits_to_f64(hi.y0[(layer, proj)])
+    if ids is None:
+        ids = wl.batch.token_adapter()
+    return oracle.lora_delta(hi.pool, hi.pt, pool.pt_off, pool.ranks, pool.scales,
+                             pool.num_layers, pool.num_proj, layer, proj, x, y0, ids,
+                             want_t=want_t)
+
+
+def small_multi(seed=7, h=64, L=2, P=3, N=5, T=24):
+    return spec.decode_workload("pin-small", seed, h, L, P, N, [1, 2, 4, 8, 16], T, None,
+                                num_pages=None, base_ids=True)
+
+
+# ----------------------------------------------------------------------------- formula pins
+
+@pytest.mark.parametrize("make", [spec.config0, small_multi])
+def test_merge_identity(make):
+    """x (W + s B A)^T == x W^T + s (x A^T) B^T (pofe.ai page, "The bottleneck": the merged
+    weight W' = W + gamma B A; fdeinterviews S-LoRA page: the update to W is a low-rank
+    product).  Dense library matmuls of the merged weight, per token and per problem."""
+    wl = make()
+    hi = host_inputs(wl)
+    rng = np.random.default_rng(3)
+    ids = wl.batch.token_adapter()
+    for (l, p) in wl.problems:
+        W = rng.normal(0.0, 0.02, size=(wl.h, wl.h))
+        xd = vg.bf16_bits_to_f64(hi.x[(l, p)])
+        y_ref, _, _ = run_oracle(wl, hi, l, p, y0=xd @ W.T)
+        for i, a in enumerate(ids):
+            if a < 0:
+                merged = W
+            else:
+                A, B = dense_adapter(wl, a, l, p)
+                merged = W + float(wl.pool.scales[a]) * (B @ A)
+            want = merged @ xd[i]
+            np.testing.assert_allclose(y_ref[i], want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max()))
+
+
+def test_gathered_bmm_form():
+    """The pofe.ai page's "Implementation sketch" form: v = bmm(A_pool[idx], x), then
+    y + scale * bmm(B_pool[idx], v), in float64 torch on CPU, with adapters zero-padded
+    to r_max in the dense pools (a library routine, not the oracle's loop)."""
+    torch = pytest.importorskip("torch")
+    wl = small_multi(seed=11, T=32)
+    hi = host_inputs(wl)
+    N, h, rmax = wl.pool.num_adapters, wl.h, wl.pool.r_max
+    ids = wl.batch.token_adapter()
+    for (l, p) in wl.problems:
+        A_pool = torch.zeros((N + 1, rmax, h), dtype=torch.float64)   # slot N = zero adapter
+        B_pool = torch.zeros((N + 1, h, rmax), dtype=torch.float64)
+        scale = torch.zeros(N + 1, dtype=torch.float64)
+        for a in range(N):
+            A, B = dense_adapter(wl, a, l, p)
+            r = A.shape[0]
+            A_pool[a, :r] = torch.from_numpy(A)
+            B_pool[a, :, :r] = torch.from_numpy(B)
+            scale[a] = float(wl.pool.scales[a])
+        idx = torch.from_numpy(np.where(ids < 0, N, ids).astype(np.int64))
+        x = torch.from_numpy(vg.bf16_bits_to_f64(hi.x[(l, p)]))
+        y0 = torch.from_numpy(vg.bf16_bits_to_f64(hi.y0[(l, p)]))
+        v = torch.bmm(A_pool[idx], x[:, :, None])
+        want = y0 + scale[idx][:, None] * torch.bmm(B_pool[idx], v).squeeze(2)
+        got, _, _ = run_oracle(wl, hi, l, p)
+        np.testing.assert_allclose(got, want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_flop_count_matches_pages():
+    """Every adapted token costs 2 r (d_in + d_out) extra flops per projection
+    (pofe.ai page, "The bottleneck"); the oracle counts its multiply-adds as it runs."""
+    wl = small_multi(seed=5, T=40)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    want = sum(2 * int(wl.pool.ranks[a]) * (wl.h + wl.h) for a in ids if a >= 0)
+    for (l, p) in wl.problems:
+        _, _, madds = run_oracle(wl, hi, l, p)
+        assert 2 * madds == want
+
+
+def test_shrink_t_matches_dense():
+    """t = A x for every adapted token (the shrink alone; orientation of A pinned)."""
+    wl = small_multi(seed=13)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    for (l, p) in wl.problems:
+        _, t, _ = run_oracle(wl, hi, l, p, want_t=True)
+        xd = vg.bf16_bits_to_f64(hi.x[(l, p)])
+        for i, a in enumerate(ids):
+            if a < 0:
+                assert np.all(t[i] == 0)
+                continue
+            A, _ = dense_adapter(wl, a, l, p)
+            np.testing.assert_allclose(t[i, :A.shape[0]], A @ xd[i], rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- exact special cases
+
+def test_zero_B_gives_zero_delta():
+    """Adapters whose B is all zero leave y exactly equal to y0."""
+    wl = small_multi(seed=17)
+    hi = host_inputs(wl)
+    ent = np.concatenate([wl.pool.block_entries(a, l, p, 1)
+                          for a in range(wl.pool.num_adapters) for (l, p) in wl.problems])
+    hi.pool[hi.pt[ent]] = 0
+    for (l, p) in wl.problems:
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, p)])
+        got, _, _ = run_oracle(wl, hi, l, p, y0=y0)
+        assert np.array_equal(got, y0)
+
+
+def test_base_only_rows_untouched():
+    wl = small_multi(seed=19, T=48)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    assert (ids == -1).any() and (ids >= 0).any()
+    for (l, p) in wl.problems:
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, p)])
+        got, _, _ = run_oracle(wl, hi, l, p, y0=y0)
+        assert np.array_equal(got[ids == -1], y0[ids == -1])
+        assert not np.array_equal(got[ids >= 0], y0[ids >= 0])
+
+
+def test_rank_r_equals_zero_padded_rmax():
+    """Mixed ranks need no padding: each adapter re-laid out at rank r_max with zero
+    A rows and zero B columns beyond r gives the identical result (scale unchanged)."""
+    wl = small_multi(seed=23)
+    hi = host_inputs(wl)
+    pool = wl.pool
+    N, L, P, rmax, h = pool.num_adapters, pool.num_layers, pool.num_proj, pool.r_max, pool.h
+    sizes = np.full(N, L * P * 2 * rmax, dtype=np.int64)
+    off2 = np.concatenate([[0], np.cumsum(sizes)[:-1]])
+    pages2 = [np.zeros(h, np.uint16)]  # page 0 = zeros
+    pt2 = np.zeros(int(sizes.sum()), dtype=np.int32)
+    for a in range(N):
+        r = int(pool.ranks[a])
+        for (l, p) in [(l, p) for l in range(L) for p in range(P)]:
+            for ab in (0, 1):
+                src = hi.pt[pool.block_entries(a, l, p, ab)]
+                base = off2[a] + ((l * P + p) * 2 + ab) * rmax
+                for j in range(rmax):
+                    if j < r and src[j] >= 0:
+                        pages2.append(hi.pool[src[j]])
+                        pt2[base + j] = len(pages2) - 1
+    pool2 = np.stack(pages2)
+    ranks2 = np.full(N, rmax, np.int32)
+    for (l, p) in wl.problems:
+        got, _, _ = run_oracle(wl, hi, l, p)
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, p)])
+        pad, _, _ = oracle.lora_delta(pool2, pt2, off2, ranks2, pool.scales, L, P, l, p,
+                                      hi.x[(l, p)], y0, wl.batch.token_adapter())
+        assert np.array_equal(got, pad)
+
+
+def test_page_placement_invariance():
+    """Moving every page to another slot of the pool (and rewriting the page table)
+    changes nothing, bit for bit."""
+    wl = small_multi(seed=29)
+    hi = host_inputs(wl)
+    rng = np.random.default_rng(0)
+    n = hi.pool.shape[0]
+    perm = rng.permutation(n)            # new slot of old page q is perm[q]
+    pool2 = np.empty_like(hi.pool)
+    pool2[perm] = hi.pool
+    pt2 = np.where(hi.pt >= 0, perm[np.maximum(hi.pt, 0)], -1).astype(np.int32)
+    for (l, p) in wl.problems:
+        a, _, _ = run_oracle(wl, hi, l, p)
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, p)])
+        b, _, _ = oracle.lora_delta(pool2, pt2, wl.pool.pt_off, wl.pool.ranks, wl.pool.scales,
+                                    wl.pool.num_layers, wl.pool.num_proj, l, p, hi.x[(l, p)],
+                                    y0, wl.batch.token_adapter())
+        assert np.array_equal(a, b)
+
+
+def test_batch_order_invariance():
+    """Permuting the tokens of the batch permutes the results, bit for bit."""
+    wl = small_multi(seed=31, T=30)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    perm = np.random.default_rng(1).permutation(ids.size)
+    for (l, p) in wl.problems:
+        a, _, _ = run_oracle(wl, hi, l, p)
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, p)])
+        b, _, _ = oracle.lora_delta(hi.pool, hi.pt, wl.pool.pt_off, wl.pool.ranks,
+                                    wl.pool.scales, wl.pool.num_layers, wl.pool.num_proj, l, p,
+                                    hi.x[(l, p)][perm], y0[perm], ids[perm])
+        assert np.array_equal(a[perm], b)
+
+
+def test_oracle_rejects_bad_inputs():
+    wl = spec.config0()
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter().copy()
+    ids[0] = wl.pool.num_adapters
+    with pytest.raises(oracle.OracleError, match="adapter"):
+        run_oracle(wl, hi, 0, 0, ids=ids)
+    ids[0] = -2
+    with pytest.raises(oracle.OracleError, match="adapter"):
+        run_oracle(wl, hi, 0, 0, ids=ids)
+    ids = wl.batch.token_adapter()
+    a = int(ids[ids >= 0][0])
+    bad = hi.pt.copy()
+    bad[wl.pool.block_entries(a, 0, 0, 1)[0]] = hi.pool.shape[0]
+    with pytest.raises(oracle.OracleError, match="page"):
+        oracle.lora_delta(hi.pool, bad, wl.pool.pt_off, wl.pool.ranks, wl.pool.scales, 1, 1, 0, 0,
+                          hi.x[(0, 0)], vg.bf16_bits_to_f64(hi.y0[(0, 0)]), ids)
+
+
+# ----------------------------------------------------------------------------- integer steps
+
+def _brute_group(ids):
+    """Enumerate every arrangement of the adapted tokens; keep the one sorted by
+    (adapter id, batch position).  Exponential: tiny inputs only."""
+    adapted = [i for i, a in enumerate(ids) if a >= 0]
+    best = None
+    for cand in itertools.permutations(adapted):
+        keys = [(ids[i], i) for i in cand]
+        if all(keys[k] < keys[k + 1] for k in range(len(keys) - 1)):
+            assert best is None
+            best = cand
+    return list(best) if best is not None else []
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_group_tokens_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    T = int(rng.integers(0, 8))
+    ids = rng.integers(-1, 3, size=T).astype(np.int32)
+    perm, gs, ga = oracle.group_tokens(ids)
+    assert list(perm) == _brute_group(list(ids))
+    # groups: one per distinct adapter present, ascending, covering perm exactly
+    distinct = sorted(set(int(a) for a in ids if a >= 0))
+    assert list(ga) == distinct
+    assert gs[0] == 0 and gs[-1] == perm.size and np.all(np.diff(gs) > 0)
+    for g, a in enumerate(ga):
+        assert np.all(ids[perm[gs[g]:gs[g + 1]]] == a)
+
+
+def test_page_list_walks_the_layout():
+    """Every page the oracle lists for (adapter, layer, proj) holds exactly the
+    generator stream of that adapter's A row j / B column j (keys fixed at build time)."""
+    wl = small_multi(seed=37)
+    pool = wl.pool
+    key_of = dict(zip(pool.page_ids.tolist(), pool.page_keys.tolist()))
+    _, _, ga = oracle.group_tokens(wl.batch.token_adapter())
+    for (l, p) in wl.problems:
+        pages = oracle.page_list(pool.pt, pool.pt_off, pool.ranks, pool.num_proj, l, p, ga)
+        pos = 0
+        for a in ga:
+            r = int(pool.ranks[a])
+            for ab in (0, 1):
+                for j in range(r):
+                    local = ((l * pool.num_proj + p) * 2 + ab) * r + j
+                    assert key_of[int(pages[pos])] == int(spec.page_key(a, local))
+                    pos += 1
+        assert pos == pages.size
+
+
+# ----------------------------------------------------------------------------- generator sanity
+
+def test_generator_moments():
+    h = 4096
+    rows = np.zeros((64, h), np.uint16)
+    keys = spec.row_key(spec.KIND_X, 0, 0, np.arange(64))
+    vg.fill_rows_host(rows, np.arange(64), keys, 1234, vg.DIST_NORMAL, vg.normal_param(1.0))
+    v = vg.bf16_bits_to_f64(rows)
+    assert abs(v.mean()) < 0.01 and abs(v.std() - 1.0) < 0.01 and np.abs(v).max() <= 3.47
+    vg.fill_rows_host(rows, np.arange(64), keys, 1234, vg.DIST_UNIFORM, a_param(h))
+    u = vg.bf16_bits_to_f64(rows)
+    b = 1 / np.sqrt(h)
+    assert np.abs(u).max() <= b * (1 + 2 ** -8) and abs(u.mean()) < 0.01 * b
+    assert abs(u.std() - b / np.sqrt(3)) < 0.01 * b
+
+
+def test_zipf_batches_match_pages_simulation():
+    """pofe.ai page, "How many adapters are actually in a batch?": 1,000 adapters with
+    Zipf popularity, batches of 64 hold 33 to 62 distinct adapters; with 64 LRU slots
+    at Zipf 1.0 about half of arrivals miss."""
+    import collections
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "worked_example_8b.json")))["simulation"]
+    rng = np.random.default_rng(0)
+    p = spec.zipf_probs(g["adapters"], 1.0)
+    draws = rng.choice(g["adapters"], size=(2000, g["batch"]), p=p)
+    distinct = np.array([np.unique(b).size for b in draws])
+    lo, hi = g["distinct_per_batch_range"]
+    assert lo <= distinct.mean() <= hi
+    arrivals = rng.choice(g["adapters"], size=200_000, p=p)
+    lru = collections.OrderedDict()
+    misses = 0
+    for k, a in enumerate(arrivals):
+        if a in lru:
+            lru.move_to_end(a)
+        else:
+            if k >= 20_000:
+                misses += 1
+            lru[a] = True
+            if len(lru) > g["slots"]:
+                lru.popitem(last=False)
+    frac = misses / (arrivals.size - 20_000)
+    assert abs(frac - g["miss_fraction_at_64_slots_zipf_1"]) < 0.08
