@@ -1,0 +1,417 @@
+"""Benchmark of the multi-LoRA delta step (one JSON line on stdout, rank 0).
+
+A step is one pass of the whole hot path over one batch: the scheduler step that
+groups the batch by adapter, then the delta kernel over every (layer, projection)
+of the model, in one C-ABI call.  Default workload: Llama-7B-shaped decode BGMV,
+h=4096, 32 layers x q/k/v/o, 64 one-token requests, 2,000 resident adapters with
+ranks in {8,16,32,64}, adapter ids Zipf(1.0).  Synthetic, seeded inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this project) on
+the host cores, on a bounded sample of the same workload.  Under torchrun (N > 1)
+every rank runs an independent replica (tokens shard with no collective on the
+data path); rank 0 prints the whole-job aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-delta tokens/s (BGMV decode, SGMV prefill); % of HBM roofline"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def workload_for(cfg: str):
+    """Configs 0-4 as named in the workload module; "1s" is a small-pool variant of
+    config 1 (4 layers, 300 adapters, ~2.4 GB pool) for profiler captures."""
+    from workloads import spec
+    if cfg == "1s":
+        return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
+                                    300, [8, 16, 32, 64], 64, 1.0)
+    if cfg == "4d":
+        return spec.config4("distinct")
+    if cfg == "4z":
+        return spec.config4("zipf")
+    return spec.CONFIGS[int(cfg)]()
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    from heterogeneous_adapters_gb300 import build
+    h = hashlib.sha256()
+    for s in build.sources():
+        h.update(open(s, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str, units_per_launch: float):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, scaled to this
+    launch by units processed; None when absent or taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    src = kernel_source_hash()
+    for line in open(p):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == src:
+            return float(f["dram_bytes"]) / float(f["units"]) * units_per_launch
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self) -> dict:
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for line in (self.out or "").strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("LORA_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the job ends when its slowest rank ends)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+class OracleRunner:
+    """The fp64 CPU oracle, as it stands, on the workload's first `n_prep` projections
+    (inputs regenerated on the host once; only the oracle calls are timed)."""
+
+    def __init__(self, wl, n_prep: int):
+        from workloads import valuegen as vg
+        from workloads.materialize import host_inputs
+        self.wl = wl
+        self.probs = wl.problems[:max(1, min(n_prep, len(wl.problems)))]
+        self.hi = host_inputs(wl, problems=self.probs)
+        self.y0 = {k: vg.bf16_bits_to_f64(v) for k, v in self.hi.y0.items()}
+        self.ids = wl.batch.token_adapter()
+        self.next = 0
+        self.threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+    def run(self, n: int) -> float:
+        """Seconds spent by the oracle on n projections (cycling through the prepared ones)."""
+        import oracle
+        pool = self.wl.pool
+        t0 = time.perf_counter()
+        for _ in range(n):
+            l, p = self.probs[self.next % len(self.probs)]
+            self.next += 1
+            oracle.lora_delta(self.hi.pool, self.hi.pt, pool.pt_off, pool.ranks, pool.scales,
+                              pool.num_layers, pool.num_proj, l, p, self.hi.x[(l, p)],
+                              self.y0[(l, p)], self.ids)
+        return time.perf_counter() - t0
+
+    def rate(self, seconds: float, n_problems: int) -> float:
+        """tokens/s of the whole step, extrapolated from n_problems projections."""
+        adapted = int((self.ids >= 0).sum())
+        return adapted / (seconds / n_problems * len(self.wl.problems))
+
+    def timed_sample(self, budget_s: float):
+        """Time as many projections as fit in about budget_s seconds."""
+        one = self.run(1)
+        n = max(1, min(len(self.wl.problems), int(budget_s / max(one, 1e-6))))
+        dt = self.run(n)
+        return self.rate(dt, n), dt, n
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    wl = workload_for(args.config)
+    runner = OracleRunner(wl, args.ref_problems)
+    one = runner.run(1)
+    for _ in range(args.warmup):
+        runner.run(1)
+    per_step_budget = args.ref_budget_s / max(1, args.steps + args.warmup)
+    n = max(1, min(len(wl.problems), int(per_step_budget / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    secs = [runner.run(n) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    value = runner.rate(statistics.mean(secs), n)
+    sample = (f"{n} of {len(wl.problems)} projections of one step per timed step (all "
+              f"{wl.batch.num_tokens} tokens), extrapolated linearly to the full step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(secs) / n * len(wl.problems),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(wl, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": runner.threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def config_dict(wl, args) -> dict:
+    from heterogeneous_adapters_gb300 import costmodel
+    p = wl.pool
+    m = costmodel.decode_step_bytes(p.ranks, wl.batch.token_adapter(), p.h, len(wl.problems))
+    return {"workload": wl.name, "h": p.h, "layers": p.num_layers, "projections": p.num_proj,
+            "tokens": wl.batch.num_tokens, "adapted_tokens": m["adapted_tokens"],
+            "adapters": p.num_adapters, "distinct_adapters": m["distinct_adapters"],
+            "ranks": sorted(set(int(r) for r in np.unique(p.ranks))), "batch": wl.batch.kind,
+            "seed": wl.seed, "bytes_per_step": m["bytes"],
+            "l2": "inputs larger than L2: every step streams %.2f GB" % (m["bytes"] / 1e9),
+            "parallelism": "replicas (weak scaling, no collective)"}
+
+
+def run_ours(args, rank: int, world: int, local: int):
+    import torch
+
+    import heterogeneous_adapters_gb300 as lora
+    from heterogeneous_adapters_gb300 import costmodel
+    from workloads.materialize import device_inputs
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = workload_for(args.config)
+    d = device_inputs(wl, device=dev, nan_dummies=False)
+    p = wl.pool
+    pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
+                     p.num_adapters, p.num_layers, p.num_proj, p.r_max)
+    b = wl.batch
+    T, S, Td = b.num_tokens, b.num_segments, b.num_decode
+    nbytes = lora.workspace_size(pool, T, S + Td)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream_obj = torch.cuda.current_stream(dev)
+    stream = stream_obj.cuda_stream
+    lora.workspace_init(ws, nbytes, stream)
+    probs = [(d.x[i], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    seg_start = d.seg_start if S else None
+    seg_adapter = d.seg_adapter if S else None
+    dec = d.dec_adapter if Td else None
+
+    def segment():
+        lora.segment(pool, seg_start, seg_adapter, S, dec, Td, T, ws, nbytes, stream)
+
+    def delta():
+        lora.delta_grouped(pool, probs, ws, nbytes, stream)
+
+    m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems))
+    launches_per_step = 1 + -(-len(probs) // lora.LORA_MAX_PROBLEMS_PER_LAUNCH)
+
+    for _ in range(max(3, args.warmup)):
+        segment()
+        delta()
+    torch.cuda.synchronize()
+    assert lora.get_device_error(ws, stream) == 0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream_obj)
+        for k in range(args.steps):
+            e0, e1, e2 = ev[k]
+            e0.record(stream_obj)
+            segment()
+            e1.record(stream_obj)
+            delta()
+            e2.record(stream_obj)
+        end.record(stream_obj)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed = start.elapsed_time(end) / 1e3
+    kern = [ev[k][1].elapsed_time(ev[k][2]) / 1e3 for k in range(args.steps)]
+    err = lora.get_device_error(ws, stream)
+    assert err == 0, f"device error bits {err:#x}"
+    elapsed_max = max_over_ranks(elapsed, world)
+    tokens_step = m["adapted_tokens"]
+    value = tokens_step * args.steps * world / elapsed_max
+
+    # roofline of the dominant kernel (the delta kernel)
+    peaks = measured_peaks()
+    kern_avg = statistics.mean(kern)
+    achieved = m["bytes"] / kern_avg / 1e9
+    traffic = ncu_traffic("fma_delta_kernel", wl.name, m["bytes"])
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": "fma_delta_kernel", "kernel_ms": kern_avg * 1e3,
+                "peak_source": peaks["source"] + " (hbm_gbs, copy kernel)",
+                "bytes_per_launch": m["bytes"]}
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    xh = torch.empty_like(d.x, device="cpu").pin_memory()
+    yh = torch.empty_like(d.y, device="cpu").pin_memory()
+    xh.copy_(d.x)
+    yh.copy_(d.y)
+    ids_h = torch.from_numpy(b.token_adapter()).pin_memory()
+    ids_d = torch.empty_like(ids_h, device=dev)
+    yo = torch.empty_like(yh).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def api_call():
+        if b.kind == "decode":
+            lora.bgmv(pool, probs, ids_d, T, ws, nbytes, stream)
+        elif b.kind == "prefill":
+            lora.sgmv(pool, probs, d.seg_start, d.seg_adapter, S, T, ws, nbytes, stream)
+        else:
+            lora.apply_mixed(pool, probs, d.seg_start, d.seg_adapter, S, d.dec_adapter, Td, T, ws,
+                             nbytes, stream)
+
+    def e2e_step():
+        d.x.copy_(xh, non_blocking=True)
+        d.y.copy_(yh, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        api_call()
+        yo.copy_(d.y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream_obj)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream_obj)
+    torch.cuda.synchronize()
+    e2e_elapsed = max_over_ranks(s0.elapsed_time(s1) / 1e3, world)
+    e2e = {"value": tokens_step * e2e_steps * world / e2e_elapsed, "unit": UNIT,
+           "h2d_bytes_per_step": d.x.numel() * 2 + d.y.numel() * 2 + ids_h.numel() * 4,
+           "d2h_bytes_per_step": d.y.numel() * 2, "steps": e2e_steps,
+           "api": "lora_bgmv (C ABI) with pinned host x, y, ids"}
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            runner = OracleRunner(wl, args.ref_problems)
+            rate, dt, done = runner.timed_sample(args.ref_seconds)
+            cpu = {"value": rate, "unit": UNIT, "cores": runner.threads, "kind": "oracle",
+                   "sample": f"{done} projections (cycling over the first {len(runner.probs)}) "
+                             f"of the {len(wl.problems)} of one step, all "
+                             f"{wl.batch.num_tokens} tokens, {dt:.1f} s of CPU time, "
+                             f"extrapolated linearly to the full step"}
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": max(3, args.warmup),
+                "ms_per_step": 1e3 * elapsed_max / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config_dict(wl, args), "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk.summary(), "impl": "ours"}
+        print(json.dumps(line), flush=True)
+    pool.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="1")
+    ap.add_argument("--ref-seconds", type=float, default=15.0,
+                    help="CPU seconds of the oracle sample beside our arm")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="total oracle seconds of the reference arm's timed steps")
+    ap.add_argument("--ref-problems", type=int, default=16,
+                    help="projections whose host inputs the oracle prepares")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""ctypes binding of liblora.so: the same names as include/lora.h, argument
+marshalling only.  Every step of the path runs in the library's CUDA kernels;
+there is no Python or CPU fallback: if the library is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+SO = os.path.join(_PKG, "liblora.so")
+
+LORA_OK, LORA_EINVAL, LORA_EALIGN, LORA_EWORKSPACE, LORA_ETOOBIG, LORA_ECUDA, LORA_EDEVICE = range(7)
+DERR = {0x1: "adapter", 0x2: "rank", 0x4: "page-table block", 0x8: "page", 0x10: "segment"}
+LORA_MAX_PROBLEMS_PER_LAUNCH = 256
+LORA_MAX_SEGMENTS = 16384
+LORA_MAX_RANK = 256
+
+EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_workspace_size", "lora_workspace_init",
+            "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
+            "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t",
+            "lora_get_device_error", "lora_last_cuda_error", "lora_status_string"]
+
+
+class lora_pool_desc(ctypes.Structure):
+    _fields_ = [("pages", ctypes.c_void_p), ("num_pages", ctypes.c_int64), ("h", ctypes.c_int32),
+                ("num_adapters", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("num_proj", ctypes.c_int32), ("r_max", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+                ("page_table_len", ctypes.c_int64), ("adapter_pt_off", ctypes.c_void_p),
+                ("ranks", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+class lora_problem(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("ldx", ctypes.c_int64),
+                ("ldy", ctypes.c_int64), ("layer", ctypes.c_int32), ("proj", ctypes.c_int32)]
+
+
+class lora_ws_view(ctypes.Structure):
+    _fields_ = [("error_word", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("perm", ctypes.c_void_p), ("grp_start", ctypes.c_void_p),
+                ("grp_adapter", ctypes.c_void_p)]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {status_string(status)}"
+        if status == LORA_ECUDA:
+            msg += f" (cudaError {lib().lora_last_cuda_error()})"
+        super().__init__(msg + (f" {detail}" if detail else ""))
+
+
+_lib = None
+
+
+def lib():
+    """Load liblora.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(SO):
+            raise RuntimeError(f"{SO} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(SO)
+        p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "lora_pool_create": [ctypes.POINTER(p), ctypes.POINTER(lora_pool_desc)],
+            "lora_pool_destroy": [p],
+            "lora_workspace_size": [p, i32, i32, ctypes.POINTER(sz)],
+            "lora_workspace_init": [p, sz, p],
+            "lora_segment": [p, p, p, i32, p, i32, i32, p, sz, p],
+            "lora_workspace_view": [p, p, sz, i32, i32, ctypes.POINTER(lora_ws_view)],
+            "lora_bgmv": [p, p, i32, p, i32, p, sz, p],
+            "lora_sgmv": [p, p, i32, p, p, i32, i32, p, sz, p],
+            "lora_apply_mixed": [p, p, i32, p, p, i32, p, i32, i32, p, sz, p],
+            "lora_delta_grouped": [p, p, i32, p, sz, p],
+            "lora_debug_page_list": [p, p, sz, i32, i32, p, i64, p, p],
+            "lora_debug_delta_with_t": [p, ctypes.POINTER(lora_problem), p, sz, p, p],
+            "lora_get_device_error": [p, p, ctypes.POINTER(ctypes.c_uint32)],
+            "lora_last_cuda_error": [],
+            "lora_status_string": [ctypes.c_int],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.lora_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().lora_status_string(st).decode()
+
+
+def _check(st: int, where: str):
+    if st != LORA_OK:
+        raise LoraError(st, where)
+
+
+def _ptr(t) -> int | None:
+    """Device or host address of a tensor / integer (None stays NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def problems_array(problems):
+    """problems: iterable of (x, y, ldx, ldy, layer, proj) with x/y tensors or addresses."""
+    problems = list(problems)
+    arr = (lora_problem * max(1, len(problems)))()
+    for i, (x, y, ldx, ldy, layer, proj) in enumerate(problems):
+        arr[i] = lora_problem(_ptr(x), _ptr(y), ldx, ldy, layer, proj)
+    return arr, len(problems)
+
+
+class Pool:
+    """Handle of a lora_pool (host metadata only; device arrays stay the caller's)."""
+
+    def __init__(self, pages, num_pages, h, page_table, page_table_len, pt_off, ranks, scales,
+                 num_adapters, num_layers, num_proj, r_max):
+        d = lora_pool_desc(_ptr(pages), num_pages, h, num_adapters, num_layers, num_proj, r_max, 0,
+                           _ptr(page_table), page_table_len, _ptr(pt_off), _ptr(ranks), _ptr(scales))
+        self._h = ctypes.c_void_p()
+        _check(lib().lora_pool_create(ctypes.byref(self._h), ctypes.byref(d)), "lora_pool_create")
+        self.h = h
+        self.r_max = r_max
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            lib().lora_pool_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def workspace_size(pool: Pool, max_tokens: int, max_segments: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().lora_workspace_size(pool.handle, max_tokens, max_segments, ctypes.byref(n)),
+           "lora_workspace_size")
+    return n.value
+
+
+def workspace_init(ws, ws_bytes: int, stream: int):
+    _check(lib().lora_workspace_init(_ptr(ws), ws_bytes, stream), "lora_workspace_init")
+
+
+def segment(pool, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes, stream):
+    _check(lib().lora_segment(pool.handle, _ptr(seg_start), _ptr(seg_adapter), S,
+                              _ptr(dec_adapter), Td, T, _ptr(ws), ws_bytes, stream), "lora_segment")
+
+
+def workspace_view(pool, ws, ws_bytes, max_tokens, max_segments) -> lora_ws_view:
+    v = lora_ws_view()
+    _check(lib().lora_workspace_view(pool.handle, _ptr(ws), ws_bytes, max_tokens, max_segments,
+                                     ctypes.byref(v)), "lora_workspace_view")
+    return v
+
+
+def bgmv(pool, problems, token_adapter, T, ws, ws_bytes, stream):
+    arr, n = problems_array(problems)
+    _check(lib().lora_bgmv(pool.handle, arr, n, _ptr(token_adapter), T, _ptr(ws), ws_bytes, stream),
+           "lora_bgmv")
+
+
+def sgmv(pool, problems, seg_start, seg_adapter, S, T, ws, ws_bytes, stream):
+    arr, n = problems_array(problems)
+    _check(lib().lora_sgmv(pool.handle, arr, n, _ptr(seg_start), _ptr(seg_adapter), S, T, _ptr(ws),
+                           ws_bytes, stream), "lora_sgmv")
+
+
+def apply_mixed(pool, problems, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes, stream):
+    arr, n = problems_array(problems)
+    _check(lib().lora_apply_mixed(pool.handle, arr, n, _ptr(seg_start), _ptr(seg_adapter), S,
+                                  _ptr(dec_adapter), Td, T, _ptr(ws), ws_bytes, stream),
+           "lora_apply_mixed")
+
+
+def delta_grouped(pool, problems, ws, ws_bytes, stream):
+    arr, n = problems_array(problems)
+    _check(lib().lora_delta_grouped(pool.handle, arr, n, _ptr(ws), ws_bytes, stream),
+           "lora_delta_grouped")
+
+
+def debug_page_list(pool, ws, ws_bytes, layer, proj, out_pages, cap, count_dev, stream):
+    _check(lib().lora_debug_page_list(pool.handle, _ptr(ws), ws_bytes, layer, proj, _ptr(out_pages),
+                                      cap, _ptr(count_dev), stream), "lora_debug_page_list")
+
+
+def debug_delta_with_t(pool, problem, ws, ws_bytes, t_out, stream):
+    arr, _ = problems_array([problem])
+    _check(lib().lora_debug_delta_with_t(pool.handle, arr, _ptr(ws), ws_bytes, _ptr(t_out), stream),
+           "lora_debug_delta_with_t")
+
+
+def get_device_error(ws, stream) -> int:
+    """Synchronises the stream; returns and clears the device error bits (no raise)."""
+    bits = ctypes.c_uint32()
+    st = lib().lora_get_device_error(_ptr(ws), stream, ctypes.byref(bits))
+    if st not in (LORA_OK, LORA_EDEVICE):
+        raise LoraError(st, "lora_get_device_error")
+    return bits.value

@@ -1,0 +1,212 @@
+/*
+ * lora.h - C ABI of the GB300 multi-LoRA delta library (liblora.so).
+ *
+ * Operation (every entry point computes this, for several projections at once):
+ *
+ *     y[i, :] += s_a * (x[i, :] . A_a^T) . B_a^T          for every token i with adapter a = a(i) >= 0
+ *
+ * where A_a is r_a x h, B_a is h x r_a and s_a = alpha / r_a is the caller's
+ * per-adapter scale.  Tokens with adapter id -1 are base-only: their y rows are
+ * neither read nor written.
+ *   Sources, by page and section:
+ *   - "Multi-LoRA serving: S-LoRA, Punica and adapter batching" (pofe.ai),
+ *     "How the kernels work": the delta is a shrink v_i = A_{a(i)} x_i followed by an
+ *     expand y_i += gamma B_{a(i)} v_i; BGMV serves decode (each token independent,
+ *     weights gathered by a(i)), SGMV serves prefill (tokens grouped into contiguous
+ *     same-adapter segments, one small GEMM per segment, one launch); an index maps
+ *     each token to its adapter.  "What the engine does each step": shrink then
+ *     expand per layer and LoRA target.
+ *   - "S-LoRA: Serving Thousands of Concurrent LoRA Adapters" (fdeinterviews),
+ *     "Unified paging" and "Kernels and tensor parallelism": one pool of pages of one
+ *     hidden-size vector each; kernels gather each request's adapter from
+ *     non-contiguous pages and handle mixed ranks without padding.
+ *   - "S-LoRA: Serving Thousands of Concurrent Adapters in 2026" (aifetchly),
+ *     "Implementation": scale = alpha / rank; A is rank x in_dim, B is out_dim x rank.
+ *
+ * Data layout (all device memory is owned by the caller; the library only borrows
+ * pointers for the duration of a call and allocates no device memory):
+ *   pool          bf16 [num_pages][h]: page q holds h contiguous values (2h bytes),
+ *                 16-byte aligned.  d_in = d_out = h.
+ *   page_table    int32 [page_table_len]; adapter a owns the block starting at
+ *                 adapter_pt_off[a] of length L*P*2*r_a.  Entry
+ *                 ((layer*P + proj)*2 + 0)*r_a + j is the page of row j of A_a and
+ *                 ((layer*P + proj)*2 + 1)*r_a + j the page of column j of B_a.
+ *   ranks         int32 [num_adapters], 1 <= r_a <= r_max (r_max <= LORA_MAX_RANK).
+ *   scales        f32 [num_adapters] (s_a).
+ *   x, y          bf16 row-major [T][ld] per problem, ld % 8 == 0, 16-byte aligned
+ *                 base pointers.  y is updated in place.
+ *
+ * Numerics: bf16 products are exact in fp32; t = A x is accumulated in fp32 and
+ * never rounded to bf16 before the expand (the tensor-core expand feeds t as an
+ * exact two-term bf16 split of the fp32 value, see DESIGN notes in lora_sgmv); the
+ * result is rounded to bf16 (round to nearest even) once, when y is stored.
+ *
+ * Calls are asynchronous on the caller's stream (a cudaStream_t passed as void*;
+ * NULL = legacy default stream) and never synchronise the host, except
+ * lora_get_device_error.  Host-side argument checks return a status at once and
+ * launch nothing.  Data-dependent errors found on the device (a bad adapter id, a
+ * rank out of range, a page id out of range, bad segment offsets) set bits of the
+ * workspace's device error word and skip the offending group; the rest of the batch
+ * is still computed.  No kernel traps or spins without a bound.
+ *
+ * Threading: a pool handle is read-only after creation and may be shared by calls
+ * on different streams.  A workspace must not be used by two calls that may run
+ * concurrently on the GPU.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LORA_MAX_RANK 256
+/* Problems per kernel launch; a call with more problems issues several launches. */
+#define LORA_MAX_PROBLEMS_PER_LAUNCH 256
+/* Maximum adapter "segments" of one call: prefill segments + decode tokens. */
+#define LORA_MAX_SEGMENTS 16384
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_EINVAL = 1,      /* null pointer, non-positive size, inconsistent sizes    */
+    LORA_EALIGN = 2,      /* pointer not 16-byte aligned or ld not a multiple of 8 */
+    LORA_EWORKSPACE = 3,  /* workspace null, misaligned or smaller than required   */
+    LORA_ETOOBIG = 4,     /* a size beyond a documented maximum                    */
+    LORA_ECUDA = 5,       /* a CUDA runtime call failed (lora_last_cuda_error)     */
+    LORA_EDEVICE = 6      /* device error bits were set (lora_get_device_error)    */
+} lora_status;
+
+/* Device error bits (data-dependent errors found by the kernels). */
+#define LORA_DERR_ADAPTER 0x1u  /* adapter id outside [-1, num_adapters)            */
+#define LORA_DERR_RANK 0x2u     /* rank outside [1, r_max]                           */
+#define LORA_DERR_PTBLOCK 0x4u  /* adapter page-table block outside the table        */
+#define LORA_DERR_PAGE 0x8u     /* page id outside [0, num_pages)                    */
+#define LORA_DERR_SEGMENT 0x10u /* segment offsets decreasing or beyond the rows     */
+
+/* Pool description: plain device pointers and sizes (copied by lora_pool_create). */
+typedef struct {
+    void* pages;                   /* device bf16 [num_pages][h]                      */
+    int64_t num_pages;
+    int32_t h;                     /* page length in bf16 values; h % 8 == 0           */
+    int32_t num_adapters;
+    int32_t num_layers;            /* L                                                */
+    int32_t num_proj;              /* P                                                */
+    int32_t r_max;                 /* largest rank present, <= LORA_MAX_RANK           */
+    int32_t reserved;
+    const int32_t* page_table;     /* device int32 [page_table_len]                    */
+    int64_t page_table_len;
+    const int64_t* adapter_pt_off; /* device int64 [num_adapters]                      */
+    const int32_t* ranks;          /* device int32 [num_adapters]                      */
+    const float* scales;           /* device f32   [num_adapters]                      */
+} lora_pool_desc;
+
+typedef struct lora_pool lora_pool; /* opaque, host memory only */
+
+/* One projection instance: y (bf16 [T][ldy]) += delta computed from x (bf16 [T][ldx])
+ * with the adapters' pages for (layer, proj).  All problems of one call share the
+ * batch (the same tokens and adapter ids). */
+typedef struct {
+    const void* x;
+    void* y;
+    int64_t ldx;                   /* elements, % 8 == 0, >= h                         */
+    int64_t ldy;
+    int32_t layer;
+    int32_t proj;
+} lora_problem;
+
+/* Validates and copies the description (host-side checks only: sizes, alignment,
+ * null pointers).  Device arrays are checked lazily by the kernels.  *out receives
+ * a host handle; free it with lora_pool_destroy.  Returns LORA_EINVAL, LORA_EALIGN
+ * or LORA_ETOOBIG on a bad description. */
+lora_status lora_pool_create(lora_pool** out, const lora_pool_desc* desc);
+lora_status lora_pool_destroy(lora_pool* pool);
+
+/* Bytes of device workspace needed by a call over at most max_tokens rows and at
+ * most max_segments segments (prefill segments + decode tokens).  The workspace
+ * holds the grouping of the batch, the work queue and the device error word. */
+lora_status lora_workspace_size(const lora_pool* pool, int32_t max_tokens, int32_t max_segments,
+                                size_t* bytes);
+
+/* Zeroes a fresh workspace (error word and queue counters).  Call once after
+ * allocating it, before its first use, on the stream that will use it. */
+lora_status lora_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Scheduler step: groups the batch by adapter, on the device.
+ * Rows [seg_start[s], seg_start[s+1]) form prefill segment s (adapter seg_adapter[s]),
+ * for s < S, and rows seg_start[S] + d, d < Td, are decode tokens (adapter
+ * dec_adapter[d]).  S may be 0 (decode only; seg_start may then be NULL and decode
+ * rows start at 0); Td may be 0 (prefill only).  T = rows of x and y.
+ * Result, in the workspace (see lora_workspace_view): the adapted rows ordered by
+ * ascending adapter id (batch order inside an adapter), group offsets and group
+ * adapter ids, and the work lists the kernels read.  All device arrays. */
+lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
+                         int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* Device pointers into a workspace written by lora_segment, for inspection. */
+typedef struct {
+    uint32_t* error_word;   /* device error bits (LORA_DERR_*)                         */
+    int32_t* counts;        /* [0] adapted rows T', [1] groups G, [2] FMA chunks,
+                               [3] MMA tiles                                          */
+    int32_t* perm;          /* [T'] adapted rows, grouped                              */
+    int32_t* grp_start;     /* [G+1] offsets into perm                                 */
+    int32_t* grp_adapter;   /* [G]                                                     */
+} lora_ws_view;
+lora_status lora_workspace_view(const lora_pool* pool, void* ws, size_t ws_bytes, int32_t max_tokens,
+                                int32_t max_segments, lora_ws_view* view);
+
+/* BGMV (decode): token_adapter[T] gives each row's adapter (-1 = base only).
+ * Groups the batch (lora_segment) and applies the delta for every problem. */
+lora_status lora_bgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                      const int32_t* token_adapter, int32_t T, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* SGMV (prefill): S segments, rows [seg_start[s], seg_start[s+1]) use seg_adapter[s];
+ * seg_start[0] >= 0, non-decreasing, seg_start[S] <= T. */
+lora_status lora_sgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                      const int32_t* seg_start, const int32_t* seg_adapter, int32_t S, int32_t T,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Mixed continuous-batching step: S prefill segments followed by Td decode tokens
+ * (rows seg_start[S] + d), one grouping and one delta launch per problem batch. */
+lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                             const int32_t* seg_start, const int32_t* seg_adapter, int32_t S,
+                             const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Delta launch only, reusing the grouping already in ws (from lora_segment with the
+ * same batch).  This is the kernel the other entry points run after grouping. */
+lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Debug export of the page-table walk (a2): for problem (layer, proj), for each group
+ * g of the grouping in ws, the r_a A-row pages then the r_a B-column pages, packed in
+ * group order into out_pages (device int32, capacity `cap`).  *count_dev receives the
+ * number written (device int32). */
+lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_bytes, int32_t layer,
+                                 int32_t proj, int32_t* out_pages, int64_t cap, int32_t* count_dev,
+                                 void* stream);
+
+/* Debug export of the fp32 shrink result: like lora_delta_grouped for ONE problem,
+ * and also writes t[row][j] = s_a * sum_k x[row,k] A_a[j,k] (fp32, the value the
+ * expand consumes) into t_out (device f32 [T][r_max]) for every adapted row. */
+lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* prob, void* ws,
+                                    size_t ws_bytes, float* t_out, void* stream);
+
+/* Synchronises `stream`, returns the device error bits accumulated in ws since the
+ * last call (in *bits) and clears them.  Returns LORA_EDEVICE if any bit was set. */
+lora_status lora_get_device_error(void* ws, void* stream, uint32_t* bits);
+
+/* The last CUDA runtime error code seen by this thread's library calls (0 = none). */
+int lora_last_cuda_error(void);
+
+/* Human-readable name of a status. */
+const char* lora_status_string(lora_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_GB300_H */

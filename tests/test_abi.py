@@ -1,0 +1,86 @@
+"""The C ABI library loads without a GPU and exports every symbol include/lora.h
+declares; host-only calls (pool creation checks, sizes, status strings) behave as
+documented.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "lora.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(lora_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from heterogeneous_adapters_gb300 import build, lib as load
+    build.build()
+    return load()
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ["lora_pool_create", "lora_bgmv", "lora_sgmv", "lora_apply_mixed", "lora_segment"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from heterogeneous_adapters_gb300 import _binding
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"liblora.so does not export {n}"
+    assert sorted(_binding.EXPORTED) == names
+
+
+def test_pool_create_host_checks(lib):
+    from heterogeneous_adapters_gb300._binding import (LORA_EALIGN, LORA_EINVAL, LORA_ETOOBIG,
+                                                       lora_pool_desc)
+    h = ctypes.c_void_p()
+    fake = 1 << 20   # never dereferenced: creation only records pointers
+
+    def desc(**kw):
+        d = dict(pages=fake, num_pages=16, h=256, num_adapters=2, num_layers=1, num_proj=1,
+                 r_max=8, reserved=0, page_table=fake, page_table_len=32, adapter_pt_off=fake,
+                 ranks=fake, scales=fake)
+        d.update(kw)
+        return lora_pool_desc(**d)
+
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc())) == 0
+    assert lib.lora_pool_destroy(h) == 0
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(pages=None))) == LORA_EINVAL
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(h=100))) == LORA_EALIGN
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(pages=fake + 8))) == LORA_EALIGN
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(r_max=257))) == LORA_ETOOBIG
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(num_adapters=0))) == LORA_EINVAL
+    assert lib.lora_pool_create(None, ctypes.byref(desc())) == LORA_EINVAL
+
+
+def test_workspace_size_and_status_strings(lib):
+    from heterogeneous_adapters_gb300._binding import LORA_ETOOBIG, lora_pool_desc
+    h = ctypes.c_void_p()
+    d = lora_pool_desc(1 << 20, 16, 256, 2, 1, 1, 8, 0, 1 << 20, 32, 1 << 20, 1 << 20, 1 << 20)
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(d)) == 0
+    n1, n2 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.lora_workspace_size(h, 64, 64, ctypes.byref(n1)) == 0
+    assert lib.lora_workspace_size(h, 100000, 16384, ctypes.byref(n2)) == 0
+    assert 256 < n1.value < n2.value and n1.value % 256 == 0
+    assert lib.lora_workspace_size(h, 1, 16385, ctypes.byref(n2)) == LORA_ETOOBIG
+    lib.lora_pool_destroy(h)
+    for s in range(7):
+        assert lib.lora_status_string(s)
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "heterogeneous_adapters_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
+                assert "lora_oracle" not in src, f

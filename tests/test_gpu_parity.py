@@ -1,0 +1,221 @@
+"""GPU path vs fp64 oracle, elementwise, through the C ABI (liblora.so).
+
+Small cases cover every element; the five full-size workloads run in the same
+launch configuration as the bench (all projections of one step in one call) and
+compare sampled projections element by element, plus properties over all of them.
+"""
+import numpy as np
+import pytest
+
+from workloads import spec
+from workloads.spec import Batch, Workload, all_problems, make_pool_all_resident
+
+from .harness import GpuCase, check_gate, full_check, oracle_problem
+
+pytestmark = pytest.mark.gpu
+
+
+def small_decode(seed, h, L, P, N, ranks, T, zipf=1.0, base=False):
+    return spec.decode_workload(f"decode-h{h}-t{T}", seed, h, L, P, N, ranks, T,
+                                None if base else zipf, base_ids=base)
+
+
+def small_prefill(seed, h, L, P, N, ranks, lens, ids=None):
+    rng = np.random.default_rng(seed)
+    ranks_a = rng.choice(np.asarray(ranks, np.int32), size=N)
+    pool = make_pool_all_resident(rng, h, L, P, ranks_a, num_pages=None)
+    lens = np.asarray(lens)
+    if ids is None:
+        ids = rng.choice(N, size=lens.size, p=spec.zipf_probs(N, 1.0))
+    seg_start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    batch = Batch(seg_start, np.asarray(ids, np.int32), np.zeros(0, np.int32))
+    return Workload(f"prefill-h{h}-s{lens.size}", seed, pool, batch, all_problems(L, P))
+
+
+def _mixed(seed, h, L, P, N, ranks, lens, n_dec, n_base):
+    rng = np.random.default_rng(seed)
+    ranks_a = rng.choice(np.asarray(ranks, np.int32), size=N)
+    n_req = len(lens) + n_dec
+    ids = rng.choice(N, size=n_req, p=spec.zipf_probs(N, 0.8))
+    ids[rng.choice(n_req, size=n_base, replace=False)] = -1
+    pool = make_pool_all_resident(rng, h, L, P, ranks_a, num_pages=None)
+    seg_start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    batch = Batch(seg_start, ids[:len(lens)].astype(np.int32), ids[len(lens):].astype(np.int32))
+    return Workload(f"mixed-h{h}", seed, pool, batch, all_problems(L, P))
+
+
+SMALL = {
+    "config0": spec.config0,
+    "decode-h512-ragged-ranks": lambda: small_decode(41, 512, 2, 4, 20, [1, 3, 8, 16, 64], 37),
+    "decode-h5120": lambda: small_decode(43, 5120, 1, 2, 10, [8, 128], 20),
+    "decode-h4096-r256": lambda: small_decode(44, 4096, 1, 1, 3, [256], 9),
+    "decode-base-uniform": lambda: small_decode(45, 1024, 1, 2, 6, [4, 16], 25, base=True),
+    "prefill-h1024-ragged": lambda: small_prefill(46, 1024, 1, 3, 8, [8, 16, 32],
+                                                  [1, 7, 130, 300, 2, 64, 129, 5, 0, 17, 255, 3]),
+    "mixed-h2048": lambda: _mixed(47, 2048, 2, 2, 30, [8, 16, 32, 64, 128], [5, 260, 131], 40, 5),
+    "mixed-h5120": lambda: _mixed(48, 5120, 1, 2, 12, [8, 128], [300, 9], 17, 3),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("y0_zero", [False, True])
+def test_small_parity(name, y0_zero):
+    wl = SMALL[name]()
+    case = GpuCase(wl, y0_zero=y0_zero)
+    try:
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+    finally:
+        case.close()
+
+
+def test_t_matches_oracle_shrink():
+    """fp32 t (the value the expand consumes, scaled) against the oracle's fp64 t."""
+    import torch
+
+    from .harness import T_ACC, magnitude_sums
+    from workloads.materialize import host_inputs
+    wl = small_decode(51, 2048, 1, 2, 12, [2, 8, 32, 64], 33)
+    case = GpuCase(wl)
+    try:
+        lora = case.lora
+        b = wl.batch
+        lora.segment(case.pool, None, None, 0, case.dev.token_adapter, b.num_decode, case.T,
+                     case.ws, case.ws_bytes, case.stream)
+        hi = host_inputs(wl)
+        ids = b.token_adapter()
+        for i, (l, p) in enumerate(case.dev.problems):
+            t_out = torch.zeros((case.T, wl.pool.r_max), dtype=torch.float32, device=case.device)
+            lora.debug_delta_with_t(case.pool, case.problems()[i], case.ws, case.ws_bytes, t_out,
+                                    case.stream)
+            assert case.error_bits() == 0
+            t_gpu = t_out.cpu().numpy().astype(np.float64)
+            _, t_ref, _ = oracle_problem(wl, hi, l, p, want_t=True)
+            S, _ = magnitude_sums(wl, hi, l, p)
+            for row in np.nonzero(ids >= 0)[0]:
+                a = ids[row]
+                r = int(wl.pool.ranks[a])
+                s = float(wl.pool.scales[a])
+                err = np.abs(t_gpu[row, :r] - s * t_ref[row, :r])
+                assert np.all(err <= s * T_ACC * S[row, :r]), (row, err.max())
+    finally:
+        case.close()
+
+
+def test_repeat_calls_accumulate():
+    """Two calls add the delta twice (y is updated in place, the queue resets itself)."""
+    wl = small_decode(52, 1024, 1, 2, 9, [4, 8], 21)
+    case = GpuCase(wl, y0_zero=True)
+    try:
+        assert case.run() == 0
+        once = [case.y_f64(i) for i in range(len(wl.problems))]
+        assert case.run() == 0
+        for i in range(len(wl.problems)):
+            twice = case.y_f64(i)
+            check_gate(twice, 2 * once[i], "second call")
+    finally:
+        case.close()
+
+
+def test_zero_B_leaves_y_bit_identical():
+    import torch
+    wl = small_decode(53, 1024, 2, 2, 10, [8, 16], 30)
+    case = GpuCase(wl)
+    try:
+        pool = wl.pool
+        b_pages = np.concatenate([pool.pt[pool.block_entries(a, l, p, 1)]
+                                  for a in range(pool.num_adapters) for (l, p) in wl.problems])
+        case.dev.pool[torch.from_numpy(b_pages.astype(np.int64)).to(case.device)] = 0
+        before = [case.y_bits(i).copy() for i in range(len(wl.problems))]
+        assert case.run() == 0
+        for i in range(len(wl.problems)):
+            after = case.y_bits(i)
+            same = (after == before[i]) | ((before[i] == 0x8000) & (after == 0))  # -0 -> +0
+            assert same.all()
+    finally:
+        case.close()
+
+
+def test_page_placement_and_batch_order_invariance():
+    """Moving pages in the pool, or permuting the batch, gives bit-identical rows."""
+    import torch
+    wl = small_decode(54, 2048, 1, 2, 15, [8, 16, 32], 40)
+    base = GpuCase(wl)
+    try:
+        assert base.run() == 0
+        ref = [base.y_bits(i).copy() for i in range(len(wl.problems))]
+        # page placement: move every page q to slot perm[q]
+        rng = np.random.default_rng(5)
+        perm = torch.from_numpy(rng.permutation(wl.pool.num_pages)).to(base.device)
+        moved = torch.empty_like(base.dev.pool)
+        moved[perm] = base.dev.pool
+        base.dev.pool.copy_(moved)
+        base.dev.pt.copy_(perm[base.dev.pt.long()].int())
+        base.dev.y.copy_(base.y_init)
+        assert base.run() == 0
+        for i in range(len(wl.problems)):
+            assert np.array_equal(base.y_bits(i), ref[i])
+        # batch order: permute rows of x, y and the adapter ids
+        order = torch.from_numpy(rng.permutation(base.T)).to(base.device)
+        base.dev.x.copy_(base.dev.x[:, order])
+        base.dev.y.copy_(base.y_init[:, order])
+        base.dev.token_adapter.copy_(base.dev.token_adapter[order])
+        assert base.run() == 0
+        o = order.cpu().numpy()
+        for i in range(len(wl.problems)):
+            assert np.array_equal(base.y_bits(i), ref[i][o])
+    finally:
+        base.close()
+
+
+def test_empty_and_all_base_batches():
+    wl = small_decode(55, 512, 1, 1, 4, [4], 8, base=True)
+    wl.batch.dec_adapter[:] = -1
+    case = GpuCase(wl)
+    try:
+        before = case.y_bits(0).copy()
+        assert case.run() == 0
+        assert np.array_equal(case.y_bits(0), before)
+    finally:
+        case.close()
+    # empty batch: T = 0 is a no-op (buffers still valid pointers)
+    case = GpuCase(small_decode(56, 512, 1, 1, 4, [4], 3))
+    try:
+        before = case.y_bits(0).copy()
+        case.lora.bgmv(case.pool, case.problems(), case.dev.token_adapter, 0, case.ws,
+                       case.ws_bytes, case.stream)
+        assert case.error_bits() == 0
+        assert np.array_equal(case.y_bits(0), before)
+    finally:
+        case.close()
+
+
+# ----------------------------------------------------------------------------- full-size configs
+
+def _sample(n, k, seed):
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(n, size=min(k, n), replace=False).tolist())
+
+
+@pytest.mark.parametrize("cfg,k", [(1, 8), (2, 2), (3, 2), ("4d", 4), ("4z", 4)])
+def test_full_config(cfg, k):
+    import torch
+    if cfg == "4d":
+        wl = spec.config4("distinct")
+    elif cfg == "4z":
+        wl = spec.config4("zipf")
+    else:
+        wl = spec.CONFIGS[cfg]()
+    case = GpuCase(wl, nan_dummies=True)
+    try:
+        assert case.run() == 0
+        # properties over every projection: finite, base rows untouched, adapted rows changed
+        ids = torch.from_numpy(wl.batch.token_adapter()).to(case.device)
+        base_rows = ids == -1
+        assert torch.isfinite(case.dev.y).all()
+        if case.y_init is not None and base_rows.any():
+            assert torch.equal(case.dev.y[:, base_rows], case.y_init[:, base_rows])
+        full_check(wl, case, _sample(len(wl.problems), k, seed=sum(map(ord, str(cfg)))),
+                   strict=False)
+    finally:
+        case.close()
