@@ -154,6 +154,12 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def aggregate_throughput(units_per_step: float, steps: int, world: int, elapsed_local: float):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    elapsed = max_over_ranks(elapsed_local, world)
+    return units_per_step * steps * world / elapsed, elapsed
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -277,7 +283,7 @@ def run_ours(args, rank: int, world: int, local: int):
         lora.segment(pool, seg_start, seg_adapter, S, dec, Td, T, ws, nbytes, stream)
 
     def delta():
-        lora.delta_grouped(pool, probs, ws, nbytes, stream)
+        lora.delta_grouped(pool, probs, T, ws, nbytes, stream)
 
     m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems))
     launches_per_step = 1 + -(-len(probs) // lora.LORA_MAX_PROBLEMS_PER_LAUNCH)
@@ -310,9 +316,8 @@ def run_ours(args, rank: int, world: int, local: int):
     kern = [ev[k][1].elapsed_time(ev[k][2]) / 1e3 for k in range(args.steps)]
     err = lora.get_device_error(ws, stream)
     assert err == 0, f"device error bits {err:#x}"
-    elapsed_max = max_over_ranks(elapsed, world)
     tokens_step = m["adapted_tokens"]
-    value = tokens_step * args.steps * world / elapsed_max
+    value, elapsed_max = aggregate_throughput(tokens_step, args.steps, world, elapsed)
 
     # roofline of the dominant kernel (the delta kernel)
     peaks = measured_peaks()

@@ -1,0 +1,450 @@
+// CUDA-core BGMV path, warp-specialised: a TMA-fed shared-memory ring.
+//
+// "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels work":
+// BGMV treats decode tokens independently, gathering the weights of each token's
+// adapter; shrink v = A x, expand y += gamma B v.  "S-LoRA: Serving Thousands of
+// Concurrent LoRA Adapters", "Kernels and tensor parallelism": each adapter is
+// gathered from non-contiguous pages, mixed ranks without padding.
+//
+// Decode is HBM-bound: the work is streaming each distinct adapter's 2 r pages once
+// per projection.  One persistent CTA per SM:
+//   warp 0 (producer)  takes work items (chunk of <= 4 rows of one adapter, projection)
+//                      in a static rank-sorted round-robin order, validates the item's page ids, and streams
+//                      into a ring of shared-memory stages with 1-D bulk copies
+//                      (cp.async.bulk, completion counted on an mbarrier): first the x
+//                      rows of the chunk, then its A-row pages, then its B-column pages,
+//                      up to kRingPages rows of 2h bytes per stage;
+//   warps 1..8         consume the stages in the same order: x into registers; each A
+//                      page -> fp32 partial dot products, reduced across the warp with a
+//                      transposing shuffle and across warps in shared memory (t, scaled);
+//                      each B page -> acc[row][col] += t[row][j] * B_j[col]; finally
+//                      y = bf16_rn(y + acc) with 16-byte stores.
+// Bytes in flight are bounded by the ring (about 190 KB per SM), not by registers.
+// Every wait is bounded in time; a timeout sets LORA_DERR_TIMEOUT and unwinds.
+#pragma once
+#include "common.cuh"
+#include "ptx.cuh"
+#include "segment.cuh"
+
+namespace lora {
+
+constexpr int kRingConsumerWarps = 8;
+constexpr int kRingConsumers = kRingConsumerWarps * 32;
+constexpr int kRingThreads = kRingConsumers + 32;
+constexpr int kRingPages = 4;              // pages (or x rows) per stage
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+constexpr uint32_t kDerrTimeout = 0x20u;
+
+enum StageKind : int32_t { kStageX = 0, kStageA = 1, kStageB = 2, kStageStop = 3, kStageSkip = 4 };
+
+struct StageMeta {
+    int32_t kind;
+    int32_t npages;   // rows carried by this stage
+    int32_t j0;       // first page index (A/B stages)
+    int32_t pr;       // problem index
+    int32_t count;    // rows of the chunk (X stage)
+    int32_t rank;
+    float scale;
+    int32_t rows[kChunk];
+    int32_t pad;
+};
+static_assert(sizeof(StageMeta) == 48, "stage meta size");
+
+struct RingParams {
+    PoolView pool;
+    char* ws;
+    float* t_out;
+    int32_t nprob;
+    int32_t stages;        // ring depth
+    int32_t stage_bytes;   // kRingPages * 2h
+    int32_t pad;
+    ProbDesc probs[LORA_MAX_PROBLEMS_PER_LAUNCH];
+};
+
+// Dynamic shared memory layout (offsets from a 1024-byte aligned base).
+struct RingSmem {
+    uint32_t ring, full, empty, cbar, meta, red, ts, pgbuf, total;
+};
+
+__host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes, int r_max) {
+    RingSmem L;
+    const int rp = (r_max + 7) / 8 * 8;
+    uint32_t o = 0;
+    L.ring = o;  o += (uint32_t)stages * stage_bytes;
+    L.full = o;  o += stages * 8;
+    L.empty = o; o += stages * 8;
+    L.cbar = o;  o += 8;
+    L.meta = o;  o += stages * sizeof(StageMeta);
+    o = (o + 15) & ~15u;
+    L.red = o;   o += kRingConsumerWarps * rp * kChunk * 4;
+    L.ts = o;    o += rp * kChunk * 4;
+    L.pgbuf = o; o += 2 * LORA_MAX_RANK * 4;
+    L.total = o;
+    return L;
+}
+
+// Column vectors (8 bf16 = 16 B) of a row handled by consumer thread c: c + 256 v.
+template <int NV, int NT>
+__device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, int stage_row_bytes,
+                                                  int npages, int h8, int c,
+                                                  const uint4 (&xv)[kChunk][NV], float* red_w,
+                                                  int j0) {
+    constexpr int V = kRingPages * kChunk;   // 16 values per warp
+    float vals[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) vals[i] = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < kRingPages; ++jj) {
+        if (jj < npages) {
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int vi = c + v * kRingConsumers;
+                if (vi < h8) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(stage + jj * stage_row_bytes + vi * 16);
+                    float a8[8];
+                    unpack8(a, a8);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        float x8[8];
+                        unpack8(xv[t][v], x8);
+                        float s = vals[jj * kChunk + t];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) s = fmaf(x8[e], a8[e], s);
+                        vals[jj * kChunk + t] = s;
+                    }
+                }
+            }
+        }
+    }
+    const float sum = warp_transpose_reduce<V>(vals);
+    const int lane = threadIdx.x & 31;
+    if ((lane & 1) == 0) red_w[j0 * kChunk + (lane >> 1)] = sum;   // index jj*kChunk + t
+}
+
+template <int NV, int NT>
+__device__ __forceinline__ void ring_expand_stage(const unsigned char* stage, int stage_row_bytes,
+                                                  int npages, int h8, int c, const float* ts, int j0,
+                                                  float (&acc)[kChunk][NV][8]) {
+#pragma unroll
+    for (int jj = 0; jj < kRingPages; ++jj) {
+        if (jj < npages) {
+            const float4 tj = *reinterpret_cast<const float4*>(ts + (j0 + jj) * kChunk);
+            const float tv[4] = {tj.x, tj.y, tj.z, tj.w};
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int vi = c + v * kRingConsumers;
+                if (vi < h8) {
+                    const uint4 b = *reinterpret_cast<const uint4*>(stage + jj * stage_row_bytes + vi * 16);
+                    float b8[8];
+                    unpack8(b, b8);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[t][v][e] = fmaf(tv[t], b8[e], acc[t][v][e]);
+                }
+            }
+        }
+    }
+}
+
+// One work item on the consumer side, specialised on the number of rows NT.
+// Returns false if a wait timed out (the kernel then unwinds).
+// Barrier of the consumer warps only, built on an mbarrier so that the wait is bounded
+// (a plain named barrier could wait forever on a warp that gave up).
+__device__ __forceinline__ bool consumer_barrier(unsigned char* base, const RingSmem& L, uint32_t& phase) {
+    __syncwarp();
+    const uint32_t bar = smem_addr(base + L.cbar);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase & 1, kWaitLimitNs);
+    ++phase;
+    return ok;
+}
+
+template <int NV, int NT>
+__device__ bool ring_consume_item(const RingParams& p, unsigned char* base, const RingSmem& L,
+                                  uint32_t& it, uint32_t& bphase, const StageMeta& mx, int c) {
+    const int h = p.pool.h, h8 = h >> 3;
+    const int row_bytes = h * 2;
+    const int S = p.stages;
+    const int warp = c >> 5, lane = c & 31;
+    const int rp = (p.pool.r_max + 7) / 8 * 8;
+    float* red = reinterpret_cast<float*>(base + L.red);
+    float* ts = reinterpret_cast<float*>(base + L.ts);
+    float* red_w = red + warp * rp * kChunk;
+    const int r = mx.rank;
+    const ProbDesc pd = p.probs[mx.pr];
+
+    // x rows (stage just waited by the caller)
+    uint4 xv[kChunk][NV];
+    {
+        const unsigned char* st = base + L.ring + (size_t)(it % S) * p.stage_bytes;
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int vi = c + v * kRingConsumers;
+                xv[t][v] = (t < mx.count && vi < h8) ? *reinterpret_cast<const uint4*>(st + t * row_bytes + vi * 16)
+                                               : make_uint4(0, 0, 0, 0);
+            }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(base + L.empty + (it % S) * 8));
+        ++it;
+    }
+    // shrink over the A stages
+    for (int j0 = 0; j0 < r; j0 += kRingPages) {
+        const uint32_t s = it % S;
+        if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
+        const int np = min(kRingPages, r - j0);
+        ring_shrink_stage<NV, NT>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, xv,
+                                  red_w, j0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
+        ++it;
+    }
+    if (!consumer_barrier(base, L, bphase)) return false;
+    for (int e = c; e < r * kChunk; e += kRingConsumers) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < kRingConsumerWarps; ++w) a += red[w * rp * kChunk + e];
+        ts[e] = a * mx.scale;
+        if (p.t_out != nullptr) {
+            const int j = e / kChunk, t = e % kChunk;
+            if (t < mx.count) p.t_out[(long long)mx.rows[t] * p.pool.r_max + j] = a * mx.scale;
+        }
+    }
+    if (!consumer_barrier(base, L, bphase)) return false;
+    // prefetch the y rows while the B pages stream in
+    uint4 yv[NT][NV];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int vi = c + v * kRingConsumers;
+            yv[t][v] = (t < mx.count && vi < h8) ? ld16(pd.y + (long long)mx.rows[t] * pd.ldy + vi * 8) : make_uint4(0, 0, 0, 0);
+        }
+    float acc[kChunk][NV][8];
+#pragma unroll
+    for (int t = 0; t < kChunk; ++t)
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[t][v][e] = 0.f;
+    for (int j0 = 0; j0 < r; j0 += kRingPages) {
+        const uint32_t s = it % S;
+        if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
+        const int np = min(kRingPages, r - j0);
+        ring_expand_stage<NV, NT>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, ts, j0,
+                                  acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
+        ++it;
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int vi = c + v * kRingConsumers;
+            if (t < mx.count && vi < h8) {
+                float y8[8];
+                unpack8(yv[t][v], y8);
+                uint4 o;
+                o.x = pack2(y8[0] + acc[t][v][0], y8[1] + acc[t][v][1]);
+                o.y = pack2(y8[2] + acc[t][v][2], y8[3] + acc[t][v][3]);
+                o.z = pack2(y8[4] + acc[t][v][4], y8[5] + acc[t][v][5]);
+                o.w = pack2(y8[6] + acc[t][v][6], y8[7] + acc[t][v][7]);
+                st16(pd.y + (long long)mx.rows[t] * pd.ldy + vi * 8, o);
+            }
+        }
+    // the next item's final reduction must not overwrite ts while a warp still reads it
+    return consumer_barrier(base, L, bphase);
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kRingThreads, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
+    extern __shared__ __align__(1024) unsigned char ring_smem_raw[];
+    unsigned char* base = ring_smem_raw;
+    const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max);
+    const int S = p.stages;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+    StageMeta* meta = reinterpret_cast<StageMeta*>(base + L.meta);
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_addr(base + L.full + s * 8), 1);
+            mbar_init(smem_addr(base + L.empty + s * 8), kRingConsumerWarps);
+        }
+        mbar_init(smem_addr(base + L.cbar), kRingConsumerWarps);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        // Items (chunk q, problem pr) = (item / nprob, item % nprob) are dealt round-robin
+        // over the CTAs (chunks are listed by descending rank, so every CTA gets a similar
+        // mix and the last round is made of the smallest items).  The metadata of the next
+        // items is loaded while the current one streams: the chunk two items ahead, the
+        // page ids one item ahead.
+        const PoolView& P = p.pool;
+        const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
+        const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
+        int32_t* pgbuf = reinterpret_cast<int32_t*>(base + L.pgbuf);
+        const uint32_t total = (uint32_t)hdr->counts[2] * (uint32_t)p.nprob;
+        const uint32_t row_bytes = (uint32_t)P.h * 2;
+        const uint32_t G = gridDim.x;
+        constexpr int kPg = 2 * LORA_MAX_RANK / 32;   // page ids per lane
+        uint32_t it = 0;
+        bool ok = true;
+        auto claim = [&](void) -> int {
+            const uint32_t s = it % S;
+            if (!mbar_wait(smem_addr(base + L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) return -1;
+            return (int)s;
+        };
+        auto load_pages = [&](const Chunk& c, uint32_t itm, int32_t (&pg)[kPg]) {
+            const long long blk = c.pt_base + (long long)p.probs[itm % p.nprob].blk * 2 * c.rank;
+#pragma unroll
+            for (int k = 0; k < kPg; ++k) {
+                const int e = lane + 32 * k;
+                pg[k] = e < 2 * c.rank ? P.pt[blk + e] : 0;
+            }
+        };
+        uint32_t item = blockIdx.x;
+        Chunk c_next, c_next2;
+        int32_t pg_next[kPg];
+        if (item < total) {
+            c_next = chunks[item / p.nprob];
+            load_pages(c_next, item, pg_next);
+        }
+        if (item + G < total) c_next2 = chunks[(item + G) / p.nprob];
+        for (; item < total; item += G) {
+            const Chunk ch = c_next;
+            const int pr = item % p.nprob;
+            int32_t pg[kPg];
+#pragma unroll
+            for (int k = 0; k < kPg; ++k) pg[k] = pg_next[k];
+            if (item + G < total) {
+                c_next = c_next2;
+                load_pages(c_next, item + G, pg_next);
+            }
+            if (item + 2 * G < total) c_next2 = chunks[(item + 2 * G) / p.nprob];
+
+            const int r = ch.rank;
+            bool bad = false;
+#pragma unroll
+            for (int k = 0; k < kPg; ++k) {
+                const int e = lane + 32 * k;
+                if (e < 2 * r) {
+                    bad |= (pg[k] < 0 || pg[k] >= P.num_pages);
+                    pgbuf[e] = pg[k];
+                }
+            }
+            bad = __any_sync(0xffffffffu, bad);
+            __syncwarp();
+            StageMeta m;
+            m.kind = bad ? kStageSkip : kStageX;
+            m.npages = ch.count;
+            m.j0 = 0;
+            m.pr = pr;
+            m.count = ch.count;
+            m.rank = r;
+            m.scale = ch.scale;
+#pragma unroll
+            for (int t = 0; t < kChunk; ++t) m.rows[t] = ch.rows[t];
+            m.pad = 0;
+            if (bad && lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
+            // x stage (or a skip marker)
+            int s = claim();
+            if (s < 0) { ok = false; break; }
+            if (lane == 0) {
+                meta[s] = m;
+                if (!bad)
+                    mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), row_bytes * ch.count);
+                else
+                    mbar_arrive(smem_addr(base + L.full + s * 8));
+            }
+            __syncwarp();
+            if (!bad && lane < ch.count) {
+                const ProbDesc& pd = p.probs[pr];
+                bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
+                         pd.x + (long long)ch.rows[lane] * pd.ldx, row_bytes,
+                         smem_addr(base + L.full + s * 8));
+            }
+            ++it;
+            if (bad) continue;
+            // A pages then B pages
+            for (int ab = 0; ab < 2 && ok; ++ab) {
+                for (int j0 = 0; j0 < r; j0 += kRingPages) {
+                    const int np = min(kRingPages, r - j0);
+                    s = claim();
+                    if (s < 0) { ok = false; break; }
+                    if (lane == 0) {
+                        StageMeta mm = m;
+                        mm.kind = ab ? kStageB : kStageA;
+                        mm.npages = np;
+                        mm.j0 = j0;
+                        meta[s] = mm;
+                        mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), row_bytes * np);
+                    }
+                    __syncwarp();
+                    if (lane < np) {
+                        const int page = pgbuf[ab * r + j0 + lane];
+                        bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
+                                 P.pages + (long long)page * P.h, row_bytes, smem_addr(base + L.full + s * 8));
+                    }
+                    ++it;
+                }
+            }
+            if (!ok) break;
+        }
+        if (ok) {
+            // stop marker for the consumers
+            const int s = claim();
+            if (s >= 0 && lane == 0) {
+                meta[s].kind = kStageStop;
+                mbar_arrive(smem_addr(base + L.full + s * 8));
+            }
+            if (s < 0) ok = false;
+        }
+        if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeout);
+        // wait (bounded) until every stage this warp filled has landed, so no copy into
+        // this CTA's shared memory is still in flight when it exits
+        if (lane == 0) {
+            const uint32_t first = it > (uint32_t)S ? it - S : 0;
+            for (uint32_t k = first; k < it; ++k)
+                mbar_wait(smem_addr(base + L.full + (k % S) * 8), (k / S) & 1, 100000000ull);
+        }
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int c = tid - 32;
+        uint32_t it = 0, bphase = 0;
+        for (;;) {
+            const uint32_t s = it % S;
+            if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) {
+                if (c == 0) set_error(&hdr->err, kDerrTimeout);
+                break;
+            }
+            const StageMeta mx = meta[s];
+            if (mx.kind == kStageStop) break;
+            if (mx.kind == kStageSkip) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
+                ++it;
+                continue;
+            }
+            bool ok;
+            if (mx.count == 1)
+                ok = ring_consume_item<NV, 1>(p, base, L, it, bphase, mx, c);
+            else if (mx.count == 2)
+                ok = ring_consume_item<NV, 2>(p, base, L, it, bphase, mx, c);
+            else
+                ok = ring_consume_item<NV, kChunk>(p, base, L, it, bphase, mx, c);
+            if (!ok) {
+                if (c == 0) set_error(&hdr->err, kDerrTimeout);
+                break;
+            }
+        }
+    }
+}
+
+}  // namespace lora

@@ -24,13 +24,19 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
-// Work item of the CUDA-core path: up to kChunk rows of one adapter.
+// Work item of the CUDA-core path: up to 4 rows of one adapter, with everything the
+// delta kernels need about it except the projection (48 bytes, read with 3 vector loads).
 struct Chunk {
     int32_t adapter;
-    int32_t begin;   // offset into the FMA row list
-    int32_t count;   // rows, 1..kChunk
+    int32_t count;     // rows, 1..4
     int32_t rank;
+    float scale;
+    int64_t pt_base;   // adapter's page-table offset
+    int32_t begin;     // offset into the CUDA-core row list
+    int32_t pad;
+    int32_t rows[4];   // x / y rows (unused slots 0)
 };
+static_assert(sizeof(Chunk) == 48, "chunk is 48 bytes");
 
 // Work item of the tensor-core path: up to 128 contiguous rows of one segment.
 struct Tile {

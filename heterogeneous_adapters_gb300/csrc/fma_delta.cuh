@@ -57,7 +57,6 @@ __global__ void __launch_bounds__(kFmaThreads, 1) fma_delta_kernel(const __grid_
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
     const WsLayout L = ws_layout(hdr->cap_tokens, hdr->cap_segments);
     const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + L.chunks);
-    const int32_t* fma_rows = reinterpret_cast<const int32_t*>(p.ws + L.fma_rows);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = P.h;
     const uint32_t total = (uint32_t)hdr->counts[2] * (uint32_t)p.nprob;
@@ -78,7 +77,7 @@ __global__ void __launch_bounds__(kFmaThreads, 1) fma_delta_kernel(const __grid_
             bad |= (page < 0 || page >= P.num_pages);
             pg[e] = page;
         }
-        if (tid < kChunk) rows[tid] = tid < ch.count ? fma_rows[ch.begin + tid] : 0;
+        if (tid < kChunk) rows[tid] = ch.rows[tid];
         if (__syncthreads_or(bad)) {
             if (tid == 0) set_error(&hdr->err, LORA_DERR_PAGE);
             continue;

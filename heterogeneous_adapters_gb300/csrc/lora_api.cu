@@ -3,6 +3,8 @@
 // Host side: argument checks, workspace layout, launch configuration.  All compute
 // runs in the kernels of segment.cuh and fma_delta.cuh (and the tensor-core kernel
 // when present); nothing here touches adapter or activation values.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -10,9 +12,11 @@
 
 #include <mutex>
 
+#include "bgmv_ring.cuh"
 #include "common.cuh"
 #include "fma_delta.cuh"
 #include "segment.cuh"
+#include "sgmv_mma.cuh"
 
 using namespace lora;
 
@@ -54,6 +58,7 @@ PoolView view_of(const lora_pool* pool) {
 // Per-device launch facts, looked up once per device.
 struct DeviceInfo {
     int sm_count = 0;
+    int smem_optin = 0;
     bool ready = false;
 };
 constexpr int kMaxDevices = 64;
@@ -69,6 +74,9 @@ lora_status device_info(DeviceInfo** out) {
     DeviceInfo& di = g_dev[dev];
     if (!di.ready) {
         st = cuda_status(cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev));
+        if (st != LORA_OK) return st;
+        st = cuda_status(
+            cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
         if (st != LORA_OK) return st;
         di.ready = true;
     }
@@ -109,10 +117,188 @@ lora_status launch_fma(const DeltaParams& prm, size_t smem, cudaStream_t stream)
     return cuda_status(cudaGetLastError());
 }
 
-lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                      float* t_out, cudaStream_t stream) {
+// Ring depth that fits the opt-in shared memory of one CTA (at most 8 stages).
+int ring_stages(int smem_optin, int stage_bytes, int r_max, size_t* smem) {
+    for (int S = 8; S >= 2; --S) {
+        const size_t need = ring_smem_layout(S, stage_bytes, r_max).total + 1024;
+        if (need <= (size_t)smem_optin) {
+            *smem = need;
+            return S;
+        }
+    }
+    return 0;
+}
+
+template <int NV>
+lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
+    static thread_local int attr_dev = -1;
+    static thread_local size_t attr_smem = 0;
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    size_t smem = 0;
+    const int S = ring_stages(di->smem_optin, prm.stage_bytes, prm.pool.r_max, &smem);
+    if (S < 2) return LORA_ETOOBIG;
+    prm.stages = S;
+    auto kern = bgmv_ring_kernel<NV>;
+    if (attr_dev != dev || attr_smem < smem) {
+        st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (st != LORA_OK) return st;
+        attr_dev = dev;
+        attr_smem = smem;
+    }
+    kern<<<di->sm_count, kRingThreads, smem, stream>>>(prm);
+    return cuda_status(cudaGetLastError());
+}
+
+bool use_legacy_fma() {
+    const char* e = getenv("LORA_DELTA_KERNEL");
+    return e != nullptr && strcmp(e, "direct") == 0;
+}
+
+lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
+                           float* t_out, cudaStream_t stream) {
     const lora_pool_desc& d = pool->d;
-    // host-side checks of every problem before any launch
+    static thread_local RingParams prm;
+    for (int32_t base = 0; base < nprob; base += LORA_MAX_PROBLEMS_PER_LAUNCH) {
+        const int32_t n = nprob - base < LORA_MAX_PROBLEMS_PER_LAUNCH ? nprob - base
+                                                                         : LORA_MAX_PROBLEMS_PER_LAUNCH;
+        memset(&prm, 0, sizeof prm);
+        prm.pool = view_of(pool);
+        prm.ws = reinterpret_cast<char*>(ws);
+        prm.t_out = t_out;
+        prm.nprob = n;
+        prm.stage_bytes = kRingPages * 2 * d.h;
+        for (int32_t i = 0; i < n; ++i) {
+            const lora_problem& pr = probs[base + i];
+            prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
+            prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
+            prm.probs[i].ldx = (int32_t)pr.ldx;
+            prm.probs[i].ldy = (int32_t)pr.ldy;
+            prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
+        }
+        const int nv = (d.h / 8 + kRingConsumers - 1) / kRingConsumers;
+        lora_status st;
+        switch (nv) {
+            case 1: st = launch_ring<1>(prm, stream); break;
+            case 2: st = launch_ring<2>(prm, stream); break;
+            case 3: st = launch_ring<3>(prm, stream); break;
+            default: st = launch_ring<4>(prm, stream); break;
+        }
+        if (st != LORA_OK) return st;
+    }
+    return LORA_OK;
+}
+
+// ---------------------------------------------------------------------------- tensor-core path
+// Segments of at least this many rows (and rank <= kMmaMaxRank) take the tensor-core
+// path when h is a multiple of 128; LORA_MMA_MIN_ROWS overrides it (0 disables).
+int mma_min_rows(const lora_pool_desc& d) {
+    if (d.h % kMmaNTile != 0) return 0;
+    const char* e = getenv("LORA_MMA_MIN_ROWS");
+    if (e != nullptr) return atoi(e) > 0 ? atoi(e) : 0;
+    return 32;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+lora_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        lora_status st = cuda_status(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                                      cudaEnableDefault, &q));
+        if (st != LORA_OK) return st;
+        if (fn == nullptr || q != cudaDriverEntryPointSuccess) return LORA_ECUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return LORA_OK;
+}
+
+// 2-D bf16 tensor map {inner, rows} with row stride `ld` elements, box {64, box_rows},
+// 128-byte swizzle, out-of-range elements read as zero.
+lora_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
+                     uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    lora_status st = encode_fn(&enc);
+    if (st != LORA_OK) return st;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = 10000 + (int)r;
+        return LORA_ECUDA;
+    }
+    return LORA_OK;
+}
+
+lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                    cudaStream_t stream) {
+    const lora_pool_desc& d = pool->d;
+    if (T <= 0 || nprob <= 0) return LORA_OK;
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    static thread_local MmaParams prm;
+    static thread_local int attr_dev = -1;
+    static thread_local size_t attr_smem = 0;
+    const int rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
+    int stage_bytes = 16384 + rp_max * 128;
+    if (rp_max * 256 > stage_bytes) stage_bytes = rp_max * 256;
+    stage_bytes = (stage_bytes + 1023) / 1024 * 1024;
+    const int t_bytes = 128 * rp_max * 2;
+    int S = 8;
+    size_t smem = 0;
+    for (; S >= 2; --S) {
+        smem = mma_smem_layout(S, stage_bytes, t_bytes).total + 1024;
+        if (smem <= (size_t)di->smem_optin) break;
+    }
+    if (S < 2) return LORA_ETOOBIG;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev || attr_smem < smem) {
+        st = cuda_status(cudaFuncSetAttribute(sgmv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)smem));
+        if (st != LORA_OK) return st;
+        attr_dev = dev;
+        attr_smem = smem;
+    }
+    for (int32_t base = 0; base < nprob; base += kMmaMaxProbs) {
+        const int32_t n = nprob - base < kMmaMaxProbs ? nprob - base : kMmaMaxProbs;
+        memset(&prm, 0, sizeof prm);
+        st = make_map(&prm.pool_map, d.pages, (uint64_t)d.h, (uint64_t)d.num_pages, (uint64_t)d.h, 1);
+        if (st != LORA_OK) return st;
+        for (int32_t i = 0; i < n; ++i) {
+            const lora_problem& pr = probs[base + i];
+            st = make_map(&prm.x_map[i], pr.x, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldx, 128);
+            if (st != LORA_OK) return st;
+            prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
+            prm.probs[i].ldy = (int32_t)pr.ldy;
+            prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
+        }
+        prm.pool = view_of(pool);
+        prm.ws = reinterpret_cast<char*>(ws);
+        prm.nprob = n;
+        prm.stages = S;
+        prm.stage_bytes = stage_bytes;
+        prm.t_bytes = t_bytes;
+        prm.rp_max = rp_max;
+        sgmv_mma_kernel<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
+        st = cuda_status(cudaGetLastError());
+        if (st != LORA_OK) return st;
+    }
+    return LORA_OK;
+}
+
+lora_status check_problems(const lora_pool_desc& d, const lora_problem* probs, int32_t nprob) {
     for (int32_t i = 0; i < nprob; ++i) {
         const lora_problem& pr = probs[i];
         if (pr.x == nullptr || pr.y == nullptr) return LORA_EINVAL;
@@ -123,6 +309,12 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
         if (pr.layer < 0 || pr.layer >= d.num_layers || pr.proj < 0 || pr.proj >= d.num_proj)
             return LORA_EINVAL;
     }
+    return LORA_OK;
+}
+
+lora_status run_delta_direct(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
+                             float* t_out, cudaStream_t stream) {
+    const lora_pool_desc& d = pool->d;
     const size_t smem = fma_smem_bytes(d.r_max);
     static thread_local DeltaParams prm;   // ~8 KiB: keep it off the stack
     for (int32_t base = 0; base < nprob; base += LORA_MAX_PROBLEMS_PER_LAUNCH) {
@@ -149,6 +341,20 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
         if (st != LORA_OK) return st;
     }
     return LORA_OK;
+}
+
+
+// The delta launches after grouping: the CUDA-core kernel over the chunk list, then
+// (when the batch may hold tensor-core tiles) the tensor-core kernel over the tile list.
+lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                      float* t_out, bool with_mma, cudaStream_t stream) {
+    lora_status st = check_problems(pool->d, probs, nprob);
+    if (st != LORA_OK) return st;
+    st = use_legacy_fma() ? run_delta_direct(pool, probs, nprob, ws, t_out, stream)
+                          : run_delta_ring(pool, probs, nprob, ws, t_out, stream);
+    if (st != LORA_OK) return st;
+    if (with_mma && mma_min_rows(pool->d) > 0) st = run_mma(pool, probs, nprob, T, ws, stream);
+    return st;
 }
 
 }  // namespace
@@ -249,20 +455,21 @@ lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const 
     sp.S = S;
     sp.Td = Td;
     sp.T = T;
-    sp.mma_min = 0;
+    sp.mma_min = mma_min_rows(pool->d);
+    sp.mma_max_rank = kMmaMaxRank;
     sp.L_tokens = T;
     sp.L_segments = S + Td;
     segment_kernel<<<1, kSegThreads, 0, (cudaStream_t)stream>>>(sp);
     return cuda_status(cudaGetLastError());
 }
 
-lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
                                void* ws, size_t ws_bytes, void* stream) {
-    if (pool == nullptr || nprob < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
+    if (pool == nullptr || nprob < 0 || T < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
     lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
     if (st != LORA_OK) return st;
     if (nprob == 0) return LORA_OK;
-    return run_delta(pool, probs, nprob, ws, nullptr, (cudaStream_t)stream);
+    return run_delta(pool, probs, nprob, T, ws, nullptr, true, (cudaStream_t)stream);
 }
 
 lora_status lora_bgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -271,7 +478,10 @@ lora_status lora_bgmv(const lora_pool* pool, const lora_problem* probs, int32_t 
     if (T > 0 && token_adapter == nullptr) return LORA_EINVAL;
     lora_status st = lora_segment(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, ws_bytes, stream);
     if (st != LORA_OK) return st;
-    return lora_delta_grouped(pool, probs, nprob, ws, ws_bytes, stream);
+    if (nprob < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
+    if (nprob == 0) return LORA_OK;
+    // decode rows are one-row segments: the CUDA-core kernel serves all of them
+    return run_delta(pool, probs, nprob, T, ws, nullptr, false, (cudaStream_t)stream);
 }
 
 lora_status lora_sgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -279,7 +489,7 @@ lora_status lora_sgmv(const lora_pool* pool, const lora_problem* probs, int32_t 
                       void* ws, size_t ws_bytes, void* stream) {
     lora_status st = lora_segment(pool, seg_start, seg_adapter, S, nullptr, 0, T, ws, ws_bytes, stream);
     if (st != LORA_OK) return st;
-    return lora_delta_grouped(pool, probs, nprob, ws, ws_bytes, stream);
+    return lora_delta_grouped(pool, probs, nprob, T, ws, ws_bytes, stream);
 }
 
 lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -289,7 +499,7 @@ lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, i
     lora_status st = lora_segment(pool, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes,
                                   stream);
     if (st != LORA_OK) return st;
-    return lora_delta_grouped(pool, probs, nprob, ws, ws_bytes, stream);
+    return lora_delta_grouped(pool, probs, nprob, T, ws, ws_bytes, stream);
 }
 
 lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_bytes, int32_t layer,
@@ -311,7 +521,7 @@ lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* p
     if (pool == nullptr || prob == nullptr || t_out == nullptr) return LORA_EINVAL;
     lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
     if (st != LORA_OK) return st;
-    return run_delta(pool, prob, 1, ws, t_out, (cudaStream_t)stream);
+    return run_delta(pool, prob, 1, 0, ws, t_out, false, (cudaStream_t)stream);
 }
 
 lora_status lora_get_device_error(void* ws, void* stream, uint32_t* bits) {

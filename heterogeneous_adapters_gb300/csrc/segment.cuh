@@ -37,6 +37,7 @@ struct SegParams {
     int32_t Td;
     int32_t T;
     int32_t mma_min;   // 0: every segment goes to the CUDA-core path
+    int32_t mma_max_rank;   // segments whose adapter rank exceeds this use the CUDA-core path
     int32_t L_tokens;  // the (max_tokens, max_segments) that L was computed from
     int32_t L_segments;
 };
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
         const int len = valid ? slen[seg] : 0;
         const int prev_a = (valid && q > 0) ? (int)(key[sorted[q - 1]] >> 32) : -1;
         const int flag = (valid && (q == 0 || a != prev_a)) ? 1 : 0;
-        const bool is_mma = valid && p.mma_min > 0 && len >= p.mma_min;
+        const bool is_mma = valid && p.mma_min > 0 && len >= p.mma_min && P.ranks[a] <= p.mma_max_rank;
         const int flen = (valid && !is_mma) ? len : 0;
         const int ntile = is_mma ? (len + kTileRows - 1) / kTileRows : 0;
         int tot_pos, tot_g, tot_f, tot_t;
@@ -191,7 +192,8 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     for (int q = warp; q < n_ad; q += nwarp) {
         const int seg = sorted[q];
         const int b = sbeg[seg], len = slen[seg];
-        const bool is_mma = p.mma_min > 0 && len >= p.mma_min;
+        const int a = (int)(key[seg] >> 32);
+        const bool is_mma = p.mma_min > 0 && len >= p.mma_min && P.ranks[a] <= p.mma_max_rank;
         const int pq = pos[q], fq = fpos[q];
         for (int t = lane; t < len; t += 32) {
             perm[pq + t] = b + t;
@@ -199,27 +201,51 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
         }
     }
 
-    // 5. CUDA-core chunks: per group, its CUDA-core rows cut into pieces of kChunk
-    int carry_c = 0;
+    // 5. CUDA-core chunks: per group, its CUDA-core rows cut into pieces of kChunk.  Groups
+    //    are listed by descending rank (ties: ascending adapter id) so that the largest
+    //    work items are taken first from the queue and the tail of a launch is short.
+    int32_t* gorder = sorted;   // the sorted-segment list is no longer needed
+    __syncthreads();
     for (int g0 = 0; g0 < G; g0 += nthr) {
         const int g = g0 + tid;
-        int first = 0, cnt = 0;
         if (g < G) {
+            const long long my = ((long long)(LORA_MAX_RANK - P.ranks[grp_adapter[g]]) << 32) | g;
+            int rank = 0;
+            for (int k = 0; k < G; ++k) {
+                const long long other = ((long long)(LORA_MAX_RANK - P.ranks[grp_adapter[k]]) << 32) | k;
+                rank += other < my;
+            }
+            gorder[rank] = g;
+        }
+    }
+    __syncthreads();
+    int carry_c = 0;
+    for (int i0 = 0; i0 < G; i0 += nthr) {
+        const int i = i0 + tid;
+        const int g = i < G ? gorder[i] : 0;
+        int first = 0, cnt = 0;
+        if (i < G) {
             first = fpos[gfirst[g]];
             cnt = fpos[gfirst[g + 1]] - first;
         }
         const int nch = (cnt + kChunk - 1) / kChunk;
         int tot;
         const int base = block_exclusive_scan(nch, scan_smem, &tot) + carry_c;
-        if (g < G) {
+        if (i < G) {
             const int a = grp_adapter[g];
             const int r = P.ranks[a];
+            const float sc = P.scales[a];
+            const long long ptb = P.pt_off[a];
             for (int c = 0; c < nch; ++c) {
                 Chunk ch;
                 ch.adapter = a;
                 ch.begin = first + c * kChunk;
                 ch.count = min(kChunk, cnt - c * kChunk);
                 ch.rank = r;
+                ch.scale = sc;
+                ch.pt_base = ptb;
+                ch.pad = 0;
+                for (int t = 0; t < kChunk; ++t) ch.rows[t] = t < ch.count ? fma_rows[ch.begin + t] : 0;
                 chunks[base + c] = ch;
             }
         }

@@ -1,0 +1,381 @@
+// Tensor-core SGMV path (prefill): one 128-row tile of one segment per work item.
+//
+// "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels work":
+// SGMV groups tokens into contiguous segments sharing an adapter and runs one small
+// GEMM per segment inside a single launch, reusing the adapter's weights across the
+// segment.  "S-LoRA: Serving Thousands of Concurrent LoRA Adapters": the prefill kernel
+// gathers the adapter from non-contiguous pages with mixed ranks.
+//
+// Per item (tile of <= 128 rows of one segment, adapter a of rank r <= 128, projection):
+//   shrink  D1[128 x r16] (TMEM, fp32) = X[128 x h] . A^T, K-loop over h in chunks of 64:
+//           X chunk by TMA (128-byte swizzle), the r A-row pages' chunks by TMA (one
+//           64-element row per request, rows r..r16-1 read out of range = zeros);
+//   convert the epilogue warps read D1, scale by s and split each fp32 value exactly into
+//           a bf16 pair t = hi + lo (|t - hi - lo| <= 2^-16 |t|), written to shared
+//           memory as two K-major operands;
+//   expand  for every 128-column slice of y: D2[128 x 128] = T_hi . B^T + T_lo . B^T with
+//           the B-column pages' slices as an MN-major operand (TMA, 128-byte swizzle),
+//           double-buffered in TMEM so the epilogue of one slice overlaps the MMA of the
+//           next; the epilogue adds D2 to y (fp32) and stores bf16 rows of the tile.
+// Roles (one persistent CTA per SM, items dealt round-robin): warp 0 TMA producer,
+// warp 1 TMEM owner + MMA issuer (one thread), warps 2-9 convert + epilogue.
+// All waits are bounded; a timeout sets an error bit and the CTA unwinds.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "segment.cuh"
+
+namespace lora {
+
+constexpr int kMmaThreads = 320;
+constexpr int kMmaEpiWarps = 8;
+constexpr int kMmaMaxProbs = 48;            // x tensor maps per launch
+constexpr int kMmaMaxRank = 128;
+constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 bytes)
+constexpr int kMmaNTile = 128;              // y columns per expand slice
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kD1Col = 0, kD2Col = 128;   // D2 buffers at columns 128 and 256
+constexpr uint32_t kDerrTimeoutMma = 0x20u;
+
+struct MmaProb {
+    __nv_bfloat16* y;
+    int32_t ldy;
+    int32_t blk;
+};
+
+struct __align__(64) MmaParams {
+    CUtensorMap pool_map;                    // {h, num_pages}, box {64, 1}, 128B swizzle
+    CUtensorMap x_map[kMmaMaxProbs];         // {h, T}, box {64, 128}, 128B swizzle
+    MmaProb probs[kMmaMaxProbs];
+    PoolView pool;
+    char* ws;
+    int32_t nprob;
+    int32_t stages;
+    int32_t stage_bytes;
+    int32_t t_bytes;        // bytes of one T operand (hi or lo)
+    int32_t rp_max;         // largest padded rank served here
+    int32_t pad[3];
+};
+
+struct MmaSmem {
+    uint32_t ring, thi, tlo, full, empty, d1_full, t_ready, d2_full, d2_empty, final_bar, tmem_slot,
+        total;
+};
+
+__host__ __device__ inline MmaSmem mma_smem_layout(int stages, int stage_bytes, int t_bytes) {
+    MmaSmem L;
+    uint32_t o = 0;
+    L.ring = o;      o += (uint32_t)stages * stage_bytes;
+    L.thi = o;       o += t_bytes;
+    L.tlo = o;       o += t_bytes;
+    L.full = o;      o += stages * 8;
+    L.empty = o;     o += stages * 8;
+    L.d1_full = o;   o += 8;
+    L.t_ready = o;   o += 8;
+    L.d2_full = o;   o += 16;
+    L.d2_empty = o;  o += 16;
+    L.final_bar = o; o += 8;
+    L.tmem_slot = o; o += 8;
+    L.total = o;
+    return L;
+}
+
+__host__ __device__ inline int mma_rpad(int r) { return r <= 16 ? 16 : (r + 15) / 16 * 16; }
+
+// All roles walk the same items; this reads one and checks its pages (every role gets
+// the same answer, so a bad item is skipped by all of them without communication).
+struct MmaItem {
+    Tile tile;
+    int pr;
+    int rp;
+    long long blk;    // first page-table entry of the A block (B block follows at +r)
+    bool ok;
+};
+
+__device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tiles, int n_tiles, uint32_t item,
+                                            int lane) {
+    MmaItem it;
+    it.tile = tiles[item % n_tiles];
+    it.pr = item / n_tiles;
+    const int r = it.tile.rank;
+    it.rp = mma_rpad(r);
+    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.probs[it.pr].blk * 2 * r;
+    bool bad = false;
+    for (int e = lane; e < 2 * r; e += 32) {
+        const int page = p.pool.pt[it.blk + e];
+        bad |= (page < 0 || page >= p.pool.num_pages);
+    }
+    it.ok = !__any_sync(0xffffffffu, bad);
+    return it;
+}
+
+__global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
+    extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
+    unsigned char* base = mma_smem_raw;
+    const MmaSmem L = mma_smem_layout(p.stages, p.stage_bytes, p.t_bytes);
+    const int S = p.stages;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+    const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
+    const Tile* tiles = reinterpret_cast<const Tile*>(p.ws + WL.tiles);
+    const int n_tiles = hdr->counts[3];
+    const uint32_t total = (uint32_t)n_tiles * (uint32_t)p.nprob;
+    const int h = p.pool.h;
+    const int n_kc = h / kMmaKChunk, n_nt = h / kMmaNTile;
+    auto bar = [&](uint32_t off) { return smem_addr(base + off); };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(L.full + s * 8), 1);
+            mbar_init(bar(L.empty + s * 8), 1);
+        }
+        mbar_init(bar(L.d1_full), 1);
+        mbar_init(bar(L.t_ready), kMmaEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L.d2_full + b * 8), 1);
+            mbar_init(bar(L.d2_empty + b * 8), kMmaEpiWarps);
+        }
+        mbar_init(bar(L.final_bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(bar(L.tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L.tmem_slot);
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&p.pool_map);
+        }
+        uint32_t it = 0;
+        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            if (!mi.ok) {
+                if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
+                continue;
+            }
+            const int r = mi.tile.rank, rp = mi.rp;
+            const void* xmap = &p.x_map[mi.pr];
+            // my lane's A / B pages (lane j, j + 32, ...); rows >= r read out of range
+            int pga[4], pgb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = lane + 32 * q;
+                pga[q] = j < r ? p.pool.pt[mi.blk + j] : (int)p.pool.num_pages;
+                pgb[q] = j < r ? p.pool.pt[mi.blk + r + j] : (int)p.pool.num_pages;
+            }
+            for (int kc = 0; kc < n_kc && ok; ++kc) {
+                const uint32_t s = it % S;
+                if (!mbar_wait(bar(L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                const uint32_t st = bar(L.ring + s * p.stage_bytes);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(L.full + s * 8), 128 * 128 + rp * 128);
+                }
+                __syncwarp();
+                if (lane == 0) tma_load_2d(st, xmap, kc * kMmaKChunk, mi.tile.row0, bar(L.full + s * 8));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = lane + 32 * q;
+                    if (j < rp) tma_load_2d(st + 16384 + j * 128, &p.pool_map, kc * kMmaKChunk, pga[q],
+                                            bar(L.full + s * 8));
+                }
+                ++it;
+            }
+            for (int nt = 0; nt < n_nt && ok; ++nt) {
+                const uint32_t s = it % S;
+                if (!mbar_wait(bar(L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                const uint32_t st = bar(L.ring + s * p.stage_bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar(L.full + s * 8), rp * 256);
+                __syncwarp();
+                // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
+                // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = lane + 32 * q;
+                    if (j < rp) {
+                        const uint32_t dst = st + (j >> 3) * 2048 + (j & 7) * 128;
+                        tma_load_2d(dst, &p.pool_map, nt * kMmaNTile, pgb[q], bar(L.full + s * 8));
+                        tma_load_2d(dst + 1024, &p.pool_map, nt * kMmaNTile + 64, pgb[q], bar(L.full + s * 8));
+                    }
+                }
+                ++it;
+            }
+        }
+        if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
+        // let every stage this warp filled land before the CTA can exit
+        if (lane == 0) {
+            const uint32_t first = it > (uint32_t)S ? it - S : 0;
+            for (uint32_t k = first; k < it; ++k)
+                mbar_wait(bar(L.full + (k % S) * 8), (k / S) & 1, 100000000ull);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        uint32_t it = 0, tcount = 0, g = 0;
+        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            if (!mi.ok) continue;
+            const int rp = mi.rp;
+            const uint32_t id_shrink = idesc_bf16(128, rp, 0, 0);
+            const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
+            for (int kc = 0; kc < n_kc && ok; ++kc) {
+                const uint32_t s = it % S;
+                if (!mbar_wait(bar(L.full + s * 8), (it / S) & 1, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t st = bar(L.ring + s * p.stage_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kMmaKChunk / 16; ++kk) {
+                        const uint64_t da = smem_desc(st + kk * 32, 16, 1024, 2);
+                        const uint64_t db = smem_desc(st + 16384 + kk * 32, 16, 1024, 2);
+                        tc_mma_f16(tmem + kD1Col, da, db, id_shrink, (kc | kk) != 0);
+                    }
+                    tc_commit(bar(L.empty + s * 8));
+                }
+                __syncwarp();
+                ++it;
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(bar(L.d1_full));
+            __syncwarp();
+            if (!mbar_wait(bar(L.t_ready), tcount & 1, kWaitLimitNs)) { ok = false; break; }
+            ++tcount;
+            tc_fence_after();
+            for (int nt = 0; nt < n_nt && ok; ++nt, ++g) {
+                const uint32_t s = it % S;
+                const uint32_t b = g & 1;
+                if (!mbar_wait(bar(L.full + s * 8), (it / S) & 1, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(bar(L.d2_empty + b * 8), ((g >> 1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t st = bar(L.ring + s * p.stage_bytes);
+                    const uint32_t d2 = tmem + kD2Col + b * kMmaNTile;
+                    const uint32_t sbo_t = (uint32_t)(rp / 8) * 128;
+                    for (int ks = 0; ks < rp / 16; ++ks) {
+                        const uint64_t dbt = smem_desc(st + ks * 4096, 1024, 2048, 2);
+                        const uint64_t dhi = smem_desc(bar(L.thi) + ks * 256, 128, sbo_t, 0);
+                        const uint64_t dlo = smem_desc(bar(L.tlo) + ks * 256, 128, sbo_t, 0);
+                        tc_mma_f16(d2, dhi, dbt, id_expand, ks != 0);
+                        tc_mma_f16(d2, dlo, dbt, id_expand, 1);
+                    }
+                    tc_commit(bar(L.empty + s * 8));
+                    tc_commit(bar(L.d2_full + b * 8));
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
+        // every MMA issued by this thread must be complete before TMEM is freed
+        if (lane == 0) {
+            tc_commit(bar(L.final_bar));
+            mbar_wait(bar(L.final_bar), 0, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ convert + epilogue
+        const int e = warp - 2;                 // 0..7
+        const int quad = warp & 3;              // TMEM lanes 32 quad .. 32 quad + 31
+        const int half = e >> 2;                // column half of each slice
+        const int m = quad * 32 + lane;         // tile row of this thread
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        uint32_t tcount = 0, g = 0;
+        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            if (!mi.ok) continue;
+            const int rp = mi.rp;
+            const float scale = p.pool.scales[mi.tile.adapter];
+            const MmaProb pb = p.probs[mi.pr];
+            const bool live = m < mi.tile.rows;
+            __nv_bfloat16* yrow = pb.y + (long long)(mi.tile.row0 + (live ? m : 0)) * pb.ldy;
+            // ---- convert D1 -> T_hi, T_lo (K-major, no swizzle: core matrices of 8 rows x 16 B,
+            //      +128 B per 8 columns, +(rp / 8) * 128 B per 8 rows)
+            if (!mbar_wait(bar(L.d1_full), tcount & 1, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sbo_t = (uint32_t)(rp / 8) * 128;
+            for (int c0 = half * (rp / 2); c0 < (half + 1) * (rp / 2); c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + kD1Col + c0, v);
+                tmem_ld_wait();
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float a = v[2 * i] * scale, b = v[2 * i + 1] * scale;
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+                    const float ha = __low2float(h2), hb = __high2float(h2);
+                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(a - ha, b - hb);
+                    hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo[i] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t off = (m >> 3) * sbo_t + ((c0 >> 3) + q) * 128 + (m & 7) * 16;
+                    *reinterpret_cast<uint4*>(base + L.thi + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+                    *reinterpret_cast<uint4*>(base + L.tlo + off) = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L.t_ready));
+            ++tcount;
+            // ---- expand epilogue over the column slices
+            const int col0 = half * 64;
+            uint4 ycur[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ycur[i] = live ? ld16(yrow + col0 + i * 8) : make_uint4(0, 0, 0, 0);
+            for (int nt = 0; nt < n_nt; ++nt, ++g) {
+                const uint32_t b = g & 1;
+                uint4 ynext[8];
+                const bool more = nt + 1 < n_nt;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    ynext[i] = (live && more) ? ld16(yrow + (nt + 1) * kMmaNTile + col0 + i * 8)
+                                              : make_uint4(0, 0, 0, 0);
+                if (!mbar_wait(bar(L.d2_full + b * 8), (g >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                float acc[64];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_base + kD2Col + b * kMmaNTile + col0 + q * 16, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[q * 16 + i] = v[i];
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L.d2_empty + b * 8));
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float y8[8];
+                        unpack8(ycur[i], y8);
+                        uint4 o;
+                        o.x = pack2(y8[0] + acc[8 * i + 0], y8[1] + acc[8 * i + 1]);
+                        o.y = pack2(y8[2] + acc[8 * i + 2], y8[3] + acc[8 * i + 3]);
+                        o.z = pack2(y8[4] + acc[8 * i + 4], y8[5] + acc[8 * i + 5]);
+                        o.w = pack2(y8[6] + acc[8 * i + 6], y8[7] + acc[8 * i + 7]);
+                        st16(yrow + nt * kMmaNTile + col0 + i * 8, o);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ycur[i] = ynext[i];
+            }
+        }
+        if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace lora

@@ -177,10 +177,11 @@ lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, i
                              const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
                              size_t ws_bytes, void* stream);
 
-/* Delta launch only, reusing the grouping already in ws (from lora_segment with the
- * same batch).  This is the kernel the other entry points run after grouping. */
+/* Delta launches only, reusing the grouping already in ws (from lora_segment with the
+ * same batch; T = the rows of x and y given to that call).  These are the kernels the
+ * other entry points run after grouping. */
 lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
-                               void* ws, size_t ws_bytes, void* stream);
+                               int32_t T, void* ws, size_t ws_bytes, void* stream);
 
 /* Debug export of the page-table walk (a2): for problem (layer, proj), for each group
  * g of the grouping in ws, the r_a A-row pages then the r_a B-column pages, packed in

@@ -52,6 +52,10 @@ SMALL = {
     "decode-base-uniform": lambda: small_decode(45, 1024, 1, 2, 6, [4, 16], 25, base=True),
     "prefill-h1024-ragged": lambda: small_prefill(46, 1024, 1, 3, 8, [8, 16, 32],
                                                   [1, 7, 130, 300, 2, 64, 129, 5, 0, 17, 255, 3]),
+    "prefill-h4096-r256-and-r8": lambda: small_prefill(49, 4096, 1, 2, 4, [8, 256],
+                                                       [200, 40, 33, 128]),
+    "prefill-h2048-all-ranks": lambda: small_prefill(50, 2048, 2, 1, 24, [1, 8, 16, 24, 32, 48, 64, 96, 128],
+                                                     [129, 257, 31, 32, 500, 128, 7, 64]),
     "mixed-h2048": lambda: _mixed(47, 2048, 2, 2, 30, [8, 16, 32, 64, 128], [5, 260, 131], 40, 5),
     "mixed-h5120": lambda: _mixed(48, 5120, 1, 2, 12, [8, 128], [300, 9], 17, 3),
 }
@@ -62,6 +66,20 @@ SMALL = {
 def test_small_parity(name, y0_zero):
     wl = SMALL[name]()
     case = GpuCase(wl, y0_zero=y0_zero)
+    try:
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("mma_min", ["0", "1", "128"])
+def test_prefill_size_classes(mma_min, monkeypatch):
+    """The same prefill batch with every segment on the CUDA-core path (0), every segment on
+    the tensor-core path (1), and only full-tile segments on it (128)."""
+    monkeypatch.setenv("LORA_MMA_MIN_ROWS", mma_min)
+    wl = small_prefill(57, 1024, 2, 2, 10, [8, 16, 32, 64, 128], [1, 2, 127, 128, 129, 300, 64, 0, 9])
+    case = GpuCase(wl, y0_zero=True)
     try:
         assert case.run() == 0
         full_check(wl, case, list(range(len(wl.problems))))
