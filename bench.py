@@ -323,10 +323,11 @@ def run_ours(args, rank: int, world: int, local: int):
     peaks = measured_peaks()
     kern_avg = statistics.mean(kern)
     achieved = m["bytes"] / kern_avg / 1e9
-    traffic = ncu_traffic("fma_delta_kernel", wl.name, m["bytes"])
+    kname = "bgmv_ring_kernel"
+    traffic = ncu_traffic(kname, wl.name, m["bytes"])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": "fma_delta_kernel", "kernel_ms": kern_avg * 1e3,
+                "kernel": kname, "kernel_ms": kern_avg * 1e3,
                 "peak_source": peaks["source"] + " (hbm_gbs, copy kernel)",
                 "bytes_per_launch": m["bytes"]}
 
@@ -372,6 +373,12 @@ def run_ours(args, rank: int, world: int, local: int):
            "d2h_bytes_per_step": d.y.numel() * 2, "steps": e2e_steps,
            "api": "lora_bgmv (C ABI) with pinned host x, y, ids"}
 
+    staging = None
+    if args.config in ("4d", "4z") and args.stage_steps > 0:
+        variant = "distinct" if args.config == "4d" else "zipf"
+        wl_steps = step_batches(wl, args.stage_steps, variant)
+        staging = run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev)
+
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -389,8 +396,180 @@ def run_ours(args, rank: int, world: int, local: int):
                 "config": config_dict(wl, args), "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk.summary(), "impl": "ours"}
+        if staging is not None:
+            line["staging"] = staging
         print(json.dumps(line), flush=True)
     pool.close()
+
+
+# ----------------------------------------------------------------------------- staging scenario
+
+class SliceCache:
+    """Host side of adapter staging for the unified-pool stress workload: an LRU over
+    adapter slices (one layer's pages of one adapter) with a fixed capacity; misses are
+    copied from a pinned host copy into free pool pages, and every page-table entry that
+    points into the slice is rewritten (one lora_stage_pages call per step)."""
+
+    def __init__(self, wl, pool_t, capacity: int):
+        p = wl.pool
+        self.wl = wl
+        self.capacity = capacity
+        n_slices = p.num_adapters
+        self.spp = p.num_proj * 2 * p.ranks.astype(np.int64)          # pages per slice
+        self.slice_off = np.concatenate([[0], np.cumsum(self.spp)[:-1]])
+        # pages are listed slice by slice in the pool description
+        owner = np.repeat(np.arange(n_slices), self.spp)
+        page_slice = np.full(p.num_pages, -1, np.int64)
+        page_slice[p.page_ids] = owner
+        page_pos = np.full(p.num_pages, -1, np.int64)
+        page_pos[p.page_ids] = np.arange(p.page_ids.size) - self.slice_off[owner]
+        # fixed maps: page-table entry -> (slice, position inside the slice)
+        self.ent_slice = page_slice[p.pt]
+        self.ent_pos = page_pos[p.pt]
+        order = np.argsort(self.ent_slice, kind="stable")
+        counts = np.bincount(self.ent_slice, minlength=n_slices)
+        self.ent_off = np.concatenate([[0], np.cumsum(counts)])
+        self.ent_sorted = order.astype(np.int64)
+        self.slice_pages = [p.page_ids[self.slice_off[s]:self.slice_off[s] + self.spp[s]].copy()
+                            for s in range(n_slices)]
+        # pinned host copy of every slice (the host tier), rows in slice order
+        self.host = None
+        if pool_t is not None:
+            import torch
+            allp = torch.from_numpy(p.page_ids.astype(np.int64)).to(pool_t.device)
+            self.host = pool_t[allp].cpu().pin_memory()
+        # initial residency: the first `capacity` slices; every other page is free
+        self.lru = {s: 0 for s in range(min(capacity, n_slices))}
+        self.clock = 0
+        used = np.zeros(p.num_pages, bool)
+        for s in self.lru:
+            used[self.slice_pages[s]] = True
+        self.free = np.nonzero(~used)[0].astype(np.int32).tolist()
+
+    def needed(self, token_adapter) -> np.ndarray:
+        """Slices read by a batch: every slice its adapters' page-table blocks point into."""
+        p = self.wl.pool
+        ids = np.unique(token_adapter[token_adapter >= 0])
+        ent = np.concatenate([np.arange(p.pt_off[a], p.pt_off[a] + p.num_layers * p.num_proj * 2 *
+                                        int(p.ranks[a])) for a in ids])
+        return np.unique(self.ent_slice[ent])
+
+    def plan(self, need: np.ndarray, keep: np.ndarray):
+        """Stage the missing slices of `need`; never evict a slice in `keep` or `need`."""
+        self.clock += 1
+        miss = [int(v) for v in need if int(v) not in self.lru]
+        for v in need:
+            if int(v) in self.lru:
+                self.lru[int(v)] = self.clock
+        protect = set(int(v) for v in need) | set(int(v) for v in keep)
+        rows, dst, upd_i, upd_p = [], [], [], []
+        for sl in miss:
+            while len(self.lru) >= self.capacity:
+                cands = [v for v in self.lru if v not in protect]
+                if not cands:      # everything resident is in use: run over capacity
+                    break
+                victim = min(cands, key=self.lru.get)
+                del self.lru[victim]
+                self.free.extend(self.slice_pages[victim].tolist())
+            n = int(self.spp[sl])
+            new = np.array(self.free[-n:], np.int32)
+            del self.free[-n:]
+            self.slice_pages[sl] = new.astype(np.int64)
+            rows.append(np.arange(self.slice_off[sl], self.slice_off[sl] + n))
+            dst.append(new)
+            ent = self.ent_sorted[self.ent_off[sl]:self.ent_off[sl + 1]]
+            upd_i.append(ent)
+            upd_p.append(new[self.ent_pos[ent]])
+            self.lru[sl] = self.clock
+        if not miss:
+            return None
+        return (np.concatenate(rows), np.concatenate(dst), np.concatenate(upd_i),
+                np.concatenate(upd_p), len(miss))
+
+
+def step_batches(wl, n: int, variant: str):
+    """n batches over the same pool: 256 distinct adapters, or Zipf(1.2) ids, per step."""
+    import dataclasses
+
+    from workloads import spec
+    out = []
+    N = wl.pool.num_adapters
+    T = wl.batch.num_tokens
+    for k in range(n):
+        rng = np.random.default_rng(wl.seed * 1000 + k)
+        if variant == "distinct":
+            ids = rng.choice(N, size=T, replace=False)
+        else:
+            ids = rng.choice(N, size=T, p=spec.zipf_probs(N, 1.2))
+        b = spec.Batch(np.zeros(1, np.int32), np.zeros(0, np.int32), ids.astype(np.int32))
+        out.append(dataclasses.replace(wl, batch=b))
+    return out
+
+
+def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
+    """Unified-pool stress with staging: every step has its own batch; the misses of step
+    k+1 are staged on a side stream while step k's delta runs."""
+    import torch
+
+    import heterogeneous_adapters_gb300 as lora
+    wl0 = wl_steps[0]
+    cache = SliceCache(wl0, d.pool, args.stage_capacity)
+    side = torch.cuda.Stream(device=dev)
+    p = wl0.pool
+    probs = [(d.x[i], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    ids_dev = [torch.from_numpy(w.batch.token_adapter()).to(dev) for w in wl_steps]
+    needs = [cache.needed(w.batch.token_adapter()) for w in wl_steps]
+    stage_ms, stage_bytes, misses, kern_ms = [], [], [], []
+    pending = []
+    # stage what step 0 needs, synchronously
+    plan = cache.plan(needs[0], np.zeros(0, np.int64))
+    staged_ev = None
+
+    def launch_stage(plan_):
+        rows, dst, ui, up, nmiss = plan_
+        src = cache.host[torch.from_numpy(rows)].pin_memory()
+        dst_t = torch.from_numpy(dst).pin_memory()
+        ui_t = torch.from_numpy(ui.astype(np.int64)).pin_memory()
+        up_t = torch.from_numpy(up.astype(np.int32)).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            e0.record(side)
+            lora.stage_pages(pool, src, dst_t, dst.size, d.pt, ui_t, up_t, ui.size, side.cuda_stream)
+            e1.record(side)
+        pending.append((src, dst_t, ui_t, up_t))
+        return e0, e1, dst.size * p.h * 2, nmiss
+
+    if plan is not None:
+        e0, e1, nb, nm = launch_stage(plan)
+        torch.cuda.synchronize()
+    for k in range(len(wl_steps)):
+        if staged_ev is not None:
+            stream_obj.wait_event(staged_ev[1])
+            staged_ev[1].synchronize()
+            stage_ms.append(staged_ev[0].elapsed_time(staged_ev[1]))
+            stage_bytes.append(staged_ev[2])
+            misses.append(staged_ev[3])
+            staged_ev = None
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream_obj)
+        T = wl_steps[k].batch.num_tokens
+        lora.bgmv(pool, probs, ids_dev[k], T, ws, nbytes, stream_obj.cuda_stream)
+        k1.record(stream_obj)
+        if k + 1 < len(wl_steps):
+            plan = cache.plan(needs[k + 1], needs[k])
+            if plan is not None:
+                staged_ev = launch_stage(plan)
+        k1.synchronize()
+        kern_ms.append(k0.elapsed_time(k1))
+    torch.cuda.synchronize()
+    err = lora.get_device_error(ws, stream_obj.cuda_stream)
+    return {"steps": len(wl_steps), "kernel_ms_median": statistics.median(kern_ms),
+            "stage_ms_median": statistics.median(stage_ms) if stage_ms else 0.0,
+            "stage_bytes_median": statistics.median(stage_bytes) if stage_bytes else 0,
+            "stage_gbs_median": (statistics.median([b / (t * 1e6) for b, t in zip(stage_bytes, stage_ms)])
+                                 if stage_ms else None),
+            "slices_staged_median": statistics.median(misses) if misses else 0,
+            "capacity_slices": cache.capacity, "device_error": err}
 
 
 def main():
@@ -407,6 +586,10 @@ def main():
     ap.add_argument("--ref-problems", type=int, default=16,
                     help="projections whose host inputs the oracle prepares")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage-capacity", type=int, default=1500,
+                    help="resident adapter slices in the unified-pool stress workload")
+    ap.add_argument("--stage-steps", type=int, default=20,
+                    help="steps of the staging scenario (configs 4d / 4z)")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -6,10 +6,11 @@ throughput against the HBM roofline."""
 from . import costmodel
 from ._binding import (DERR, LORA_MAX_PROBLEMS_PER_LAUNCH, LORA_MAX_RANK, LORA_MAX_SEGMENTS,
                        LoraError, Pool, apply_mixed, bgmv, debug_delta_with_t, debug_page_list,
-                       delta_grouped, get_device_error, lib, segment, sgmv, workspace_init,
+                       delta_grouped, get_device_error, lib, segment, sgmv, stage_pages, workspace_init,
                        workspace_size, workspace_view)
 
 __all__ = ["costmodel", "DERR", "LORA_MAX_PROBLEMS_PER_LAUNCH", "LORA_MAX_RANK",
            "LORA_MAX_SEGMENTS", "LoraError", "Pool", "apply_mixed", "bgmv", "debug_delta_with_t",
            "debug_page_list", "delta_grouped", "get_device_error", "lib", "segment", "sgmv",
+           "stage_pages",
            "workspace_init", "workspace_size", "workspace_view"]

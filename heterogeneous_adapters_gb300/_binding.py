@@ -19,7 +19,8 @@ LORA_MAX_RANK = 256
 EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_workspace_size", "lora_workspace_init",
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
             "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t",
-            "lora_get_device_error", "lora_last_cuda_error", "lora_status_string"]
+            "lora_stage_pages", "lora_get_device_error", "lora_last_cuda_error",
+            "lora_status_string"]
 
 
 class lora_pool_desc(ctypes.Structure):
@@ -75,6 +76,7 @@ def lib():
             "lora_delta_grouped": [p, p, i32, i32, p, sz, p],
             "lora_debug_page_list": [p, p, sz, i32, i32, p, i64, p, p],
             "lora_debug_delta_with_t": [p, ctypes.POINTER(lora_problem), p, sz, p, p],
+            "lora_stage_pages": [p, p, p, i32, p, p, p, i64, p],
             "lora_get_device_error": [p, p, ctypes.POINTER(ctypes.c_uint32)],
             "lora_last_cuda_error": [],
             "lora_status_string": [ctypes.c_int],
@@ -200,6 +202,13 @@ def debug_delta_with_t(pool, problem, ws, ws_bytes, t_out, stream):
     arr, _ = problems_array([problem])
     _check(lib().lora_debug_delta_with_t(pool.handle, arr, _ptr(ws), ws_bytes, _ptr(t_out), stream),
            "lora_debug_delta_with_t")
+
+
+def stage_pages(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_page, nupd, stream):
+    """host_rows, dst_pages, upd_index, upd_page: pinned host tensors (or addresses)."""
+    _check(lib().lora_stage_pages(pool.handle, _ptr(host_rows), _ptr(dst_pages), npages,
+                                  _ptr(page_table), _ptr(upd_index), _ptr(upd_page), nupd, stream),
+           "lora_stage_pages")
 
 
 def get_device_error(ws, stream) -> int:

@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) bgmv_ring_kernel(const __grid
                 mbar_arrive(smem_addr(base + L.full + s * 8));
             }
             if (s < 0) ok = false;
+            else ++it;   // the stop stage is a use of its barrier like any other
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeout);
         // wait (bounded) until every stage this warp filled has landed, so no copy into

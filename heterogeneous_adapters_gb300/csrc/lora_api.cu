@@ -17,6 +17,7 @@
 #include "fma_delta.cuh"
 #include "segment.cuh"
 #include "sgmv_mma.cuh"
+#include "stage.cuh"
 
 using namespace lora;
 
@@ -522,6 +523,43 @@ lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* p
     lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
     if (st != LORA_OK) return st;
     return run_delta(pool, prob, 1, 0, ws, t_out, false, (cudaStream_t)stream);
+}
+
+lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const int32_t* dst_pages,
+                             int32_t npages, int32_t* page_table, const int64_t* upd_index,
+                             const int32_t* upd_page, int64_t nupd, void* stream) {
+    if (pool == nullptr || npages < 0 || nupd < 0) return LORA_EINVAL;
+    const lora_pool_desc& d = pool->d;
+    if (npages > 0 && (host_rows == nullptr || dst_pages == nullptr)) return LORA_EINVAL;
+    if (nupd > 0 && (page_table == nullptr || upd_index == nullptr || upd_page == nullptr))
+        return LORA_EINVAL;
+    if (nupd > 0 && page_table != d.page_table) return LORA_EINVAL;
+    if (npages > 0 && !aligned16(host_rows)) return LORA_EALIGN;
+    for (int32_t i = 0; i < npages; ++i)
+        if (dst_pages[i] < 0 || dst_pages[i] >= d.num_pages) return LORA_EINVAL;
+    for (int64_t k = 0; k < nupd; ++k) {
+        if (upd_index[k] < 0 || upd_index[k] >= d.page_table_len) return LORA_EINVAL;
+        if (upd_page[k] < 0 || upd_page[k] >= d.num_pages) return LORA_EINVAL;
+    }
+    if (npages == 0 && nupd == 0) return LORA_OK;
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    StageParams sp;
+    sp.host_rows = reinterpret_cast<const uint4*>(host_rows);
+    sp.dst_pages = dst_pages;
+    sp.pages = reinterpret_cast<__nv_bfloat16*>(d.pages);
+    sp.pt = page_table;
+    sp.upd_index = upd_index;
+    sp.upd_page = upd_page;
+    sp.nupd = nupd;
+    sp.npages = npages;
+    sp.vec_per_row = d.h / 8;
+    int grid = di->sm_count * 4;
+    if (npages > 0 && npages < grid) grid = npages;
+    if (grid < 1) grid = 1;
+    stage_kernel<<<grid, kStageThreads, 0, (cudaStream_t)stream>>>(sp);
+    return cuda_status(cudaGetLastError());
 }
 
 lora_status lora_get_device_error(void* ws, void* stream, uint32_t* bits) {

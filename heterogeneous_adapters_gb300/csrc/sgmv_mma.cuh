@@ -300,7 +300,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             if (!mbar_wait(bar(L.d1_full), tcount & 1, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sbo_t = (uint32_t)(rp / 8) * 128;
-            for (int c0 = half * (rp / 2); c0 < (half + 1) * (rp / 2); c0 += 16) {
+            // the rp / 16 column chunks of D1 are split between the two warpgroups
+            const int nck = rp / 16;
+            const int ck_begin = half ? (nck + 1) / 2 : 0, ck_end = half ? nck : (nck + 1) / 2;
+            for (int c0 = ck_begin * 16; c0 < ck_end * 16; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + lane_base + kD1Col + c0, v);
                 tmem_ld_wait();

@@ -197,6 +197,22 @@ lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_byte
 lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* prob, void* ws,
                                     size_t ws_bytes, float* t_out, void* stream);
 
+/* Adapter staging from host memory (side-stream prefetch).
+ * "S-LoRA: Serving Thousands of Concurrent LoRA Adapters", "Host memory for adapters":
+ * adapters live in host memory and the ones a batch needs are copied to the GPU ahead
+ * of use.  One kernel on `stream` copies npages page rows from host_rows (pinned host
+ * memory; row i is h bf16 values at host_rows + i * 2h bytes, 16-byte aligned) into
+ * pool pages dst_pages[i], then sets page_table[upd_index[k]] = upd_page[k], k < nupd.
+ * dst_pages, upd_index and upd_page must be pinned host memory: they are validated on
+ * the host before the launch (page ids in [0, num_pages), entries in
+ * [0, page_table_len)) and read by the kernel through the same pointers.  page_table
+ * must be the pool's page table (passed writable).  The caller keeps the host buffers
+ * alive until the kernel has finished, orders consumers after it with an event, and
+ * must not stage into pages that a running kernel reads. */
+lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const int32_t* dst_pages,
+                             int32_t npages, int32_t* page_table, const int64_t* upd_index,
+                             const int32_t* upd_page, int64_t nupd, void* stream);
+
 /* Synchronises `stream`, returns the device error bits accumulated in ws since the
  * last call (in *bits) and clears them.  Returns LORA_EDEVICE if any bit was set. */
 lora_status lora_get_device_error(void* ws, void* stream, uint32_t* bits);

@@ -84,3 +84,28 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
                 assert "lora_oracle" not in src, f
+
+
+def test_stage_pages_host_checks(lib):
+    """Staging validates its host-side index arrays before launching anything."""
+    import numpy as np
+
+    from heterogeneous_adapters_gb300._binding import LORA_EALIGN, LORA_EINVAL, lora_pool_desc
+    h = ctypes.c_void_p()
+    pt = np.zeros(32, np.int32)
+    d = lora_pool_desc(1 << 20, 16, 256, 2, 1, 1, 8, 0, pt.ctypes.data, 32, 1 << 20, 1 << 20, 1 << 20)
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(d)) == 0
+    rows = np.zeros((2, 256), np.uint16)
+    good = np.array([3, 4], np.int32)
+    bad = np.array([3, 16], np.int32)
+    idx = np.array([0, 31], np.int64)
+    bad_idx = np.array([0, 32], np.int64)
+    pg = np.array([1, 2], np.int32)
+    c = lambda a: a.ctypes.data  # noqa: E731
+    assert lib.lora_stage_pages(h, c(rows), c(bad), 2, None, None, None, 0, None) == LORA_EINVAL
+    assert lib.lora_stage_pages(h, c(rows) + 2, c(good), 2, None, None, None, 0, None) == LORA_EALIGN
+    assert lib.lora_stage_pages(h, None, None, 0, c(pt), c(bad_idx), c(pg), 2, None) == LORA_EINVAL
+    other = np.zeros(32, np.int32)
+    assert lib.lora_stage_pages(h, None, None, 0, c(other), c(idx), c(pg), 2, None) == LORA_EINVAL
+    assert lib.lora_stage_pages(h, None, None, 0, None, None, None, 0, None) == 0
+    lib.lora_pool_destroy(h)
