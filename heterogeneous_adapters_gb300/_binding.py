@@ -15,12 +15,13 @@ DERR = {0x1: "adapter", 0x2: "rank", 0x4: "page-table block", 0x8: "page", 0x10:
 LORA_MAX_PROBLEMS_PER_LAUNCH = 256
 LORA_MAX_SEGMENTS = 16384
 LORA_MAX_RANK = 256
+LORA_NOALLOC_MAX_TOKENS = 4096
 
 EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_workspace_size", "lora_workspace_init",
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
             "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t",
-            "lora_stage_pages", "lora_get_device_error", "lora_last_cuda_error",
-            "lora_status_string"]
+            "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error",
+            "lora_last_cuda_error", "lora_status_string"]
 
 
 class lora_pool_desc(ctypes.Structure):
@@ -77,6 +78,7 @@ def lib():
             "lora_debug_page_list": [p, p, sz, i32, i32, p, i64, p, p],
             "lora_debug_delta_with_t": [p, ctypes.POINTER(lora_problem), p, sz, p, p],
             "lora_stage_pages": [p, p, p, i32, p, p, p, i64, p],
+            "lora_bgmv_noalloc": [p, p, i32, p, i32, p, p],
             "lora_get_device_error": [p, p, ctypes.POINTER(ctypes.c_uint32)],
             "lora_last_cuda_error": [],
             "lora_status_string": [ctypes.c_int],
@@ -209,6 +211,13 @@ def stage_pages(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_p
     _check(lib().lora_stage_pages(pool.handle, _ptr(host_rows), _ptr(dst_pages), npages,
                                   _ptr(page_table), _ptr(upd_index), _ptr(upd_page), nupd, stream),
            "lora_stage_pages")
+
+
+def bgmv_noalloc(pool, problems, token_adapter, T, error_bits, stream):
+    """BGMV with the library's own fixed scratch (no caller workspace, no allocation)."""
+    arr, n = problems_array(problems)
+    _check(lib().lora_bgmv_noalloc(pool.handle, arr, n, _ptr(token_adapter), T, _ptr(error_bits),
+                                   stream), "lora_bgmv_noalloc")
 
 
 def get_device_error(ws, stream) -> int:

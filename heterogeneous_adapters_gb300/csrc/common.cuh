@@ -52,10 +52,10 @@ struct WsLayout {
         fma_rows, chunks, tiles, total;
 };
 
-__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+__host__ __device__ constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-__host__ __device__ inline WsLayout ws_layout(int32_t max_tokens, int32_t max_segments) {
-    WsLayout L;
+__host__ __device__ constexpr WsLayout ws_layout(int32_t max_tokens, int32_t max_segments) {
+    WsLayout L{};
     size_t o = sizeof(WsHeader);
     const size_t n = (size_t)max_segments + 1, t = (size_t)max_tokens + 1;
     L.seg_key = o;      o = align256(o + n * 8);

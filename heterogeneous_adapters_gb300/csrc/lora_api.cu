@@ -358,6 +358,37 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     return st;
 }
 
+// ---------------------------------------------------------------------------- allocation-free BGMV
+// Scratch of lora_bgmv_noalloc: a workspace for up to LORA_NOALLOC_MAX_TOKENS decode
+// rows, living in a file-scope device array that every GPU loading this library holds
+// until the process exits.  Host code must not pass `g_noalloc_ws` itself to a kernel
+// (on the host it is only a stand-in symbol): its device address is looked up once per
+// device with cudaGetSymbolAddress.
+constexpr size_t kNoallocWsBytes = ws_layout(LORA_NOALLOC_MAX_TOKENS, LORA_NOALLOC_MAX_TOKENS).total;
+static __device__ __align__(256) unsigned char g_noalloc_ws[kNoallocWsBytes];
+
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// First call on a device (that device current): find the array's device address and
+// zero its header.  Later calls reuse the cached address.
+lora_status noalloc_workspace(void** out, cudaStream_t stream) {
+    int dev = 0;
+    lora_status st = cuda_status(cudaGetDevice(&dev));
+    if (st != LORA_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return LORA_ETOOBIG;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        st = cuda_status(cudaGetSymbolAddress(&ptr, g_noalloc_ws));
+        if (st != LORA_OK) return st;
+        st = cuda_status(cudaMemsetAsync(ptr, 0, sizeof(WsHeader), stream));
+        if (st != LORA_OK) return st;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return LORA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -560,6 +591,33 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
     if (grid < 1) grid = 1;
     stage_kernel<<<grid, kStageThreads, 0, (cudaStream_t)stream>>>(sp);
     return cuda_status(cudaGetLastError());
+}
+
+lora_status lora_bgmv_noalloc(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                              const int32_t* token_adapter, int32_t T, uint32_t* error_bits,
+                              void* stream) {
+    if (pool == nullptr || T < 0 || nprob < 0) return LORA_EINVAL;
+    if (T > LORA_NOALLOC_MAX_TOKENS) return LORA_ETOOBIG;
+    if ((T > 0 && token_adapter == nullptr) || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
+    lora_status st = check_problems(pool->d, probs, nprob);
+    if (st != LORA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    void* ws = nullptr;
+    st = noalloc_workspace(&ws, s);
+    if (st != LORA_OK) return st;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    // the error word is per call; the grouping kernel re-initialises everything else
+    st = cuda_status(cudaMemsetAsync(&hdr->err, 0, sizeof(uint32_t), s));
+    if (st != LORA_OK) return st;
+    st = lora_segment(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, kNoallocWsBytes, stream);
+    if (st != LORA_OK) return st;
+    if (nprob > 0) {
+        st = run_delta(pool, probs, nprob, T, ws, nullptr, false, s);
+        if (st != LORA_OK) return st;
+    }
+    if (error_bits != nullptr)
+        st = cuda_status(cudaMemcpyAsync(error_bits, &hdr->err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));
+    return st;
 }
 
 lora_status lora_get_device_error(void* ws, void* stream, uint32_t* bits) {

@@ -213,6 +213,30 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
                              int32_t npages, int32_t* page_table, const int64_t* upd_index,
                              const int32_t* upd_page, int64_t nupd, void* stream);
 
+/* Allocation-free BGMV.  The pages this library follows have no counterpart of this
+ * call; it exists for callers that cannot allocate device memory: code running inside
+ * a CUDA graph being captured, allocators that forbid extra device allocations (a
+ * serving engine that has carved the GPU into a fixed pool), or plugins that are handed
+ * only their inputs and outputs.  It computes exactly what lora_bgmv computes, with the
+ * grouping and work lists kept in a fixed-size array inside the library instead of a
+ * caller workspace, and calls no cudaMalloc, cudaFree or allocating routine.
+ *   - T must be <= LORA_NOALLOC_MAX_TOKENS (decode rows); larger batches return
+ *     LORA_ETOOBIG and launch nothing.
+ *   - The array is shared by every call in the process on a given GPU and keeps the
+ *     last call's contents: calls whose kernels may overlap on the GPU (different
+ *     streams without ordering, or several host threads) race with each other; order
+ *     them on one stream.
+ *   - The first call on each device (that device current) looks up the array's device
+ *     address and zeroes its header; make that first call before capturing a stream.
+ *   - error_bits (a device uint32, may be NULL) receives this call's device error bits
+ *     (LORA_DERR_*), copied on `stream` after the kernels.
+ * Every GPU that loads this library holds the array (about 0.5 MB) until the process
+ * exits. */
+#define LORA_NOALLOC_MAX_TOKENS 4096
+lora_status lora_bgmv_noalloc(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                              const int32_t* token_adapter, int32_t T, uint32_t* error_bits,
+                              void* stream);
+
 /* Synchronises `stream`, returns the device error bits accumulated in ws since the
  * last call (in *bits) and clears them.  Returns LORA_EDEVICE if any bit was set. */
 lora_status lora_get_device_error(void* ws, void* stream, uint32_t* bits);
