@@ -36,12 +36,16 @@ UNIT = "tokens/s"
 # ----------------------------------------------------------------------------- helpers
 
 def workload_for(cfg: str):
-    """Configs 0-4 as named in the workload module; "1s" is a small-pool variant of
-    config 1 (4 layers, 300 adapters, ~2.4 GB pool) for profiler captures."""
+    """Configs 0-4 as named in the workload module; "1s" (4 layers, 300 adapters, ~2.4 GB
+    pool) and "2s" (2 layers x 2 projections, ~2 GB on the device) are small variants of
+    configs 1 and 2 for profiler captures."""
     from workloads import spec
     if cfg == "1s":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
                                     300, [8, 16, 32, 64], 64, 1.0)
+    if cfg == "2s":
+        return spec.prefill_workload("llama7b-prefill-sgmv-h4096-s32-a1000-l2p2", 1002, 4096, 2, 2,
+                                     1000, [8, 16, 32, 64], 32, 64, 1024, 1.0)
     if cfg == "4d":
         return spec.config4("distinct")
     if cfg == "4z":
@@ -57,11 +61,18 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
-    from heterogeneous_adapters_gb300 import build
+KERNEL_SOURCES = {
+    "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh", "segment.cuh"],
+    "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh", "segment.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the source files a kernel is built from (traffic figures taken on other
+    sources are not reused)."""
     h = hashlib.sha256()
-    for s in build.sources():
-        h.update(open(s, "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "heterogeneous_adapters_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -71,7 +82,7 @@ def ncu_traffic(kernel: str, workload: str, units_per_launch: float):
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     for line in open(p):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == src:

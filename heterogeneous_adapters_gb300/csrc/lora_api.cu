@@ -279,11 +279,13 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
         if (st != LORA_OK) return st;
         for (int32_t i = 0; i < n; ++i) {
             const lora_problem& pr = probs[base + i];
-            st = make_map(&prm.x_map[i], pr.x, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldx, 128);
+            st = make_map(&prm.x_map[i], pr.x, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldx, kMmaRowBlock);
             if (st != LORA_OK) return st;
-            prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
-            prm.probs[i].ldy = (int32_t)pr.ldy;
-            prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
+            st = make_map(&prm.y_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, kMmaRowBlock);
+            if (st != LORA_OK) return st;
+            st = make_map(&prm.y1_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, 1);
+            if (st != LORA_OK) return st;
+            prm.blk[i] = pr.layer * d.num_proj + pr.proj;
         }
         prm.pool = view_of(pool);
         prm.ws = reinterpret_cast<char*>(ws);

@@ -206,17 +206,23 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     //    work items are taken first from the queue and the tail of a launch is short.
     int32_t* gorder = sorted;   // the sorted-segment list is no longer needed
     __syncthreads();
+    for (int g = tid; g < G; g += nthr)   // group keys, reusing the segment-key array
+        key[g] = ((long long)(LORA_MAX_RANK - P.ranks[grp_adapter[g]]) << 32) | g;
+    __syncthreads();
     for (int g0 = 0; g0 < G; g0 += nthr) {
         const int g = g0 + tid;
-        if (g < G) {
-            const long long my = ((long long)(LORA_MAX_RANK - P.ranks[grp_adapter[g]]) << 32) | g;
-            int rank = 0;
-            for (int k = 0; k < G; ++k) {
-                const long long other = ((long long)(LORA_MAX_RANK - P.ranks[grp_adapter[k]]) << 32) | k;
-                rank += other < my;
+        const long long my = g < G ? key[g] : kNone;
+        int rank = 0;
+        for (int k0 = 0; k0 < G; k0 += kKeyTile) {
+            __syncthreads();
+            for (int k = tid; k < kKeyTile; k += nthr) key_tile[k] = (k0 + k < G) ? key[k0 + k] : kNone;
+            __syncthreads();
+            if (g < G) {
+                const int kn = min(kKeyTile, G - k0);
+                for (int k = 0; k < kn; ++k) rank += key_tile[k] < my;
             }
-            gorder[rank] = g;
         }
+        if (g < G) gorder[rank] = g;
     }
     __syncthreads();
     int carry_c = 0;

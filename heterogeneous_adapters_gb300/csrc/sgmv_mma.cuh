@@ -31,24 +31,22 @@ namespace lora {
 
 constexpr int kMmaThreads = 320;
 constexpr int kMmaEpiWarps = 8;
-constexpr int kMmaMaxProbs = 48;            // x tensor maps per launch
+constexpr int kMmaMaxProbs = 48;            // problems per launch (3 tensor maps each)
 constexpr int kMmaMaxRank = 128;
 constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 bytes)
 constexpr int kMmaNTile = 128;              // y columns per expand slice
+constexpr int kMmaRowBlock = 32;            // rows per x / y TMA box
+constexpr int kMmaYStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kD1Col = 0, kD2Col = 128;   // D2 buffers at columns 128 and 256
 constexpr uint32_t kDerrTimeoutMma = 0x20u;
 
-struct MmaProb {
-    __nv_bfloat16* y;
-    int32_t ldy;
-    int32_t blk;
-};
-
 struct __align__(64) MmaParams {
     CUtensorMap pool_map;                    // {h, num_pages}, box {64, 1}, 128B swizzle
-    CUtensorMap x_map[kMmaMaxProbs];         // {h, T}, box {64, 128}, 128B swizzle
-    MmaProb probs[kMmaMaxProbs];
+    CUtensorMap x_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
+    CUtensorMap y_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
+    CUtensorMap y1_map[kMmaMaxProbs];        // {h, T}, box {64, 1}
+    int32_t blk[kMmaMaxProbs];               // layer * P + proj
     PoolView pool;
     char* ws;
     int32_t nprob;
@@ -60,18 +58,21 @@ struct __align__(64) MmaParams {
 };
 
 struct MmaSmem {
-    uint32_t ring, thi, tlo, full, empty, d1_full, t_ready, d2_full, d2_empty, final_bar, tmem_slot,
-        total;
+    uint32_t ring, yring, thi, tlo, full, empty, yfull, yempty, d1_full, t_ready, d2_full, d2_empty,
+        final_bar, tmem_slot, total;
 };
 
 __host__ __device__ inline MmaSmem mma_smem_layout(int stages, int stage_bytes, int t_bytes) {
     MmaSmem L;
     uint32_t o = 0;
     L.ring = o;      o += (uint32_t)stages * stage_bytes;
+    L.yring = o;     o += kMmaYStages * 32768;
     L.thi = o;       o += t_bytes;
     L.tlo = o;       o += t_bytes;
     L.full = o;      o += stages * 8;
     L.empty = o;     o += stages * 8;
+    L.yfull = o;     o += kMmaYStages * 8;
+    L.yempty = o;    o += kMmaYStages * 8;
     L.d1_full = o;   o += 8;
     L.t_ready = o;   o += 8;
     L.d2_full = o;   o += 16;
@@ -101,7 +102,7 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
     it.pr = item / n_tiles;
     const int r = it.tile.rank;
     it.rp = mma_rpad(r);
-    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.probs[it.pr].blk * 2 * r;
+    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * 2 * r;
     bool bad = false;
     for (int e = lane; e < 2 * r; e += 32) {
         const int page = p.pool.pt[it.blk + e];
@@ -113,7 +114,9 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
 
 __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
-    unsigned char* base = mma_smem_raw;
+    // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023) & ~uintptr_t(1023));
     const MmaSmem L = mma_smem_layout(p.stages, p.stage_bytes, p.t_bytes);
     const int S = p.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -130,6 +133,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(L.full + s * 8), 1);
             mbar_init(bar(L.empty + s * 8), 1);
+        }
+        for (int s = 0; s < kMmaYStages; ++s) {
+            mbar_init(bar(L.yfull + s * 8), 1);
+            mbar_init(bar(L.yempty + s * 8), kMmaEpiWarps);
         }
         mbar_init(bar(L.d1_full), 1);
         mbar_init(bar(L.t_ready), kMmaEpiWarps);
@@ -152,18 +159,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            prefetch_tmap(&p.pool_map);
-        }
-        uint32_t it = 0;
+        if (lane == 0) prefetch_tmap(&p.pool_map);
+        uint32_t it = 0, gy = 0;
         for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
             const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
             if (!mi.ok) {
                 if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
                 continue;
             }
-            const int r = mi.tile.rank, rp = mi.rp;
+            const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
+            const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
             const void* xmap = &p.x_map[mi.pr];
+            const void* ymap = &p.y_map[mi.pr];
             // my lane's A / B pages (lane j, j + 32, ...); rows >= r read out of range
             int pga[4], pgb[4];
 #pragma unroll
@@ -172,15 +179,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                 pga[q] = j < r ? p.pool.pt[mi.blk + j] : (int)p.pool.num_pages;
                 pgb[q] = j < r ? p.pool.pt[mi.blk + r + j] : (int)p.pool.num_pages;
             }
+            // shrink stages: x rows (32-row boxes, only the tile's blocks) + A chunk
             for (int kc = 0; kc < n_kc && ok; ++kc) {
                 const uint32_t s = it % S;
                 if (!mbar_wait(bar(L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
                 const uint32_t st = bar(L.ring + s * p.stage_bytes);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(L.full + s * 8), 128 * 128 + rp * 128);
-                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar(L.full + s * 8), nblk * kMmaRowBlock * 128 + rp * 128);
                 __syncwarp();
-                if (lane == 0) tma_load_2d(st, xmap, kc * kMmaKChunk, mi.tile.row0, bar(L.full + s * 8));
+                if (lane < nblk)
+                    tma_load_2d(st + lane * kMmaRowBlock * 128, xmap, kc * kMmaKChunk, row0 + lane * kMmaRowBlock,
+                                bar(L.full + s * 8));
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int j = lane + 32 * q;
@@ -189,10 +198,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                 }
                 ++it;
             }
-            for (int nt = 0; nt < n_nt && ok; ++nt) {
-                const uint32_t s = it % S;
+            // expand: per 128-column slice, the B^T operand (main ring) and the y tile (y ring)
+            for (int nt = 0; nt < n_nt && ok; ++nt, ++gy) {
+                uint32_t s = it % S;
                 if (!mbar_wait(bar(L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                const uint32_t st = bar(L.ring + s * p.stage_bytes);
+                uint32_t st = bar(L.ring + s * p.stage_bytes);
                 if (lane == 0) mbar_arrive_expect_tx(bar(L.full + s * 8), rp * 256);
                 __syncwarp();
                 // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
@@ -207,6 +217,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                     }
                 }
                 ++it;
+                // y tile: half hf (64 columns) at hf * 16 KB, 32-row block b at + b * 4 KB
+                const uint32_t ys = gy % kMmaYStages;
+                if (!mbar_wait(bar(L.yempty + ys * 8), ((gy / kMmaYStages) & 1) ^ 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                st = bar(L.yring + ys * 32768);
+                if (lane == 0) mbar_arrive_expect_tx(bar(L.yfull + ys * 8), 2 * nblk * kMmaRowBlock * 128);
+                __syncwarp();
+                if (lane < 2 * nblk) {
+                    const int hf = lane & 1, b = lane >> 1;
+                    tma_load_2d(st + hf * 16384 + b * kMmaRowBlock * 128, ymap, nt * kMmaNTile + hf * 64,
+                                row0 + b * kMmaRowBlock, bar(L.yfull + ys * 8));
+                }
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
@@ -215,6 +239,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             const uint32_t first = it > (uint32_t)S ? it - S : 0;
             for (uint32_t k = first; k < it; ++k)
                 mbar_wait(bar(L.full + (k % S) * 8), (k / S) & 1, 100000000ull);
+            const uint32_t yfirst = gy > (uint32_t)kMmaYStages ? gy - kMmaYStages : 0;
+            for (uint32_t k = yfirst; k < gy; ++k)
+                mbar_wait(bar(L.yfull + (k % kMmaYStages) * 8), (k / kMmaYStages) & 1, 100000000ull);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
@@ -287,14 +314,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
         const int m = quad * 32 + lane;         // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint32_t tcount = 0, g = 0;
+        bool stored = false;
         for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
             const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
-            const int rp = mi.rp;
+            const int rp = mi.rp, rows = mi.tile.rows, row0 = mi.tile.row0;
             const float scale = p.pool.scales[mi.tile.adapter];
-            const MmaProb pb = p.probs[mi.pr];
-            const bool live = m < mi.tile.rows;
-            __nv_bfloat16* yrow = pb.y + (long long)(mi.tile.row0 + (live ? m : 0)) * pb.ldy;
+            const bool live = m < rows;
+            const bool block_full = quad * kMmaRowBlock + kMmaRowBlock <= rows;
+            const bool block_part = !block_full && quad * kMmaRowBlock < rows;
             // ---- convert D1 -> T_hi, T_lo (K-major, no swizzle: core matrices of 8 rows x 16 B,
             //      +128 B per 8 columns, +(rp / 8) * 128 B per 8 rows)
             if (!mbar_wait(bar(L.d1_full), tcount & 1, kWaitLimitNs)) { ok = false; break; }
@@ -329,26 +357,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L.t_ready));
             ++tcount;
-            // ---- expand epilogue over the column slices
-            const int col0 = half * 64;
-            uint4 ycur[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ycur[i] = live ? ld16(yrow + col0 + i * 8) : make_uint4(0, 0, 0, 0);
+            // ---- expand epilogue over the column slices: y (in the y ring) += D2
             for (int nt = 0; nt < n_nt; ++nt, ++g) {
                 const uint32_t b = g & 1;
-                uint4 ynext[8];
-                const bool more = nt + 1 < n_nt;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    ynext[i] = (live && more) ? ld16(yrow + (nt + 1) * kMmaNTile + col0 + i * 8)
-                                              : make_uint4(0, 0, 0, 0);
+                const uint32_t ys = g % kMmaYStages;
                 if (!mbar_wait(bar(L.d2_full + b * 8), (g >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 float acc[64];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float v[16];
-                    tmem_ld16(tmem + lane_base + kD2Col + b * kMmaNTile + col0 + q * 16, v);
+                    tmem_ld16(tmem + lane_base + kD2Col + b * kMmaNTile + half * 64 + q * 16, v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[q * 16 + i] = v[i];
                 }
@@ -356,24 +375,46 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L.d2_empty + b * 8));
+                if (!mbar_wait(bar(L.yfull + ys * 8), (g / kMmaYStages) & 1, kWaitLimitNs)) { ok = false; break; }
+                // this warp's box: rows 32 quad .. +31 of column half `half` (128-byte swizzle)
+                unsigned char* yrow = base + L.yring + ys * 32768 + half * 16384 + m * 128;
                 if (live) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int c = 0; c < 8; ++c) {
+                        uint4* ptr = reinterpret_cast<uint4*>(yrow + ((c ^ (m & 7)) << 4));
                         float y8[8];
-                        unpack8(ycur[i], y8);
+                        unpack8(*ptr, y8);
                         uint4 o;
-                        o.x = pack2(y8[0] + acc[8 * i + 0], y8[1] + acc[8 * i + 1]);
-                        o.y = pack2(y8[2] + acc[8 * i + 2], y8[3] + acc[8 * i + 3]);
-                        o.z = pack2(y8[4] + acc[8 * i + 4], y8[5] + acc[8 * i + 5]);
-                        o.w = pack2(y8[6] + acc[8 * i + 6], y8[7] + acc[8 * i + 7]);
-                        st16(yrow + nt * kMmaNTile + col0 + i * 8, o);
+                        o.x = pack2(y8[0] + acc[8 * c + 0], y8[1] + acc[8 * c + 1]);
+                        o.y = pack2(y8[2] + acc[8 * c + 2], y8[3] + acc[8 * c + 3]);
+                        o.z = pack2(y8[4] + acc[8 * c + 4], y8[5] + acc[8 * c + 5]);
+                        o.w = pack2(y8[6] + acc[8 * c + 6], y8[7] + acc[8 * c + 7]);
+                        *ptr = o;
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ycur[i] = ynext[i];
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int col = nt * kMmaNTile + half * 64;
+                if (block_full) {
+                    if (lane == 0) {
+                        tma_store_2d(&p.y_map[mi.pr], col, row0 + quad * kMmaRowBlock,
+                                     smem_addr(base + L.yring + ys * 32768 + half * 16384 + quad * 4096));
+                        bulk_commit();
+                        bulk_wait_read0();
+                        stored = true;
+                    }
+                } else if (block_part && live) {
+                    tma_store_2d(&p.y1_map[mi.pr], col, row0 + m, smem_addr(yrow));
+                    bulk_commit();
+                    bulk_wait_read0();
+                    stored = true;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L.yempty + ys * 8));
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
+        if (stored) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
