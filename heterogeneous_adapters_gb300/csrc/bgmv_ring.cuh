@@ -28,9 +28,7 @@
 
 namespace lora {
 
-constexpr int kRingConsumerWarps = 8;
-constexpr int kRingConsumers = kRingConsumerWarps * 32;
-constexpr int kRingThreads = kRingConsumers + 32;
+constexpr int kRingMaxConsumerWarps = 16;
 constexpr int kRingPages = 4;              // pages (or x rows) per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint32_t kDerrTimeout = 0x20u;
@@ -66,7 +64,7 @@ struct RingSmem {
     uint32_t ring, full, empty, cbar, meta, red, ts, pgbuf, total;
 };
 
-__host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes, int r_max) {
+__host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes, int r_max, int cwarps) {
     RingSmem L;
     const int rp = (r_max + 7) / 8 * 8;
     uint32_t o = 0;
@@ -76,15 +74,15 @@ __host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes
     L.cbar = o;  o += 8;
     L.meta = o;  o += stages * sizeof(StageMeta);
     o = (o + 15) & ~15u;
-    L.red = o;   o += kRingConsumerWarps * rp * kChunk * 4;
+    L.red = o;   o += cwarps * rp * kChunk * 4;
     L.ts = o;    o += rp * kChunk * 4;
     L.pgbuf = o; o += 2 * LORA_MAX_RANK * 4;
     L.total = o;
     return L;
 }
 
-// Column vectors (8 bf16 = 16 B) of a row handled by consumer thread c: c + 256 v.
-template <int NV, int NT>
+// Column vectors (8 bf16 = 16 B) of a row handled by consumer thread c: c + 32 CW v.
+template <int NV, int NT, int CW>
 __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, int stage_row_bytes,
                                                   int npages, int h8, int c,
                                                   const uint4 (&xv)[kChunk][NV], float* red_w,
@@ -98,7 +96,7 @@ __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, in
         if (jj < npages) {
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
-                const int vi = c + v * kRingConsumers;
+                const int vi = c + v * (CW * 32);
                 if (vi < h8) {
                     const uint4 a = *reinterpret_cast<const uint4*>(stage + jj * stage_row_bytes + vi * 16);
                     float a8[8];
@@ -121,7 +119,7 @@ __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, in
     if ((lane & 1) == 0) red_w[j0 * kChunk + (lane >> 1)] = sum;   // index jj*kChunk + t
 }
 
-template <int NV, int NT>
+template <int NV, int NT, int CW>
 __device__ __forceinline__ void ring_expand_stage(const unsigned char* stage, int stage_row_bytes,
                                                   int npages, int h8, int c, const float* ts, int j0,
                                                   float (&acc)[kChunk][NV][8]) {
@@ -132,7 +130,7 @@ __device__ __forceinline__ void ring_expand_stage(const unsigned char* stage, in
             const float tv[4] = {tj.x, tj.y, tj.z, tj.w};
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
-                const int vi = c + v * kRingConsumers;
+                const int vi = c + v * (CW * 32);
                 if (vi < h8) {
                     const uint4 b = *reinterpret_cast<const uint4*>(stage + jj * stage_row_bytes + vi * 16);
                     float b8[8];
@@ -160,7 +158,7 @@ __device__ __forceinline__ bool consumer_barrier(unsigned char* base, const Ring
     return ok;
 }
 
-template <int NV, int NT>
+template <int NV, int NT, int CW>
 __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, const RingSmem& L,
                                   uint32_t& it, uint32_t& bphase, const StageMeta& mx, int c) {
     const int h = p.pool.h, h8 = h >> 3;
@@ -182,7 +180,7 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
         for (int t = 0; t < kChunk; ++t)
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
-                const int vi = c + v * kRingConsumers;
+                const int vi = c + v * (CW * 32);
                 xv[t][v] = (t < mx.count && vi < h8) ? *reinterpret_cast<const uint4*>(st + t * row_bytes + vi * 16)
                                                : make_uint4(0, 0, 0, 0);
             }
@@ -195,17 +193,17 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
         const uint32_t s = it % S;
         if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
         const int np = min(kRingPages, r - j0);
-        ring_shrink_stage<NV, NT>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, xv,
+        ring_shrink_stage<NV, NT, CW>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, xv,
                                   red_w, j0);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
         ++it;
     }
     if (!consumer_barrier(base, L, bphase)) return false;
-    for (int e = c; e < r * kChunk; e += kRingConsumers) {
+    for (int e = c; e < r * kChunk; e += CW * 32) {
         float a = 0.f;
 #pragma unroll
-        for (int w = 0; w < kRingConsumerWarps; ++w) a += red[w * rp * kChunk + e];
+        for (int w = 0; w < CW; ++w) a += red[w * rp * kChunk + e];
         ts[e] = a * mx.scale;
         if (p.t_out != nullptr) {
             const int j = e / kChunk, t = e % kChunk;
@@ -219,7 +217,7 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
     for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int vi = c + v * kRingConsumers;
+            const int vi = c + v * (CW * 32);
             yv[t][v] = (t < mx.count && vi < h8) ? ld16(pd.y + (long long)mx.rows[t] * pd.ldy + vi * 8) : make_uint4(0, 0, 0, 0);
         }
     float acc[kChunk][NV][8];
@@ -233,7 +231,7 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
         const uint32_t s = it % S;
         if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
         const int np = min(kRingPages, r - j0);
-        ring_expand_stage<NV, NT>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, ts, j0,
+        ring_expand_stage<NV, NT, CW>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, ts, j0,
                                   acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
@@ -243,7 +241,7 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
     for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int vi = c + v * kRingConsumers;
+            const int vi = c + v * (CW * 32);
             if (t < mx.count && vi < h8) {
                 float y8[8];
                 unpack8(yv[t][v], y8);
@@ -259,11 +257,13 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
     return consumer_barrier(base, L, bphase);
 }
 
-template <int NV>
-__global__ void __launch_bounds__(kRingThreads, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
+// NV: 16-byte column vectors per consumer thread; CW: consumer warps (h = 8 * 32 * CW * NV
+// or less).
+template <int NV, int CW>
+__global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
     extern __shared__ __align__(1024) unsigned char ring_smem_raw[];
     unsigned char* base = ring_smem_raw;
-    const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max);
+    const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max, CW);
     const int S = p.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
@@ -272,9 +272,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) bgmv_ring_kernel(const __grid
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(base + L.full + s * 8), 1);
-            mbar_init(smem_addr(base + L.empty + s * 8), kRingConsumerWarps);
+            mbar_init(smem_addr(base + L.empty + s * 8), CW);
         }
-        mbar_init(smem_addr(base + L.cbar), kRingConsumerWarps);
+        mbar_init(smem_addr(base + L.cbar), CW);
         fence_mbar_init();
     }
     __syncthreads();
@@ -435,11 +435,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) bgmv_ring_kernel(const __grid
             }
             bool ok;
             if (mx.count == 1)
-                ok = ring_consume_item<NV, 1>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 1, CW>(p, base, L, it, bphase, mx, c);
             else if (mx.count == 2)
-                ok = ring_consume_item<NV, 2>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 2, CW>(p, base, L, it, bphase, mx, c);
             else
-                ok = ring_consume_item<NV, kChunk>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, kChunk, CW>(p, base, L, it, bphase, mx, c);
             if (!ok) {
                 if (c == 0) set_error(&hdr->err, kDerrTimeout);
                 break;

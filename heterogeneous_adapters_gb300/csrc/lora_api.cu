@@ -119,9 +119,9 @@ lora_status launch_fma(const DeltaParams& prm, size_t smem, cudaStream_t stream)
 }
 
 // Ring depth that fits the opt-in shared memory of one CTA (at most 8 stages).
-int ring_stages(int smem_optin, int stage_bytes, int r_max, size_t* smem) {
+int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* smem) {
     for (int S = 8; S >= 2; --S) {
-        const size_t need = ring_smem_layout(S, stage_bytes, r_max).total + 1024;
+        const size_t need = ring_smem_layout(S, stage_bytes, r_max, cwarps).total + 1024;
         if (need <= (size_t)smem_optin) {
             *smem = need;
             return S;
@@ -130,7 +130,7 @@ int ring_stages(int smem_optin, int stage_bytes, int r_max, size_t* smem) {
     return 0;
 }
 
-template <int NV>
+template <int NV, int CW>
 lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
@@ -140,17 +140,17 @@ lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
     int dev = 0;
     cudaGetDevice(&dev);
     size_t smem = 0;
-    const int S = ring_stages(di->smem_optin, prm.stage_bytes, prm.pool.r_max, &smem);
+    const int S = ring_stages(di->smem_optin, prm.stage_bytes, prm.pool.r_max, CW, &smem);
     if (S < 2) return LORA_ETOOBIG;
     prm.stages = S;
-    auto kern = bgmv_ring_kernel<NV>;
+    auto kern = bgmv_ring_kernel<NV, CW>;
     if (attr_dev != dev || attr_smem < smem) {
         st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         if (st != LORA_OK) return st;
         attr_dev = dev;
         attr_smem = smem;
     }
-    kern<<<di->sm_count, kRingThreads, smem, stream>>>(prm);
+    kern<<<di->sm_count, CW * 32 + 32, smem, stream>>>(prm);
     return cuda_status(cudaGetLastError());
 }
 
@@ -180,14 +180,19 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
             prm.probs[i].ldy = (int32_t)pr.ldy;
             prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
         }
-        const int nv = (d.h / 8 + kRingConsumers - 1) / kRingConsumers;
+        // consumer warps x vectors per thread cover the h / 8 16-byte vectors of a row
+        const int h8 = d.h / 8;
         lora_status st;
-        switch (nv) {
-            case 1: st = launch_ring<1>(prm, stream); break;
-            case 2: st = launch_ring<2>(prm, stream); break;
-            case 3: st = launch_ring<3>(prm, stream); break;
-            default: st = launch_ring<4>(prm, stream); break;
-        }
+        if (h8 <= 256)
+            st = launch_ring<1, 8>(prm, stream);
+        else if (h8 <= 512)
+            st = launch_ring<2, 8>(prm, stream);
+        else if (h8 <= 640)
+            st = launch_ring<2, 10>(prm, stream);
+        else if (h8 <= 768)
+            st = launch_ring<2, 12>(prm, stream);
+        else
+            st = launch_ring<2, 16>(prm, stream);
         if (st != LORA_OK) return st;
     }
     return LORA_OK;
@@ -252,17 +257,20 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
     const int rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
-    int stage_bytes = 16384 + rp_max * 128;
-    if (rp_max * 256 > stage_bytes) stage_bytes = rp_max * 256;
-    stage_bytes = (stage_bytes + 1023) / 1024 * 1024;
-    const int t_bytes = 128 * rp_max * 2;
-    int S = 8;
+    const int s1_bytes = (16384 + rp_max * 128 + 1023) / 1024 * 1024;   // x chunk + A chunk
+    const int s2_bytes = (rp_max * 256 + 1023) / 1024 * 1024;           // B^T slice
+    // y ring of 3 when the shrink ring still gets 3 stages, else 2; B^T ring of 2
+    int s1 = 0, s3 = 3;
+    const int s2 = 2;
     size_t smem = 0;
-    for (; S >= 2; --S) {
-        smem = mma_smem_layout(S, stage_bytes, t_bytes).total + 1024;
-        if (smem <= (size_t)di->smem_optin) break;
+    for (; s3 >= 2; --s3) {
+        for (s1 = kMmaMaxStages; s1 >= 2; --s1) {
+            smem = mma_smem_layout(s1, s1_bytes, s2, s2_bytes, s3).total + 1024;
+            if (smem <= (size_t)di->smem_optin) break;
+        }
+        if (s1 >= 3 || s3 == 2) break;
     }
-    if (S < 2) return LORA_ETOOBIG;
+    if (s1 < 2) return LORA_ETOOBIG;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev || attr_smem < smem) {
@@ -272,8 +280,11 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
         attr_dev = dev;
         attr_smem = smem;
     }
-    for (int32_t base = 0; base < nprob; base += kMmaMaxProbs) {
-        const int32_t n = nprob - base < kMmaMaxProbs ? nprob - base : kMmaMaxProbs;
+    // balanced launches of at most kMmaMaxProbs problems (no short last launch)
+    const int32_t nlaunch = (nprob + kMmaMaxProbs - 1) / kMmaMaxProbs;
+    const int32_t per = (nprob + nlaunch - 1) / nlaunch;
+    for (int32_t base = 0; base < nprob; base += per) {
+        const int32_t n = nprob - base < per ? nprob - base : per;
         memset(&prm, 0, sizeof prm);
         st = make_map(&prm.pool_map, d.pages, (uint64_t)d.h, (uint64_t)d.num_pages, (uint64_t)d.h, 1);
         if (st != LORA_OK) return st;
@@ -290,9 +301,11 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
         prm.pool = view_of(pool);
         prm.ws = reinterpret_cast<char*>(ws);
         prm.nprob = n;
-        prm.stages = S;
-        prm.stage_bytes = stage_bytes;
-        prm.t_bytes = t_bytes;
+        prm.s1 = s1;
+        prm.s2 = s2;
+        prm.s3 = s3;
+        prm.s1_bytes = s1_bytes;
+        prm.s2_bytes = s2_bytes;
         prm.rp_max = rp_max;
         sgmv_mma_kernel<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
         st = cuda_status(cudaGetLastError());
@@ -493,7 +506,22 @@ lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const 
     sp.mma_max_rank = kMmaMaxRank;
     sp.L_tokens = T;
     sp.L_segments = S + Td;
-    segment_kernel<<<1, kSegThreads, 0, (cudaStream_t)stream>>>(sp);
+    size_t smem = 0;
+    if (S + Td <= kSegSmemMax) {
+        static thread_local int attr_dev = -1;
+        int dev = 0;
+        st = cuda_status(cudaGetDevice(&dev));
+        if (st != LORA_OK) return st;
+        if (attr_dev != dev) {
+            st = cuda_status(cudaFuncSetAttribute(segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)seg_smem_bytes(kSegSmemMax)));
+            if (st != LORA_OK) return st;
+            attr_dev = dev;
+        }
+        sp.smem_segs = S + Td;
+        smem = seg_smem_bytes(S + Td);
+    }
+    segment_kernel<<<1, kSegThreads, smem, (cudaStream_t)stream>>>(sp);
     return cuda_status(cudaGetLastError());
 }
 

@@ -40,7 +40,14 @@ struct SegParams {
     int32_t mma_max_rank;   // segments whose adapter rank exceeds this use the CUDA-core path
     int32_t L_tokens;  // the (max_tokens, max_segments) that L was computed from
     int32_t L_segments;
+    int32_t smem_segs; // > 0: the per-segment scratch arrays live in dynamic shared memory
+    int32_t pad;
 };
+
+// Dynamic shared memory of the grouping kernel when the per-segment arrays fit there
+// (key 8 B + six int arrays per segment).
+constexpr int kSegSmemMax = 1536;
+__host__ __device__ constexpr size_t seg_smem_bytes(int n) { return (size_t)(n + 1) * 32 + 64; }
 
 __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p) {
     __shared__ int scan_smem[33];
@@ -49,13 +56,29 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
-    long long* key = reinterpret_cast<long long*>(p.ws + p.L.seg_key);
-    int32_t* sbeg = reinterpret_cast<int32_t*>(p.ws + p.L.seg_begin);
-    int32_t* slen = reinterpret_cast<int32_t*>(p.ws + p.L.seg_len);
-    int32_t* sorted = reinterpret_cast<int32_t*>(p.ws + p.L.sorted);
-    int32_t* pos = reinterpret_cast<int32_t*>(p.ws + p.L.pos);
-    int32_t* fpos = reinterpret_cast<int32_t*>(p.ws + p.L.fpos);
-    int32_t* gfirst = reinterpret_cast<int32_t*>(p.ws + p.L.gfirst);
+    // per-segment scratch: in shared memory for small batches (the phases below hand data
+    // to each other through it), else in the workspace
+    extern __shared__ __align__(16) unsigned char seg_smem[];
+    long long* key;
+    int32_t *sbeg, *slen, *sorted, *pos, *fpos, *gfirst;
+    if (p.smem_segs > 0) {
+        const int m = p.smem_segs + 1;
+        key = reinterpret_cast<long long*>(seg_smem);
+        sbeg = reinterpret_cast<int32_t*>(key + m);
+        slen = sbeg + m;
+        sorted = slen + m;
+        pos = sorted + m;
+        fpos = pos + m;
+        gfirst = fpos + m;
+    } else {
+        key = reinterpret_cast<long long*>(p.ws + p.L.seg_key);
+        sbeg = reinterpret_cast<int32_t*>(p.ws + p.L.seg_begin);
+        slen = reinterpret_cast<int32_t*>(p.ws + p.L.seg_len);
+        sorted = reinterpret_cast<int32_t*>(p.ws + p.L.sorted);
+        pos = reinterpret_cast<int32_t*>(p.ws + p.L.pos);
+        fpos = reinterpret_cast<int32_t*>(p.ws + p.L.fpos);
+        gfirst = reinterpret_cast<int32_t*>(p.ws + p.L.gfirst);
+    }
     int32_t* perm = reinterpret_cast<int32_t*>(p.ws + p.L.perm);
     int32_t* grp_start = reinterpret_cast<int32_t*>(p.ws + p.L.grp_start);
     int32_t* grp_adapter = reinterpret_cast<int32_t*>(p.ws + p.L.grp_adapter);

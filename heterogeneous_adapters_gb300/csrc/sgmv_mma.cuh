@@ -11,14 +11,17 @@
 //           X chunk by TMA (128-byte swizzle), the r A-row pages' chunks by TMA (one
 //           64-element row per request, rows r..r16-1 read out of range = zeros);
 //   convert the epilogue warps read D1, scale by s and split each fp32 value exactly into
-//           a bf16 pair t = hi + lo (|t - hi - lo| <= 2^-16 |t|), written to shared
-//           memory as two K-major operands;
+//           a bf16 pair t = hi + lo (|t - hi - lo| <= 2^-16 |t|), written back to TMEM
+//           as two K-major A operands;
 //   expand  for every 128-column slice of y: D2[128 x 128] = T_hi . B^T + T_lo . B^T with
 //           the B-column pages' slices as an MN-major operand (TMA, 128-byte swizzle),
 //           double-buffered in TMEM so the epilogue of one slice overlaps the MMA of the
 //           next; the epilogue adds D2 to y (fp32) and stores bf16 rows of the tile.
-// Roles (one persistent CTA per SM, items dealt round-robin): warp 0 TMA producer,
-// warp 1 TMEM owner + MMA issuer (one thread), warps 2-9 convert + epilogue.
+// Roles (one persistent CTA per SM, items dealt round-robin): warp 0 streams the shrink
+// operands (x and A chunks), warp 2 the expand operands (B^T slices and y tiles), warp 1
+// owns TMEM and issues the MMAs -- while it expands tile k it also issues tile k+1's
+// shrink chunks as they land, so the x stream of the next tile overlaps the y stream of
+// this one -- and warps 3-10 convert D1 and run the epilogue.  T lives in TMEM.
 // All waits are bounded; a timeout sets an error bit and the CTA unwinds.
 #pragma once
 #include <cuda.h>
@@ -29,19 +32,21 @@
 
 namespace lora {
 
-constexpr int kMmaThreads = 320;
+constexpr int kMmaThreads = 352;
 constexpr int kMmaEpiWarps = 8;
-constexpr int kMmaMaxProbs = 48;            // problems per launch (3 tensor maps each)
+constexpr int kMmaMaxProbs = 64;            // problems per launch (3 tensor maps each)
 constexpr int kMmaMaxRank = 128;
 constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 bytes)
 constexpr int kMmaNTile = 128;              // y columns per expand slice
 constexpr int kMmaRowBlock = 32;            // rows per x / y TMA box
-constexpr int kMmaYStages = 2;
+constexpr int kMmaMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kD1Col = 0, kD2Col = 128;   // D2 buffers at columns 128 and 256
+// TMEM columns: D1 (shrink, fp32) 0..127, D2 (expand, fp32, two buffers) 128..383,
+// T_hi and T_lo (bf16 pairs, K / 2 columns each) 384..447 and 448..511.
+constexpr uint32_t kD1Col = 0, kD2Col = 128, kThiCol = 384, kTloCol = 448;
 constexpr uint32_t kDerrTimeoutMma = 0x20u;
 
-struct __align__(64) MmaParams {
+struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
     CUtensorMap pool_map;                    // {h, num_pages}, box {64, 1}, 128B swizzle
     CUtensorMap x_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
     CUtensorMap y_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
@@ -50,29 +55,29 @@ struct __align__(64) MmaParams {
     PoolView pool;
     char* ws;
     int32_t nprob;
-    int32_t stages;
-    int32_t stage_bytes;
-    int32_t t_bytes;        // bytes of one T operand (hi or lo)
-    int32_t rp_max;         // largest padded rank served here
-    int32_t pad[3];
+    int32_t s1, s2, s3;                      // depths of the shrink, B^T and y rings
+    int32_t s1_bytes, s2_bytes;              // stage sizes (y stages are 32 KB)
+    int32_t rp_max;
+    int32_t pad;
 };
 
 struct MmaSmem {
-    uint32_t ring, yring, thi, tlo, full, empty, yfull, yempty, d1_full, t_ready, d2_full, d2_empty,
-        final_bar, tmem_slot, total;
+    uint32_t ring1, ring2, ring3, full1, empty1, full2, empty2, full3, empty3, d1_full, t_ready, d2_full,
+        d2_empty, final_bar, tmem_slot, total;
 };
 
-__host__ __device__ inline MmaSmem mma_smem_layout(int stages, int stage_bytes, int t_bytes) {
+__host__ __device__ inline MmaSmem mma_smem_layout(int s1, int s1_bytes, int s2, int s2_bytes, int s3) {
     MmaSmem L;
     uint32_t o = 0;
-    L.ring = o;      o += (uint32_t)stages * stage_bytes;
-    L.yring = o;     o += kMmaYStages * 32768;
-    L.thi = o;       o += t_bytes;
-    L.tlo = o;       o += t_bytes;
-    L.full = o;      o += stages * 8;
-    L.empty = o;     o += stages * 8;
-    L.yfull = o;     o += kMmaYStages * 8;
-    L.yempty = o;    o += kMmaYStages * 8;
+    L.ring1 = o;     o += (uint32_t)s1 * s1_bytes;
+    L.ring2 = o;     o += (uint32_t)s2 * s2_bytes;
+    L.ring3 = o;     o += (uint32_t)s3 * 32768;
+    L.full1 = o;     o += kMmaMaxStages * 8;
+    L.empty1 = o;    o += kMmaMaxStages * 8;
+    L.full2 = o;     o += kMmaMaxStages * 8;
+    L.empty2 = o;    o += kMmaMaxStages * 8;
+    L.full3 = o;     o += kMmaMaxStages * 8;
+    L.empty3 = o;    o += kMmaMaxStages * 8;
     L.d1_full = o;   o += 8;
     L.t_ready = o;   o += 8;
     L.d2_full = o;   o += 16;
@@ -112,13 +117,33 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
     return it;
 }
 
+// The next processable item at or after `item` (skipping items with bad pages), or total.
+__device__ __forceinline__ uint32_t mma_next_ok(const MmaParams& p, const Tile* tiles, int n_tiles,
+                                                uint32_t item, uint32_t total, int lane, MmaItem& mi) {
+    for (; item < total; item += gridDim.x) {
+        mi = mma_item(p, tiles, n_tiles, item, lane);
+        if (mi.ok) return item;
+    }
+    return total;
+}
+
+// Issue the four shrink MMAs of one K chunk (stage at shared address st) into D1.
+__device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t st, uint32_t idesc, int kc) {
+#pragma unroll
+    for (int kk = 0; kk < kMmaKChunk / 16; ++kk) {
+        const uint64_t da = smem_desc(st + kk * 32, 16, 1024, 2);
+        const uint64_t db = smem_desc(st + 16384 + kk * 32, 16, 1024, 2);
+        tc_mma_f16(tmem + kD1Col, da, db, idesc, (kc | kk) != 0);
+    }
+}
+
 __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
     // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023) & ~uintptr_t(1023));
-    const MmaSmem L = mma_smem_layout(p.stages, p.stage_bytes, p.t_bytes);
-    const int S = p.stages;
+    const MmaSmem L = mma_smem_layout(p.s1, p.s1_bytes, p.s2, p.s2_bytes, p.s3);
+    const uint32_t S1 = p.s1, S2 = p.s2, S3 = p.s3;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
     const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
@@ -130,13 +155,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
     auto bar = [&](uint32_t off) { return smem_addr(base + off); };
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar(L.full + s * 8), 1);
-            mbar_init(bar(L.empty + s * 8), 1);
+        for (uint32_t s = 0; s < S1; ++s) {
+            mbar_init(bar(L.full1 + s * 8), 1);
+            mbar_init(bar(L.empty1 + s * 8), 1);
         }
-        for (int s = 0; s < kMmaYStages; ++s) {
-            mbar_init(bar(L.yfull + s * 8), 1);
-            mbar_init(bar(L.yempty + s * 8), kMmaEpiWarps);
+        for (uint32_t s = 0; s < S2; ++s) {
+            mbar_init(bar(L.full2 + s * 8), 1);
+            mbar_init(bar(L.empty2 + s * 8), 1);
+        }
+        for (uint32_t s = 0; s < S3; ++s) {
+            mbar_init(bar(L.full3 + s * 8), 1);
+            mbar_init(bar(L.empty3 + s * 8), kMmaEpiWarps);
         }
         mbar_init(bar(L.d1_full), 1);
         mbar_init(bar(L.t_ready), kMmaEpiWarps);
@@ -158,9 +187,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
     bool ok = true;
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------------ shrink producer
         if (lane == 0) prefetch_tmap(&p.pool_map);
-        uint32_t it = 0, gy = 0;
+        uint32_t it = 0;
         for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
             const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
             if (!mi.ok) {
@@ -170,134 +199,197 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
             const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
             const void* xmap = &p.x_map[mi.pr];
-            const void* ymap = &p.y_map[mi.pr];
-            // my lane's A / B pages (lane j, j + 32, ...); rows >= r read out of range
-            int pga[4], pgb[4];
+            int pga[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = lane + 32 * q;
                 pga[q] = j < r ? p.pool.pt[mi.blk + j] : (int)p.pool.num_pages;
-                pgb[q] = j < r ? p.pool.pt[mi.blk + r + j] : (int)p.pool.num_pages;
             }
-            // shrink stages: x rows (32-row boxes, only the tile's blocks) + A chunk
-            for (int kc = 0; kc < n_kc && ok; ++kc) {
-                const uint32_t s = it % S;
-                if (!mbar_wait(bar(L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                const uint32_t st = bar(L.ring + s * p.stage_bytes);
+            for (int kc = 0; kc < n_kc; ++kc) {
+                const uint32_t s = it % S1;
+                if (!mbar_wait(bar(L.empty1 + s * 8), ((it / S1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                const uint32_t st = bar(L.ring1 + s * p.s1_bytes);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(bar(L.full + s * 8), nblk * kMmaRowBlock * 128 + rp * 128);
+                    mbar_arrive_expect_tx(bar(L.full1 + s * 8), nblk * kMmaRowBlock * 128 + rp * 128);
                 __syncwarp();
                 if (lane < nblk)
                     tma_load_2d(st + lane * kMmaRowBlock * 128, xmap, kc * kMmaKChunk, row0 + lane * kMmaRowBlock,
-                                bar(L.full + s * 8));
+                                bar(L.full1 + s * 8));
+                // A rows: groups of four real rows with one gather (lane 4k issues rows
+                // 4k..4k+3, page ids taken from the next three lanes); padding rows (>= r)
+                // and a ragged last group one row each, read out of range (zeros)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int j = lane + 32 * q;
-                    if (j < rp) tma_load_2d(st + 16384 + j * 128, &p.pool_map, kc * kMmaKChunk, pga[q],
-                                            bar(L.full + s * 8));
-                }
-                ++it;
-            }
-            // expand: per 128-column slice, the B^T operand (main ring) and the y tile (y ring)
-            for (int nt = 0; nt < n_nt && ok; ++nt, ++gy) {
-                uint32_t s = it % S;
-                if (!mbar_wait(bar(L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                uint32_t st = bar(L.ring + s * p.stage_bytes);
-                if (lane == 0) mbar_arrive_expect_tx(bar(L.full + s * 8), rp * 256);
-                __syncwarp();
-                // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
-                // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = lane + 32 * q;
+                    const int p1 = __shfl_down_sync(0xffffffffu, pga[q], 1);
+                    const int p2 = __shfl_down_sync(0xffffffffu, pga[q], 2);
+                    const int p3 = __shfl_down_sync(0xffffffffu, pga[q], 3);
                     if (j < rp) {
-                        const uint32_t dst = st + (j >> 3) * 2048 + (j & 7) * 128;
-                        tma_load_2d(dst, &p.pool_map, nt * kMmaNTile, pgb[q], bar(L.full + s * 8));
-                        tma_load_2d(dst + 1024, &p.pool_map, nt * kMmaNTile + 64, pgb[q], bar(L.full + s * 8));
+                        if ((j | 3) < r) {
+                            if ((j & 3) == 0)
+                                tma_gather4(st + 16384 + j * 128, &p.pool_map, kc * kMmaKChunk, pga[q], p1, p2, p3,
+                                            bar(L.full1 + s * 8));
+                        } else {
+                            tma_load_2d(st + 16384 + j * 128, &p.pool_map, kc * kMmaKChunk, pga[q],
+                                        bar(L.full1 + s * 8));
+                        }
                     }
                 }
                 ++it;
-                // y tile: half hf (64 columns) at hf * 16 KB, 32-row block b at + b * 4 KB
-                const uint32_t ys = gy % kMmaYStages;
-                if (!mbar_wait(bar(L.yempty + ys * 8), ((gy / kMmaYStages) & 1) ^ 1, kWaitLimitNs)) {
-                    ok = false;
-                    break;
+            }
+        }
+        if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
+        if (lane == 0) {   // let every stage this warp filled land before the CTA can exit
+            for (uint32_t k = it > S1 ? it - S1 : 0; k < it; ++k)
+                mbar_wait(bar(L.full1 + (k % S1) * 8), (k / S1) & 1, 100000000ull);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------------ expand producer
+        uint32_t it2 = 0, it3 = 0;
+        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            if (!mi.ok) continue;
+            const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
+            const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
+            const void* ymap = &p.y_map[mi.pr];
+            int pgb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = lane + 32 * q;
+                pgb[q] = j < r ? p.pool.pt[mi.blk + r + j] : (int)p.pool.num_pages;
+            }
+            for (int nt = 0; nt < n_nt; ++nt) {
+                // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
+                // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
+                uint32_t s = it2 % S2;
+                if (!mbar_wait(bar(L.empty2 + s * 8), ((it2 / S2) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                uint32_t st = bar(L.ring2 + s * p.s2_bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar(L.full2 + s * 8), rp * 256);
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = lane + 32 * q;
+                    const int p1 = __shfl_down_sync(0xffffffffu, pgb[q], 1);
+                    const int p2 = __shfl_down_sync(0xffffffffu, pgb[q], 2);
+                    const int p3 = __shfl_down_sync(0xffffffffu, pgb[q], 3);
+                    if (j < rp) {
+                        const uint32_t dst = st + (j >> 3) * 2048 + (j & 7) * 128;
+                        if ((j | 3) < r) {
+                            if ((j & 3) == 0) {
+                                tma_gather4(dst, &p.pool_map, nt * kMmaNTile, pgb[q], p1, p2, p3, bar(L.full2 + s * 8));
+                                tma_gather4(dst + 1024, &p.pool_map, nt * kMmaNTile + 64, pgb[q], p1, p2, p3,
+                                            bar(L.full2 + s * 8));
+                            }
+                        } else {
+                            tma_load_2d(dst, &p.pool_map, nt * kMmaNTile, pgb[q], bar(L.full2 + s * 8));
+                            tma_load_2d(dst + 1024, &p.pool_map, nt * kMmaNTile + 64, pgb[q], bar(L.full2 + s * 8));
+                        }
+                    }
                 }
-                st = bar(L.yring + ys * 32768);
-                if (lane == 0) mbar_arrive_expect_tx(bar(L.yfull + ys * 8), 2 * nblk * kMmaRowBlock * 128);
+                ++it2;
+                // y tile: half hf (64 columns) at hf * 16 KB, 32-row block b at + b * 4 KB
+                s = it3 % S3;
+                if (!mbar_wait(bar(L.empty3 + s * 8), ((it3 / S3) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                st = bar(L.ring3 + s * 32768);
+                if (lane == 0) mbar_arrive_expect_tx(bar(L.full3 + s * 8), 2 * nblk * kMmaRowBlock * 128);
                 __syncwarp();
                 if (lane < 2 * nblk) {
                     const int hf = lane & 1, b = lane >> 1;
                     tma_load_2d(st + hf * 16384 + b * kMmaRowBlock * 128, ymap, nt * kMmaNTile + hf * 64,
-                                row0 + b * kMmaRowBlock, bar(L.yfull + ys * 8));
+                                row0 + b * kMmaRowBlock, bar(L.full3 + s * 8));
                 }
+                ++it3;
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
-        // let every stage this warp filled land before the CTA can exit
         if (lane == 0) {
-            const uint32_t first = it > (uint32_t)S ? it - S : 0;
-            for (uint32_t k = first; k < it; ++k)
-                mbar_wait(bar(L.full + (k % S) * 8), (k / S) & 1, 100000000ull);
-            const uint32_t yfirst = gy > (uint32_t)kMmaYStages ? gy - kMmaYStages : 0;
-            for (uint32_t k = yfirst; k < gy; ++k)
-                mbar_wait(bar(L.yfull + (k % kMmaYStages) * 8), (k / kMmaYStages) & 1, 100000000ull);
+            for (uint32_t k = it2 > S2 ? it2 - S2 : 0; k < it2; ++k)
+                mbar_wait(bar(L.full2 + (k % S2) * 8), (k / S2) & 1, 100000000ull);
+            for (uint32_t k = it3 > S3 ? it3 - S3 : 0; k < it3; ++k)
+                mbar_wait(bar(L.full3 + (k % S3) * 8), (k / S3) & 1, 100000000ull);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        uint32_t it = 0, tcount = 0, g = 0;
-        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
-            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
-            if (!mi.ok) continue;
-            const int rp = mi.rp;
-            const uint32_t id_shrink = idesc_bf16(128, rp, 0, 0);
-            const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
-            for (int kc = 0; kc < n_kc && ok; ++kc) {
-                const uint32_t s = it % S;
-                if (!mbar_wait(bar(L.full + s * 8), (it / S) & 1, kWaitLimitNs)) { ok = false; break; }
+        uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0;
+        MmaItem cur, nxt;
+        uint32_t item = mma_next_ok(p, tiles, n_tiles, blockIdx.x, total, lane, cur);
+        int kc_next = 0;   // shrink chunks of `nxt` already issued
+        // shrink of the first tile
+        if (item < total) {
+            const uint32_t id_shrink = idesc_bf16(128, cur.rp, 0, 0);
+            for (int kc = 0; kc < n_kc && ok; ++kc, ++it1) {
+                const uint32_t s = it1 % S1;
+                if (!mbar_wait(bar(L.full1 + s * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t st = bar(L.ring + s * p.stage_bytes);
-#pragma unroll
-                    for (int kk = 0; kk < kMmaKChunk / 16; ++kk) {
-                        const uint64_t da = smem_desc(st + kk * 32, 16, 1024, 2);
-                        const uint64_t db = smem_desc(st + 16384 + kk * 32, 16, 1024, 2);
-                        tc_mma_f16(tmem + kD1Col, da, db, id_shrink, (kc | kk) != 0);
-                    }
-                    tc_commit(bar(L.empty + s * 8));
+                    mma_shrink_chunk(tmem, bar(L.ring1 + s * p.s1_bytes), id_shrink, kc);
+                    tc_commit(bar(L.empty1 + s * 8));
                 }
                 __syncwarp();
-                ++it;
+            }
+            if (lane == 0) tc_commit(bar(L.d1_full));
+            __syncwarp();
+        }
+        while (item < total && ok) {
+            const uint32_t next_item = mma_next_ok(p, tiles, n_tiles, item + gridDim.x, total, lane, nxt);
+            const bool has_next = next_item < total;
+            const uint32_t id_next = has_next ? idesc_bf16(128, nxt.rp, 0, 0) : 0;
+            kc_next = 0;
+            // D1 is free once this tile's convert has read it
+            if (!mbar_wait(bar(L.t_ready), tcount & 1, kWaitLimitNs)) { ok = false; break; }
+            ++tcount;
+            tc_fence_after();
+            const int rp = cur.rp;
+            const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
+            for (int nt = 0; nt < n_nt && ok; ++nt, ++g, ++it2) {
+                const uint32_t s = it2 % S2;
+                const uint32_t b = g & 1;
+                if (!mbar_wait(bar(L.full2 + s * 8), (it2 / S2) & 1, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(bar(L.d2_empty + b * 8), ((g >> 1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t st = bar(L.ring2 + s * p.s2_bytes);
+                    const uint32_t d2 = tmem + kD2Col + b * kMmaNTile;
+                    for (int ks = 0; ks < rp / 16; ++ks) {
+                        const uint64_t dbt = smem_desc(st + ks * 4096, 1024, 2048, 2);
+                        tc_mma_f16_ts(d2, tmem + kThiCol + ks * 8, dbt, id_expand, ks != 0);
+                        tc_mma_f16_ts(d2, tmem + kTloCol + ks * 8, dbt, id_expand, 1);
+                    }
+                    tc_commit(bar(L.empty2 + s * 8));
+                    tc_commit(bar(L.d2_full + b * 8));
+                }
+                __syncwarp();
+                // the next tile's shrink chunks that have already landed
+                while (has_next && kc_next < n_kc) {
+                    const uint32_t s1 = it1 % S1;
+                    if (!mbar_try_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
+                        tc_commit(bar(L.empty1 + s1 * 8));
+                    }
+                    __syncwarp();
+                    ++kc_next;
+                    ++it1;
+                }
+            }
+            if (!ok || !has_next) break;
+            // the rest of the next tile's shrink
+            for (; kc_next < n_kc && ok; ++kc_next, ++it1) {
+                const uint32_t s1 = it1 % S1;
+                if (!mbar_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
+                    tc_commit(bar(L.empty1 + s1 * 8));
+                }
+                __syncwarp();
             }
             if (!ok) break;
             if (lane == 0) tc_commit(bar(L.d1_full));
             __syncwarp();
-            if (!mbar_wait(bar(L.t_ready), tcount & 1, kWaitLimitNs)) { ok = false; break; }
-            ++tcount;
-            tc_fence_after();
-            for (int nt = 0; nt < n_nt && ok; ++nt, ++g) {
-                const uint32_t s = it % S;
-                const uint32_t b = g & 1;
-                if (!mbar_wait(bar(L.full + s * 8), (it / S) & 1, kWaitLimitNs)) { ok = false; break; }
-                if (!mbar_wait(bar(L.d2_empty + b * 8), ((g >> 1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t st = bar(L.ring + s * p.stage_bytes);
-                    const uint32_t d2 = tmem + kD2Col + b * kMmaNTile;
-                    const uint32_t sbo_t = (uint32_t)(rp / 8) * 128;
-                    for (int ks = 0; ks < rp / 16; ++ks) {
-                        const uint64_t dbt = smem_desc(st + ks * 4096, 1024, 2048, 2);
-                        const uint64_t dhi = smem_desc(bar(L.thi) + ks * 256, 128, sbo_t, 0);
-                        const uint64_t dlo = smem_desc(bar(L.tlo) + ks * 256, 128, sbo_t, 0);
-                        tc_mma_f16(d2, dhi, dbt, id_expand, ks != 0);
-                        tc_mma_f16(d2, dlo, dbt, id_expand, 1);
-                    }
-                    tc_commit(bar(L.empty + s * 8));
-                    tc_commit(bar(L.d2_full + b * 8));
-                }
-                __syncwarp();
-                ++it;
-            }
+            cur = nxt;
+            item = next_item;
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
         // every MMA issued by this thread must be complete before TMEM is freed
@@ -308,7 +400,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ convert + epilogue
-        const int e = warp - 2;                 // 0..7
+        const int e = warp - 3;                 // 0..7
         const int quad = warp & 3;              // TMEM lanes 32 quad .. 32 quad + 31
         const int half = e >> 2;                // column half of each slice
         const int m = quad * 32 + lane;         // tile row of this thread
@@ -323,11 +415,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             const bool live = m < rows;
             const bool block_full = quad * kMmaRowBlock + kMmaRowBlock <= rows;
             const bool block_part = !block_full && quad * kMmaRowBlock < rows;
-            // ---- convert D1 -> T_hi, T_lo (K-major, no swizzle: core matrices of 8 rows x 16 B,
-            //      +128 B per 8 columns, +(rp / 8) * 128 B per 8 rows)
+            // ---- convert D1 -> T_hi, T_lo in TMEM (bf16 pairs, column c / 2 holds k = c, c + 1)
             if (!mbar_wait(bar(L.d1_full), tcount & 1, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sbo_t = (uint32_t)(rp / 8) * 128;
             // the rp / 16 column chunks of D1 are split between the two warpgroups
             const int nck = rp / 16;
             const int ck_begin = half ? (nck + 1) / 2 : 0, ck_end = half ? nck : (nck + 1) / 2;
@@ -345,14 +435,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                     hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
                     lo[i] = *reinterpret_cast<const uint32_t*>(&l2);
                 }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint32_t off = (m >> 3) * sbo_t + ((c0 >> 3) + q) * 128 + (m & 7) * 16;
-                    *reinterpret_cast<uint4*>(base + L.thi + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-                    *reinterpret_cast<uint4*>(base + L.tlo + off) = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-                }
+                tmem_st8(tmem + lane_base + kThiCol + c0 / 2, hi);
+                tmem_st8(tmem + lane_base + kTloCol + c0 / 2, lo);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L.t_ready));
@@ -360,7 +446,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             // ---- expand epilogue over the column slices: y (in the y ring) += D2
             for (int nt = 0; nt < n_nt; ++nt, ++g) {
                 const uint32_t b = g & 1;
-                const uint32_t ys = g % kMmaYStages;
+                const uint32_t ys = g % S3;
                 if (!mbar_wait(bar(L.d2_full + b * 8), (g >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 float acc[64];
@@ -375,9 +461,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L.d2_empty + b * 8));
-                if (!mbar_wait(bar(L.yfull + ys * 8), (g / kMmaYStages) & 1, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(bar(L.full3 + ys * 8), (g / S3) & 1, kWaitLimitNs)) { ok = false; break; }
                 // this warp's box: rows 32 quad .. +31 of column half `half` (128-byte swizzle)
-                unsigned char* yrow = base + L.yring + ys * 32768 + half * 16384 + m * 128;
+                unsigned char* yrow = base + L.ring3 + ys * 32768 + half * 16384 + m * 128;
                 if (live) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -398,19 +484,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                 if (block_full) {
                     if (lane == 0) {
                         tma_store_2d(&p.y_map[mi.pr], col, row0 + quad * kMmaRowBlock,
-                                     smem_addr(base + L.yring + ys * 32768 + half * 16384 + quad * 4096));
-                        bulk_commit();
-                        bulk_wait_read0();
+                                     smem_addr(base + L.ring3 + ys * 32768 + half * 16384 + quad * 4096));
                         stored = true;
                     }
                 } else if (block_part && live) {
                     tma_store_2d(&p.y1_map[mi.pr], col, row0 + m, smem_addr(yrow));
-                    bulk_commit();
-                    bulk_wait_read0();
                     stored = true;
                 }
+                // one commit group per slice; the slot of the previous slice is released
+                // once its stores have read shared memory, so a store overlaps the next slice
+                bulk_commit();
+                bulk_wait_read1();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L.yempty + ys * 8));
+                if (lane == 0 && g > 0) mbar_arrive(bar(L.empty3 + ((g - 1) % S3) * 8));
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
