@@ -334,8 +334,11 @@ def run_ours(args, rank: int, world: int, local: int):
     peaks = measured_peaks()
     kern_avg = statistics.mean(kern)
     achieved = m["bytes"] / kern_avg / 1e9
-    kname = "bgmv_ring_kernel"
-    traffic = ncu_traffic(kname, wl.name, m["bytes"])
+    # the delta launches of the step: the CUDA-core kernel for decode batches, the tensor-core
+    # kernel (plus the CUDA-core one for short segments) for prefill and mixed batches
+    kname = {"decode": "bgmv_ring_kernel", "prefill": "sgmv_mma_kernel"}.get(
+        b.kind, "bgmv_ring_kernel+sgmv_mma_kernel")
+    traffic = ncu_traffic(kname, wl.name, m["bytes"]) if kname in KERNEL_SOURCES else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "kernel": kname, "kernel_ms": kern_avg * 1e3,
@@ -574,7 +577,25 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
         kern_ms.append(k0.elapsed_time(k1))
     torch.cuda.synchronize()
     err = lora.get_device_error(ws, stream_obj.cuda_stream)
+    # the same copy path with nothing else running: stage 64 resident slices into free pages
+    iso = None
+    victims = [v for v in list(cache.lru)[:64]]
+    if victims and cache.host is not None:
+        rows = np.concatenate([np.arange(cache.slice_off[v], cache.slice_off[v] + cache.spp[v]) for v in victims])
+        free = np.array(cache.free[-rows.size:], np.int32) if len(cache.free) >= rows.size else None
+        if free is not None:
+            src = cache.host[torch.from_numpy(rows)].pin_memory()
+            dst_t = torch.from_numpy(free).pin_memory()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for rep in range(3):
+                e0.record(side)
+                lora.stage_pages(pool, src, dst_t, free.size, None, None, None, 0, side.cuda_stream)
+                e1.record(side)
+                e1.synchronize()
+            iso = {"bytes": int(free.size) * p.h * 2, "ms": e0.elapsed_time(e1),
+                   "gbs": free.size * p.h * 2 / (e0.elapsed_time(e1) * 1e6)}
     return {"steps": len(wl_steps), "kernel_ms_median": statistics.median(kern_ms),
+            "isolated_stage": iso,
             "stage_ms_median": statistics.median(stage_ms) if stage_ms else 0.0,
             "stage_bytes_median": statistics.median(stage_bytes) if stage_bytes else 0,
             "stage_gbs_median": (statistics.median([b / (t * 1e6) for b, t in zip(stage_bytes, stage_ms)])

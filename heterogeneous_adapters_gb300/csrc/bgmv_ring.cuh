@@ -48,7 +48,8 @@ struct StageMeta {
 };
 static_assert(sizeof(StageMeta) == 48, "stage meta size");
 
-struct RingParams {
+template <int MAXP>
+struct RingParamsT {
     PoolView pool;
     char* ws;
     float* t_out;
@@ -56,8 +57,9 @@ struct RingParams {
     int32_t stages;        // ring depth
     int32_t stage_bytes;   // kRingPages * 2h
     int32_t pad;
-    ProbDesc probs[LORA_MAX_PROBLEMS_PER_LAUNCH];
+    ProbDesc probs[MAXP];
 };
+using RingParams = RingParamsT<LORA_MAX_PROBLEMS_PER_LAUNCH>;
 
 // Dynamic shared memory layout (offsets from a 1024-byte aligned base).
 struct RingSmem {
@@ -158,8 +160,8 @@ __device__ __forceinline__ bool consumer_barrier(unsigned char* base, const Ring
     return ok;
 }
 
-template <int NV, int NT, int CW>
-__device__ bool ring_consume_item(const RingParams& p, unsigned char* base, const RingSmem& L,
+template <int NV, int NT, int CW, class P>
+__device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSmem& L,
                                   uint32_t& it, uint32_t& bphase, const StageMeta& mx, int c) {
     const int h = p.pool.h, h8 = h >> 3;
     const int row_bytes = h * 2;
@@ -257,12 +259,12 @@ __device__ bool ring_consume_item(const RingParams& p, unsigned char* base, cons
     return consumer_barrier(base, L, bphase);
 }
 
+// One CTA of the ring kernel: CTA `cta` of `ncta` taking part (threads beyond the
+// producer and the CW consumer warps only join the initial barrier).
 // NV: 16-byte column vectors per consumer thread; CW: consumer warps (h = 8 * 32 * CW * NV
 // or less).
-template <int NV, int CW>
-__global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
-    extern __shared__ __align__(1024) unsigned char ring_smem_raw[];
-    unsigned char* base = ring_smem_raw;
+template <int NV, int CW, class P>
+__device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32_t cta, uint32_t ncta) {
     const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max, CW);
     const int S = p.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -286,13 +288,13 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid
         // mix and the last round is made of the smallest items).  The metadata of the next
         // items is loaded while the current one streams: the chunk two items ahead, the
         // page ids one item ahead.
-        const PoolView& P = p.pool;
+        const PoolView& PV = p.pool;
         const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
         const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
         int32_t* pgbuf = reinterpret_cast<int32_t*>(base + L.pgbuf);
         const uint32_t total = (uint32_t)hdr->counts[2] * (uint32_t)p.nprob;
-        const uint32_t row_bytes = (uint32_t)P.h * 2;
-        const uint32_t G = gridDim.x;
+        const uint32_t row_bytes = (uint32_t)PV.h * 2;
+        const uint32_t G = ncta;
         constexpr int kPg = 2 * LORA_MAX_RANK / 32;   // page ids per lane
         uint32_t it = 0;
         bool ok = true;
@@ -306,10 +308,10 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid
 #pragma unroll
             for (int k = 0; k < kPg; ++k) {
                 const int e = lane + 32 * k;
-                pg[k] = e < 2 * c.rank ? P.pt[blk + e] : 0;
+                pg[k] = e < 2 * c.rank ? PV.pt[blk + e] : 0;
             }
         };
-        uint32_t item = blockIdx.x;
+        uint32_t item = cta;
         Chunk c_next, c_next2;
         int32_t pg_next[kPg];
         if (item < total) {
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid
             for (int k = 0; k < kPg; ++k) {
                 const int e = lane + 32 * k;
                 if (e < 2 * r) {
-                    bad |= (pg[k] < 0 || pg[k] >= P.num_pages);
+                    bad |= (pg[k] < 0 || pg[k] >= PV.num_pages);
                     pgbuf[e] = pg[k];
                 }
             }
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid
                     if (lane < np) {
                         const int page = pgbuf[ab * r + j0 + lane];
                         bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
-                                 P.pages + (long long)page * P.h, row_bytes, smem_addr(base + L.full + s * 8));
+                                 PV.pages + (long long)page * PV.h, row_bytes, smem_addr(base + L.full + s * 8));
                     }
                     ++it;
                 }
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid
             for (uint32_t k = first; k < it; ++k)
                 mbar_wait(smem_addr(base + L.full + (k % S) * 8), (k / S) & 1, 100000000ull);
         }
-    } else {
+    } else if (tid < CW * 32 + 32) {
         // ------------------------------------------------------------------ consumers
         const int c = tid - 32;
         uint32_t it = 0, bphase = 0;
@@ -435,17 +437,23 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid
             }
             bool ok;
             if (mx.count == 1)
-                ok = ring_consume_item<NV, 1, CW>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 1, CW, P>(p, base, L, it, bphase, mx, c);
             else if (mx.count == 2)
-                ok = ring_consume_item<NV, 2, CW>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 2, CW, P>(p, base, L, it, bphase, mx, c);
             else
-                ok = ring_consume_item<NV, kChunk, CW>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, kChunk, CW, P>(p, base, L, it, bphase, mx, c);
             if (!ok) {
                 if (c == 0) set_error(&hdr->err, kDerrTimeout);
                 break;
             }
         }
     }
+}
+
+template <int NV, int CW>
+__global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
+    extern __shared__ __align__(1024) unsigned char ring_smem_raw[];
+    ring_cta<NV, CW>(p, ring_smem_raw, blockIdx.x, gridDim.x);
 }
 
 }  // namespace lora

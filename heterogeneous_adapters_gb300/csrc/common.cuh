@@ -20,7 +20,8 @@ struct WsHeader {
     uint32_t work_counter2;  // second queue (tensor-core items)
     int32_t cap_tokens;      // layout of the arrays below the header (set by grouping)
     int32_t cap_segments;
-    uint32_t pad[54];
+    unsigned long long weight[2];   // bytes one projection streams: CUDA-core, tensor-core class
+    uint32_t pad[50];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

@@ -1,0 +1,44 @@
+// One delta launch for a batch that holds both work classes (prefill segments long enough
+// for the tensor cores, and decode tokens / short segments for the CUDA-core ring).
+//
+// "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "What the engine does each
+// step": a continuous-batching step mixes requests in prefill and in decode; SGMV suits
+// the former and BGMV the latter.  Here both run in the same persistent grid: the CTAs
+// are split between the two bodies in proportion to the bytes each class streams per
+// projection (weights written by the grouping kernel), so the two HBM streams proceed
+// side by side and end together instead of one after the other.
+#pragma once
+#include "bgmv_ring.cuh"
+#include "sgmv_mma.cuh"
+
+namespace lora {
+
+struct FusedParams {
+    MmaParams mma;
+    RingParamsT<kMmaMaxProbs> ring;
+};
+
+// CTAs given to the CUDA-core class out of G (0 if it has no work, G if the tensor-core
+// class has none; otherwise at least one each).
+__device__ __forceinline__ uint32_t fused_split(const WsHeader* hdr, uint32_t G) {
+    const unsigned long long wf = hdr->weight[0], wm = hdr->weight[1];
+    if (wm == 0) return G;
+    if (wf == 0) return 0;
+    uint32_t gf = (uint32_t)((double)G * (double)wf / ((double)wf + (double)wm) + 0.5);
+    if (gf < 1) gf = 1;
+    if (gf > G - 1) gf = G - 1;
+    return gf;
+}
+
+template <int NV, int CW>
+__global__ void __launch_bounds__(kMmaThreads, 1) delta_fused_kernel(const __grid_constant__ FusedParams p) {
+    static_assert(CW * 32 + 32 <= kMmaThreads, "ring body must fit the fused CTA");
+    extern __shared__ __align__(1024) unsigned char fused_smem_raw[];
+    const uint32_t gf = fused_split(reinterpret_cast<const WsHeader*>(p.mma.ws), gridDim.x);
+    if (blockIdx.x < gf)
+        ring_cta<NV, CW>(p.ring, fused_smem_raw, blockIdx.x, gf);
+    else
+        mma_cta(p.mma, fused_smem_raw, blockIdx.x - gf, gridDim.x - gf);
+}
+
+}  // namespace lora

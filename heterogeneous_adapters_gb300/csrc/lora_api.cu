@@ -15,6 +15,7 @@
 #include "bgmv_ring.cuh"
 #include "common.cuh"
 #include "fma_delta.cuh"
+#include "fused.cuh"
 #include "segment.cuh"
 #include "sgmv_mma.cuh"
 #include "stage.cuh"
@@ -246,68 +247,150 @@ lora_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return LORA_OK;
 }
 
+// Shared-memory plan of the tensor-core kernel for this pool.
+struct MmaConfig {
+    int rp_max, s1, s2, s3, s1_bytes, s2_bytes;
+    size_t smem;
+};
+
+lora_status mma_config(const lora_pool_desc& d, int smem_optin, MmaConfig* c) {
+    c->rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
+    c->s1_bytes = (16384 + c->rp_max * 128 + 1023) / 1024 * 1024;   // x chunk + A chunk
+    c->s2_bytes = (c->rp_max * 256 + 1023) / 1024 * 1024;           // B^T slice
+    // the deepest y ring (<= 4) that leaves the shrink ring two stages (the shrink of the
+    // next tile runs under the expand of this one and needs little depth), B^T ring of 2
+    c->s2 = 2;
+    for (c->s3 = 4; c->s3 >= 2; --c->s3) {
+        for (c->s1 = kMmaMaxStages; c->s1 >= 2; --c->s1) {
+            c->smem = mma_smem_layout(c->s1, c->s1_bytes, c->s2, c->s2_bytes, c->s3).total + 1024;
+            if (c->smem <= (size_t)smem_optin) break;
+        }
+        if (c->s1 >= 2) break;
+    }
+    return c->s1 < 2 ? LORA_ETOOBIG : LORA_OK;
+}
+
+lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, int32_t T,
+                     void* ws, const MmaConfig& c) {
+    const lora_pool_desc& d = pool->d;
+    memset(&prm, 0, sizeof prm);
+    lora_status st = make_map(&prm.pool_map, d.pages, (uint64_t)d.h, (uint64_t)d.num_pages, (uint64_t)d.h, 1);
+    if (st != LORA_OK) return st;
+    for (int32_t i = 0; i < n; ++i) {
+        const lora_problem& pr = probs[i];
+        st = make_map(&prm.x_map[i], pr.x, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldx, kMmaRowBlock);
+        if (st != LORA_OK) return st;
+        st = make_map(&prm.y_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, kMmaRowBlock);
+        if (st != LORA_OK) return st;
+        st = make_map(&prm.y1_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, 1);
+        if (st != LORA_OK) return st;
+        prm.blk[i] = pr.layer * d.num_proj + pr.proj;
+    }
+    prm.pool = view_of(pool);
+    prm.ws = reinterpret_cast<char*>(ws);
+    prm.nprob = n;
+    prm.s1 = c.s1;
+    prm.s2 = c.s2;
+    prm.s3 = c.s3;
+    prm.s1_bytes = c.s1_bytes;
+    prm.s2_bytes = c.s2_bytes;
+    prm.rp_max = c.rp_max;
+    return LORA_OK;
+}
+
+template <int MAXP>
+void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, void* ws,
+               float* t_out, int stages) {
+    const lora_pool_desc& d = pool->d;
+    memset(&prm, 0, sizeof prm);
+    prm.pool = view_of(pool);
+    prm.ws = reinterpret_cast<char*>(ws);
+    prm.t_out = t_out;
+    prm.nprob = n;
+    prm.stages = stages;
+    prm.stage_bytes = kRingPages * 2 * d.h;
+    for (int32_t i = 0; i < n; ++i) {
+        const lora_problem& pr = probs[i];
+        prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
+        prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
+        prm.probs[i].ldx = (int32_t)pr.ldx;
+        prm.probs[i].ldy = (int32_t)pr.ldy;
+        prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
+    }
+}
+
+// Balanced batches of at most `cap` problems (no short last launch).
+int32_t batch_size(int32_t nprob, int32_t cap) {
+    const int32_t nb = (nprob + cap - 1) / cap;
+    return (nprob + nb - 1) / nb;
+}
+
 lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
                     cudaStream_t stream) {
-    const lora_pool_desc& d = pool->d;
     if (T <= 0 || nprob <= 0) return LORA_OK;
     DeviceInfo* di = nullptr;
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
+    MmaConfig c;
+    st = mma_config(pool->d, di->smem_optin, &c);
+    if (st != LORA_OK) return st;
     static thread_local MmaParams prm;
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
-    const int rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
-    const int s1_bytes = (16384 + rp_max * 128 + 1023) / 1024 * 1024;   // x chunk + A chunk
-    const int s2_bytes = (rp_max * 256 + 1023) / 1024 * 1024;           // B^T slice
-    // y ring of 3 when the shrink ring still gets 3 stages, else 2; B^T ring of 2
-    int s1 = 0, s3 = 3;
-    const int s2 = 2;
-    size_t smem = 0;
-    for (; s3 >= 2; --s3) {
-        for (s1 = kMmaMaxStages; s1 >= 2; --s1) {
-            smem = mma_smem_layout(s1, s1_bytes, s2, s2_bytes, s3).total + 1024;
-            if (smem <= (size_t)di->smem_optin) break;
-        }
-        if (s1 >= 3 || s3 == 2) break;
-    }
-    if (s1 < 2) return LORA_ETOOBIG;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (attr_dev != dev || attr_smem < smem) {
+    if (attr_dev != dev || attr_smem < c.smem) {
         st = cuda_status(cudaFuncSetAttribute(sgmv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)smem));
+                                              (int)c.smem));
+        if (st != LORA_OK) return st;
+        attr_dev = dev;
+        attr_smem = c.smem;
+    }
+    const int32_t per = batch_size(nprob, kMmaMaxProbs);
+    for (int32_t base = 0; base < nprob; base += per) {
+        const int32_t n = nprob - base < per ? nprob - base : per;
+        st = fill_mma(prm, pool, probs + base, n, T, ws, c);
+        if (st != LORA_OK) return st;
+        sgmv_mma_kernel<<<di->sm_count, kMmaThreads, c.smem, stream>>>(prm);
+        st = cuda_status(cudaGetLastError());
+        if (st != LORA_OK) return st;
+    }
+    return LORA_OK;
+}
+
+// Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0).
+template <int NV, int CW>
+lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                         cudaStream_t stream) {
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    MmaConfig c;
+    st = mma_config(pool->d, di->smem_optin, &c);
+    if (st != LORA_OK) return st;
+    size_t ring_smem = 0;
+    const int S = ring_stages(di->smem_optin, kRingPages * 2 * pool->d.h, pool->d.r_max, CW, &ring_smem);
+    if (S < 2) return LORA_ETOOBIG;
+    const size_t smem = c.smem > ring_smem ? c.smem : ring_smem;
+    static thread_local FusedParams prm;
+    static thread_local int attr_dev = -1;
+    static thread_local size_t attr_smem = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto kern = delta_fused_kernel<NV, CW>;
+    if (attr_dev != dev || attr_smem < smem) {
+        st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         if (st != LORA_OK) return st;
         attr_dev = dev;
         attr_smem = smem;
     }
-    // balanced launches of at most kMmaMaxProbs problems (no short last launch)
-    const int32_t nlaunch = (nprob + kMmaMaxProbs - 1) / kMmaMaxProbs;
-    const int32_t per = (nprob + nlaunch - 1) / nlaunch;
+    const int32_t per = batch_size(nprob, kMmaMaxProbs);
     for (int32_t base = 0; base < nprob; base += per) {
         const int32_t n = nprob - base < per ? nprob - base : per;
-        memset(&prm, 0, sizeof prm);
-        st = make_map(&prm.pool_map, d.pages, (uint64_t)d.h, (uint64_t)d.num_pages, (uint64_t)d.h, 1);
+        st = fill_mma(prm.mma, pool, probs + base, n, T, ws, c);
         if (st != LORA_OK) return st;
-        for (int32_t i = 0; i < n; ++i) {
-            const lora_problem& pr = probs[base + i];
-            st = make_map(&prm.x_map[i], pr.x, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldx, kMmaRowBlock);
-            if (st != LORA_OK) return st;
-            st = make_map(&prm.y_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, kMmaRowBlock);
-            if (st != LORA_OK) return st;
-            st = make_map(&prm.y1_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, 1);
-            if (st != LORA_OK) return st;
-            prm.blk[i] = pr.layer * d.num_proj + pr.proj;
-        }
-        prm.pool = view_of(pool);
-        prm.ws = reinterpret_cast<char*>(ws);
-        prm.nprob = n;
-        prm.s1 = s1;
-        prm.s2 = s2;
-        prm.s3 = s3;
-        prm.s1_bytes = s1_bytes;
-        prm.s2_bytes = s2_bytes;
-        prm.rp_max = rp_max;
-        sgmv_mma_kernel<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
+        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, S);
+        kern<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
         st = cuda_status(cudaGetLastError());
         if (st != LORA_OK) return st;
     }
@@ -366,6 +449,14 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
                       float* t_out, bool with_mma, cudaStream_t stream) {
     lora_status st = check_problems(pool->d, probs, nprob);
     if (st != LORA_OK) return st;
+    const int h8 = pool->d.h / 8;
+    if (with_mma && mma_min_rows(pool->d) > 0 && !use_legacy_fma() && t_out == nullptr && h8 <= 640 &&
+        T > 0) {
+        // one launch per batch of projections for both work classes
+        if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
+        if (h8 <= 512) return launch_fused<2, 8>(pool, probs, nprob, T, ws, stream);
+        return launch_fused<2, 10>(pool, probs, nprob, T, ws, stream);
+    }
     st = use_legacy_fma() ? run_delta_direct(pool, probs, nprob, ws, t_out, stream)
                           : run_delta_ring(pool, probs, nprob, ws, t_out, stream);
     if (st != LORA_OK) return st;

@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     __shared__ int scan_smem[33];
     __shared__ long long key_tile[kKeyTile];
     __shared__ int n_adapted_s;
+    __shared__ unsigned long long weight_s[2];
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
@@ -89,7 +90,10 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     const long long kNone = 0x7fffffffffffffffLL;
 
     const int n = p.S + p.Td;
-    if (tid == 0) n_adapted_s = 0;
+    if (tid == 0) {
+        n_adapted_s = 0;
+        weight_s[0] = weight_s[1] = 0;
+    }
     __syncthreads();
     const int dec_base = p.S > 0 ? p.seg_start[p.S] : 0;
 
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
                 gfirst[e_g] = q;
             }
             const int r = P.ranks[a];
+            if (ntile > 0)   // x read + y read and write, plus the pages once per tile
+                atomicAdd(&weight_s[1], (unsigned long long)P.h * 2 * (3ull * len + 2ull * r * ntile));
             for (int k = 0; k < ntile; ++k) {
                 Tile tl;
                 tl.adapter = a;
@@ -265,6 +271,8 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
             const int r = P.ranks[a];
             const float sc = P.scales[a];
             const long long ptb = P.pt_off[a];
+            if (nch > 0)     // rows read and written, plus the pages once per chunk
+                atomicAdd(&weight_s[0], (unsigned long long)P.h * 2 * (3ull * cnt + 2ull * r * nch));
             for (int c = 0; c < nch; ++c) {
                 Chunk ch;
                 ch.adapter = a;
@@ -290,6 +298,11 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
         hdr->done_counter = 0;
         hdr->cap_tokens = p.L_tokens;
         hdr->cap_segments = p.L_segments;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        hdr->weight[0] = weight_s[0];
+        hdr->weight[1] = weight_s[1];
     }
 }
 

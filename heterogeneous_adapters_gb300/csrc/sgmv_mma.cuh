@@ -18,10 +18,10 @@
 //           double-buffered in TMEM so the epilogue of one slice overlaps the MMA of the
 //           next; the epilogue adds D2 to y (fp32) and stores bf16 rows of the tile.
 // Roles (one persistent CTA per SM, items dealt round-robin): warp 0 streams the shrink
-// operands (x and A chunks), warp 2 the expand operands (B^T slices and y tiles), warp 1
-// owns TMEM and issues the MMAs -- while it expands tile k it also issues tile k+1's
-// shrink chunks as they land, so the x stream of the next tile overlaps the y stream of
-// this one -- and warps 3-10 convert D1 and run the epilogue.  T lives in TMEM.
+// operands (x and A chunks), warp 2 the B^T slices, warp 3 the y tiles, warp 1 owns TMEM
+// and issues the MMAs -- while it expands tile k it also issues tile k+1's shrink chunks
+// as they land, so the x stream of the next tile overlaps the y stream of this one -- and
+// warps 4-11 convert D1 and run the epilogue.  T lives in TMEM.
 // All waits are bounded; a timeout sets an error bit and the CTA unwinds.
 #pragma once
 #include <cuda.h>
@@ -32,7 +32,7 @@
 
 namespace lora {
 
-constexpr int kMmaThreads = 352;
+constexpr int kMmaThreads = 384;
 constexpr int kMmaEpiWarps = 8;
 constexpr int kMmaMaxProbs = 64;            // problems per launch (3 tensor maps each)
 constexpr int kMmaMaxRank = 128;
@@ -119,8 +119,9 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
 
 // The next processable item at or after `item` (skipping items with bad pages), or total.
 __device__ __forceinline__ uint32_t mma_next_ok(const MmaParams& p, const Tile* tiles, int n_tiles,
-                                                uint32_t item, uint32_t total, int lane, MmaItem& mi) {
-    for (; item < total; item += gridDim.x) {
+                                                uint32_t item, uint32_t total, uint32_t ncta, int lane,
+                                                MmaItem& mi) {
+    for (; item < total; item += ncta) {
         mi = mma_item(p, tiles, n_tiles, item, lane);
         if (mi.ok) return item;
     }
@@ -137,11 +138,11 @@ __device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t st, uin
     }
 }
 
-__global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
-    extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
+// One CTA of the tensor-core kernel: CTA `cta` of `ncta` taking part (all kMmaThreads threads).
+__device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_raw, uint32_t cta, uint32_t ncta) {
     // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
     unsigned char* base = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(mma_smem_raw) + 1023) & ~uintptr_t(1023));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const MmaSmem L = mma_smem_layout(p.s1, p.s1_bytes, p.s2, p.s2_bytes, p.s3);
     const uint32_t S1 = p.s1, S2 = p.s2, S3 = p.s3;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
         // ------------------------------------------------------------------ shrink producer
         if (lane == 0) prefetch_tmap(&p.pool_map);
         uint32_t it = 0;
-        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        for (uint32_t item = cta; item < total && ok; item += ncta) {
             const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
             if (!mi.ok) {
                 if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
@@ -244,26 +245,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                 mbar_wait(bar(L.full1 + (k % S1) * 8), (k / S1) & 1, 100000000ull);
         }
     } else if (warp == 2) {
-        // ------------------------------------------------------------------ expand producer
-        uint32_t it2 = 0, it3 = 0;
-        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        // ------------------------------------------------------------------ B^T producer
+        uint32_t it2 = 0;
+        for (uint32_t item = cta; item < total && ok; item += ncta) {
             const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
-            const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
-            const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
-            const void* ymap = &p.y_map[mi.pr];
+            const int r = mi.tile.rank, rp = mi.rp;
             int pgb[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = lane + 32 * q;
                 pgb[q] = j < r ? p.pool.pt[mi.blk + r + j] : (int)p.pool.num_pages;
             }
-            for (int nt = 0; nt < n_nt; ++nt) {
+            for (int nt = 0; nt < n_nt; ++nt, ++it2) {
                 // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
                 // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
-                uint32_t s = it2 % S2;
+                const uint32_t s = it2 % S2;
                 if (!mbar_wait(bar(L.empty2 + s * 8), ((it2 / S2) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                uint32_t st = bar(L.ring2 + s * p.s2_bytes);
+                const uint32_t st = bar(L.ring2 + s * p.s2_bytes);
                 if (lane == 0) mbar_arrive_expect_tx(bar(L.full2 + s * 8), rp * 256);
                 __syncwarp();
 #pragma unroll
@@ -286,11 +285,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                         }
                     }
                 }
-                ++it2;
+            }
+        }
+        if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
+        if (lane == 0) {
+            for (uint32_t k = it2 > S2 ? it2 - S2 : 0; k < it2; ++k)
+                mbar_wait(bar(L.full2 + (k % S2) * 8), (k / S2) & 1, 100000000ull);
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------------ y producer
+        uint32_t it3 = 0;
+        for (uint32_t item = cta; item < total && ok; item += ncta) {
+            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            if (!mi.ok) continue;
+            const int row0 = mi.tile.row0;
+            const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
+            const void* ymap = &p.y_map[mi.pr];
+            for (int nt = 0; nt < n_nt; ++nt, ++it3) {
                 // y tile: half hf (64 columns) at hf * 16 KB, 32-row block b at + b * 4 KB
-                s = it3 % S3;
+                const uint32_t s = it3 % S3;
                 if (!mbar_wait(bar(L.empty3 + s * 8), ((it3 / S3) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                st = bar(L.ring3 + s * 32768);
+                const uint32_t st = bar(L.ring3 + s * 32768);
                 if (lane == 0) mbar_arrive_expect_tx(bar(L.full3 + s * 8), 2 * nblk * kMmaRowBlock * 128);
                 __syncwarp();
                 if (lane < 2 * nblk) {
@@ -298,13 +313,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
                     tma_load_2d(st + hf * 16384 + b * kMmaRowBlock * 128, ymap, nt * kMmaNTile + hf * 64,
                                 row0 + b * kMmaRowBlock, bar(L.full3 + s * 8));
                 }
-                ++it3;
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
         if (lane == 0) {
-            for (uint32_t k = it2 > S2 ? it2 - S2 : 0; k < it2; ++k)
-                mbar_wait(bar(L.full2 + (k % S2) * 8), (k / S2) & 1, 100000000ull);
             for (uint32_t k = it3 > S3 ? it3 - S3 : 0; k < it3; ++k)
                 mbar_wait(bar(L.full3 + (k % S3) * 8), (k / S3) & 1, 100000000ull);
         }
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
         // ------------------------------------------------------------------ MMA issuer
         uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0;
         MmaItem cur, nxt;
-        uint32_t item = mma_next_ok(p, tiles, n_tiles, blockIdx.x, total, lane, cur);
+        uint32_t item = mma_next_ok(p, tiles, n_tiles, cta, total, ncta, lane, cur);
         int kc_next = 0;   // shrink chunks of `nxt` already issued
         // shrink of the first tile
         if (item < total) {
@@ -331,7 +343,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
             __syncwarp();
         }
         while (item < total && ok) {
-            const uint32_t next_item = mma_next_ok(p, tiles, n_tiles, item + gridDim.x, total, lane, nxt);
+            const uint32_t next_item = mma_next_ok(p, tiles, n_tiles, item + ncta, total, ncta, lane, nxt);
             const bool has_next = next_item < total;
             const uint32_t id_next = has_next ? idesc_bf16(128, nxt.rp, 0, 0) : 0;
             kc_next = 0;
@@ -400,14 +412,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ convert + epilogue
-        const int e = warp - 3;                 // 0..7
+        const int e = warp - 4;                 // 0..7
         const int quad = warp & 3;              // TMEM lanes 32 quad .. 32 quad + 31
         const int half = e >> 2;                // column half of each slice
         const int m = quad * 32 + lane;         // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint32_t tcount = 0, g = 0;
         bool stored = false;
-        for (uint32_t item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        for (uint32_t item = cta; item < total && ok; item += ncta) {
             const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
             const int rp = mi.rp, rows = mi.tile.rows, row0 = mi.tile.row0;
@@ -506,6 +518,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+__global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
+    extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
+    mma_cta(p, mma_smem_raw, blockIdx.x, gridDim.x);
 }
 
 }  // namespace lora
