@@ -11,7 +11,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(_PKG, "liblora.so")
 
 LORA_OK, LORA_EINVAL, LORA_EALIGN, LORA_EWORKSPACE, LORA_ETOOBIG, LORA_ECUDA, LORA_EDEVICE = range(7)
-DERR = {0x1: "adapter", 0x2: "rank", 0x4: "page-table block", 0x8: "page", 0x10: "segment"}
+DERR = {0x1: "adapter", 0x2: "rank", 0x4: "page-table block", 0x8: "page", 0x10: "segment",
+        0x20: "timeout"}
 LORA_MAX_PROBLEMS_PER_LAUNCH = 256
 LORA_MAX_SEGMENTS = 16384
 LORA_MAX_RANK = 256

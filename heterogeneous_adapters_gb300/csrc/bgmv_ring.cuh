@@ -31,7 +31,7 @@ namespace lora {
 constexpr int kRingMaxConsumerWarps = 16;
 constexpr int kRingPages = 4;              // pages (or x rows) per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
-constexpr uint32_t kDerrTimeout = 0x20u;
+constexpr uint32_t kDerrTimeout = LORA_DERR_TIMEOUT;
 
 enum StageKind : int32_t { kStageX = 0, kStageA = 1, kStageB = 2, kStageStop = 3, kStageSkip = 4 };
 

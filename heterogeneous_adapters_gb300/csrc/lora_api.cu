@@ -1,8 +1,8 @@
 // C ABI of liblora.so (declarations and contracts in include/lora.h).
 //
-// Host side: argument checks, workspace layout, launch configuration.  All compute
-// runs in the kernels of segment.cuh and fma_delta.cuh (and the tensor-core kernel
-// when present); nothing here touches adapter or activation values.
+// Host side: argument checks, workspace layout, launch configuration.  All compute runs in
+// the kernels of segment.cuh, bgmv_ring.cuh, sgmv_mma.cuh, fused.cuh and stage.cuh;
+// nothing here touches adapter or activation values.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -14,7 +14,6 @@
 
 #include "bgmv_ring.cuh"
 #include "common.cuh"
-#include "fma_delta.cuh"
 #include "fused.cuh"
 #include "segment.cuh"
 #include "sgmv_mma.cuh"
@@ -92,33 +91,6 @@ lora_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
     return LORA_OK;
 }
 
-// Launch the CUDA-core delta kernel for one group of <= LORA_MAX_PROBLEMS_PER_LAUNCH
-// problems.  The grid is persistent: (resident CTAs per SM) x (SM count).
-template <int NV, int JU>
-lora_status launch_fma(const DeltaParams& prm, size_t smem, cudaStream_t stream) {
-    static thread_local int attr_set_dev = -1;
-    static thread_local size_t attr_smem = 0;
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    auto kern = fma_delta_kernel<NV, JU>;
-    if (attr_set_dev != dev || attr_smem < smem) {
-        st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)smem));
-        if (st != LORA_OK) return st;
-        attr_set_dev = dev;
-        attr_smem = smem;
-    }
-    int per_sm = 0;
-    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFmaThreads, smem));
-    if (st != LORA_OK) return st;
-    if (per_sm < 1) per_sm = 1;
-    kern<<<per_sm * di->sm_count, kFmaThreads, smem, stream>>>(prm);
-    return cuda_status(cudaGetLastError());
-}
-
 // Ring depth that fits the opt-in shared memory of one CTA (at most 8 stages).
 int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* smem) {
     for (int S = 8; S >= 2; --S) {
@@ -153,11 +125,6 @@ lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
     }
     kern<<<di->sm_count, CW * 32 + 32, smem, stream>>>(prm);
     return cuda_status(cudaGetLastError());
-}
-
-bool use_legacy_fma() {
-    const char* e = getenv("LORA_DELTA_KERNEL");
-    return e != nullptr && strcmp(e, "direct") == 0;
 }
 
 lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
@@ -411,36 +378,6 @@ lora_status check_problems(const lora_pool_desc& d, const lora_problem* probs, i
     return LORA_OK;
 }
 
-lora_status run_delta_direct(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                             float* t_out, cudaStream_t stream) {
-    const lora_pool_desc& d = pool->d;
-    const size_t smem = fma_smem_bytes(d.r_max);
-    static thread_local DeltaParams prm;   // ~8 KiB: keep it off the stack
-    for (int32_t base = 0; base < nprob; base += LORA_MAX_PROBLEMS_PER_LAUNCH) {
-        const int32_t n = nprob - base < LORA_MAX_PROBLEMS_PER_LAUNCH ? nprob - base
-                                                                         : LORA_MAX_PROBLEMS_PER_LAUNCH;
-        memset(&prm, 0, sizeof prm);
-        prm.pool = view_of(pool);
-        prm.ws = reinterpret_cast<char*>(ws);
-        prm.t_out = t_out;
-        prm.nprob = n;
-        for (int32_t i = 0; i < n; ++i) {
-            const lora_problem& pr = probs[base + i];
-            prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
-            prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
-            prm.probs[i].ldx = (int32_t)pr.ldx;
-            prm.probs[i].ldy = (int32_t)pr.ldy;
-            prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
-        }
-        lora_status st;
-        if (d.h <= 4096)
-            st = launch_fma<1, 8>(prm, smem, stream);
-        else
-            st = launch_fma<2, 4>(prm, smem, stream);
-        if (st != LORA_OK) return st;
-    }
-    return LORA_OK;
-}
 
 
 // The delta launches after grouping: the CUDA-core kernel over the chunk list, then
@@ -450,15 +387,13 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     lora_status st = check_problems(pool->d, probs, nprob);
     if (st != LORA_OK) return st;
     const int h8 = pool->d.h / 8;
-    if (with_mma && mma_min_rows(pool->d) > 0 && !use_legacy_fma() && t_out == nullptr && h8 <= 640 &&
-        T > 0) {
+    if (with_mma && mma_min_rows(pool->d) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
         // one launch per batch of projections for both work classes
         if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
         if (h8 <= 512) return launch_fused<2, 8>(pool, probs, nprob, T, ws, stream);
         return launch_fused<2, 10>(pool, probs, nprob, T, ws, stream);
     }
-    st = use_legacy_fma() ? run_delta_direct(pool, probs, nprob, ws, t_out, stream)
-                          : run_delta_ring(pool, probs, nprob, ws, t_out, stream);
+    st = run_delta_ring(pool, probs, nprob, ws, t_out, stream);
     if (st != LORA_OK) return st;
     if (with_mma && mma_min_rows(pool->d) > 0) st = run_mma(pool, probs, nprob, T, ws, stream);
     return st;

@@ -44,7 +44,7 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns: D1 (shrink, fp32) 0..127, D2 (expand, fp32, two buffers) 128..383,
 // T_hi and T_lo (bf16 pairs, K / 2 columns each) 384..447 and 448..511.
 constexpr uint32_t kD1Col = 0, kD2Col = 128, kThiCol = 384, kTloCol = 448;
-constexpr uint32_t kDerrTimeoutMma = 0x20u;
+constexpr uint32_t kDerrTimeoutMma = LORA_DERR_TIMEOUT;
 
 struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
     CUtensorMap pool_map;                    // {h, num_pages}, box {64, 1}, 128B swizzle

@@ -37,9 +37,9 @@
  *                 base pointers.  y is updated in place.
  *
  * Numerics: bf16 products are exact in fp32; t = A x is accumulated in fp32 and
- * never rounded to bf16 before the expand (the tensor-core expand feeds t as an
- * exact two-term bf16 split of the fp32 value, see DESIGN notes in lora_sgmv); the
- * result is rounded to bf16 (round to nearest even) once, when y is stored.
+ * never rounded to a single bf16 before the expand (the tensor-core expand consumes
+ * each fp32 value as a bf16 pair hi + lo with |t - hi - lo| <= 2^-16 |t|); the result
+ * is rounded to bf16 (round to nearest even) once, when y is stored.
  *
  * Calls are asynchronous on the caller's stream (a cudaStream_t passed as void*;
  * NULL = legacy default stream) and never synchronise the host, except
@@ -47,7 +47,8 @@
  * launch nothing.  Data-dependent errors found on the device (a bad adapter id, a
  * rank out of range, a page id out of range, bad segment offsets) set bits of the
  * workspace's device error word and skip the offending group; the rest of the batch
- * is still computed.  No kernel traps or spins without a bound.
+ * is still computed.  No kernel traps or spins without a bound: every wait inside a
+ * kernel gives up after a time limit and reports LORA_DERR_TIMEOUT.
  *
  * Threading: a pool handle is read-only after creation and may be shared by calls
  * on different streams.  A workspace must not be used by two calls that may run
@@ -85,6 +86,8 @@ typedef enum {
 #define LORA_DERR_PTBLOCK 0x4u  /* adapter page-table block outside the table        */
 #define LORA_DERR_PAGE 0x8u     /* page id outside [0, num_pages)                    */
 #define LORA_DERR_SEGMENT 0x10u /* segment offsets decreasing or beyond the rows     */
+#define LORA_DERR_TIMEOUT 0x20u /* a kernel wait exceeded its time limit (2 s); the
+                                   kernel unwound and its outputs are incomplete      */
 
 /* Pool description: plain device pointers and sizes (copied by lora_pool_create). */
 typedef struct {

@@ -41,6 +41,7 @@ CASES = {
     "decode-zipf": lambda: small_decode(61, 256, 1, 1, 50, [4], 300),
     "decode-base": lambda: small_decode(62, 256, 1, 1, 7, [4], 500, base=True),
     "decode-large": lambda: small_decode(63, 256, 1, 1, 3000, [4], 5000),
+    "decode-max-segments": lambda: small_decode(66, 64, 1, 1, 20000, [1, 2], 16384, base=True),
     "prefill": lambda: small_prefill(64, 256, 1, 1, 9, [4], [3, 0, 200, 1, 77, 128, 129, 5]),
     "mixed": lambda: _mixed(65, 256, 1, 1, 40, [4, 8], [5, 260, 131, 1], 300, 30),
 }

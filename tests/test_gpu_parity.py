@@ -49,6 +49,10 @@ SMALL = {
     "decode-h512-ragged-ranks": lambda: small_decode(41, 512, 2, 4, 20, [1, 3, 8, 16, 64], 37),
     "decode-h5120": lambda: small_decode(43, 5120, 1, 2, 10, [8, 128], 20),
     "decode-h4096-r256": lambda: small_decode(44, 4096, 1, 1, 3, [256], 9),
+    "decode-h6144": lambda: small_decode(58, 6144, 1, 2, 8, [8, 64], 13),
+    "decode-h8192": lambda: small_decode(59, 8192, 1, 1, 6, [16, 128], 11),
+    "prefill-h8192": lambda: small_prefill(60, 8192, 1, 1, 5, [8, 64, 128], [150, 40, 3]),
+    "mixed-h6144": lambda: _mixed(61, 6144, 1, 1, 9, [16, 128], [140, 7], 12, 2),
     "decode-base-uniform": lambda: small_decode(45, 1024, 1, 2, 6, [4, 16], 25, base=True),
     "prefill-h1024-ragged": lambda: small_prefill(46, 1024, 1, 3, 8, [8, 16, 32],
                                                   [1, 7, 130, 300, 2, 64, 129, 5, 0, 17, 255, 3]),
