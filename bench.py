@@ -294,7 +294,7 @@ def run_ours(args, rank: int, world: int, local: int):
         lora.segment(pool, seg_start, seg_adapter, S, dec, Td, T, ws, nbytes, stream)
 
     def delta():
-        lora.delta_grouped(pool, probs, T, ws, nbytes, stream)
+        lora.delta_grouped(pool, probs, T, S, ws, nbytes, stream)
 
     m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems))
     launches_per_step = 1 + -(-len(probs) // lora.LORA_MAX_PROBLEMS_PER_LAUNCH)

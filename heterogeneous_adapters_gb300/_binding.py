@@ -75,7 +75,7 @@ def lib():
             "lora_bgmv": [p, p, i32, p, i32, p, sz, p],
             "lora_sgmv": [p, p, i32, p, p, i32, i32, p, sz, p],
             "lora_apply_mixed": [p, p, i32, p, p, i32, p, i32, i32, p, sz, p],
-            "lora_delta_grouped": [p, p, i32, i32, p, sz, p],
+            "lora_delta_grouped": [p, p, i32, i32, i32, p, sz, p],
             "lora_debug_page_list": [p, p, sz, i32, i32, p, i64, p, p],
             "lora_debug_delta_with_t": [p, ctypes.POINTER(lora_problem), p, sz, p, p],
             "lora_stage_pages": [p, p, p, i32, p, p, p, i64, p],
@@ -190,9 +190,9 @@ def apply_mixed(pool, problems, seg_start, seg_adapter, S, dec_adapter, Td, T, w
            "lora_apply_mixed")
 
 
-def delta_grouped(pool, problems, T, ws, ws_bytes, stream):
+def delta_grouped(pool, problems, T, S, ws, ws_bytes, stream):
     arr, n = problems_array(problems)
-    _check(lib().lora_delta_grouped(pool.handle, arr, n, T, _ptr(ws), ws_bytes, stream),
+    _check(lib().lora_delta_grouped(pool.handle, arr, n, T, S, _ptr(ws), ws_bytes, stream),
            "lora_delta_grouped")
 
 

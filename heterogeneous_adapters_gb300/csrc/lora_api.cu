@@ -10,6 +10,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "bgmv_ring.cuh"
@@ -172,7 +173,8 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
 int mma_min_rows(const lora_pool_desc& d) {
     if (d.h % kMmaNTile != 0) return 0;
     const char* e = getenv("LORA_MMA_MIN_ROWS");
-    if (e != nullptr) return atoi(e) > 0 ? atoi(e) : 0;
+    // one-row (decode) segments always stay on the CUDA-core path
+    if (e != nullptr) return atoi(e) > 0 ? std::max(2, atoi(e)) : 0;
     return 32;
 }
 
@@ -552,12 +554,14 @@ lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const 
 }
 
 lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
-                               void* ws, size_t ws_bytes, void* stream) {
-    if (pool == nullptr || nprob < 0 || T < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
+                               int32_t S, void* ws, size_t ws_bytes, void* stream) {
+    if (pool == nullptr || nprob < 0 || T < 0 || S < 0 || (nprob > 0 && probs == nullptr))
+        return LORA_EINVAL;
     lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
     if (st != LORA_OK) return st;
     if (nprob == 0) return LORA_OK;
-    return run_delta(pool, probs, nprob, T, ws, nullptr, true, (cudaStream_t)stream);
+    // without prefill segments every segment has one row: no tensor-core tile exists
+    return run_delta(pool, probs, nprob, T, ws, nullptr, S > 0, (cudaStream_t)stream);
 }
 
 lora_status lora_bgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -577,7 +581,7 @@ lora_status lora_sgmv(const lora_pool* pool, const lora_problem* probs, int32_t 
                       void* ws, size_t ws_bytes, void* stream) {
     lora_status st = lora_segment(pool, seg_start, seg_adapter, S, nullptr, 0, T, ws, ws_bytes, stream);
     if (st != LORA_OK) return st;
-    return lora_delta_grouped(pool, probs, nprob, T, ws, ws_bytes, stream);
+    return lora_delta_grouped(pool, probs, nprob, T, S, ws, ws_bytes, stream);
 }
 
 lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -587,7 +591,7 @@ lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, i
     lora_status st = lora_segment(pool, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes,
                                   stream);
     if (st != LORA_OK) return st;
-    return lora_delta_grouped(pool, probs, nprob, T, ws, ws_bytes, stream);
+    return lora_delta_grouped(pool, probs, nprob, T, S, ws, ws_bytes, stream);
 }
 
 lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_bytes, int32_t layer,

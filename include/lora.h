@@ -181,10 +181,12 @@ lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, i
                              size_t ws_bytes, void* stream);
 
 /* Delta launches only, reusing the grouping already in ws (from lora_segment with the
- * same batch; T = the rows of x and y given to that call).  These are the kernels the
- * other entry points run after grouping. */
+ * same batch; T and S = the rows of x and y and the number of prefill segments given to
+ * that call).  These are the kernels the other entry points run after grouping.  With
+ * S == 0 every segment is a one-row decode segment, which the CUDA-core kernel serves
+ * alone (the launch lora_bgmv makes); with S > 0 the tensor-core tiles are served too. */
 lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
-                               int32_t T, void* ws, size_t ws_bytes, void* stream);
+                               int32_t T, int32_t S, void* ws, size_t ws_bytes, void* stream);
 
 /* Debug export of the page-table walk (a2): for problem (layer, proj), for each group
  * g of the grouping in ws, the r_a A-row pages then the r_a B-column pages, packed in
