@@ -13,7 +13,9 @@
 //                      into a ring of shared-memory stages with 1-D bulk copies
 //                      (cp.async.bulk, completion counted on an mbarrier): first the x
 //                      rows of the chunk, then its A-row pages, then its B-column pages,
-//                      up to kRingPages rows of 2h bytes per stage;
+//                      up to RP rows of 2h bytes per stage (RP = 4 or 8: the fewer,
+//                      larger stages the better a bulk-copy ring streams, as long as
+//                      three of them fit);
 //   warps 1..8         consume the stages in the same order: x into registers; each A
 //                      page -> fp32 partial dot products, reduced across the warp with a
 //                      transposing shuffle and across warps in shared memory (t, scaled);
@@ -29,7 +31,8 @@
 namespace lora {
 
 constexpr int kRingMaxConsumerWarps = 16;
-constexpr int kRingPages = 4;              // pages (or x rows) per stage
+constexpr int kRingPagesSmall = 4;   // pages (or x rows) per stage: the two choices
+constexpr int kRingPagesLarge = 8;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint32_t kDerrTimeout = LORA_DERR_TIMEOUT;
 
@@ -55,7 +58,7 @@ struct RingParamsT {
     float* t_out;
     int32_t nprob;
     int32_t stages;        // ring depth
-    int32_t stage_bytes;   // kRingPages * 2h
+    int32_t stage_bytes;   // RP * 2h
     int32_t pad;
     ProbDesc probs[MAXP];
 };
@@ -84,17 +87,18 @@ __host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes
 }
 
 // Column vectors (8 bf16 = 16 B) of a row handled by consumer thread c: c + 32 CW v.
-template <int NV, int NT, int CW>
+template <int NV, int NT, int CW, int RP>
 __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, int stage_row_bytes,
                                                   int npages, int h8, int c,
                                                   const uint4 (&xv)[kChunk][NV], float* red_w,
                                                   int j0) {
-    constexpr int V = kRingPages * kChunk;   // 16 values per warp
+    constexpr int V = RP * kChunk;   // 16 or 32 values per warp
+    static_assert(V <= 32 && RP >= kChunk, "stage shape");
     float vals[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) vals[i] = 0.f;
 #pragma unroll
-    for (int jj = 0; jj < kRingPages; ++jj) {
+    for (int jj = 0; jj < RP; ++jj) {
         if (jj < npages) {
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
@@ -118,15 +122,16 @@ __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, in
     }
     const float sum = warp_transpose_reduce<V>(vals);
     const int lane = threadIdx.x & 31;
-    if ((lane & 1) == 0) red_w[j0 * kChunk + (lane >> 1)] = sum;   // index jj*kChunk + t
+    constexpr int kRep = 32 / V;   // lanes holding each sum
+    if (lane % kRep == 0) red_w[j0 * kChunk + lane / kRep] = sum;   // index jj*kChunk + t
 }
 
-template <int NV, int NT, int CW>
+template <int NV, int NT, int CW, int RP>
 __device__ __forceinline__ void ring_expand_stage(const unsigned char* stage, int stage_row_bytes,
                                                   int npages, int h8, int c, const float* ts, int j0,
                                                   float (&acc)[kChunk][NV][8]) {
 #pragma unroll
-    for (int jj = 0; jj < kRingPages; ++jj) {
+    for (int jj = 0; jj < RP; ++jj) {
         if (jj < npages) {
             const float4 tj = *reinterpret_cast<const float4*>(ts + (j0 + jj) * kChunk);
             const float tv[4] = {tj.x, tj.y, tj.z, tj.w};
@@ -160,7 +165,7 @@ __device__ __forceinline__ bool consumer_barrier(unsigned char* base, const Ring
     return ok;
 }
 
-template <int NV, int NT, int CW, class P>
+template <int NV, int NT, int CW, int RP, class P>
 __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSmem& L,
                                   uint32_t& it, uint32_t& bphase, const StageMeta& mx, int c) {
     const int h = p.pool.h, h8 = h >> 3;
@@ -169,8 +174,8 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
     const int warp = c >> 5, lane = c & 31;
     const int rp = (p.pool.r_max + 7) / 8 * 8;
     float* red = reinterpret_cast<float*>(base + L.red);
-    float* ts = reinterpret_cast<float*>(base + L.ts);
     float* red_w = red + warp * rp * kChunk;
+    float* ts = reinterpret_cast<float*>(base + L.ts);
     const int r = mx.rank;
     const ProbDesc pd = p.probs[mx.pr];
 
@@ -191,26 +196,31 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
         ++it;
     }
     // shrink over the A stages
-    for (int j0 = 0; j0 < r; j0 += kRingPages) {
+    for (int j0 = 0; j0 < r; j0 += RP) {
         const uint32_t s = it % S;
         if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
-        const int np = min(kRingPages, r - j0);
-        ring_shrink_stage<NV, NT, CW>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, xv,
+        const int np = min(RP, r - j0);
+        ring_shrink_stage<NV, NT, CW, RP>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, xv,
                                   red_w, j0);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
         ++it;
     }
+    // Two barriers per item: every warp's partial sums are in red, then t is complete.
+    // The next item writes red only after the second one (every warp is done reading
+    // red) and t only after its own first one, which every warp reaches after its expand
+    // of this item, so no barrier is needed at the end of the item.
     if (!consumer_barrier(base, L, bphase)) return false;
-    for (int e = c; e < r * kChunk; e += CW * 32) {
+    // only the NT rows the expand reads (entries of t for rows >= NT are never read)
+    for (int e = c; e < r * NT; e += CW * 32) {
+        const int j = e / NT, t = e % NT;
+        const int idx = j * kChunk + t;
         float a = 0.f;
 #pragma unroll
-        for (int w = 0; w < CW; ++w) a += red[w * rp * kChunk + e];
-        ts[e] = a * mx.scale;
-        if (p.t_out != nullptr) {
-            const int j = e / kChunk, t = e % kChunk;
-            if (t < mx.count) p.t_out[(long long)mx.rows[t] * p.pool.r_max + j] = a * mx.scale;
-        }
+        for (int w = 0; w < CW; ++w) a += red[w * rp * kChunk + idx];
+        ts[idx] = a * mx.scale;
+        if (p.t_out != nullptr && t < mx.count)
+            p.t_out[(long long)mx.rows[t] * p.pool.r_max + j] = a * mx.scale;
     }
     if (!consumer_barrier(base, L, bphase)) return false;
     // prefetch the y rows while the B pages stream in
@@ -229,11 +239,11 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
         for (int v = 0; v < NV; ++v)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[t][v][e] = 0.f;
-    for (int j0 = 0; j0 < r; j0 += kRingPages) {
+    for (int j0 = 0; j0 < r; j0 += RP) {
         const uint32_t s = it % S;
         if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
-        const int np = min(kRingPages, r - j0);
-        ring_expand_stage<NV, NT, CW>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, ts, j0,
+        const int np = min(RP, r - j0);
+        ring_expand_stage<NV, NT, CW, RP>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, ts, j0,
                                   acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
@@ -255,15 +265,14 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
                 st16(pd.y + (long long)mx.rows[t] * pd.ldy + vi * 8, o);
             }
         }
-    // the next item's final reduction must not overwrite ts while a warp still reads it
-    return consumer_barrier(base, L, bphase);
+    return true;
 }
 
 // One CTA of the ring kernel: CTA `cta` of `ncta` taking part (threads beyond the
 // producer and the CW consumer warps only join the initial barrier).
 // NV: 16-byte column vectors per consumer thread; CW: consumer warps (h = 8 * 32 * CW * NV
-// or less).
-template <int NV, int CW, class P>
+// or less); RP: rows per stage (stage_bytes = RP * 2h).
+template <int NV, int CW, int RP, class P>
 __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32_t cta, uint32_t ncta) {
     const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max, CW);
     const int S = p.stages;
@@ -376,8 +385,8 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
             if (bad) continue;
             // A pages then B pages
             for (int ab = 0; ab < 2 && ok; ++ab) {
-                for (int j0 = 0; j0 < r; j0 += kRingPages) {
-                    const int np = min(kRingPages, r - j0);
+                for (int j0 = 0; j0 < r; j0 += RP) {
+                    const int np = min(RP, r - j0);
                     s = claim();
                     if (s < 0) { ok = false; break; }
                     if (lane == 0) {
@@ -437,11 +446,11 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
             }
             bool ok;
             if (mx.count == 1)
-                ok = ring_consume_item<NV, 1, CW, P>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 1, CW, RP, P>(p, base, L, it, bphase, mx, c);
             else if (mx.count == 2)
-                ok = ring_consume_item<NV, 2, CW, P>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 2, CW, RP, P>(p, base, L, it, bphase, mx, c);
             else
-                ok = ring_consume_item<NV, kChunk, CW, P>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, kChunk, CW, RP, P>(p, base, L, it, bphase, mx, c);
             if (!ok) {
                 if (c == 0) set_error(&hdr->err, kDerrTimeout);
                 break;
@@ -450,10 +459,10 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
     }
 }
 
-template <int NV, int CW>
+template <int NV, int CW, int RP>
 __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
     extern __shared__ __align__(1024) unsigned char ring_smem_raw[];
-    ring_cta<NV, CW>(p, ring_smem_raw, blockIdx.x, gridDim.x);
+    ring_cta<NV, CW, RP>(p, ring_smem_raw, blockIdx.x, gridDim.x);
 }
 
 }  // namespace lora

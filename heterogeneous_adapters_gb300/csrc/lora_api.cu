@@ -104,28 +104,59 @@ int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* 
     return 0;
 }
 
-template <int NV, int CW>
-lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
+// Shape of the ring for one launch: rows per stage, depth and the shared memory it takes.
+struct RingShape {
+    int rp, stages;
+    size_t smem;
+};
+
+// Rows per stage: the larger stages when three of them fit (a bulk-copy ring streams
+// closer to the HBM read rate with fewer, larger stages), else the small ones.
+// LORA_RING_PAGES = 4 or 8 forces the choice where two such stages fit.
+RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps) {
+    const char* e = getenv("LORA_RING_PAGES");
+    const int force = e != nullptr ? atoi(e) : 0;
+    RingShape fallback{0, 0, 0};
+    for (int rp : {kRingPagesLarge, kRingPagesSmall}) {
+        size_t smem = 0;
+        const int S = ring_stages(smem_optin, rp * 2 * h, r_max, cwarps, &smem);
+        if (S < 2) continue;
+        const RingShape sh{rp, S, smem};
+        if (force == rp || (force == 0 && S >= 3)) return sh;
+        if (fallback.stages == 0) fallback = sh;
+    }
+    return fallback;
+}
+
+template <int NV, int CW, int RP>
+lora_status launch_ring_rp(RingParams& prm, const DeviceInfo* di, const RingShape& sh, cudaStream_t stream) {
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
     int dev = 0;
     cudaGetDevice(&dev);
-    size_t smem = 0;
-    const int S = ring_stages(di->smem_optin, prm.stage_bytes, prm.pool.r_max, CW, &smem);
-    if (S < 2) return LORA_ETOOBIG;
-    prm.stages = S;
-    auto kern = bgmv_ring_kernel<NV, CW>;
+    prm.stage_bytes = RP * 2 * prm.pool.h;
+    prm.stages = sh.stages;
+    const size_t smem = sh.smem;
+    auto kern = bgmv_ring_kernel<NV, CW, RP>;
     if (attr_dev != dev || attr_smem < smem) {
-        st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        lora_status st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         if (st != LORA_OK) return st;
         attr_dev = dev;
         attr_smem = smem;
     }
     kern<<<di->sm_count, CW * 32 + 32, smem, stream>>>(prm);
     return cuda_status(cudaGetLastError());
+}
+
+template <int NV, int CW>
+lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW);
+    if (sh.stages < 2) return LORA_ETOOBIG;
+    if (sh.rp == kRingPagesLarge) return launch_ring_rp<NV, CW, kRingPagesLarge>(prm, di, sh, stream);
+    return launch_ring_rp<NV, CW, kRingPagesSmall>(prm, di, sh, stream);
 }
 
 lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
@@ -140,7 +171,6 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
         prm.ws = reinterpret_cast<char*>(ws);
         prm.t_out = t_out;
         prm.nprob = n;
-        prm.stage_bytes = kRingPages * 2 * d.h;
         for (int32_t i = 0; i < n; ++i) {
             const lora_problem& pr = probs[base + i];
             prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
@@ -277,7 +307,7 @@ void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem
     prm.t_out = t_out;
     prm.nprob = n;
     prm.stages = stages;
-    prm.stage_bytes = kRingPages * 2 * d.h;
+    prm.stage_bytes = kRingPagesSmall * 2 * d.h;
     for (int32_t i = 0; i < n; ++i) {
         const lora_problem& pr = probs[i];
         prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
@@ -337,8 +367,9 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     MmaConfig c;
     st = mma_config(pool->d, di->smem_optin, &c);
     if (st != LORA_OK) return st;
+    // the ring body of this kernel uses the small stages
     size_t ring_smem = 0;
-    const int S = ring_stages(di->smem_optin, kRingPages * 2 * pool->d.h, pool->d.r_max, CW, &ring_smem);
+    const int S = ring_stages(di->smem_optin, kRingPagesSmall * 2 * pool->d.h, pool->d.r_max, CW, &ring_smem);
     if (S < 2) return LORA_ETOOBIG;
     const size_t smem = c.smem > ring_smem ? c.smem : ring_smem;
     static thread_local FusedParams prm;

@@ -91,6 +91,20 @@ def test_prefill_size_classes(mma_min, monkeypatch):
         case.close()
 
 
+@pytest.mark.parametrize("pages", ["4", "8"])
+def test_decode_ring_stage_shapes(pages, monkeypatch):
+    """The decode ring with 4 and with 8 rows per stage on the same batch: ranks that are
+    not multiples of either and chunks of 1 to 4 rows (a skewed adapter mix)."""
+    monkeypatch.setenv("LORA_RING_PAGES", pages)
+    wl = small_decode(65, 2048, 1, 3, 12, [1, 3, 5, 8, 13, 64, 100], 57, zipf=1.3)
+    case = GpuCase(wl)
+    try:
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+    finally:
+        case.close()
+
+
 def test_t_matches_oracle_shrink():
     """fp32 t (the value the expand consumes, scaled) against the oracle's fp64 t."""
     import torch
