@@ -37,8 +37,8 @@ UNIT = "tokens/s"
 
 def workload_for(cfg: str):
     """Configs 0-4 as named in the workload module; "1s" (4 layers, 300 adapters, ~2.4 GB
-    pool) and "2s" (2 layers x 2 projections, ~2 GB on the device) are small variants of
-    configs 1 and 2 for profiler captures."""
+    pool), "2s" (2 layers x 2 projections, ~2 GB on the device) and "3s" (1 layer x 2
+    projections) are small variants of configs 1, 2 and 3 for profiler captures."""
     from workloads import spec
     if cfg == "1s":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
@@ -46,6 +46,10 @@ def workload_for(cfg: str):
     if cfg == "2s":
         return spec.prefill_workload("llama7b-prefill-sgmv-h4096-s32-a1000-l2p2", 1002, 4096, 2, 2,
                                      1000, [8, 16, 32, 64], 32, 64, 1024, 1.0)
+    if cfg == "3s":
+        return spec.mixed_workload("13b-mixed-h5120-p8-d192-a2000-l1p2", 1003, 5120, 1, 2, 2000,
+                                   [8, 16, 32, 64, 128], 8, 128, 2048, 192, 20, 0.8,
+                                   pool_pages=1 << 18)
     if cfg == "4d":
         return spec.config4("distinct")
     if cfg == "4z":
@@ -64,6 +68,8 @@ def measured_peaks() -> dict:
 KERNEL_SOURCES = {
     "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh", "segment.cuh"],
     "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh", "segment.cuh"],
+    "delta_fused_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh",
+                           "segment.cuh"],
 }
 
 
@@ -298,7 +304,20 @@ def run_ours(args, rank: int, world: int, local: int):
         lora.delta_grouped(pool, probs, T, S, ws, nbytes, stream)
 
     m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems))
-    launches_per_step = 1 + -(-len(probs) // lora.LORA_MAX_PROBLEMS_PER_LAUNCH)
+    # the delta launches of the step: the CUDA-core kernel alone for decode batches (up to
+    # 256 projections a launch); for batches with prefill segments the fused two-class
+    # kernel where h allows it (h a multiple of 128, h <= 5120; up to 64 projections a
+    # launch), else the CUDA-core kernel followed by the tensor-core one (64 a launch)
+    ceil = lambda a, c: -(-a // c)  # noqa: E731
+    nprob = len(probs)
+    if b.kind == "decode":
+        kname, delta_launches = "bgmv_ring_kernel", ceil(nprob, lora.LORA_MAX_PROBLEMS_PER_LAUNCH)
+    elif p.h % 128 == 0 and p.h // 8 <= 640:
+        kname, delta_launches = "delta_fused_kernel", ceil(nprob, 64)
+    else:
+        kname = "bgmv_ring_kernel+sgmv_mma_kernel"
+        delta_launches = ceil(nprob, lora.LORA_MAX_PROBLEMS_PER_LAUNCH) + ceil(nprob, 64)
+    launches_per_step = 1 + delta_launches   # the grouping kernel and the delta launches
 
     for _ in range(max(3, args.warmup)):
         segment()
@@ -331,20 +350,18 @@ def run_ours(args, rank: int, world: int, local: int):
     tokens_step = m["adapted_tokens"]
     value, elapsed_max = aggregate_throughput(tokens_step, args.steps, world, elapsed)
 
-    # roofline of the dominant kernel (the delta kernel)
+    # roofline of the dominant kernel (the delta kernel): per launch, the step's delta
+    # launches being of equal size (problems are split into balanced batches)
     peaks = measured_peaks()
-    kern_avg = statistics.mean(kern)
-    achieved = m["bytes"] / kern_avg / 1e9
-    # the delta launches of the step: the CUDA-core kernel for decode batches, the tensor-core
-    # kernel (plus the CUDA-core one for short segments) for prefill and mixed batches
-    kname = {"decode": "bgmv_ring_kernel", "prefill": "sgmv_mma_kernel"}.get(
-        b.kind, "bgmv_ring_kernel+sgmv_mma_kernel")
-    traffic = ncu_traffic(kname, wl.name, m["bytes"]) if kname in KERNEL_SOURCES else None
+    kern_avg = statistics.mean(kern) / delta_launches
+    bytes_launch = m["bytes"] / delta_launches
+    achieved = bytes_launch / kern_avg / 1e9
+    traffic = ncu_traffic(kname, wl.name, bytes_launch) if kname in KERNEL_SOURCES else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": kname, "kernel_ms": kern_avg * 1e3,
+                "kernel": kname, "kernel_ms": kern_avg * 1e3, "launches_per_step": delta_launches,
                 "peak_source": peaks["source"] + " (hbm_gbs, copy kernel)",
-                "bytes_per_launch": m["bytes"]}
+                "bytes_per_launch": bytes_launch}
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     xh = torch.empty_like(d.x, device="cpu").pin_memory()

@@ -256,10 +256,14 @@ lora_status mma_config(const lora_pool_desc& d, int smem_optin, MmaConfig* c) {
     c->rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
     c->s1_bytes = (16384 + c->rp_max * 128 + 1023) / 1024 * 1024;   // x chunk + A chunk
     c->s2_bytes = (c->rp_max * 256 + 1023) / 1024 * 1024;           // B^T slice
-    // the deepest y ring (<= 4) that leaves the shrink ring two stages (the shrink of the
-    // next tile runs under the expand of this one and needs little depth), B^T ring of 2
+    // the deepest y ring (<= 3) that leaves the shrink ring two stages, and the rest to
+    // the shrink ring (the next tile's shrink streams under this tile's expand and must
+    // end with it); B^T ring of 2.  On the Llama-7B prefill a 3-slot y ring with a 4-stage
+    // shrink ring beat both 4 + 2 (13% slower) and 2 + 6 (18% slower).
     c->s2 = 2;
-    for (c->s3 = 4; c->s3 >= 2; --c->s3) {
+    const char* ys = getenv("LORA_MMA_Y_STAGES");   // tuning override: 2..4
+    const int s3_max = ys != nullptr && atoi(ys) >= 2 && atoi(ys) <= 4 ? atoi(ys) : 3;
+    for (c->s3 = s3_max; c->s3 >= 2; --c->s3) {
         for (c->s1 = kMmaMaxStages; c->s1 >= 2; --c->s1) {
             c->smem = mma_smem_layout(c->s1, c->s1_bytes, c->s2, c->s2_bytes, c->s3).total + 1024;
             if (c->smem <= (size_t)smem_optin) break;

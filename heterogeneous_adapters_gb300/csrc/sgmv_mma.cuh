@@ -371,10 +371,11 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     tc_commit(bar(L.d2_full + b * 8));
                 }
                 __syncwarp();
-                // the next tile's shrink chunks that have already landed
+                // the next tile's shrink chunks that have already landed (a test, not a
+                // wait: a suspending wait here would hold the expand back for the whole shrink)
                 while (has_next && kc_next < n_kc) {
                     const uint32_t s1 = it1 % S1;
-                    if (!mbar_try_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) break;
+                    if (!mbar_test_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) break;
                     tc_fence_after();
                     if (lane == 0) {
                         mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
