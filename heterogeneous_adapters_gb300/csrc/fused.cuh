@@ -6,7 +6,10 @@
 // the former and BGMV the latter.  Here both run in the same persistent grid: the CTAs
 // are split between the two bodies in proportion to the bytes each class streams per
 // projection (weights written by the grouping kernel), so the two HBM streams proceed
-// side by side and end together instead of one after the other.
+// side by side and end together instead of one after the other.  A CTA of the ring body
+// streams bytes faster than one of the tensor-core body (it only reads pages, where the
+// other also reads and writes y in place), so the split weighs the two byte counts by their
+// per-CTA rates.
 #pragma once
 #include "bgmv_ring.cuh"
 #include "sgmv_mma.cuh"
@@ -16,15 +19,18 @@ namespace lora {
 struct FusedParams {
     MmaParams mma;
     RingParamsT<kMmaMaxProbs> ring;
+    float ring_speed;   // bytes per CTA-second of the ring body / those of the tensor-core body
 };
 
 // CTAs given to the CUDA-core class out of G (0 if it has no work, G if the tensor-core
-// class has none; otherwise at least one each).
-__device__ __forceinline__ uint32_t fused_split(const WsHeader* hdr, uint32_t G) {
+// class has none; otherwise at least one each), so that both classes' CTAs need about the
+// same time: G * (wf / speed) / (wf / speed + wm).
+__device__ __forceinline__ uint32_t fused_split(const WsHeader* hdr, uint32_t G, float ring_speed) {
     const unsigned long long wf = hdr->weight[0], wm = hdr->weight[1];
     if (wm == 0) return G;
     if (wf == 0) return 0;
-    uint32_t gf = (uint32_t)((double)G * (double)wf / ((double)wf + (double)wm) + 0.5);
+    const double tf = (double)wf / (double)ring_speed;
+    uint32_t gf = (uint32_t)((double)G * tf / (tf + (double)wm) + 0.5);
     if (gf < 1) gf = 1;
     if (gf > G - 1) gf = G - 1;
     return gf;
@@ -34,7 +40,7 @@ template <int NV, int CW>
 __global__ void __launch_bounds__(kMmaThreads, 1) delta_fused_kernel(const __grid_constant__ FusedParams p) {
     static_assert(CW * 32 + 32 <= kMmaThreads, "ring body must fit the fused CTA");
     extern __shared__ __align__(1024) unsigned char fused_smem_raw[];
-    const uint32_t gf = fused_split(reinterpret_cast<const WsHeader*>(p.mma.ws), gridDim.x);
+    const uint32_t gf = fused_split(reinterpret_cast<const WsHeader*>(p.mma.ws), gridDim.x, p.ring_speed);
     if (blockIdx.x < gf)
         ring_cta<NV, CW, kRingPagesSmall>(p.ring, fused_smem_raw, blockIdx.x, gf);
     else

@@ -361,6 +361,8 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
     return LORA_OK;
 }
 
+constexpr float kFusedRingSpeed = 1.22f;
+
 // Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0).
 template <int NV, int CW>
 lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
@@ -377,6 +379,11 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     if (S < 2) return LORA_ETOOBIG;
     const size_t smem = c.smem > ring_smem ? c.smem : ring_smem;
     static thread_local FusedParams prm;
+    // per-CTA byte rate of the ring body relative to the tensor-core body, measured on the
+    // 13B mixed step (ring CTAs split by bytes alone ended 18% before the tensor-core ones);
+    // LORA_FUSED_RING_SPEED overrides it
+    const char* rs = getenv("LORA_FUSED_RING_SPEED");
+    const float ring_speed = rs != nullptr && atof(rs) > 0.1 && atof(rs) < 10.0 ? (float)atof(rs) : kFusedRingSpeed;
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
     int dev = 0;
@@ -394,6 +401,7 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
         st = fill_mma(prm.mma, pool, probs + base, n, T, ws, c);
         if (st != LORA_OK) return st;
         fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, S);
+        prm.ring_speed = ring_speed;
         kern<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
         st = cuda_status(cudaGetLastError());
         if (st != LORA_OK) return st;
