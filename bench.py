@@ -57,6 +57,19 @@ def workload_for(cfg: str):
     return spec.CONFIGS[int(cfg)]()
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu reports it (architecture if unavailable)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip() + f" ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -218,6 +231,21 @@ class OracleRunner:
         adapted = int((self.ids >= 0).sum())
         return adapted / (seconds / n_problems * len(self.wl.problems))
 
+    def single_thread_sample(self, budget_s: float):
+        """timed_sample with the oracle's OpenMP team cut to one thread (restored after);
+        None where the OpenMP runtime cannot be reached."""
+        import ctypes
+        try:
+            gomp = ctypes.CDLL("libgomp.so.1")
+        except OSError:
+            return None
+        before = gomp.omp_get_max_threads()
+        gomp.omp_set_num_threads(1)
+        try:
+            return self.timed_sample(budget_s)
+        finally:
+            gomp.omp_set_num_threads(before)
+
     def timed_sample(self, budget_s: float):
         """Time as many projections as fit in about budget_s seconds of wall time (more
         than one step's worth when a step is quicker than that, up to 64 steps)."""
@@ -249,7 +277,7 @@ def run_reference(args, rank: int, world: int):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(wl, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": runner.threads,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": wall}
@@ -257,6 +285,33 @@ def run_reference(args, rank: int, world: int):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+
+def graph_timing(capture_fn, tokens_step: int, dev, replays: int) -> dict:
+    """Capture capture_fn(stream handle) once in a CUDA graph, replay it 10 times untimed,
+    then `replays` times, each between two events; median and p10 / p90 in ms."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=cap):
+        capture_fn(cap.cuda_stream)
+    for _ in range(10):
+        g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(replays)]
+    for e0, e1 in ev:
+        e0.record(cur)
+        g.replay()
+        e1.record(cur)
+    torch.cuda.synchronize()
+    ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
+    med = float(np.median(ms))
+    return {"ms_median": med, "ms_p10": float(np.percentile(ms, 10)),
+            "ms_p90": float(np.percentile(ms, 90)), "replays": replays,
+            "tokens_per_s": tokens_step / (med / 1e3)}
+
 
 def config_dict(wl, args) -> dict:
     from heterogeneous_adapters_gb300 import costmodel
@@ -363,6 +418,20 @@ def run_ours(args, rank: int, world: int, local: int):
                 "peak_source": peaks["source"] + " (hbm_gbs, copy kernel)",
                 "bytes_per_launch": bytes_launch}
 
+    # one step (grouping + delta launches) captured in a CUDA graph and replayed: median and
+    # p10 / p90 of the replays; for decode also with one delta launch per projection (the
+    # shape of a serving loop that applies each projection's delta next to its base GEMM)
+    graph = {"step": graph_timing(lambda st: (lora.segment(pool, seg_start, seg_adapter, S, dec, Td, T, ws,
+                                                           nbytes, st),
+                                              lora.delta_grouped(pool, probs, T, S, ws, nbytes, st)),
+                                  tokens_step, dev, args.graph_replays)}
+    if b.kind == "decode":
+        graph["per_projection"] = graph_timing(
+            lambda st: (lora.segment(pool, seg_start, seg_adapter, S, dec, Td, T, ws, nbytes, st),
+                        [lora.delta_grouped(pool, [pr], T, S, ws, nbytes, st) for pr in probs]),
+            tokens_step, dev, args.graph_replays)
+    assert lora.get_device_error(ws, stream) == 0
+
     # end to end through the C ABI with host buffers: every step copies its inputs (x, y and
     # the batch's adapter ids) in from pinned host memory and reads its result y back, inside
     # the timed region.  Steps run as a serving loop runs them, over three device slots: the
@@ -461,17 +530,78 @@ def run_ours(args, rank: int, world: int, local: int):
                    "sample": f"{done} projection deltas ({done / len(wl.problems):.2f} steps of "
                              f"{len(wl.problems)}, cycling over the first {len(runner.probs)}), "
                              f"all {wl.batch.num_tokens} tokens each, {dt:.1f} s wall on "
-                             f"{runner.threads} threads, rate scaled to whole steps"}
+                             f"{runner.threads} threads, rate scaled to whole steps",
+                   "cpu_model": cpu_model()}
+            one = runner.single_thread_sample(args.ref_seconds / 3)
+            if one is not None:
+                rate1, dt1, done1 = one
+                cpu["single_thread"] = {"value": rate1, "unit": UNIT,
+                                        "sample": f"{done1} projection deltas, {dt1:.1f} s wall on 1 thread"}
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": max(3, args.warmup),
                 "ms_per_step": 1e3 * elapsed_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config_dict(wl, args), "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary(), "impl": "ours"}
+                "graph": graph, "clocks": clk.summary(), "impl": "ours"}
         if staging is not None:
             line["staging"] = staging
         print(json.dumps(line), flush=True)
+    pool.close()
+
+
+# ----------------------------------------------------------------------------- distinct-adapter sweep
+
+def run_sweep_distinct(args, local: int):
+    """Config 1's pool and projections; the 64 decode tokens spread round-robin over D
+    adapters drawn without replacement from the 2,000 (seed 7000 + D), D = 1, 2, 4, ..., 64.
+    One JSON line per D: step time of the delta launch (CUDA events, K steps after W warm-up),
+    adapted tokens/s and the fraction of the measured HBM peak."""
+    import torch
+
+    import heterogeneous_adapters_gb300 as lora
+    from heterogeneous_adapters_gb300 import costmodel
+    from workloads.materialize import device_inputs
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = workload_for("1")
+    d = device_inputs(wl, device=dev, nan_dummies=False)
+    p = wl.pool
+    pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
+                     p.num_adapters, p.num_layers, p.num_proj, p.r_max)
+    T = wl.batch.num_tokens
+    nbytes = lora.workspace_size(pool, T, T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream_obj = torch.cuda.current_stream(dev)
+    stream = stream_obj.cuda_stream
+    lora.workspace_init(ws, nbytes, stream)
+    probs = [(d.x[i], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    peaks = measured_peaks()
+    for D in (1, 2, 4, 8, 16, 32, 64):
+        rng = np.random.default_rng(7000 + D)
+        chosen = rng.choice(p.num_adapters, size=D, replace=False)
+        ids = chosen[np.arange(T) % D].astype(np.int32)
+        d.token_adapter.copy_(torch.from_numpy(ids))
+        lora.segment(pool, None, None, 0, d.token_adapter, T, T, ws, nbytes, stream)
+        for _ in range(max(3, args.warmup)):
+            lora.delta_grouped(pool, probs, T, 0, ws, nbytes, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream_obj)
+        for _ in range(args.steps):
+            lora.delta_grouped(pool, probs, T, 0, ws, nbytes, stream)
+        e1.record(stream_obj)
+        torch.cuda.synchronize()
+        assert lora.get_device_error(ws, stream) == 0
+        ms = e0.elapsed_time(e1) / args.steps
+        m = costmodel.decode_step_bytes(p.ranks, ids, p.h, len(probs))
+        gbs = m["bytes"] / (ms / 1e3) / 1e9
+        print(json.dumps({"sweep": "distinct_adapters", "workload": wl.name, "distinct": D,
+                          "ranks_mean": float(p.ranks[chosen].mean()), "delta_ms": ms,
+                          "tokens_per_s": T / (ms / 1e3), "bytes_per_step": m["bytes"],
+                          "achieved_gbs": gbs, "frac_of_peak": gbs / peaks["hbm_gbs"],
+                          "steps": args.steps}), flush=True)
     pool.close()
 
 
@@ -670,6 +800,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="1")
+    ap.add_argument("--graph-replays", type=int, default=50,
+                    help="timed replays of the CUDA graph of one step")
     ap.add_argument("--e2e-slots", type=int, default=3, choices=[1, 2, 3, 4],
                     help="device slots of the end-to-end leg's copy/compute pipeline")
     ap.add_argument("--ref-seconds", type=float, default=15.0,
@@ -683,10 +815,15 @@ def main():
                     help="resident adapter slices in the unified-pool stress workload")
     ap.add_argument("--stage-steps", type=int, default=20,
                     help="steps of the staging scenario (configs 4d / 4z)")
+    ap.add_argument("--sweep-distinct", action="store_true",
+                    help="instead of the bench line: decode tokens/s against the number of "
+                         "distinct adapters in the batch (1..64) at config 1's shape")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.sweep_distinct:
+        run_sweep_distinct(args, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:
