@@ -10,7 +10,9 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(_PKG, "liblora.so")
 
-LORA_OK, LORA_EINVAL, LORA_EALIGN, LORA_EWORKSPACE, LORA_ETOOBIG, LORA_ECUDA, LORA_EDEVICE = range(7)
+(LORA_OK, LORA_EINVAL, LORA_EALIGN, LORA_EWORKSPACE, LORA_ETOOBIG, LORA_ECUDA, LORA_EDEVICE,
+ LORA_ENOSPACE) = range(8)
+LORA_UNIT_ABSENT, LORA_UNIT_LOADING, LORA_UNIT_READY = range(3)
 DERR = {0x1: "adapter", 0x2: "rank", 0x4: "page-table block", 0x8: "page", 0x10: "segment",
         0x20: "timeout"}
 LORA_MAX_PROBLEMS_PER_LAUNCH = 256
@@ -22,7 +24,11 @@ EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_workspace_size", "lor
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
             "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t",
             "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error",
-            "lora_last_cuda_error", "lora_status_string"]
+            "lora_last_cuda_error", "lora_status_string",
+            # host runtime (include/lora_runtime.h)
+            "lora_cache_create", "lora_cache_destroy", "lora_cache_acquire", "lora_cache_loaded",
+            "lora_cache_release", "lora_cache_query", "lora_cache_stats", "lora_sched_create",
+            "lora_sched_destroy", "lora_sched_enqueue", "lora_sched_pick", "lora_sched_pending"]
 
 
 class lora_pool_desc(ctypes.Structure):
@@ -83,6 +89,19 @@ def lib():
             "lora_get_device_error": [p, p, ctypes.POINTER(ctypes.c_uint32)],
             "lora_last_cuda_error": [],
             "lora_status_string": [ctypes.c_int],
+            "lora_cache_create": [ctypes.POINTER(p), p, i64, p, i32],
+            "lora_cache_destroy": [p],
+            "lora_cache_acquire": [p, i32, ctypes.POINTER(i32), p, i64, p, i32, ctypes.POINTER(i32)],
+            "lora_cache_loaded": [p, i32],
+            "lora_cache_release": [p, i32],
+            "lora_cache_query": [p, i32, ctypes.POINTER(i32), ctypes.POINTER(i32), p, i64],
+            "lora_cache_stats": [p] + [ctypes.POINTER(i64)] * 4,
+            "lora_sched_create": [ctypes.POINTER(p), p],
+            "lora_sched_destroy": [p],
+            "lora_sched_enqueue": [p, i64, i32, i32],
+            "lora_sched_pick": [p, i32, i32, p, p, p, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                ctypes.POINTER(i32)],
+            "lora_sched_pending": [p, ctypes.POINTER(i64)],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -228,3 +247,109 @@ def get_device_error(ws, stream) -> int:
     if st not in (LORA_OK, LORA_EDEVICE):
         raise LoraError(st, "lora_get_device_error")
     return bits.value
+
+
+# ----------------------------------------------------------------------------- host runtime
+
+def _np_ptr(a):
+    return a.ctypes.data if a is not None and a.size else None
+
+
+class AdapterCache:
+    """lora_cache_*: LRU residency of units (adapters or adapter slices) in pool pages."""
+
+    def __init__(self, managed_pages, unit_pages):
+        import numpy as np
+        self._np = np
+        self.managed = np.ascontiguousarray(managed_pages, np.int32)
+        self.unit_pages = np.ascontiguousarray(unit_pages, np.int32)
+        h = ctypes.c_void_p()
+        _check(lib().lora_cache_create(ctypes.byref(h), _np_ptr(self.managed), self.managed.size,
+                                       _np_ptr(self.unit_pages), self.unit_pages.size), "lora_cache_create")
+        self.handle = h
+
+    def _unit_pages(self, u: int) -> int:
+        # out-of-range units go to the library, which rejects them
+        return int(self.unit_pages[u]) if 0 <= u < self.unit_pages.size else 1
+
+    def acquire(self, u: int, evicted_cap: int = 64):
+        """(loaded, pages or None, evicted units); raises LoraError (LORA_ENOSPACE) when full."""
+        np = self._np
+        pages = np.empty(self._unit_pages(u), np.int32)
+        ev = np.empty(evicted_cap, np.int32)
+        loaded, n_ev = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().lora_cache_acquire(self.handle, u, ctypes.byref(loaded), pages.ctypes.data, pages.size,
+                                        ev.ctypes.data, evicted_cap, ctypes.byref(n_ev)), "lora_cache_acquire")
+        return bool(loaded.value), (pages if loaded.value else None), ev[:min(n_ev.value, evicted_cap)].copy()
+
+    def try_acquire(self, u: int):
+        """acquire, or None when no pages can be freed."""
+        try:
+            return self.acquire(u)
+        except LoraError as e:
+            if e.status == LORA_ENOSPACE:
+                return None
+            raise
+
+    def loaded(self, u: int):
+        _check(lib().lora_cache_loaded(self.handle, u), "lora_cache_loaded")
+
+    def release(self, u: int):
+        _check(lib().lora_cache_release(self.handle, u), "lora_cache_release")
+
+    def query(self, u: int):
+        """(state, users, pages of a resident unit)."""
+        np = self._np
+        st, us = ctypes.c_int32(), ctypes.c_int32()
+        pages = np.empty(self._unit_pages(u), np.int32)
+        _check(lib().lora_cache_query(self.handle, u, ctypes.byref(st), ctypes.byref(us), pages.ctypes.data,
+                                      pages.size), "lora_cache_query")
+        return st.value, us.value, (pages if st.value != LORA_UNIT_ABSENT else None)
+
+    def stats(self):
+        """dict of hits, misses, evictions, free_pages."""
+        v = [ctypes.c_int64() for _ in range(4)]
+        _check(lib().lora_cache_stats(self.handle, *[ctypes.byref(x) for x in v]), "lora_cache_stats")
+        return dict(zip(("hits", "misses", "evictions", "free_pages"), (x.value for x in v)))
+
+    def close(self):
+        if self.handle:
+            lib().lora_cache_destroy(self.handle)
+            self.handle = None
+
+
+class Scheduler:
+    """lora_sched_*: arrival-ordered request queue and the per-step batch pick."""
+
+    def __init__(self, cache: AdapterCache | None = None):
+        h = ctypes.c_void_p()
+        _check(lib().lora_sched_create(ctypes.byref(h), cache.handle if cache is not None else None),
+               "lora_sched_create")
+        self.handle = h
+        self.cache = cache
+
+    def enqueue(self, req_id: int, adapter: int, tokens: int = 1):
+        _check(lib().lora_sched_enqueue(self.handle, req_id, adapter, tokens), "lora_sched_enqueue")
+
+    def pick(self, max_tokens: int, max_distinct: int, cap: int = 4096):
+        """(ids, adapters, tokens) of the batch, numpy arrays in queue order."""
+        import numpy as np
+        ids = np.empty(cap, np.int64)
+        ad = np.empty(cap, np.int32)
+        tk = np.empty(cap, np.int32)
+        n, nt, nd = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().lora_sched_pick(self.handle, max_tokens, max_distinct, ids.ctypes.data, ad.ctypes.data,
+                                     tk.ctypes.data, cap, ctypes.byref(n), ctypes.byref(nt), ctypes.byref(nd)),
+               "lora_sched_pick")
+        k = n.value
+        return ids[:k].copy(), ad[:k].copy(), tk[:k].copy()
+
+    def pending(self) -> int:
+        v = ctypes.c_int64()
+        _check(lib().lora_sched_pending(self.handle, ctypes.byref(v)), "lora_sched_pending")
+        return v.value
+
+    def close(self):
+        if self.handle:
+            lib().lora_sched_destroy(self.handle)
+            self.handle = None

@@ -10,6 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SO = os.path.join(PKG, "liblora.so")
 MAIN = os.path.join(PKG, "csrc", "lora_api.cu")
+RUNTIME = os.path.join(PKG, "csrc", "runtime.cpp")   # host-only: adapter cache, scheduler
 
 
 def nvcc() -> str:
@@ -22,7 +23,7 @@ def nvcc() -> str:
 def build_cmd(extra=()) -> list[str]:
     return [nvcc(), "-O3", "-shared", "-Xcompiler", "-fPIC", "-std=c++17",
             "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-            "-I", os.path.join(ROOT, "include"), *extra, "-o", SO, MAIN]
+            "-I", os.path.join(ROOT, "include"), *extra, "-o", SO, MAIN, RUNTIME]
 
 
 def sources() -> list[str]:

@@ -488,6 +488,7 @@ const char* lora_status_string(lora_status s) {
         case LORA_ETOOBIG: return "size beyond a documented maximum";
         case LORA_ECUDA: return "CUDA runtime error";
         case LORA_EDEVICE: return "device-detected data error";
+        case LORA_ENOSPACE: return "no pool pages can be freed: every resident adapter is in use";
     }
     return "unknown status";
 }

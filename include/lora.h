@@ -77,7 +77,8 @@ typedef enum {
     LORA_EWORKSPACE = 3,  /* workspace null, misaligned or smaller than required   */
     LORA_ETOOBIG = 4,     /* a size beyond a documented maximum                    */
     LORA_ECUDA = 5,       /* a CUDA runtime call failed (lora_last_cuda_error)     */
-    LORA_EDEVICE = 6      /* device error bits were set (lora_get_device_error)    */
+    LORA_EDEVICE = 6,     /* device error bits were set (lora_get_device_error)    */
+    LORA_ENOSPACE = 7     /* adapter cache: no pages can be freed (all units in use) */
 } lora_status;
 
 /* Device error bits (data-dependent errors found by the kernels). */

@@ -1,4 +1,4 @@
-"""The C ABI library loads without a GPU and exports every symbol include/lora.h
+"""The C ABI library loads without a GPU and exports every symbol include/*.h
 declares; host-only calls (pool creation checks, sizes, status strings) behave as
 documented.  No kernel is launched here."""
 import ctypes
@@ -11,7 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "lora.h")).read()
+    import glob
+    src = "".join(open(f).read() for f in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(lora_\w+)\s*\(", src, flags=re.M)))
 
