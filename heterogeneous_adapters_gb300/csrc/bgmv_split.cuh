@@ -1,0 +1,234 @@
+// CUDA-core BGMV for launches with few projections: the work of each chunk (up to 4 rows
+// of one adapter) is split across CTAs in two phases, so that even one projection's
+// chunks fill the GPU.
+//
+// "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels work": the
+// LoRA term is a shrink v = A x followed by an expand y += gamma B v; engines issue these
+// per projection, next to each projection's base GEMM.  One projection of a decode batch
+// holds only a few dozen chunks, fewer than the SMs, so the persistent ring kernel (one
+// chunk per CTA at a time) leaves most of the GPU idle there.
+//
+//   phase 1 (split_shrink_kernel): item = (projection, chunk, 8 consecutive A rows j).
+//     Warp w computes t[row][j0 + w] = s * sum_k x[row,k] A[j0+w,k] over the full row
+//     (no partial sums cross CTAs) and writes it, fp32, to the workspace.
+//   phase 2 (split_expand_kernel): item = (projection, chunk, 512-column slice of y).
+//     Every B column's slice is read once; 4 groups of threads take every 4th j, their
+//     sums meet in shared memory, and y = bf16_rn(y + sum) is stored for the slice.
+//     Per item, the page ids, t values and y rows come in one round trip, then the B
+//     vectors, up to 16 per thread in flight.
+// A chunk whose A or B pages are out of range is skipped (its y rows are left as they
+// are) and reported in the device error word.
+#pragma once
+#include "common.cuh"
+#include "segment.cuh"
+
+namespace lora {
+
+constexpr int kSplitMaxProbs = 8;        // projections of one split launch at most
+constexpr int kSplitDefaultProbs = 2;    // the default limit (measured against the ring kernel)
+constexpr int kSplitMaxTokens = 1024;    // batches (rows) the workspace reserves t for
+constexpr int kSplitRows = 8;            // A rows per phase-1 item (one per warp)
+constexpr int kSplitVecs = 64;           // 16-byte column vectors per phase-2 item (512 columns)
+constexpr int kSplitThreads = 256;
+
+struct SplitParams {
+    PoolView pool;
+    char* ws;
+    int32_t nprob;
+    int32_t pad;
+    ProbDesc probs[kSplitMaxProbs];
+};
+
+// t of the split path: [problem][token row][r_max] fp32, after the workspace's other arrays.
+__device__ __forceinline__ float* split_t(const SplitParams& p, const WsHeader* hdr) {
+    return reinterpret_cast<float*>(p.ws + ws_layout(hdr->cap_tokens, hdr->cap_segments).total);
+}
+
+// Phase 1.  Per item every lane first issues the loads of its share of its warp's A row
+// (up to kSplitLoads 16-byte vectors at once), the CTA meanwhile stages the chunk's x rows
+// in shared memory, and the dot products are then taken from registers and shared memory.
+constexpr int kSplitLoads = 16;
+
+__global__ void __launch_bounds__(kSplitThreads) split_shrink_kernel(const __grid_constant__ SplitParams p) {
+    extern __shared__ __align__(16) unsigned char split_smem[];   // x rows: kChunk * h bf16
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+    const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
+    const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
+    float* tbuf = split_t(p, hdr);
+    const int n_chunks = hdr->counts[2];
+    const int T = hdr->cap_tokens;
+    const PoolView& P = p.pool;
+    const int h8 = P.h >> 3, r_max = P.r_max;
+    const int n_js = (r_max + kSplitRows - 1) / kSplitRows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4* xs = reinterpret_cast<uint4*>(split_smem);
+    const long long total = (long long)p.nprob * n_chunks * n_js;
+    auto chunk_of = [&](long long it) { return (int)((it / n_js) % n_chunks); };
+    Chunk next;
+    if (blockIdx.x < total) next = chunks[chunk_of(blockIdx.x)];
+    for (long long item = blockIdx.x; item < total; item += gridDim.x) {
+        const int js = (int)(item % n_js);
+        const int pr = (int)(item / ((long long)n_js * n_chunks));
+        const Chunk ch = next;   // loaded while the previous item was being computed
+        if (item + gridDim.x < total) next = chunks[chunk_of(item + gridDim.x)];
+        const int r = ch.rank;
+        if (js * kSplitRows >= r) continue;   // this adapter has fewer rows
+        const ProbDesc pd = p.probs[pr];
+        const long long blk0 = ch.pt_base + (long long)pd.blk * 2 * r;
+        // each warp checks its own A row's page; a bad page leaves that t entry unwritten
+        // (the expand of this chunk checks every page of it and skips it)
+        const int j = js * kSplitRows + warp;
+        const int page = j < r ? P.pt[blk0 + j] : 0;
+        const bool page_ok = page >= 0 && page < P.num_pages;
+        if (j < r && !page_ok && lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
+        const bool live = j < r && page_ok;
+        const __nv_bfloat16* a = P.pages + (long long)(live ? page : 0) * P.h;
+        float acc[kChunk] = {0.f, 0.f, 0.f, 0.f};
+        for (int v0 = 0; v0 < h8; v0 += 32 * kSplitLoads) {
+            uint4 av[kSplitLoads];
+#pragma unroll
+            for (int k = 0; k < kSplitLoads; ++k) {
+                const int v = v0 + lane + 32 * k;
+                av[k] = (live && v < h8) ? ld_stream16(a + v * 8) : make_uint4(0, 0, 0, 0);
+            }
+            if (v0 == 0) {   // the x rows, while the A loads are in flight
+                for (int e = threadIdx.x; e < ch.count * h8; e += blockDim.x) {
+                    const int t = e / h8, v = e % h8;
+                    xs[t * h8 + v] = ld16(pd.x + (long long)ch.rows[t] * pd.ldx + v * 8);
+                }
+                __syncthreads();
+            }
+#pragma unroll
+            for (int k = 0; k < kSplitLoads; ++k) {
+                const int v = v0 + lane + 32 * k;
+                if (v < h8) {
+                    float a8[8];
+                    unpack8(av[k], a8);
+#pragma unroll
+                    for (int t = 0; t < kChunk; ++t) {
+                        if (t < ch.count) {
+                            float x8[8];
+                            unpack8(xs[t * h8 + v], x8);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[t] = fmaf(x8[e], a8[e], acc[t]);
+                        }
+                    }
+                }
+            }
+        }
+        if (live) {
+#pragma unroll
+            for (int t = 0; t < kChunk; ++t) {
+                float s = acc[t];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0 && t < ch.count)
+                    tbuf[((long long)pr * T + ch.rows[t]) * r_max + j] = s * ch.scale;
+            }
+        }
+        __syncthreads();   // xs is reused by the next item
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __grid_constant__ SplitParams p) {
+    constexpr int kGroups = kSplitThreads / kSplitVecs;   // threads sharing one column vector
+    __shared__ float ts[kChunk][LORA_MAX_RANK];
+    __shared__ int32_t pg[LORA_MAX_RANK];
+    __shared__ float red[kGroups - 1][kChunk][kSplitVecs][8];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
+    const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
+    const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
+    const float* tbuf = split_t(p, hdr);
+    const int n_chunks = hdr->counts[2];
+    const int T = hdr->cap_tokens;
+    const PoolView& P = p.pool;
+    const int h8 = P.h >> 3, r_max = P.r_max;
+    const int n_sl = (h8 + kSplitVecs - 1) / kSplitVecs;
+    const int vl = threadIdx.x % kSplitVecs, g = threadIdx.x / kSplitVecs;
+    const long long total = (long long)p.nprob * n_chunks * n_sl;
+    auto chunk_of = [&](long long it) { return (int)((it / n_sl) % n_chunks); };
+    Chunk next;
+    if (blockIdx.x < total) next = chunks[chunk_of(blockIdx.x)];
+    for (long long item = blockIdx.x; item < total; item += gridDim.x) {
+        const int sl = (int)(item % n_sl);
+        const int pr = (int)(item / ((long long)n_sl * n_chunks));
+        const Chunk ch = next;   // loaded while the previous item was being computed
+        if (item + gridDim.x < total) next = chunks[chunk_of(item + gridDim.x)];
+        const int r = ch.rank;
+        const ProbDesc pd = p.probs[pr];
+        const long long blk0 = ch.pt_base + (long long)pd.blk * 2 * r;
+        const int v = sl * kSplitVecs + vl;
+        // one round trip: the chunk's page ids (all checked: the A rows' too, whose t a bad
+        // page left unwritten), its t values and this thread's y vectors
+        bool bad = false;
+        for (int e = threadIdx.x; e < 2 * r; e += blockDim.x) {
+            const int page = P.pt[blk0 + e];
+            bad |= (page < 0 || page >= P.num_pages);
+            if (e >= r) pg[e - r] = page;
+        }
+        for (int e = threadIdx.x; e < kChunk * r; e += blockDim.x) {
+            const int t = e / r, j = e % r;
+            ts[t][j] = t < ch.count ? tbuf[((long long)pr * T + ch.rows[t]) * r_max + j] : 0.f;
+        }
+        uint4 yv[kChunk];
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t)
+            yv[t] = (g == 0 && v < h8 && t < ch.count) ? ld16(pd.y + (long long)ch.rows[t] * pd.ldy + v * 8)
+                                                       : make_uint4(0, 0, 0, 0);
+        if (__syncthreads_or(bad)) {
+            if (threadIdx.x == 0) set_error(&hdr->err, LORA_DERR_PAGE);
+            continue;
+        }
+        float acc[kChunk][8];
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+        if (v < h8) {
+#pragma unroll 16
+            for (int j = g; j < r; j += kGroups) {
+                float b8[8];
+                unpack8(ld_stream16(P.pages + (long long)pg[j] * P.h + v * 8), b8);
+#pragma unroll
+                for (int t = 0; t < kChunk; ++t) {
+                    const float tj = ts[t][j];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(tj, b8[e], acc[t][e]);
+                }
+            }
+        }
+        if (g > 0) {
+#pragma unroll
+            for (int t = 0; t < kChunk; ++t)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) red[g - 1][t][vl][e] = acc[t][e];
+        }
+        __syncthreads();
+        if (g == 0 && v < h8) {
+#pragma unroll
+            for (int t = 0; t < kChunk; ++t) {
+                if (t >= ch.count) break;
+                __nv_bfloat16* yp = pd.y + (long long)ch.rows[t] * pd.ldy + v * 8;
+                float y8[8];
+                unpack8(yv[t], y8);
+                float s8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float s = acc[t][e];
+#pragma unroll
+                    for (int k = 0; k < kGroups - 1; ++k) s += red[k][t][vl][e];
+                    s8[e] = y8[e] + s;
+                }
+                uint4 o;
+                o.x = pack2(s8[0], s8[1]);
+                o.y = pack2(s8[2], s8[3]);
+                o.z = pack2(s8[4], s8[5]);
+                o.w = pack2(s8[6], s8[7]);
+                st16(yp, o);
+            }
+        }
+        __syncthreads();   // ts, pg and red are reused by the next item
+    }
+}
+
+}  // namespace lora

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "bgmv_ring.cuh"
+#include "bgmv_split.cuh"
 #include "common.cuh"
 #include "fused.cuh"
 #include "segment.cuh"
@@ -425,13 +426,70 @@ lora_status check_problems(const lora_pool_desc& d, const lora_problem* probs, i
 
 
 
+// ---------------------------------------------------------------------------- split path
+// Workspace bytes the split path's t takes for batches of up to max_tokens rows (none
+// above kSplitMaxTokens: larger batches never take that path).
+size_t split_t_bytes(const lora_pool_desc& d, int32_t max_tokens) {
+    if (max_tokens > kSplitMaxTokens) return 0;
+    return (size_t)kSplitMaxProbs * (size_t)max_tokens * (size_t)d.r_max * sizeof(float);
+}
+
+// The two-phase CUDA-core path serves launches of few projections of a decode-sized batch
+// (a chunk of one projection per CTA would leave most SMs idle), when the workspace has
+// room for its t.  LORA_SPLIT_MAX_PROBS overrides the projection limit (0 turns it off).
+bool split_fits(const lora_pool_desc& d, int32_t nprob, int32_t T, size_t ws_bytes) {
+    const char* e = getenv("LORA_SPLIT_MAX_PROBS");
+    const int max_p = e != nullptr ? std::min(atoi(e), kSplitMaxProbs) : kSplitDefaultProbs;
+    if (nprob < 1 || nprob > max_p || T < 1 || T > kSplitMaxTokens) return false;
+    // the grouping laid the workspace out for (T, segments); decode segments number at most T
+    return ws_bytes >= ws_layout(T, T).total + split_t_bytes(d, T);
+}
+
+lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
+                      cudaStream_t stream) {
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    static thread_local SplitParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.pool = view_of(pool);
+    prm.ws = reinterpret_cast<char*>(ws);
+    prm.nprob = nprob;
+    for (int32_t i = 0; i < nprob; ++i) {
+        const lora_problem& pr = probs[i];
+        prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
+        prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
+        prm.probs[i].ldx = (int32_t)pr.ldx;
+        prm.probs[i].ldy = (int32_t)pr.ldy;
+        prm.probs[i].blk = pr.layer * pool->d.num_proj + pr.proj;
+    }
+    const int grid = di->sm_count * 4;
+    const size_t xs_bytes = (size_t)kChunk * pool->d.h * 2;   // the chunk's x rows
+    static thread_local int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        st = cuda_status(cudaFuncSetAttribute(split_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)(kChunk * 8192 * 2)));   // h <= 8192
+        if (st != LORA_OK) return st;
+        attr_dev = dev;
+    }
+    split_shrink_kernel<<<grid, kSplitThreads, xs_bytes, stream>>>(prm);
+    st = cuda_status(cudaGetLastError());
+    if (st != LORA_OK) return st;
+    split_expand_kernel<<<grid, kSplitThreads, 0, stream>>>(prm);
+    return cuda_status(cudaGetLastError());
+}
+
 // The delta launches after grouping: the CUDA-core kernel over the chunk list, then
 // (when the batch may hold tensor-core tiles) the tensor-core kernel over the tile list.
 lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
-                      float* t_out, bool with_mma, cudaStream_t stream) {
+                      size_t ws_bytes, float* t_out, bool with_mma, cudaStream_t stream) {
     lora_status st = check_problems(pool->d, probs, nprob);
     if (st != LORA_OK) return st;
     const int h8 = pool->d.h / 8;
+    if (!with_mma && t_out == nullptr && split_fits(pool->d, nprob, T, ws_bytes))
+        return run_split(pool, probs, nprob, ws, stream);
     if (with_mma && mma_min_rows(pool->d) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
         // one launch per batch of projections for both work classes
         if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
@@ -526,7 +584,7 @@ lora_status lora_workspace_size(const lora_pool* pool, int32_t max_tokens, int32
     if (pool == nullptr || bytes == nullptr || max_tokens < 0 || max_segments < 0)
         return LORA_EINVAL;
     if (max_segments > LORA_MAX_SEGMENTS || max_tokens > (1 << 28)) return LORA_ETOOBIG;
-    *bytes = ws_layout(max_tokens, max_segments).total;
+    *bytes = ws_layout(max_tokens, max_segments).total + split_t_bytes(pool->d, max_tokens);
     return LORA_OK;
 }
 
@@ -552,16 +610,19 @@ lora_status lora_workspace_view(const lora_pool* pool, void* ws, size_t ws_bytes
     return LORA_OK;
 }
 
-lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
+// The grouping launch.  with_split_room: the workspace must also hold the split path's t
+// (the size lora_workspace_size reports); the allocation-free entry point, whose fixed
+// scratch has no such room and which never takes that path, passes false.
+static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
                          int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
-                         size_t ws_bytes, void* stream) {
+                         size_t ws_bytes, bool with_split_room, void* stream) {
     if (pool == nullptr || S < 0 || Td < 0 || T < 0) return LORA_EINVAL;
     if ((int64_t)S + Td > LORA_MAX_SEGMENTS || T > (1 << 28)) return LORA_ETOOBIG;
     if (S > 0 && (seg_start == nullptr || seg_adapter == nullptr)) return LORA_EINVAL;
     if (Td > 0 && dec_adapter == nullptr) return LORA_EINVAL;
     if (S == 0 && Td > T) return LORA_EINVAL;
     const WsLayout L = ws_layout(T, S + Td);
-    lora_status st = check_ws(ws, ws_bytes, L.total);
+    lora_status st = check_ws(ws, ws_bytes, L.total + (with_split_room ? split_t_bytes(pool->d, T) : 0));
     if (st != LORA_OK) return st;
     SegParams sp;
     memset(&sp, 0, sizeof sp);
@@ -597,6 +658,12 @@ lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const 
     return cuda_status(cudaGetLastError());
 }
 
+lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
+                         int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
+                         size_t ws_bytes, void* stream) {
+    return segment_impl(pool, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes, true, stream);
+}
+
 lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
                                int32_t S, void* ws, size_t ws_bytes, void* stream) {
     if (pool == nullptr || nprob < 0 || T < 0 || S < 0 || (nprob > 0 && probs == nullptr))
@@ -605,7 +672,7 @@ lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs,
     if (st != LORA_OK) return st;
     if (nprob == 0) return LORA_OK;
     // without prefill segments every segment has one row: no tensor-core tile exists
-    return run_delta(pool, probs, nprob, T, ws, nullptr, S > 0, (cudaStream_t)stream);
+    return run_delta(pool, probs, nprob, T, ws, ws_bytes, nullptr, S > 0, (cudaStream_t)stream);
 }
 
 lora_status lora_bgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -617,7 +684,7 @@ lora_status lora_bgmv(const lora_pool* pool, const lora_problem* probs, int32_t 
     if (nprob < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
     if (nprob == 0) return LORA_OK;
     // decode rows are one-row segments: the CUDA-core kernel serves all of them
-    return run_delta(pool, probs, nprob, T, ws, nullptr, false, (cudaStream_t)stream);
+    return run_delta(pool, probs, nprob, T, ws, ws_bytes, nullptr, false, (cudaStream_t)stream);
 }
 
 lora_status lora_sgmv(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
@@ -657,7 +724,7 @@ lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* p
     if (pool == nullptr || prob == nullptr || t_out == nullptr) return LORA_EINVAL;
     lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
     if (st != LORA_OK) return st;
-    return run_delta(pool, prob, 1, 0, ws, t_out, false, (cudaStream_t)stream);
+    return run_delta(pool, prob, 1, 0, ws, ws_bytes, t_out, false, (cudaStream_t)stream);
 }
 
 lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const int32_t* dst_pages,
@@ -713,10 +780,10 @@ lora_status lora_bgmv_noalloc(const lora_pool* pool, const lora_problem* probs, 
     // the error word is per call; the grouping kernel re-initialises everything else
     st = cuda_status(cudaMemsetAsync(&hdr->err, 0, sizeof(uint32_t), s));
     if (st != LORA_OK) return st;
-    st = lora_segment(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, kNoallocWsBytes, stream);
+    st = segment_impl(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, kNoallocWsBytes, false, stream);
     if (st != LORA_OK) return st;
     if (nprob > 0) {
-        st = run_delta(pool, probs, nprob, T, ws, nullptr, false, s);
+        st = run_delta(pool, probs, nprob, T, ws, kNoallocWsBytes, nullptr, false, s);
         if (st != LORA_OK) return st;
     }
     if (error_bits != nullptr)

@@ -130,7 +130,10 @@ lora_status lora_pool_destroy(lora_pool* pool);
 
 /* Bytes of device workspace needed by a call over at most max_tokens rows and at
  * most max_segments segments (prefill segments + decode tokens).  The workspace
- * holds the grouping of the batch, the work queue and the device error word. */
+ * holds the grouping of the batch, the work queue, the device error word and, for
+ * batches of up to 1024 rows, the fp32 t of launches of up to 8 projections
+ * (8 * max_tokens * r_max * 4 bytes), which such launches compute in a first phase
+ * and expand in a second so that a few projections still fill the GPU. */
 lora_status lora_workspace_size(const lora_pool* pool, int32_t max_tokens, int32_t max_segments,
                                 size_t* bytes);
 

@@ -96,7 +96,25 @@ def test_decode_ring_stage_shapes(pages, monkeypatch):
     """The decode ring with 4 and with 8 rows per stage on the same batch: ranks that are
     not multiples of either and chunks of 1 to 4 rows (a skewed adapter mix)."""
     monkeypatch.setenv("LORA_RING_PAGES", pages)
+    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", "0")   # the ring kernel, not the split path
     wl = small_decode(65, 2048, 1, 3, 12, [1, 3, 5, 8, 13, 64, 100], 57, zipf=1.3)
+    case = GpuCase(wl)
+    try:
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("split", ["0", "8"])
+@pytest.mark.parametrize("h", [512, 4096, 5120])
+def test_decode_split_and_ring_paths(split, h, monkeypatch):
+    """The same few-projection decode batch through the two-phase split kernels (up to 8
+    projections) and through the ring kernel: ranks not multiples of 8 rows, chunks of 1
+    to 4 rows, base-only rows, ranks up to 128."""
+    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", split)
+    wl = small_decode(66, h, 2, 3, 10, [1, 5, 8, 16, 64, 128], 47, zipf=1.2)
+    wl.batch.dec_adapter[::9] = -1
     case = GpuCase(wl)
     try:
         assert case.run() == 0
