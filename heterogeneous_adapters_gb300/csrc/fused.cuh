@@ -36,13 +36,13 @@ __device__ __forceinline__ uint32_t fused_split(const WsHeader* hdr, uint32_t G,
     return gf;
 }
 
-template <int NV, int CW>
+template <int NV, int CW, int RP>
 __global__ void __launch_bounds__(kMmaThreads, 1) delta_fused_kernel(const __grid_constant__ FusedParams p) {
     static_assert(CW * 32 + 32 <= kMmaThreads, "ring body must fit the fused CTA");
     extern __shared__ __align__(1024) unsigned char fused_smem_raw[];
     const uint32_t gf = fused_split(reinterpret_cast<const WsHeader*>(p.mma.ws), gridDim.x, p.ring_speed);
     if (blockIdx.x < gf)
-        ring_cta<NV, CW, kRingPagesSmall>(p.ring, fused_smem_raw, blockIdx.x, gf);
+        ring_cta<NV, CW, RP>(p.ring, fused_smem_raw, blockIdx.x, gf);
     else
         mma_cta(p.mma, fused_smem_raw, blockIdx.x - gf, gridDim.x - gf);
 }

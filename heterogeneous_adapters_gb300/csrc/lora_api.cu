@@ -304,7 +304,7 @@ lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* 
 
 template <int MAXP>
 void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, void* ws,
-               float* t_out, int stages) {
+               float* t_out, int stages, int rows_per_stage) {
     const lora_pool_desc& d = pool->d;
     memset(&prm, 0, sizeof prm);
     prm.pool = view_of(pool);
@@ -312,7 +312,7 @@ void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem
     prm.t_out = t_out;
     prm.nprob = n;
     prm.stages = stages;
-    prm.stage_bytes = kRingPagesSmall * 2 * d.h;
+    prm.stage_bytes = rows_per_stage * 2 * d.h;
     for (int32_t i = 0; i < n; ++i) {
         const lora_problem& pr = probs[i];
         prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
@@ -364,21 +364,13 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
 
 constexpr float kFusedRingSpeed = 1.22f;
 
-// Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0).
-template <int NV, int CW>
-lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
-                         cudaStream_t stream) {
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    MmaConfig c;
-    st = mma_config(pool->d, di->smem_optin, &c);
-    if (st != LORA_OK) return st;
-    // the ring body of this kernel uses the small stages
-    size_t ring_smem = 0;
-    const int S = ring_stages(di->smem_optin, kRingPagesSmall * 2 * pool->d.h, pool->d.r_max, CW, &ring_smem);
-    if (S < 2) return LORA_ETOOBIG;
-    const size_t smem = c.smem > ring_smem ? c.smem : ring_smem;
+// Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0); the
+// ring body takes the stage shape the stand-alone ring kernel would take.
+template <int NV, int CW, int RP>
+lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
+                            void* ws, const DeviceInfo* di, const MmaConfig& c, const RingShape& sh,
+                            cudaStream_t stream) {
+    const size_t smem = c.smem > sh.smem ? c.smem : sh.smem;
     static thread_local FusedParams prm;
     // per-CTA byte rate of the ring body relative to the tensor-core body, measured on the
     // 13B mixed step (ring CTAs split by bytes alone ended 18% before the tensor-core ones);
@@ -389,7 +381,8 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     static thread_local size_t attr_smem = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = delta_fused_kernel<NV, CW>;
+    auto kern = delta_fused_kernel<NV, CW, RP>;
+    lora_status st;
     if (attr_dev != dev || attr_smem < smem) {
         st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         if (st != LORA_OK) return st;
@@ -401,13 +394,29 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
         const int32_t n = nprob - base < per ? nprob - base : per;
         st = fill_mma(prm.mma, pool, probs + base, n, T, ws, c);
         if (st != LORA_OK) return st;
-        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, S);
+        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, sh.stages, RP);
         prm.ring_speed = ring_speed;
         kern<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
         st = cuda_status(cudaGetLastError());
         if (st != LORA_OK) return st;
     }
     return LORA_OK;
+}
+
+template <int NV, int CW>
+lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                         cudaStream_t stream) {
+    DeviceInfo* di = nullptr;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    MmaConfig c;
+    st = mma_config(pool->d, di->smem_optin, &c);
+    if (st != LORA_OK) return st;
+    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW);
+    if (sh.stages < 2) return LORA_ETOOBIG;
+    if (sh.rp == kRingPagesLarge)
+        return launch_fused_rp<NV, CW, kRingPagesLarge>(pool, probs, nprob, T, ws, di, c, sh, stream);
+    return launch_fused_rp<NV, CW, kRingPagesSmall>(pool, probs, nprob, T, ws, di, c, sh, stream);
 }
 
 lora_status check_problems(const lora_pool_desc& d, const lora_problem* probs, int32_t nprob) {
