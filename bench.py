@@ -255,10 +255,19 @@ class OracleRunner:
         return self.rate(dt, n), dt, n
 
 
+def selected_workload(args):
+    """The workload of --config, with q, k and v reading one x per layer under --shared-x."""
+    import dataclasses
+    wl = workload_for(args.config)
+    if args.shared_x:
+        wl = dataclasses.replace(wl, shared_x=True, name=wl.name + "-shared-x")
+    return wl
+
+
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
-    wl = workload_for(args.config)
+    wl = selected_workload(args)
     runner = OracleRunner(wl, args.ref_problems)
     one = runner.run(1)
     for _ in range(args.warmup):
@@ -316,12 +325,13 @@ def graph_timing(capture_fn, tokens_step: int, dev, replays: int) -> dict:
 def config_dict(wl, args) -> dict:
     from heterogeneous_adapters_gb300 import costmodel
     p = wl.pool
-    m = costmodel.decode_step_bytes(p.ranks, wl.batch.token_adapter(), p.h, len(wl.problems))
+    x_buffers = len({wl.x_source(l, pj) for (l, pj) in wl.problems})
+    m = costmodel.decode_step_bytes(p.ranks, wl.batch.token_adapter(), p.h, len(wl.problems), x_buffers)
     return {"workload": wl.name, "h": p.h, "layers": p.num_layers, "projections": p.num_proj,
             "tokens": wl.batch.num_tokens, "adapted_tokens": m["adapted_tokens"],
             "adapters": p.num_adapters, "distinct_adapters": m["distinct_adapters"],
             "ranks": sorted(set(int(r) for r in np.unique(p.ranks))), "batch": wl.batch.kind,
-            "seed": wl.seed, "bytes_per_step": m["bytes"],
+            "seed": wl.seed, "shared_x": wl.shared_x, "bytes_per_step": m["bytes"],
             "l2": "inputs larger than L2: every step streams %.2f GB" % (m["bytes"] / 1e9),
             "parallelism": "replicas (weak scaling, no collective)"}
 
@@ -335,7 +345,7 @@ def run_ours(args, rank: int, world: int, local: int):
 
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    wl = workload_for(args.config)
+    wl = selected_workload(args)
     d = device_inputs(wl, device=dev, nan_dummies=False)
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
@@ -343,11 +353,12 @@ def run_ours(args, rank: int, world: int, local: int):
     b = wl.batch
     T, S, Td = b.num_tokens, b.num_segments, b.num_decode
     nbytes = lora.workspace_size(pool, T, S + Td)
+    x_idx = sorted(set(d.x_src))   # the distinct x buffers (fewer when inputs are shared)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream_obj = torch.cuda.current_stream(dev)
     stream = stream_obj.cuda_stream
     lora.workspace_init(ws, nbytes, stream)
-    probs = [(d.x[i], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    probs = [(d.x[d.x_src[i]], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
     seg_start = d.seg_start if S else None
     seg_adapter = d.seg_adapter if S else None
     dec = d.dec_adapter if Td else None
@@ -358,7 +369,7 @@ def run_ours(args, rank: int, world: int, local: int):
     def delta():
         lora.delta_grouped(pool, probs, T, S, ws, nbytes, stream)
 
-    m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems))
+    m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems), len(x_idx))
     # the delta launches of the step: the CUDA-core kernel alone for decode batches (up to
     # 256 projections a launch); for batches with prefill segments the fused two-class
     # kernel where h allows it (h a multiple of 128, h <= 5120; up to 64 projections a
@@ -456,7 +467,7 @@ def run_ours(args, rank: int, world: int, local: int):
         xs = d.x if k == 0 else torch.empty_like(d.x)
         ys = d.y if k == 0 else torch.empty_like(d.y)
         metas = [torch.empty_like(m) for m in meta_src]
-        probs_k = [(xs[i], ys[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+        probs_k = [(xs[d.x_src[i]], ys[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
         slots.append((xs, ys, metas, probs_k))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     e2e_steps = max(3, min(args.steps, 50))
@@ -482,7 +493,11 @@ def run_ours(args, rank: int, world: int, local: int):
                     first_event.record(s_in)
                 if ev_out[k % n_slots] is not None:
                     s_in.wait_event(ev_out[k % n_slots])
-                xs.copy_(xh, non_blocking=True)
+                if len(x_idx) == len(d.problems):
+                    xs.copy_(xh, non_blocking=True)
+                else:   # only the x buffers that are read
+                    for i in x_idx:
+                        xs[i].copy_(xh[i], non_blocking=True)
                 ys.copy_(yh, non_blocking=True)
                 for m_d, m_h in zip(metas, meta_h):
                     m_d.copy_(m_h, non_blocking=True)
@@ -510,7 +525,8 @@ def run_ours(args, rank: int, world: int, local: int):
     e2e_elapsed = max_over_ranks(s0.elapsed_time(s1) / 1e3, world)
     api_name = {"decode": "lora_bgmv", "prefill": "lora_sgmv"}.get(b.kind, "lora_apply_mixed")
     e2e = {"value": tokens_step * e2e_steps * world / e2e_elapsed, "unit": UNIT,
-           "h2d_bytes_per_step": d.x.numel() * 2 + d.y.numel() * 2 + sum(m.numel() * 4 for m in meta_h),
+           "h2d_bytes_per_step": d.x[0].numel() * 2 * len(x_idx) + d.y.numel() * 2 +
+                                 sum(m.numel() * 4 for m in meta_h),
            "d2h_bytes_per_step": d.y.numel() * 2, "steps": e2e_steps,
            "api": f"{api_name} (C ABI); pinned host x, y and adapter ids in, y out, every step; "
                   f"three device slots, copies of neighbouring steps overlapping the call"}
@@ -815,6 +831,8 @@ def main():
                     help="resident adapter slices in the unified-pool stress workload")
     ap.add_argument("--stage-steps", type=int, default=20,
                     help="steps of the staging scenario (configs 4d / 4z)")
+    ap.add_argument("--shared-x", action="store_true",
+                    help="q, k and v of a layer read one x (as in a transformer), not one each")
     ap.add_argument("--sweep-distinct", action="store_true",
                     help="instead of the bench line: decode tokens/s against the number of "
                          "distinct adapters in the batch (1..64) at config 1's shape")

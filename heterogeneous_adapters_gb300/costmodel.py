@@ -39,20 +39,24 @@ def transfer_seconds(nbytes: float, bytes_per_s: float) -> float:
 
 
 def decode_step_bytes(ranks_by_adapter: np.ndarray, token_adapter: np.ndarray, h: int,
-                      nprob: int) -> dict:
+                      nprob: int, x_buffers: int | None = None) -> dict:
     """Algorithmic bytes and flops of one multi-problem launch over nprob projections
-    of size h x h, for a batch whose per-token adapter ids are token_adapter."""
+    of size h x h, for a batch whose per-token adapter ids are token_adapter.
+    x_buffers: the distinct x buffers the projections read (projections that share their
+    input, as q, k and v of a layer do, read it once); nprob if None."""
     ids = np.asarray(token_adapter, dtype=np.int64)
     adapted = ids[ids >= 0]
     distinct = np.unique(adapted)
     r_d = np.asarray(ranks_by_adapter, dtype=np.int64)[distinct]
     r_t = np.asarray(ranks_by_adapter, dtype=np.int64)[adapted]
     page_bytes = int(2 * r_d.sum()) * h * BF16
-    xy_bytes = adapted.size * 3 * h * BF16
+    x_bytes = adapted.size * h * BF16            # x read
+    y_bytes = adapted.size * 2 * h * BF16        # y read and written
     meta_bytes = int(2 * r_d.sum()) * 4 + ids.size * 4
-    per_prob = page_bytes + xy_bytes + meta_bytes
+    xb = nprob if x_buffers is None else x_buffers
+    xy_total = x_bytes * xb + y_bytes * nprob
     flops = int(adapted.size and (2 * r_t * (2 * h)).sum())
-    return {"bytes": per_prob * nprob, "page_bytes": page_bytes * nprob,
-            "xy_bytes": xy_bytes * nprob, "meta_bytes": meta_bytes * nprob,
+    return {"bytes": (page_bytes + meta_bytes) * nprob + xy_total, "page_bytes": page_bytes * nprob,
+            "xy_bytes": xy_total, "meta_bytes": meta_bytes * nprob,
             "flops": flops * nprob, "adapted_tokens": int(adapted.size),
             "tokens": int(ids.size), "distinct_adapters": int(distinct.size)}

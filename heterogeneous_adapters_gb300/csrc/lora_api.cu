@@ -290,6 +290,16 @@ lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* 
         if (st != LORA_OK) return st;
         prm.blk[i] = pr.layer * d.num_proj + pr.proj;
     }
+    // runs of consecutive problems reading the same x form the item order's groups
+    for (int32_t i = 0; i < n;) {
+        int32_t j = i + 1;
+        while (j < n && probs[j].x == probs[i].x && probs[j].ldx == probs[i].ldx) ++j;
+        for (int32_t k = i; k < j; ++k) {
+            prm.xgrp_off[k] = (uint8_t)(k - i);
+            prm.xgrp_size[k] = (uint8_t)(j - i);
+        }
+        i = j;
+    }
     prm.pool = view_of(pool);
     prm.ws = reinterpret_cast<char*>(ws);
     prm.nprob = n;

@@ -59,6 +59,8 @@ struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
     int32_t s1_bytes, s2_bytes;              // stage sizes (y stages are 32 KB)
     int32_t rp_max;
     int32_t pad;
+    uint8_t xgrp_off[kMmaMaxProbs];          // position of each problem in its shared-x group
+    uint8_t xgrp_size[kMmaMaxProbs];         // size of that group
 };
 
 struct MmaSmem {
@@ -100,11 +102,20 @@ struct MmaItem {
     bool ok;
 };
 
+// Item order.  Projections that read the same x (consecutive problems with the same input,
+// as q, k and v of a layer) form a group; a group's items are tile-major, so the group's
+// projections of one tile are neighbouring items, dealt to neighbouring CTAs at the same
+// time, and each x tile comes from DRAM once and from L2 for the others.  Across groups,
+// and for a projection alone in its group, items are projection-major, so consecutive
+// tiles of one segment (which read the same adapter pages) run side by side.
 __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tiles, int n_tiles, uint32_t item,
                                             int lane) {
     MmaItem it;
-    it.tile = tiles[item % n_tiles];
-    it.pr = item / n_tiles;
+    const uint32_t p0 = item / (uint32_t)n_tiles;          // projection-major position
+    const uint32_t start = p0 - p.xgrp_off[p0];           // the group's first projection
+    const uint32_t local = item - (uint32_t)n_tiles * start;
+    it.tile = tiles[local / p.xgrp_size[p0]];
+    it.pr = start + local % p.xgrp_size[p0];
     const int r = it.tile.rank;
     it.rp = mma_rpad(r);
     it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * 2 * r;

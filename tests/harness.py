@@ -52,7 +52,7 @@ class GpuCase:
 
     def problems(self):
         h = self.wl.h
-        return [(self.dev.x[i], self.dev.y[i], h, h, l, p)
+        return [(self.dev.x[self.dev.x_src[i]], self.dev.y[i], h, h, l, p)
                 for i, (l, p) in enumerate(self.dev.problems)]
 
     def run(self, mode=None):

@@ -123,6 +123,35 @@ def test_decode_split_and_ring_paths(split, h, monkeypatch):
         case.close()
 
 
+@pytest.mark.parametrize("kind", ["prefill", "mixed", "decode"])
+def test_shared_x_inputs(kind):
+    """q, k and v of a layer read one x buffer (the other projections' own x buffers hold
+    NaN, so reading one of them would show); the tensor-core items of a tile for those
+    projections run side by side."""
+    import dataclasses
+
+    import torch
+    if kind == "prefill":
+        wl = small_prefill(67, 1024, 2, 4, 8, [8, 16, 64], [200, 33, 7, 130])
+    elif kind == "mixed":
+        wl = _mixed(68, 2048, 1, 4, 12, [8, 32, 128], [150, 40], 30, 3)
+    else:
+        wl = small_decode(69, 2048, 2, 4, 15, [4, 16, 64], 40)
+    wl = dataclasses.replace(wl, shared_x=True)
+    case = GpuCase(wl)
+    try:
+        used = set(case.dev.x_src)
+        assert len(used) < len(wl.problems)
+        for i in range(len(wl.problems)):
+            if i not in used:
+                case.dev.x[i].fill_(float("nan"))
+        torch.cuda.synchronize()
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+    finally:
+        case.close()
+
+
 def test_t_matches_oracle_shrink():
     """fp32 t (the value the expand consumes, scaled) against the oracle's fp64 t."""
     import torch

@@ -73,7 +73,7 @@ def host_inputs(wl: Workload, problems=None, adapters=None, with_xy: bool = True
     if with_xy:
         T = wl.batch.num_tokens
         for (l, p) in problems:
-            x[(l, p)] = host_rows(wl, KIND_X, l, p, T)
+            x[(l, p)] = host_rows(wl, KIND_X, *wl.x_source(l, p), T)
             y0[(l, p)] = host_rows(wl, KIND_Y, l, p, T)
     return HostInputs(compact, pt, x, y0)
 
@@ -102,6 +102,7 @@ class DeviceInputs:
     dec_adapter: object       # torch int32 [Td]
     token_adapter: object     # torch int32 [T]
     problems: list
+    x_src: list = None        # problem i reads x[x_src[i]] (its own x unless inputs are shared)
 
 
 def device_fill_pool(wl: Workload, pool_t, stream: int, nan_dummies: bool = True) -> None:
@@ -125,7 +126,8 @@ def device_fill_rows(wl: Workload, buf, kind: int, problems, stream: int) -> Non
     """Fill buf [nprob, T, h] with the x or y0 rows of the given problems."""
     import torch
     T = buf.shape[1]
-    keys = np.concatenate([row_key(kind, l, p, np.arange(T)) for (l, p) in problems])
+    src = [wl.x_source(l, p) if kind == KIND_X else (l, p) for (l, p) in problems]
+    keys = np.concatenate([row_key(kind, l, p, np.arange(T)) for (l, p) in src])
     rows = torch.arange(len(problems) * T, dtype=torch.int64, device=buf.device)
     keys_t = torch.from_numpy(keys.view(np.int64)).to(buf.device)
     sigma = SIGMA_X if kind == KIND_X else SIGMA_Y
@@ -161,4 +163,6 @@ def device_inputs(wl: Workload, problems=None, device="cuda", nan_dummies: bool 
         ranks=i32(pool.ranks), scales=torch.from_numpy(pool.scales).to(device),
         x=x, y=y, seg_start=i32(b.seg_start), seg_adapter=i32(b.seg_adapter),
         dec_adapter=i32(b.dec_adapter), token_adapter=i32(b.token_adapter()),
-        problems=list(problems))
+        problems=list(problems),
+        x_src=[problems.index(wl.x_source(l, p)) if wl.x_source(l, p) in problems else i
+               for i, (l, p) in enumerate(problems)])

@@ -125,10 +125,16 @@ class Workload:
     batch: Batch
     problems: list = field(default_factory=list)   # [(layer, proj)] of one step
     notes: str = ""
+    # q, k and v (projections 0, 1, 2) of a layer read one input x, as in a transformer
+    shared_x: bool = False
 
     @property
     def h(self) -> int:
         return self.pool.h
+
+    def x_source(self, l: int, p: int):
+        """The (layer, projection) whose x buffer problem (l, p) reads."""
+        return (l, 0) if self.shared_x and p < 3 else (l, p)
 
 
 # ----------------------------------------------------------------------------- pool layouts
