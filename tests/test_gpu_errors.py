@@ -18,8 +18,15 @@ def _wl():
     return small_decode(71, 512, 1, 2, 6, [4, 8], 20)
 
 
-def test_bad_adapter_id_sets_bit_and_skips_only_that_token():
+# the decode batches here have 2 projections: the split path by default, the ring kernel
+# when the split path is turned off
+PATHS = {"split": "8", "ring": "0"}
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_bad_adapter_id_sets_bit_and_skips_only_that_token(path, monkeypatch):
     import torch
+    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
     wl = _wl()
     case = GpuCase(wl)
     try:
@@ -39,8 +46,10 @@ def test_bad_adapter_id_sets_bit_and_skips_only_that_token():
         case.close()
 
 
-def test_bad_page_rank_and_block_bits():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_bad_page_rank_and_block_bits(path, monkeypatch):
     import torch
+    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
     wl = _wl()
     case = GpuCase(wl)
     try:
@@ -57,6 +66,32 @@ def test_bad_page_rank_and_block_bits():
         assert case.run() & 0x4
         case.dev.pt_off[a] = int(wl.pool.pt_off[a])
         assert case.run() == 0
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("ab", [0, 1])
+def test_bad_page_skips_that_adapter_in_that_projection_only(path, ab, monkeypatch):
+    """An out-of-range A-row (ab=0) or B-column (ab=1) page of adapter a in projection 0:
+    the page bit is set, a's rows of projection 0 keep their y, everything else is right."""
+    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
+    wl = _wl()
+    case = GpuCase(wl)
+    try:
+        ids = wl.batch.token_adapter()
+        a = int(ids[ids >= 0][0])
+        l, p = wl.problems[0]
+        e = int(wl.pool.block_entries(a, l, p, ab)[-1])
+        case.dev.pt[e] = wl.pool.num_pages
+        before = case.y_bits(0).copy()
+        assert case.run() & 0x8
+        rows = ids == a
+        assert np.array_equal(case.y_bits(0)[rows], before[rows])
+        full_check(wl, case, [1])                          # projection 1 is untouched by the error
+        # projection 0's other rows: compare with the oracle taking a's rows as base rows
+        wl.batch.dec_adapter[rows] = -1                    # decode only: rows are the decode ids
+        full_check(wl, case, [0])
     finally:
         case.close()
 
