@@ -51,7 +51,7 @@ def _load():
         lib = ctypes.CDLL(SO)
         p = ctypes.c_void_p
         i32, i64 = ctypes.c_int32, ctypes.c_int64
-        lib.oracle_lora_delta.argtypes = [p, i64, i32, p, i64, p, p, p, i32, i32, i32, i32,
+        lib.oracle_lora_delta.argtypes = [p, i64, i32, p, i64, p, p, p, i32, i32, i32, i32, p,
                                           i32, i32, p, i64, p, i64, p, i32, p, i64, p, p]
         lib.oracle_lora_delta.restype = ctypes.c_int
         _lib = lib
@@ -65,12 +65,13 @@ class OracleError(RuntimeError):
 def lora_delta(pool: np.ndarray, pt: np.ndarray, pt_off: np.ndarray, ranks: np.ndarray,
                scales: np.ndarray, num_layers: int, num_proj: int, layer: int, proj: int,
                x: np.ndarray, y0: np.ndarray, token_adapter: np.ndarray,
-               want_t: bool = False):
+               want_t: bool = False, proj_dims=None):
     """y_ref = y0 + delta for one (layer, proj) problem, in float64.
 
-    pool: uint16 [num_pages, h] raw bf16 bits;  x: uint16 [T, h] raw bf16 bits;
-    y0: float64 [T, h] (bf16 inputs widened by the caller); token_adapter int32 [T].
-    Returns (y_ref [T, h] float64, t [T, r_max] float64 or None, multiply-adds).
+    pool: uint16 [num_pages, h] raw bf16 bits;  x: uint16 [T, d_in] raw bf16 bits;
+    y0: float64 [T, d_out] (bf16 inputs widened by the caller); token_adapter int32 [T].
+    proj_dims: (d_in, d_out) of every projection, or None for h x h everywhere.
+    Returns (y_ref [T, d_out] float64, t [T, r_max] float64 or None, multiply-adds).
     """
     pool = np.ascontiguousarray(pool, dtype=np.uint16)
     x = np.ascontiguousarray(x, dtype=np.uint16)
@@ -82,16 +83,19 @@ def lora_delta(pool: np.ndarray, pt: np.ndarray, pt_off: np.ndarray, ranks: np.n
     ids = np.ascontiguousarray(token_adapter, dtype=np.int32)
     T = ids.size
     h = pool.shape[1]
-    assert x.shape == (T, h) and y0.shape == (T, h)
+    dims = None if proj_dims is None else np.ascontiguousarray(proj_dims, dtype=np.int32).reshape(-1)
+    d_in, d_out = (h, h) if dims is None else (int(dims[2 * proj]), int(dims[2 * proj + 1]))
+    assert x.shape == (T, d_in) and y0.shape == (T, d_out)
     r_max = int(ranks.max()) if ranks.size else 1
-    y = np.empty((T, h), dtype=np.float64)
+    y = np.empty((T, d_out), dtype=np.float64)
     t = np.empty((T, r_max), dtype=np.float64) if want_t else None
     madds = ctypes.c_int64(0)
     err = _load().oracle_lora_delta(
         pool.ctypes.data, pool.shape[0], h, pt.ctypes.data, pt.size, pt_off.ctypes.data,
         ranks.ctypes.data, scales.ctypes.data, ranks.size, num_layers, num_proj, r_max,
-        layer, proj, x.ctypes.data, h, y0.ctypes.data, h, ids.ctypes.data, T,
-        y.ctypes.data, h, t.ctypes.data if t is not None else None, ctypes.byref(madds))
+        dims.ctypes.data if dims is not None else None,
+        layer, proj, x.ctypes.data, d_in, y0.ctypes.data, d_out, ids.ctypes.data, T,
+        y.ctypes.data, d_out, t.ctypes.data if t is not None else None, ctypes.byref(madds))
     if err:
         raise OracleError(ERRORS.get(err, str(err)))
     return y, t, int(madds.value)
@@ -113,15 +117,31 @@ def group_tokens(token_adapter: np.ndarray):
     return perm.astype(np.int32), grp_start, sid[starts].astype(np.int32)
 
 
+def block_units(num_proj: int, h: int, proj_dims=None):
+    """Page-table layout in units of an adapter's rank: (units of one layer, units before
+    projection p, pages per A row of p, pages per B column of p) for every p; a vector of
+    length d takes ceil(d / h) pages."""
+    def pv(d):
+        return -(-int(d) // h)
+    dims = [(h, h)] * num_proj if proj_dims is None else [tuple(map(int, d)) for d in
+                                                         np.asarray(proj_dims).reshape(-1, 2)]
+    pre, acc = [], 0
+    for d_in, d_out in dims:
+        pre.append(acc)
+        acc += pv(d_in) + pv(d_out)
+    return acc, pre, [pv(d[0]) for d in dims], [pv(d[1]) for d in dims]
+
+
 def page_list(pt: np.ndarray, pt_off: np.ndarray, ranks: np.ndarray, num_proj: int,
-              layer: int, proj: int, grp_adapter: np.ndarray) -> np.ndarray:
-    """Gathered page ids of one problem, group by group: the r_a A-row pages then the
-    r_a B-column pages of each group's adapter (page-table walk)."""
+              layer: int, proj: int, grp_adapter: np.ndarray, h: int = 0, proj_dims=None) -> np.ndarray:
+    """Gathered page ids of one problem, group by group: the A-row pages then the
+    B-column pages of each group's adapter (page-table walk), each block page block by
+    page block (page kb of every row, then page kb + 1)."""
+    U, pre, pv_in, pv_out = block_units(num_proj, max(h, 1), proj_dims)
     out = []
     for a in np.asarray(grp_adapter, dtype=np.int64):
         r = int(ranks[a])
-        for ab in (0, 1):
-            base = int(pt_off[a]) + ((layer * num_proj + proj) * 2 + ab) * r
-            out.append(np.asarray(pt[base:base + r], dtype=np.int32))
+        base = int(pt_off[a]) + r * (layer * U + pre[proj])
+        out.append(np.asarray(pt[base:base + r * (pv_in[proj] + pv_out[proj])], dtype=np.int32))
     return np.concatenate(out) if out else np.zeros(0, np.int32)
 

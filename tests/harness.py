@@ -51,8 +51,8 @@ class GpuCase:
         lora.workspace_init(self.ws, self.ws_bytes, self.stream)
 
     def problems(self):
-        h = self.wl.h
-        return [(self.dev.x[self.dev.x_src[i]], self.dev.y[i], h, h, l, p)
+        ldx, ldy = self.dev.x.shape[2], self.dev.y.shape[2]
+        return [(self.dev.x[self.dev.x_src[i]], self.dev.y[i], ldx, ldy, l, p)
                 for i, (l, p) in enumerate(self.dev.problems)]
 
     def run(self, mode=None):
@@ -74,7 +74,9 @@ class GpuCase:
         return self.lora.get_device_error(self.ws, self.stream)
 
     def y_bits(self, idx) -> np.ndarray:
-        return self.dev.y[idx].view(self.torch.int16).cpu().numpy().view(np.uint16)
+        """y rows of problem idx, its d_out columns."""
+        d_out = self.wl.pool.dims(self.dev.problems[idx][1])[1]
+        return self.dev.y[idx, :, :d_out].contiguous().view(self.torch.int16).cpu().numpy().view(np.uint16)
 
     def y_f64(self, idx) -> np.ndarray:
         return vg.bf16_bits_to_f64(self.y_bits(idx))
@@ -88,12 +90,24 @@ class GpuCase:
 
 def oracle_problem(wl, hi, l, p, y0_zero=False, ids=None, want_t=False):
     pool = wl.pool
-    y0 = np.zeros((wl.batch.num_tokens, wl.h)) if y0_zero else vg.bf16_bits_to_f64(hi.y0[(l, p)])
+    d_out = pool.dims(p)[1]
+    y0 = np.zeros((wl.batch.num_tokens, d_out)) if y0_zero else vg.bf16_bits_to_f64(hi.y0[(l, p)])
     ids = wl.batch.token_adapter() if ids is None else ids
     y_ref, t_ref, _ = oracle.lora_delta(hi.pool, hi.pt, pool.pt_off, pool.ranks, pool.scales,
                                         pool.num_layers, pool.num_proj, l, p, hi.x[(l, p)], y0,
-                                        ids, want_t=want_t)
+                                        ids, want_t=want_t, proj_dims=pool.proj_dims)
     return y_ref, t_ref, y0
+
+
+def block_values(wl, hi, a, l, p, ab):
+    """A rows (ab=0, [r, d_in]) or B columns (ab=1, [r, d_out]) of adapter a for (l, p),
+    float64, assembled from their pages (page kb of every vector, then page kb + 1)."""
+    pool = wl.pool
+    r = int(pool.ranks[a])
+    d = pool.dims(p)[ab]
+    pages = vg.bf16_bits_to_f64(hi.pool[hi.pt[pool.block_entries(a, l, p, ab)]])   # [pv * r, h]
+    pv = pages.shape[0] // r
+    return pages.reshape(pv, r, pool.h).transpose(1, 0, 2).reshape(r, pv * pool.h)[:, :d]
 
 
 def magnitude_sums(wl, hi, l, p):
@@ -102,17 +116,17 @@ def magnitude_sums(wl, hi, l, p):
     pool = wl.pool
     ids = wl.batch.token_adapter()
     xa = np.abs(vg.bf16_bits_to_f64(hi.x[(l, p)]))
-    T, h = xa.shape
+    T = xa.shape[0]
     S = np.zeros((T, pool.r_max))
-    M = np.zeros((T, h))
+    M = np.zeros((T, pool.dims(p)[1]))
     for a in np.unique(ids[ids >= 0]):
         rows = np.nonzero(ids == a)[0]
-        A = np.abs(vg.bf16_bits_to_f64(hi.pool[hi.pt[pool.block_entries(a, l, p, 0)]]))
-        B = np.abs(vg.bf16_bits_to_f64(hi.pool[hi.pt[pool.block_entries(a, l, p, 1)]]))
+        A = block_values(wl, hi, a, l, p, 0)
+        B = np.abs(block_values(wl, hi, a, l, p, 1))
         Xa = vg.bf16_bits_to_f64(hi.x[(l, p)])[rows]
         r = A.shape[0]
-        S[rows, :r] = xa[rows] @ A.T
-        tabs = np.abs(Xa @ vg.bf16_bits_to_f64(hi.pool[hi.pt[pool.block_entries(a, l, p, 0)]]).T)
+        S[rows, :r] = xa[rows] @ np.abs(A).T
+        tabs = np.abs(Xa @ A.T)
         M[rows] = float(pool.scales[a]) * ((tabs + T_ACC * S[rows, :r]) @ B)
     return S, M
 

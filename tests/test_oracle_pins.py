@@ -79,6 +79,69 @@ def test_merge_identity(make):
             np.testing.assert_allclose(y_ref[i], want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max()))
 
 
+def dense_adapter_widths(wl, a, layer, proj):
+    """Dense A (r x d_in) and B (d_out x r) of adapter a for (layer, proj) of a pool with
+    per-projection widths, from the generator keys of the layout convention: a vector of
+    length d takes ceil(d/h) pages, the block of (layer, proj, A or B) lists page kb of every
+    vector, then page kb + 1; blocks in (layer, proj, A, B) order.  Never through the page
+    table."""
+    pool = wl.pool
+    r, h, P = int(pool.ranks[a]), pool.h, pool.num_proj
+    dims = [tuple(int(v) for v in d) for d in pool.proj_dims]
+    npg = [(-(-di // h), -(-do // h)) for di, do in dims]
+    layer_units = sum(pi + po for pi, po in npg)
+    unit0 = layer * layer_units + sum(pi + po for pi, po in npg[:proj])
+    out = []
+    for ab, dist, param in ((0, vg.DIST_UNIFORM, a_param(h)),
+                            (1, vg.DIST_NORMAL, vg.normal_param(spec.SIGMA_B))):
+        d = dims[proj][ab]
+        first = unit0 + (npg[proj][0] if ab else 0)
+        full = np.zeros((r, npg[proj][ab] * h))
+        for kb in range(npg[proj][ab]):
+            local = (first + kb) * r + np.arange(r)
+            rows = np.zeros((r, h), np.uint16)
+            vg.fill_rows_host(rows, np.arange(r), spec.page_key(a, local), wl.seed, dist, param)
+            full[:, kb * h:(kb + 1) * h] = vg.bf16_bits_to_f64(rows)
+        out.append(full[:, :d])
+    A, Bcols = out
+    return A, Bcols.T
+
+
+def test_merge_identity_projection_widths():
+    """The merge identity on a pool whose projections are not h x h ("Multi-LoRA serving:
+    S-LoRA, Punica and adapter batching", "Worked example": grouped-query k/v narrower than
+    h, the MLP wider, every projection adapted): widths below one page, spanning several
+    pages, and ending mid-page, for A and B."""
+    h = 64
+    dims = [(64, 16), (64, 160), (160, 64), (40, 24)]
+    wl = spec.decode_workload("pin-widths", 21, h, 2, len(dims), 5, [1, 2, 4, 8, 16], 24, None,
+                              base_ids=True, proj_dims=dims)
+    hi = host_inputs(wl)
+    rng = np.random.default_rng(4)
+    ids = wl.batch.token_adapter()
+    for (l, p) in wl.problems:
+        d_in, d_out = dims[p]
+        assert hi.x[(l, p)].shape[1] == d_in
+        W = rng.normal(0.0, 0.02, size=(d_out, d_in))
+        xd = vg.bf16_bits_to_f64(hi.x[(l, p)])
+        y_ref, _, madds = oracle.lora_delta(hi.pool, hi.pt, wl.pool.pt_off, wl.pool.ranks, wl.pool.scales,
+                                            wl.pool.num_layers, wl.pool.num_proj, l, p, hi.x[(l, p)],
+                                            xd @ W.T, ids, proj_dims=dims)
+        assert y_ref.shape == (ids.size, d_out)
+        for i, a in enumerate(ids):
+            if a < 0:
+                merged = W
+            else:
+                A, B = dense_adapter_widths(wl, a, l, p)
+                assert A.shape == (wl.pool.ranks[a], d_in) and B.shape == (d_out, wl.pool.ranks[a])
+                merged = W + float(wl.pool.scales[a]) * (B @ A)
+            want = merged @ xd[i]
+            np.testing.assert_allclose(y_ref[i], want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max()))
+        # flop count: r (d_in + d_out) multiply-adds per adapted token
+        r_t = wl.pool.ranks[ids[ids >= 0]].astype(np.int64)
+        assert madds == int((r_t * (d_in + d_out)).sum())
+
+
 def test_gathered_bmm_form():
     """The pofe.ai page's "Implementation sketch" form: v = bmm(A_pool[idx], x), then
     y + scale * bmm(B_pool[idx], v), in float64 torch on CPU, with adapters zero-padded

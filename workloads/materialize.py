@@ -73,15 +73,17 @@ def host_inputs(wl: Workload, problems=None, adapters=None, with_xy: bool = True
     if with_xy:
         T = wl.batch.num_tokens
         for (l, p) in problems:
-            x[(l, p)] = host_rows(wl, KIND_X, *wl.x_source(l, p), T)
-            y0[(l, p)] = host_rows(wl, KIND_Y, l, p, T)
+            d_in, d_out = pool.dims(p)
+            x[(l, p)] = host_rows(wl, KIND_X, *wl.x_source(l, p), T, width=d_in)
+            y0[(l, p)] = host_rows(wl, KIND_Y, l, p, T, width=d_out)
     return HostInputs(compact, pt, x, y0)
 
 
-def host_rows(wl: Workload, kind: int, l: int, p: int, T: int, rows=None) -> np.ndarray:
-    """x (KIND_X) or y0 (KIND_Y) rows of problem (l, p) as uint16 [len(rows), h]."""
+def host_rows(wl: Workload, kind: int, l: int, p: int, T: int, rows=None, width=None) -> np.ndarray:
+    """x (KIND_X) or y0 (KIND_Y) rows of problem (l, p) as uint16 [len(rows), width]
+    (width h by default); element e of a row does not depend on the width."""
     rows = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
-    out = np.zeros((rows.size, wl.h), dtype=np.uint16)
+    out = np.zeros((rows.size, wl.h if width is None else width), dtype=np.uint16)
     sigma = SIGMA_X if kind == KIND_X else SIGMA_Y
     vg.fill_rows_host(out, np.arange(rows.size), row_key(kind, l, p, rows), wl.seed,
                       vg.DIST_NORMAL, vg.normal_param(sigma))
@@ -95,8 +97,8 @@ class DeviceInputs:
     pt_off: object            # torch int64
     ranks: object             # torch int32
     scales: object            # torch float32
-    x: object                 # torch bf16 [nprob, T, h]
-    y: object                 # torch bf16 [nprob, T, h]
+    x: object                 # torch bf16 [nprob, T, max d_in]  (h x h pools: h)
+    y: object                 # torch bf16 [nprob, T, max d_out]
     seg_start: object         # torch int32 [S+1]
     seg_adapter: object       # torch int32 [S]
     dec_adapter: object       # torch int32 [Td]
@@ -131,7 +133,7 @@ def device_fill_rows(wl: Workload, buf, kind: int, problems, stream: int) -> Non
     rows = torch.arange(len(problems) * T, dtype=torch.int64, device=buf.device)
     keys_t = torch.from_numpy(keys.view(np.int64)).to(buf.device)
     sigma = SIGMA_X if kind == KIND_X else SIGMA_Y
-    vg.fill_rows_dev(buf.data_ptr(), wl.h, rows.data_ptr(), keys_t.data_ptr(), rows.numel(),
+    vg.fill_rows_dev(buf.data_ptr(), buf.shape[2], rows.data_ptr(), keys_t.data_ptr(), rows.numel(),
                      wl.seed, vg.DIST_NORMAL, vg.normal_param(sigma), stream)
     torch.cuda.current_stream(buf.device).synchronize()
 
@@ -147,8 +149,10 @@ def device_inputs(wl: Workload, problems=None, device="cuda", nan_dummies: bool 
         pool_t = torch.empty((pool.num_pages, pool.h), dtype=torch.bfloat16, device=device)
         device_fill_pool(wl, pool_t, stream, nan_dummies)
     T = wl.batch.num_tokens
-    x = torch.empty((len(problems), T, pool.h), dtype=torch.bfloat16, device=device)
-    y = torch.empty_like(x)
+    w_in = max(pool.dims(p)[0] for (_, p) in problems) if problems else pool.h
+    w_out = max(pool.dims(p)[1] for (_, p) in problems) if problems else pool.h
+    x = torch.empty((len(problems), T, w_in), dtype=torch.bfloat16, device=device)
+    y = torch.empty((len(problems), T, w_out), dtype=torch.bfloat16, device=device)
     if T > 0 and problems:
         device_fill_rows(wl, x, KIND_X, problems, stream)
         device_fill_rows(wl, y, KIND_Y, problems, stream)

@@ -66,6 +66,11 @@ class Pool:
     page_keys: np.ndarray        # uint64 [n_filled]
     page_ab: np.ndarray          # uint8 [n_filled]
     r_max: int = 0
+    # (d_in, d_out) of every projection, int32 [P, 2]; None: all h x h.  A vector of
+    # length d takes ceil(d / h) pages; an adapter's block for (layer, proj, A or B) holds
+    # r * pages-per-vector entries, page block by page block (page kb of every row or
+    # column, then page kb + 1), blocks in (layer, proj, A, B) order.
+    proj_dims: np.ndarray | None = None
 
     @property
     def num_adapters(self) -> int:
@@ -75,11 +80,25 @@ class Pool:
     def scales(self) -> np.ndarray:
         return (ALPHA / self.ranks.astype(np.float64)).astype(np.float32)
 
+    def dims(self, proj: int):
+        """(d_in, d_out) of projection proj."""
+        if self.proj_dims is None:
+            return self.h, self.h
+        return int(self.proj_dims[proj][0]), int(self.proj_dims[proj][1])
+
+    def layout_units(self):
+        """(units of one layer, units before each projection, pages per A row and per B
+        column of each projection); one unit = r_a page-table entries."""
+        return layout_units(self.h, self.num_proj, self.proj_dims)
+
     def block_entries(self, adapter: int, layer: int, proj: int, ab: int) -> np.ndarray:
-        """Indices into pt of the r_a pages of A (ab=0) or B (ab=1) for (adapter, layer, proj)."""
+        """Indices into pt of the pages of A (ab=0) or B (ab=1) for (adapter, layer, proj):
+        r_a * pages-per-vector entries, page block by page block."""
         r = int(self.ranks[adapter])
-        base = int(self.pt_off[adapter]) + ((layer * self.num_proj + proj) * 2 + ab) * r
-        return np.arange(base, base + r, dtype=np.int64)
+        U, pre, pv_in, pv_out = self.layout_units()
+        base = int(self.pt_off[adapter]) + r * (layer * U + pre[proj] + (pv_in[proj] if ab else 0))
+        n = r * (pv_out[proj] if ab else pv_in[proj])
+        return np.arange(base, base + n, dtype=np.int64)
 
 
 @dataclass
@@ -139,32 +158,49 @@ class Workload:
 
 # ----------------------------------------------------------------------------- pool layouts
 
-def _block_sizes(ranks: np.ndarray, L: int, P: int) -> np.ndarray:
-    return (L * P * 2) * ranks.astype(np.int64)
+def layout_units(h: int, P: int, proj_dims=None):
+    """Page-table layout in units of r_a entries: (units of one layer, units before each
+    projection, pages per A row and per B column of each projection)."""
+    dims = [(h, h)] * P if proj_dims is None else [(int(a), int(b)) for a, b in np.asarray(proj_dims)]
+    pv = lambda d: -(-d // h)   # noqa: E731
+    pre, acc = [], 0
+    for d_in, d_out in dims:
+        pre.append(acc)
+        acc += pv(d_in) + pv(d_out)
+    return acc, pre, [pv(d[0]) for d in dims], [pv(d[1]) for d in dims]
 
 
-def _entry_owner_local(ranks: np.ndarray, pt_off: np.ndarray, sizes: np.ndarray):
+def _block_sizes(ranks: np.ndarray, L: int, P: int, h: int = 1, proj_dims=None) -> np.ndarray:
+    U = layout_units(h, P, proj_dims)[0]
+    return (L * U) * ranks.astype(np.int64)
+
+
+def _entry_owner_local(ranks: np.ndarray, pt_off: np.ndarray, sizes: np.ndarray, h: int = 1,
+                       P: int = 1, proj_dims=None):
     owner = np.repeat(np.arange(ranks.size, dtype=np.int64), sizes)
     local = np.arange(int(sizes.sum()), dtype=np.int64) - pt_off[owner]
-    ab = ((local // ranks[owner].astype(np.int64)) & 1).astype(np.uint8)
+    U, _, pv_in, pv_out = layout_units(h, P, proj_dims)
+    unit_ab = np.concatenate([[0] * a + [1] * b for a, b in zip(pv_in, pv_out)]).astype(np.uint8)
+    ab = unit_ab[(local // ranks[owner].astype(np.int64)) % U]
     return owner, local, ab
 
 
 def make_pool_all_resident(rng: np.random.Generator, h: int, L: int, P: int, ranks: np.ndarray,
-                           num_pages: int | None = None) -> Pool:
+                           num_pages: int | None = None, proj_dims=None) -> Pool:
     """Every adapter page resident, placed at shuffled page indices of the pool."""
     ranks = ranks.astype(np.int32)
-    sizes = _block_sizes(ranks, L, P)
+    sizes = _block_sizes(ranks, L, P, h, proj_dims)
     pt_off = np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64)
     pt_len = int(sizes.sum())
     if num_pages is None:
         num_pages = pt_len
     assert num_pages >= pt_len
     placement = rng.permutation(num_pages)[:pt_len].astype(np.int64)
-    owner, local, ab = _entry_owner_local(ranks, pt_off, sizes)
+    owner, local, ab = _entry_owner_local(ranks, pt_off, sizes, h, P, proj_dims)
     return Pool(h=h, num_layers=L, num_proj=P, ranks=ranks, pt_off=pt_off,
                 pt=placement.astype(np.int32), num_pages=num_pages, page_ids=placement,
-                page_keys=page_key(owner, local), page_ab=ab, r_max=int(ranks.max()))
+                page_keys=page_key(owner, local), page_ab=ab, r_max=int(ranks.max()),
+                proj_dims=None if proj_dims is None else np.asarray(proj_dims, np.int32).reshape(P, 2))
 
 
 def make_pool_subset_resident(rng: np.random.Generator, h: int, L: int, P: int,
@@ -236,7 +272,7 @@ def all_problems(L: int, P: int) -> list:
 def decode_workload(name: str, seed: int, h: int, L: int, P: int, num_adapters: int,
                     rank_choices, T: int, zipf_s: float | None, num_pages: int | None = None,
                     base_ids: bool = False, distinct: bool = False, layer_slices: bool = False,
-                    notes: str = "") -> Workload:
+                    notes: str = "", proj_dims=None) -> Workload:
     """Decode batch of T one-token requests.  Adapter ids: Zipf(zipf_s) over the
     adapters, or uniform over {-1..N-1} when base_ids, or distinct (sampled
     without replacement) when distinct."""
@@ -249,9 +285,10 @@ def decode_workload(name: str, seed: int, h: int, L: int, P: int, num_adapters: 
     else:
         ids = rng.choice(num_adapters, size=T, p=zipf_probs(num_adapters, zipf_s))
     if layer_slices:
+        assert proj_dims is None
         pool = make_pool_layer_slices(rng, h, L, P, ranks, num_pages)
     else:
-        pool = make_pool_all_resident(rng, h, L, P, ranks, num_pages)
+        pool = make_pool_all_resident(rng, h, L, P, ranks, num_pages, proj_dims)
     batch = Batch(seg_start=np.zeros(1, np.int32), seg_adapter=np.zeros(0, np.int32),
                   dec_adapter=ids.astype(np.int32))
     return Workload(name, seed, pool, batch, all_problems(L, P), notes)
