@@ -38,7 +38,8 @@ UNIT = "tokens/s"
 def workload_for(cfg: str):
     """Configs 0-4 as named in the workload module; "1s" (4 layers, 300 adapters, ~2.4 GB
     pool), "2s" (2 layers x 2 projections, ~2 GB on the device) and "3s" (1 layer x 2
-    projections) are small variants of configs 1, 2 and 3 for profiler captures."""
+    projections) are small variants of configs 1, 2 and 3 for profiler captures; "8b" is a
+    Llama-3-8B decode batch over all seven projections at their own widths ("8bs": 1 layer)."""
     from workloads import spec
     if cfg == "1s":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
@@ -50,6 +51,10 @@ def workload_for(cfg: str):
         return spec.mixed_workload("13b-mixed-h5120-p8-d192-a2000-l1p2", 1003, 5120, 1, 2, 2000,
                                    [8, 16, 32, 64, 128], 8, 128, 2048, 192, 20, 0.8,
                                    pool_pages=1 << 18)
+    if cfg == "8b":
+        return spec.llama3_8b_decode()
+    if cfg == "8bs":
+        return spec.llama3_8b_decode(layers=1)
     if cfg == "4d":
         return spec.config4("distinct")
     if cfg == "4z":
@@ -223,7 +228,7 @@ class OracleRunner:
             self.next += 1
             oracle.lora_delta(self.hi.pool, self.hi.pt, pool.pt_off, pool.ranks, pool.scales,
                               pool.num_layers, pool.num_proj, l, p, self.hi.x[(l, p)],
-                              self.y0[(l, p)], self.ids)
+                              self.y0[(l, p)], self.ids, proj_dims=pool.proj_dims)
         return time.perf_counter() - t0
 
     def rate(self, seconds: float, n_problems: int) -> float:
@@ -322,11 +327,23 @@ def graph_timing(capture_fn, tokens_step: int, dev, replays: int) -> dict:
             "tokens_per_s": tokens_step / (med / 1e3)}
 
 
-def config_dict(wl, args) -> dict:
+def step_model(wl, ids=None, problems=None) -> dict:
+    """Algorithmic bytes and flops of one launch over the given problems (all of the
+    workload's by default): each projection at its own widths, each distinct x buffer
+    read once."""
     from heterogeneous_adapters_gb300 import costmodel
     p = wl.pool
-    x_buffers = len({wl.x_source(l, pj) for (l, pj) in wl.problems})
-    m = costmodel.decode_step_bytes(p.ranks, wl.batch.token_adapter(), p.h, len(wl.problems), x_buffers)
+    problems = wl.problems if problems is None else problems
+    ids = wl.batch.token_adapter() if ids is None else ids
+    dims = [p.dims(pj) for (_, pj) in problems]
+    x_widths = [p.dims(pj)[0] for (_, pj) in {wl.x_source(l, pj) for (l, pj) in problems}]
+    return costmodel.decode_step_bytes(p.ranks, ids, p.h, len(problems), dims=dims,
+                                       x_widths=x_widths)
+
+
+def config_dict(wl, args) -> dict:
+    p = wl.pool
+    m = step_model(wl)
     return {"workload": wl.name, "h": p.h, "layers": p.num_layers, "projections": p.num_proj,
             "tokens": wl.batch.num_tokens, "adapted_tokens": m["adapted_tokens"],
             "adapters": p.num_adapters, "distinct_adapters": m["distinct_adapters"],
@@ -340,7 +357,6 @@ def run_ours(args, rank: int, world: int, local: int):
     import torch
 
     import heterogeneous_adapters_gb300 as lora
-    from heterogeneous_adapters_gb300 import costmodel
     from workloads.materialize import device_inputs
 
     torch.cuda.set_device(local)
@@ -349,7 +365,7 @@ def run_ours(args, rank: int, world: int, local: int):
     d = device_inputs(wl, device=dev, nan_dummies=False)
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
-                     p.num_adapters, p.num_layers, p.num_proj, p.r_max)
+                     p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
     b = wl.batch
     T, S, Td = b.num_tokens, b.num_segments, b.num_decode
     nbytes = lora.workspace_size(pool, T, S + Td)
@@ -358,7 +374,8 @@ def run_ours(args, rank: int, world: int, local: int):
     stream_obj = torch.cuda.current_stream(dev)
     stream = stream_obj.cuda_stream
     lora.workspace_init(ws, nbytes, stream)
-    probs = [(d.x[d.x_src[i]], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    probs = [(d.x[d.x_src[i]], d.y[i], d.x.shape[2], d.y.shape[2], l, pj)
+             for i, (l, pj) in enumerate(d.problems)]
     seg_start = d.seg_start if S else None
     seg_adapter = d.seg_adapter if S else None
     dec = d.dec_adapter if Td else None
@@ -369,7 +386,7 @@ def run_ours(args, rank: int, world: int, local: int):
     def delta():
         lora.delta_grouped(pool, probs, T, S, ws, nbytes, stream)
 
-    m = costmodel.decode_step_bytes(p.ranks, b.token_adapter(), p.h, len(wl.problems), len(x_idx))
+    m = step_model(wl)
     # the delta launches of the step: the CUDA-core kernel alone for decode batches (up to
     # 256 projections a launch); for batches with prefill segments the fused two-class
     # kernel where h allows it (h a multiple of 128, h <= 5120; up to 64 projections a
@@ -467,7 +484,8 @@ def run_ours(args, rank: int, world: int, local: int):
         xs = d.x if k == 0 else torch.empty_like(d.x)
         ys = d.y if k == 0 else torch.empty_like(d.y)
         metas = [torch.empty_like(m) for m in meta_src]
-        probs_k = [(xs[d.x_src[i]], ys[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+        probs_k = [(xs[d.x_src[i]], ys[i], xs.shape[2], ys.shape[2], l, pj)
+                   for i, (l, pj) in enumerate(d.problems)]
         slots.append((xs, ys, metas, probs_k))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     e2e_steps = max(3, min(args.steps, 50))
@@ -576,7 +594,6 @@ def run_sweep_distinct(args, local: int):
     import torch
 
     import heterogeneous_adapters_gb300 as lora
-    from heterogeneous_adapters_gb300 import costmodel
     from workloads.materialize import device_inputs
 
     torch.cuda.set_device(local)
@@ -585,14 +602,14 @@ def run_sweep_distinct(args, local: int):
     d = device_inputs(wl, device=dev, nan_dummies=False)
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
-                     p.num_adapters, p.num_layers, p.num_proj, p.r_max)
+                     p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
     T = wl.batch.num_tokens
     nbytes = lora.workspace_size(pool, T, T)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream_obj = torch.cuda.current_stream(dev)
     stream = stream_obj.cuda_stream
     lora.workspace_init(ws, nbytes, stream)
-    probs = [(d.x[i], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    probs = [(d.x[i], d.y[i], d.x.shape[2], d.y.shape[2], l, pj) for i, (l, pj) in enumerate(d.problems)]
     peaks = measured_peaks()
     for D in (1, 2, 4, 8, 16, 32, 64):
         rng = np.random.default_rng(7000 + D)
@@ -611,7 +628,7 @@ def run_sweep_distinct(args, local: int):
         torch.cuda.synchronize()
         assert lora.get_device_error(ws, stream) == 0
         ms = e0.elapsed_time(e1) / args.steps
-        m = costmodel.decode_step_bytes(p.ranks, ids, p.h, len(probs))
+        m = step_model(wl, ids=ids)
         gbs = m["bytes"] / (ms / 1e3) / 1e9
         print(json.dumps({"sweep": "distinct_adapters", "workload": wl.name, "distinct": D,
                           "ranks_mean": float(p.ranks[chosen].mean()), "delta_ms": ms,
@@ -735,7 +752,7 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
     cache = SliceCache(wl0, d.pool, args.stage_capacity)
     side = torch.cuda.Stream(device=dev)
     p = wl0.pool
-    probs = [(d.x[i], d.y[i], p.h, p.h, l, pj) for i, (l, pj) in enumerate(d.problems)]
+    probs = [(d.x[i], d.y[i], d.x.shape[2], d.y.shape[2], l, pj) for i, (l, pj) in enumerate(d.problems)]
     ids_dev = [torch.from_numpy(w.batch.token_adapter()).to(dev) for w in wl_steps]
     needs = [cache.needed(w.batch.token_adapter()) for w in wl_steps]
     stage_ms, stage_bytes, misses, kern_ms = [], [], [], []

@@ -37,7 +37,8 @@ class lora_pool_desc(ctypes.Structure):
                 ("num_proj", ctypes.c_int32), ("r_max", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("page_table", ctypes.c_void_p),
                 ("page_table_len", ctypes.c_int64), ("adapter_pt_off", ctypes.c_void_p),
-                ("ranks", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+                ("ranks", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("proj_dims", ctypes.c_void_p)]
 
 
 class lora_problem(ctypes.Structure):
@@ -143,9 +144,14 @@ class Pool:
     """Handle of a lora_pool (host metadata only; device arrays stay the caller's)."""
 
     def __init__(self, pages, num_pages, h, page_table, page_table_len, pt_off, ranks, scales,
-                 num_adapters, num_layers, num_proj, r_max):
+                 num_adapters, num_layers, num_proj, r_max, proj_dims=None):
+        """proj_dims: (d_in, d_out) of every projection (copied by the library), or None
+        for h x h projections."""
+        import numpy as np
+        dims = None if proj_dims is None else np.ascontiguousarray(proj_dims, np.int32).reshape(-1)
         d = lora_pool_desc(_ptr(pages), num_pages, h, num_adapters, num_layers, num_proj, r_max, 0,
-                           _ptr(page_table), page_table_len, _ptr(pt_off), _ptr(ranks), _ptr(scales))
+                           _ptr(page_table), page_table_len, _ptr(pt_off), _ptr(ranks), _ptr(scales),
+                           dims.ctypes.data if dims is not None else None)
         self._h = ctypes.c_void_p()
         _check(lib().lora_pool_create(ctypes.byref(self._h), ctypes.byref(d)), "lora_pool_create")
         self.h = h

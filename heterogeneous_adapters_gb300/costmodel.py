@@ -39,24 +39,30 @@ def transfer_seconds(nbytes: float, bytes_per_s: float) -> float:
 
 
 def decode_step_bytes(ranks_by_adapter: np.ndarray, token_adapter: np.ndarray, h: int,
-                      nprob: int, x_buffers: int | None = None) -> dict:
-    """Algorithmic bytes and flops of one multi-problem launch over nprob projections
-    of size h x h, for a batch whose per-token adapter ids are token_adapter.
-    x_buffers: the distinct x buffers the projections read (projections that share their
-    input, as q, k and v of a layer do, read it once); nprob if None."""
+                      nprob: int, x_buffers: int | None = None, dims=None, x_widths=None) -> dict:
+    """Algorithmic bytes and flops of one multi-problem launch over nprob projections,
+    for a batch whose per-token adapter ids are token_adapter.
+    dims: the projections' (d_in, d_out) widths; h x h each if None.  Only the d_in + d_out
+    used elements of an adapter's vectors count, not the unused tail of their last page.
+    x_widths: the widths of the distinct x buffers the launch reads (projections that
+    share their input, as q, k and v of a layer do, read it once); one buffer per
+    projection of its d_in if None, or x_buffers buffers of width h when that is given."""
     ids = np.asarray(token_adapter, dtype=np.int64)
     adapted = ids[ids >= 0]
     distinct = np.unique(adapted)
     r_d = np.asarray(ranks_by_adapter, dtype=np.int64)[distinct]
     r_t = np.asarray(ranks_by_adapter, dtype=np.int64)[adapted]
-    page_bytes = int(2 * r_d.sum()) * h * BF16
-    x_bytes = adapted.size * h * BF16            # x read
-    y_bytes = adapted.size * 2 * h * BF16        # y read and written
-    meta_bytes = int(2 * r_d.sum()) * 4 + ids.size * 4
-    xb = nprob if x_buffers is None else x_buffers
-    xy_total = x_bytes * xb + y_bytes * nprob
-    flops = int(adapted.size and (2 * r_t * (2 * h)).sum())
-    return {"bytes": (page_bytes + meta_bytes) * nprob + xy_total, "page_bytes": page_bytes * nprob,
-            "xy_bytes": xy_total, "meta_bytes": meta_bytes * nprob,
-            "flops": flops * nprob, "adapted_tokens": int(adapted.size),
+    dims = [(h, h)] * nprob if dims is None else [(int(a), int(b)) for a, b in dims]
+    assert len(dims) == nprob
+    if x_widths is None:
+        x_widths = [di for di, _ in dims] if x_buffers is None else [h] * x_buffers
+    rs, rt = int(r_d.sum()), int(r_t.sum())
+    page_bytes = sum(rs * (di + do) * BF16 for di, do in dims)
+    meta_bytes = sum(rs * (-(-di // h) + -(-do // h)) * 4 + ids.size * 4 for di, do in dims)
+    x_bytes = adapted.size * sum(x_widths) * BF16                      # x read
+    y_bytes = adapted.size * 2 * sum(do for _, do in dims) * BF16      # y read and written
+    flops = sum(2 * rt * (di + do) for di, do in dims)
+    return {"bytes": page_bytes + meta_bytes + x_bytes + y_bytes, "page_bytes": page_bytes,
+            "xy_bytes": x_bytes + y_bytes, "meta_bytes": meta_bytes,
+            "flops": flops, "adapted_tokens": int(adapted.size),
             "tokens": int(ids.size), "distinct_adapters": int(distinct.size)}

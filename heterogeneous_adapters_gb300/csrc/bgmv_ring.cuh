@@ -47,7 +47,7 @@ struct StageMeta {
     int32_t rank;
     float scale;
     int32_t rows[kChunk];
-    int32_t pad;
+    int32_t blk;      // page block of the input (x, A stages) or of the output (B stages)
 };
 static_assert(sizeof(StageMeta) == 48, "stage meta size");
 
@@ -88,10 +88,12 @@ __host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes
 
 // Column vectors (8 bf16 = 16 B) of a row handled by consumer thread c: c + 32 CW v.
 template <int NV, int NT, int CW, int RP>
+// h8: the 16-byte vectors of this page block that are used (a partly used last page
+// stops early); accumulate: add to the partial sums of earlier page blocks of the rows.
 __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, int stage_row_bytes,
                                                   int npages, int h8, int c,
                                                   const uint4 (&xv)[kChunk][NV], float* red_w,
-                                                  int j0) {
+                                                  int j0, bool accumulate) {
     constexpr int V = RP * kChunk;   // 16 or 32 values per warp
     static_assert(V <= 32 && RP >= kChunk, "stage shape");
     float vals[V];
@@ -123,7 +125,10 @@ __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, in
     const float sum = warp_transpose_reduce<V>(vals);
     const int lane = threadIdx.x & 31;
     constexpr int kRep = 32 / V;   // lanes holding each sum
-    if (lane % kRep == 0) red_w[j0 * kChunk + lane / kRep] = sum;   // index jj*kChunk + t
+    if (lane % kRep == 0) {   // index jj*kChunk + t; the same lane owns it in every block
+        float* dst = red_w + j0 * kChunk + lane / kRep;
+        *dst = accumulate ? *dst + sum : sum;
+    }
 }
 
 template <int NV, int NT, int CW, int RP>
@@ -165,7 +170,9 @@ __device__ __forceinline__ bool consumer_barrier(unsigned char* base, const Ring
     return ok;
 }
 
-template <int NV, int NT, int CW, int RP, class P>
+// W: the pool has projections whose widths differ from h (vectors of several page blocks,
+// a partly used last page); W = false compiles the h x h case with one block each.
+template <int NV, int NT, int CW, int RP, bool W, class P>
 __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSmem& L,
                                   uint32_t& it, uint32_t& bphase, const StageMeta& mx, int c) {
     const int h = p.pool.h, h8 = h >> 3;
@@ -179,32 +186,38 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
     const int r = mx.rank;
     const ProbDesc pd = p.probs[mx.pr];
 
-    // x rows (stage just waited by the caller)
-    uint4 xv[kChunk][NV];
-    {
-        const unsigned char* st = base + L.ring + (size_t)(it % S) * p.stage_bytes;
+    // for each page block kb of the input: the x rows' block (the first one's stage was
+    // waited by the caller), then page kb of the A rows; partial sums add up over blocks
+    const int pv_in = W ? vec_pages(pd.d_in, h) : 1, pv_out = W ? vec_pages(pd.d_out, h) : 1;
+    for (int kb = 0; kb < pv_in; ++kb) {
+        const int w8 = W ? min(h8, (pd.d_in - kb * h) >> 3) : h8;   // used vectors of this block
+        if (kb > 0 && !mbar_wait(smem_addr(base + L.full + (it % S) * 8), (it / S) & 1, kWaitLimitNs))
+            return false;
+        uint4 xv[kChunk][NV];
+        {
+            const unsigned char* st = base + L.ring + (size_t)(it % S) * p.stage_bytes;
 #pragma unroll
-        for (int t = 0; t < kChunk; ++t)
+            for (int t = 0; t < kChunk; ++t)
 #pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const int vi = c + v * (CW * 32);
-                xv[t][v] = (t < mx.count && vi < h8) ? *reinterpret_cast<const uint4*>(st + t * row_bytes + vi * 16)
-                                               : make_uint4(0, 0, 0, 0);
-            }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(base + L.empty + (it % S) * 8));
-        ++it;
-    }
-    // shrink over the A stages
-    for (int j0 = 0; j0 < r; j0 += RP) {
-        const uint32_t s = it % S;
-        if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
-        const int np = min(RP, r - j0);
-        ring_shrink_stage<NV, NT, CW, RP>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, xv,
-                                  red_w, j0);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
-        ++it;
+                for (int v = 0; v < NV; ++v) {
+                    const int vi = c + v * (CW * 32);
+                    xv[t][v] = (t < mx.count && vi < w8) ? *reinterpret_cast<const uint4*>(st + t * row_bytes + vi * 16)
+                                                   : make_uint4(0, 0, 0, 0);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(base + L.empty + (it % S) * 8));
+            ++it;
+        }
+        for (int j0 = 0; j0 < r; j0 += RP) {
+            const uint32_t s = it % S;
+            if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
+            const int np = min(RP, r - j0);
+            ring_shrink_stage<NV, NT, CW, RP>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, w8, c, xv,
+                                              red_w, j0, W && kb > 0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
+            ++it;
+        }
     }
     // Two barriers per item: every warp's partial sums are in red, then t is complete.
     // The next item writes red only after the second one (every warp is done reading
@@ -223,48 +236,54 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
             p.t_out[(long long)mx.rows[t] * p.pool.r_max + j] = a * mx.scale;
     }
     if (!consumer_barrier(base, L, bphase)) return false;
-    // prefetch the y rows while the B pages stream in
-    uint4 yv[NT][NV];
+    // for each page block q of the output: y's block q (loaded while its B pages stream
+    // in), page q of the B columns, y = bf16_rn(y + acc) for the block's used columns
+    for (int q = 0; q < pv_out; ++q) {
+        const int w8 = W ? min(h8, (pd.d_out - q * h) >> 3) : h8;
+        __nv_bfloat16* yq = W ? pd.y + (long long)q * h : pd.y;
+        uint4 yv[NT][NV];
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int vi = c + v * (CW * 32);
-            yv[t][v] = (t < mx.count && vi < h8) ? ld16(pd.y + (long long)mx.rows[t] * pd.ldy + vi * 8) : make_uint4(0, 0, 0, 0);
-        }
-    float acc[kChunk][NV][8];
-#pragma unroll
-    for (int t = 0; t < kChunk; ++t)
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[t][v][e] = 0.f;
-    for (int j0 = 0; j0 < r; j0 += RP) {
-        const uint32_t s = it % S;
-        if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
-        const int np = min(RP, r - j0);
-        ring_expand_stage<NV, NT, CW, RP>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, h8, c, ts, j0,
-                                  acc);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
-        ++it;
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int vi = c + v * (CW * 32);
-            if (t < mx.count && vi < h8) {
-                float y8[8];
-                unpack8(yv[t][v], y8);
-                uint4 o;
-                o.x = pack2(y8[0] + acc[t][v][0], y8[1] + acc[t][v][1]);
-                o.y = pack2(y8[2] + acc[t][v][2], y8[3] + acc[t][v][3]);
-                o.z = pack2(y8[4] + acc[t][v][4], y8[5] + acc[t][v][5]);
-                o.w = pack2(y8[6] + acc[t][v][6], y8[7] + acc[t][v][7]);
-                st16(pd.y + (long long)mx.rows[t] * pd.ldy + vi * 8, o);
+            for (int v = 0; v < NV; ++v) {
+                const int vi = c + v * (CW * 32);
+                yv[t][v] = (t < mx.count && vi < w8) ? ld16(yq + (long long)mx.rows[t] * pd.ldy + vi * 8)
+                                                     : make_uint4(0, 0, 0, 0);
             }
+        float acc[kChunk][NV][8];
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t)
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[t][v][e] = 0.f;
+        for (int j0 = 0; j0 < r; j0 += RP) {
+            const uint32_t s = it % S;
+            if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
+            const int np = min(RP, r - j0);
+            ring_expand_stage<NV, NT, CW, RP>(base + L.ring + (size_t)s * p.stage_bytes, row_bytes, np, w8, c, ts,
+                                              j0, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
+            ++it;
         }
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int vi = c + v * (CW * 32);
+                if (t < mx.count && vi < w8) {
+                    float y8[8];
+                    unpack8(yv[t][v], y8);
+                    uint4 o;
+                    o.x = pack2(y8[0] + acc[t][v][0], y8[1] + acc[t][v][1]);
+                    o.y = pack2(y8[2] + acc[t][v][2], y8[3] + acc[t][v][3]);
+                    o.z = pack2(y8[4] + acc[t][v][4], y8[5] + acc[t][v][5]);
+                    o.w = pack2(y8[6] + acc[t][v][6], y8[7] + acc[t][v][7]);
+                    st16(yq + (long long)mx.rows[t] * pd.ldy + vi * 8, o);
+                }
+            }
+    }
     return true;
 }
 
@@ -272,7 +291,7 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
 // producer and the CW consumer warps only join the initial barrier).
 // NV: 16-byte column vectors per consumer thread; CW: consumer warps (h = 8 * 32 * CW * NV
 // or less); RP: rows per stage (stage_bytes = RP * 2h).
-template <int NV, int CW, int RP, class P>
+template <int NV, int CW, int RP, bool W, class P>
 __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32_t cta, uint32_t ncta) {
     const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max, CW);
     const int S = p.stages;
@@ -312,12 +331,15 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
             if (!mbar_wait(smem_addr(base + L.empty + s * 8), ((it / S) & 1) ^ 1, kWaitLimitNs)) return -1;
             return (int)s;
         };
+        // page ids of an item's first A block and first B block (all of them for h x h pools)
         auto load_pages = [&](const Chunk& c, uint32_t itm, int32_t (&pg)[kPg]) {
-            const long long blk = c.pt_base + (long long)p.probs[itm % p.nprob].blk * 2 * c.rank;
+            const ProbDesc& pd = p.probs[itm % p.nprob];
+            const long long a0 = c.pt_base + (long long)pd.blk * c.rank;
+            const long long b0 = a0 + (long long)(W ? vec_pages(pd.d_in, PV.h) : 1) * c.rank;
 #pragma unroll
             for (int k = 0; k < kPg; ++k) {
                 const int e = lane + 32 * k;
-                pg[k] = e < 2 * c.rank ? PV.pt[blk + e] : 0;
+                pg[k] = e < c.rank ? PV.pt[a0 + e] : (e < 2 * c.rank ? PV.pt[b0 + e - c.rank] : 0);
             }
         };
         uint32_t item = cta;
@@ -341,6 +363,10 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
             if (item + 2 * G < total) c_next2 = chunks[(item + 2 * G) / p.nprob];
 
             const int r = ch.rank;
+            const ProbDesc& pd = p.probs[pr];
+            const int pv_in = W ? vec_pages(pd.d_in, PV.h) : 1, pv_out = W ? vec_pages(pd.d_out, PV.h) : 1;
+            const long long a0 = ch.pt_base + (long long)pd.blk * r;   // first A-block entry
+            const long long b0 = a0 + (long long)pv_in * r;            // first B-block entry
             bool bad = false;
 #pragma unroll
             for (int k = 0; k < kPg; ++k) {
@@ -348,6 +374,17 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
                 if (e < 2 * r) {
                     bad |= (pg[k] < 0 || pg[k] >= PV.num_pages);
                     pgbuf[e] = pg[k];
+                }
+            }
+            // vectors longer than a page: the item's other page blocks are checked too
+            if (W) {
+                for (long long e = lane; e < (long long)(pv_in - 1) * r; e += 32) {
+                    const int q = PV.pt[a0 + r + e];
+                    bad |= (q < 0 || q >= PV.num_pages);
+                }
+                for (long long e = lane; e < (long long)(pv_out - 1) * r; e += 32) {
+                    const int q = PV.pt[b0 + r + e];
+                    bad |= (q < 0 || q >= PV.num_pages);
                 }
             }
             bad = __any_sync(0xffffffffu, bad);
@@ -362,49 +399,76 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
             m.scale = ch.scale;
 #pragma unroll
             for (int t = 0; t < kChunk; ++t) m.rows[t] = ch.rows[t];
-            m.pad = 0;
+            m.blk = 0;
             if (bad && lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
-            // x stage (or a skip marker)
-            int s = claim();
-            if (s < 0) { ok = false; break; }
-            if (lane == 0) {
-                meta[s] = m;
-                if (!bad)
-                    mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), row_bytes * ch.count);
-                else
+            if (bad) {   // a skip marker in place of the item
+                const int s = claim();
+                if (s < 0) { ok = false; break; }
+                if (lane == 0) {
+                    meta[s] = m;
                     mbar_arrive(smem_addr(base + L.full + s * 8));
+                }
+                __syncwarp();
+                ++it;
+                continue;
             }
-            __syncwarp();
-            if (!bad && lane < ch.count) {
-                const ProbDesc& pd = p.probs[pr];
-                bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
-                         pd.x + (long long)ch.rows[lane] * pd.ldx, row_bytes,
-                         smem_addr(base + L.full + s * 8));
-            }
-            ++it;
-            if (bad) continue;
-            // A pages then B pages
-            for (int ab = 0; ab < 2 && ok; ++ab) {
+            // Stages of the item: for each page block kb of the input, the x rows' block
+            // kb then page kb of the A rows; then, for each page block q of the output,
+            // page q of the B columns.  Only the used part of a partly used page is copied.
+            // emit_pages: stage(s) of page block `blk_idx` (ids from pgbuf[off ..]) of kind
+            auto emit_pages = [&](int kind, int blk_idx, int off, uint32_t bytes) {
                 for (int j0 = 0; j0 < r; j0 += RP) {
                     const int np = min(RP, r - j0);
-                    s = claim();
-                    if (s < 0) { ok = false; break; }
+                    const int s = claim();
+                    if (s < 0) return false;
                     if (lane == 0) {
                         StageMeta mm = m;
-                        mm.kind = ab ? kStageB : kStageA;
+                        mm.kind = kind;
                         mm.npages = np;
                         mm.j0 = j0;
+                        mm.blk = blk_idx;
                         meta[s] = mm;
-                        mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), row_bytes * np);
+                        mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), bytes * np);
                     }
                     __syncwarp();
                     if (lane < np) {
-                        const int page = pgbuf[ab * r + j0 + lane];
+                        const int page = pgbuf[off + j0 + lane];
                         bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
-                                 PV.pages + (long long)page * PV.h, row_bytes, smem_addr(base + L.full + s * 8));
+                                 PV.pages + (long long)page * PV.h, bytes, smem_addr(base + L.full + s * 8));
                     }
                     ++it;
                 }
+                return true;
+            };
+            // page ids of block kb of a multi-page vector, into pgbuf[off ..]
+            auto fetch_block = [&](long long first, int off) {
+                __syncwarp();   // every lane has read the previous block's ids
+                for (int e = lane; e < r; e += 32) pgbuf[off + e] = PV.pt[first + e];
+                __syncwarp();
+            };
+            for (int kb = 0; kb < pv_in && ok; ++kb) {
+                const uint32_t bytes = W ? (uint32_t)min(PV.h, pd.d_in - kb * PV.h) * 2 : row_bytes;
+                const int s = claim();
+                if (s < 0) { ok = false; break; }
+                if (lane == 0) {
+                    StageMeta mx = m;
+                    mx.blk = kb;
+                    meta[s] = mx;
+                    mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), bytes * ch.count);
+                }
+                __syncwarp();
+                if (lane < ch.count)
+                    bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
+                             pd.x + (long long)ch.rows[lane] * pd.ldx + (long long)kb * PV.h, bytes,
+                             smem_addr(base + L.full + s * 8));
+                ++it;
+                if (kb > 0) fetch_block(a0 + (long long)kb * r, 0);
+                if (!emit_pages(kStageA, kb, 0, bytes)) ok = false;
+            }
+            for (int q = 0; q < pv_out && ok; ++q) {
+                const uint32_t bytes = W ? (uint32_t)min(PV.h, pd.d_out - q * PV.h) * 2 : row_bytes;
+                if (q > 0) fetch_block(b0 + (long long)q * r, r);
+                if (!emit_pages(kStageB, q, r, bytes)) ok = false;
             }
             if (!ok) break;
         }
@@ -446,11 +510,11 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
             }
             bool ok;
             if (mx.count == 1)
-                ok = ring_consume_item<NV, 1, CW, RP, P>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 1, CW, RP, W, P>(p, base, L, it, bphase, mx, c);
             else if (mx.count == 2)
-                ok = ring_consume_item<NV, 2, CW, RP, P>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, 2, CW, RP, W, P>(p, base, L, it, bphase, mx, c);
             else
-                ok = ring_consume_item<NV, kChunk, CW, RP, P>(p, base, L, it, bphase, mx, c);
+                ok = ring_consume_item<NV, kChunk, CW, RP, W, P>(p, base, L, it, bphase, mx, c);
             if (!ok) {
                 if (c == 0) set_error(&hdr->err, kDerrTimeout);
                 break;
@@ -459,10 +523,10 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
     }
 }
 
-template <int NV, int CW, int RP>
+template <int NV, int CW, int RP, bool W>
 __global__ void __launch_bounds__(CW * 32 + 32, 1) bgmv_ring_kernel(const __grid_constant__ RingParams p) {
     extern __shared__ __align__(1024) unsigned char ring_smem_raw[];
-    ring_cta<NV, CW, RP>(p, ring_smem_raw, blockIdx.x, gridDim.x);
+    ring_cta<NV, CW, RP, W>(p, ring_smem_raw, blockIdx.x, gridDim.x);
 }
 
 }  // namespace lora

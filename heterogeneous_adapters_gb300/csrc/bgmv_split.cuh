@@ -35,7 +35,7 @@ struct SplitParams {
     PoolView pool;
     char* ws;
     int32_t nprob;
-    int32_t pad;
+    int32_t out_blocks;   // the most output page blocks of the launch's projections
     ProbDesc probs[kSplitMaxProbs];
 };
 
@@ -49,6 +49,9 @@ __device__ __forceinline__ float* split_t(const SplitParams& p, const WsHeader* 
 // in shared memory, and the dot products are then taken from registers and shared memory.
 constexpr int kSplitLoads = 16;
 
+// W: the pool has projections whose widths differ from h (see the ring kernel); W = false
+// compiles the h x h case with one page block per vector.
+template <bool W>
 __global__ void __launch_bounds__(kSplitThreads) split_shrink_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(16) unsigned char split_smem[];   // x rows: kChunk * h bf16
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
@@ -74,47 +77,54 @@ __global__ void __launch_bounds__(kSplitThreads) split_shrink_kernel(const __gri
         const int r = ch.rank;
         if (js * kSplitRows >= r) continue;   // this adapter has fewer rows
         const ProbDesc pd = p.probs[pr];
-        const long long blk0 = ch.pt_base + (long long)pd.blk * 2 * r;
-        // each warp checks its own A row's page; a bad page leaves that t entry unwritten
-        // (the expand of this chunk checks every page of it and skips it)
+        const long long a0 = ch.pt_base + (long long)pd.blk * r;   // A block: page kb of row j at a0 + kb r + j
+        const int pv_in = W ? vec_pages(pd.d_in, P.h) : 1;
         const int j = js * kSplitRows + warp;
-        const int page = j < r ? P.pt[blk0 + j] : 0;
-        const bool page_ok = page >= 0 && page < P.num_pages;
-        if (j < r && !page_ok && lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
-        const bool live = j < r && page_ok;
-        const __nv_bfloat16* a = P.pages + (long long)(live ? page : 0) * P.h;
+        // each warp checks its own A row's pages; a bad page leaves that t entry unwritten
+        // (the expand of this chunk checks every page of it and skips it)
+        bool live = j < r;
         float acc[kChunk] = {0.f, 0.f, 0.f, 0.f};
-        for (int v0 = 0; v0 < h8; v0 += 32 * kSplitLoads) {
-            uint4 av[kSplitLoads];
-#pragma unroll
-            for (int k = 0; k < kSplitLoads; ++k) {
-                const int v = v0 + lane + 32 * k;
-                av[k] = (live && v < h8) ? ld_stream16(a + v * 8) : make_uint4(0, 0, 0, 0);
+        for (int kb = 0; kb < pv_in; ++kb) {
+            const int w8 = W ? min(h8, (pd.d_in - kb * P.h) >> 3) : h8;   // used vectors of this block
+            const int page = live ? P.pt[a0 + (long long)kb * r + j] : 0;
+            if (live && (page < 0 || page >= P.num_pages)) {
+                if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
+                live = false;
             }
-            if (v0 == 0) {   // the x rows, while the A loads are in flight
-                for (int e = threadIdx.x; e < ch.count * h8; e += blockDim.x) {
-                    const int t = e / h8, v = e % h8;
-                    xs[t * h8 + v] = ld16(pd.x + (long long)ch.rows[t] * pd.ldx + v * 8);
+            const __nv_bfloat16* a = P.pages + (long long)(live ? page : 0) * P.h;
+            for (int v0 = 0; v0 < w8; v0 += 32 * kSplitLoads) {
+                uint4 av[kSplitLoads];
+#pragma unroll
+                for (int k = 0; k < kSplitLoads; ++k) {
+                    const int v = v0 + lane + 32 * k;
+                    av[k] = (live && v < w8) ? ld_stream16(a + v * 8) : make_uint4(0, 0, 0, 0);
                 }
-                __syncthreads();
-            }
+                if (v0 == 0) {   // the x rows' block kb, while the A loads are in flight
+                    for (int e = threadIdx.x; e < ch.count * w8; e += blockDim.x) {
+                        const int t = e / w8, v = e % w8;
+                        xs[t * h8 + v] = ld16(pd.x + (long long)ch.rows[t] * pd.ldx + (long long)kb * P.h + v * 8);
+                    }
+                    __syncthreads();
+                }
 #pragma unroll
-            for (int k = 0; k < kSplitLoads; ++k) {
-                const int v = v0 + lane + 32 * k;
-                if (v < h8) {
-                    float a8[8];
-                    unpack8(av[k], a8);
+                for (int k = 0; k < kSplitLoads; ++k) {
+                    const int v = v0 + lane + 32 * k;
+                    if (v < w8) {
+                        float a8[8];
+                        unpack8(av[k], a8);
 #pragma unroll
-                    for (int t = 0; t < kChunk; ++t) {
-                        if (t < ch.count) {
-                            float x8[8];
-                            unpack8(xs[t * h8 + v], x8);
+                        for (int t = 0; t < kChunk; ++t) {
+                            if (t < ch.count) {
+                                float x8[8];
+                                unpack8(xs[t * h8 + v], x8);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[t] = fmaf(x8[e], a8[e], acc[t]);
+                                for (int e = 0; e < 8; ++e) acc[t] = fmaf(x8[e], a8[e], acc[t]);
+                            }
                         }
                     }
                 }
             }
+            if (kb + 1 < pv_in) __syncthreads();   // xs holds the next block's rows next
         }
         if (live) {
 #pragma unroll
@@ -130,6 +140,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_shrink_kernel(const __gri
     }
 }
 
+template <bool W>
 __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __grid_constant__ SplitParams p) {
     constexpr int kGroups = kSplitThreads / kSplitVecs;   // threads sharing one column vector
     __shared__ float ts[kChunk][LORA_MAX_RANK];
@@ -143,7 +154,9 @@ __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __gri
     const int T = hdr->cap_tokens;
     const PoolView& P = p.pool;
     const int h8 = P.h >> 3, r_max = P.r_max;
-    const int n_sl = (h8 + kSplitVecs - 1) / kSplitVecs;
+    // item = (projection, chunk, output page block q, slice of the block)
+    const int n_slb = (h8 + kSplitVecs - 1) / kSplitVecs;
+    const int n_sl = n_slb * (W ? p.out_blocks : 1);
     const int vl = threadIdx.x % kSplitVecs, g = threadIdx.x / kSplitVecs;
     const long long total = (long long)p.nprob * n_chunks * n_sl;
     auto chunk_of = [&](long long it) { return (int)((it / n_sl) % n_chunks); };
@@ -156,16 +169,24 @@ __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __gri
         if (item + gridDim.x < total) next = chunks[chunk_of(item + gridDim.x)];
         const int r = ch.rank;
         const ProbDesc pd = p.probs[pr];
-        const long long blk0 = ch.pt_base + (long long)pd.blk * 2 * r;
-        const int v = sl * kSplitVecs + vl;
+        const int q = W ? sl / n_slb : 0;                // output page block
+        const int pv_in = W ? vec_pages(pd.d_in, P.h) : 1, pv_out = W ? vec_pages(pd.d_out, P.h) : 1;
+        if (W && q >= pv_out) continue;                  // a narrower projection
+        const int w8 = W ? min(h8, (pd.d_out - q * P.h) >> 3) : h8;
+        const int v = (W ? sl % n_slb : sl) * kSplitVecs + vl;   // vector within the block
+        __nv_bfloat16* yq = W ? pd.y + (long long)q * P.h : pd.y;
+        const long long a0 = ch.pt_base + (long long)pd.blk * r;
+        const long long bq = a0 + (long long)(pv_in + q) * r;   // page q of the B columns
         // one round trip: the chunk's page ids (all checked: the A rows' too, whose t a bad
         // page left unwritten), its t values and this thread's y vectors
         bool bad = false;
-        for (int e = threadIdx.x; e < 2 * r; e += blockDim.x) {
-            const int page = P.pt[blk0 + e];
+        for (long long e = threadIdx.x; e < (long long)(pv_in + pv_out) * r; e += blockDim.x) {
+            const int page = P.pt[a0 + e];
             bad |= (page < 0 || page >= P.num_pages);
-            if (e >= r) pg[e - r] = page;
+            if (!W && e >= r) pg[e - r] = page;
         }
+        if (W)
+            for (int e = threadIdx.x; e < r; e += blockDim.x) pg[e] = P.pt[bq + e];
         for (int e = threadIdx.x; e < kChunk * r; e += blockDim.x) {
             const int t = e / r, j = e % r;
             ts[t][j] = t < ch.count ? tbuf[((long long)pr * T + ch.rows[t]) * r_max + j] : 0.f;
@@ -173,7 +194,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __gri
         uint4 yv[kChunk];
 #pragma unroll
         for (int t = 0; t < kChunk; ++t)
-            yv[t] = (g == 0 && v < h8 && t < ch.count) ? ld16(pd.y + (long long)ch.rows[t] * pd.ldy + v * 8)
+            yv[t] = (g == 0 && v < w8 && t < ch.count) ? ld16(yq + (long long)ch.rows[t] * pd.ldy + v * 8)
                                                        : make_uint4(0, 0, 0, 0);
         if (__syncthreads_or(bad)) {
             if (threadIdx.x == 0) set_error(&hdr->err, LORA_DERR_PAGE);
@@ -184,7 +205,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __gri
         for (int t = 0; t < kChunk; ++t)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
-        if (v < h8) {
+        if (v < w8) {
 #pragma unroll 16
             for (int j = g; j < r; j += kGroups) {
                 float b8[8];
@@ -204,11 +225,11 @@ __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __gri
                 for (int e = 0; e < 8; ++e) red[g - 1][t][vl][e] = acc[t][e];
         }
         __syncthreads();
-        if (g == 0 && v < h8) {
+        if (g == 0 && v < w8) {
 #pragma unroll
             for (int t = 0; t < kChunk; ++t) {
                 if (t >= ch.count) break;
-                __nv_bfloat16* yp = pd.y + (long long)ch.rows[t] * pd.ldy + v * 8;
+                __nv_bfloat16* yp = yq + (long long)ch.rows[t] * pd.ldy + v * 8;
                 float y8[8];
                 unpack8(yv[t], y8);
                 float s8[8];

@@ -90,7 +90,7 @@ struct PoolView {
     int32_t num_layers;
     int32_t num_proj;
     int32_t r_max;
-    int32_t pad;
+    int32_t units;   // U: page-table entries of one layer, in units of r_a (2 P for h x h)
 };
 
 // One projection instance inside a launch (32 bytes; many fit in kernel parameters).
@@ -99,9 +99,14 @@ struct ProbDesc {
     __nv_bfloat16* y;
     int32_t ldx;
     int32_t ldy;
-    int32_t blk;   // layer * P + proj
+    int32_t blk;     // the A block's offset in units of r_a entries: l * U + pre(p)
+    int32_t d_in;    // x columns read (h for h x h pools)
+    int32_t d_out;   // y columns updated
     int32_t pad;
 };
+
+// Pages one vector of length d spans on pages of h values.
+__host__ __device__ __forceinline__ int vec_pages(int d, int h) { return (d + h - 1) / h; }
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
 

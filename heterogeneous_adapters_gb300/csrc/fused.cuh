@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) delta_fused_kernel(const __gri
     extern __shared__ __align__(1024) unsigned char fused_smem_raw[];
     const uint32_t gf = fused_split(reinterpret_cast<const WsHeader*>(p.mma.ws), gridDim.x, p.ring_speed);
     if (blockIdx.x < gf)
-        ring_cta<NV, CW, RP>(p.ring, fused_smem_raw, blockIdx.x, gf);
+        ring_cta<NV, CW, RP, false>(p.ring, fused_smem_raw, blockIdx.x, gf);
     else
         mma_cta(p.mma, fused_smem_raw, blockIdx.x - gf, gridDim.x - gf);
 }

@@ -12,6 +12,8 @@
 
 #include <algorithm>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "bgmv_ring.cuh"
 #include "bgmv_split.cuh"
@@ -24,7 +26,11 @@
 using namespace lora;
 
 struct lora_pool {
-    lora_pool_desc d;
+    lora_pool_desc d;                 // proj_dims is not kept (a host array of the caller)
+    std::vector<int32_t> d_in, d_out; // widths of each projection
+    std::vector<int32_t> pre;         // units before each projection in a layer
+    int32_t units = 0;                // units of one layer
+    bool square = true;               // every projection h x h
 };
 
 namespace {
@@ -54,8 +60,23 @@ PoolView view_of(const lora_pool* pool) {
     v.num_layers = d.num_layers;
     v.num_proj = d.num_proj;
     v.r_max = d.r_max;
-    v.pad = 0;
+    v.units = pool->units;
     return v;
+}
+
+// Kernel descriptor of one problem: pointers, strides, widths and the offset of its A
+// block (in units of r_a page-table entries).
+ProbDesc prob_desc(const lora_pool* pool, const lora_problem& pr) {
+    ProbDesc o;
+    o.x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
+    o.y = reinterpret_cast<__nv_bfloat16*>(pr.y);
+    o.ldx = (int32_t)pr.ldx;
+    o.ldy = (int32_t)pr.ldy;
+    o.blk = pr.layer * pool->units + pool->pre[pr.proj];
+    o.d_in = pool->d_in[pr.proj];
+    o.d_out = pool->d_out[pr.proj];
+    o.pad = 0;
+    return o;
 }
 
 // Per-device launch facts, looked up once per device.
@@ -129,7 +150,7 @@ RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps) {
     return fallback;
 }
 
-template <int NV, int CW, int RP>
+template <int NV, int CW, int RP, bool W>
 lora_status launch_ring_rp(RingParams& prm, const DeviceInfo* di, const RingShape& sh, cudaStream_t stream) {
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
@@ -138,7 +159,7 @@ lora_status launch_ring_rp(RingParams& prm, const DeviceInfo* di, const RingShap
     prm.stage_bytes = RP * 2 * prm.pool.h;
     prm.stages = sh.stages;
     const size_t smem = sh.smem;
-    auto kern = bgmv_ring_kernel<NV, CW, RP>;
+    auto kern = bgmv_ring_kernel<NV, CW, RP, W>;
     if (attr_dev != dev || attr_smem < smem) {
         lora_status st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         if (st != LORA_OK) return st;
@@ -149,15 +170,21 @@ lora_status launch_ring_rp(RingParams& prm, const DeviceInfo* di, const RingShap
     return cuda_status(cudaGetLastError());
 }
 
-template <int NV, int CW>
-lora_status launch_ring(RingParams& prm, cudaStream_t stream) {
+template <int NV, int CW, bool W>
+lora_status launch_ring_w(RingParams& prm, cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
     const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW);
     if (sh.stages < 2) return LORA_ETOOBIG;
-    if (sh.rp == kRingPagesLarge) return launch_ring_rp<NV, CW, kRingPagesLarge>(prm, di, sh, stream);
-    return launch_ring_rp<NV, CW, kRingPagesSmall>(prm, di, sh, stream);
+    if (sh.rp == kRingPagesLarge) return launch_ring_rp<NV, CW, kRingPagesLarge, W>(prm, di, sh, stream);
+    return launch_ring_rp<NV, CW, kRingPagesSmall, W>(prm, di, sh, stream);
+}
+
+// h x h pools take the kernels compiled for one page block per vector
+template <int NV, int CW>
+lora_status launch_ring(RingParams& prm, bool square, cudaStream_t stream) {
+    return square ? launch_ring_w<NV, CW, false>(prm, stream) : launch_ring_w<NV, CW, true>(prm, stream);
 }
 
 lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
@@ -173,26 +200,21 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
         prm.t_out = t_out;
         prm.nprob = n;
         for (int32_t i = 0; i < n; ++i) {
-            const lora_problem& pr = probs[base + i];
-            prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
-            prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
-            prm.probs[i].ldx = (int32_t)pr.ldx;
-            prm.probs[i].ldy = (int32_t)pr.ldy;
-            prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
+            prm.probs[i] = prob_desc(pool, probs[base + i]);
         }
         // consumer warps x vectors per thread cover the h / 8 16-byte vectors of a row
         const int h8 = d.h / 8;
         lora_status st;
         if (h8 <= 256)
-            st = launch_ring<1, 8>(prm, stream);
+            st = launch_ring<1, 8>(prm, pool->square, stream);
         else if (h8 <= 512)
-            st = launch_ring<2, 8>(prm, stream);
+            st = launch_ring<2, 8>(prm, pool->square, stream);
         else if (h8 <= 640)
-            st = launch_ring<2, 10>(prm, stream);
+            st = launch_ring<2, 10>(prm, pool->square, stream);
         else if (h8 <= 768)
-            st = launch_ring<2, 12>(prm, stream);
+            st = launch_ring<2, 12>(prm, pool->square, stream);
         else
-            st = launch_ring<2, 16>(prm, stream);
+            st = launch_ring<2, 16>(prm, pool->square, stream);
         if (st != LORA_OK) return st;
     }
     return LORA_OK;
@@ -201,8 +223,9 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
 // ---------------------------------------------------------------------------- tensor-core path
 // Segments of at least this many rows (and rank <= kMmaMaxRank) take the tensor-core
 // path when h is a multiple of 128; LORA_MMA_MIN_ROWS overrides it (0 disables).
-int mma_min_rows(const lora_pool_desc& d) {
-    if (d.h % kMmaNTile != 0) return 0;
+int mma_min_rows(const lora_pool* pool) {
+    const lora_pool_desc& d = pool->d;
+    if (d.h % kMmaNTile != 0 || !pool->square) return 0;   // tensor-core tiles: h x h pools
     const char* e = getenv("LORA_MMA_MIN_ROWS");
     // one-row (decode) segments always stay on the CUDA-core path
     if (e != nullptr) return atoi(e) > 0 ? std::max(2, atoi(e)) : 0;
@@ -288,7 +311,7 @@ lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* 
         if (st != LORA_OK) return st;
         st = make_map(&prm.y1_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, 1);
         if (st != LORA_OK) return st;
-        prm.blk[i] = pr.layer * d.num_proj + pr.proj;
+        prm.blk[i] = pr.layer * pool->units + pool->pre[pr.proj];
     }
     // runs of consecutive problems reading the same x form the item order's groups
     for (int32_t i = 0; i < n;) {
@@ -324,12 +347,7 @@ void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem
     prm.stages = stages;
     prm.stage_bytes = rows_per_stage * 2 * d.h;
     for (int32_t i = 0; i < n; ++i) {
-        const lora_problem& pr = probs[i];
-        prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
-        prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
-        prm.probs[i].ldx = (int32_t)pr.ldx;
-        prm.probs[i].ldy = (int32_t)pr.ldy;
-        prm.probs[i].blk = pr.layer * d.num_proj + pr.proj;
+        prm.probs[i] = prob_desc(pool, probs[i]);
     }
 }
 
@@ -429,15 +447,17 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     return launch_fused_rp<NV, CW, kRingPagesSmall>(pool, probs, nprob, T, ws, di, c, sh, stream);
 }
 
-lora_status check_problems(const lora_pool_desc& d, const lora_problem* probs, int32_t nprob) {
+lora_status check_problems(const lora_pool* pool, const lora_problem* probs, int32_t nprob) {
+    const lora_pool_desc& d = pool->d;
     for (int32_t i = 0; i < nprob; ++i) {
         const lora_problem& pr = probs[i];
         if (pr.x == nullptr || pr.y == nullptr) return LORA_EINVAL;
         if (!aligned16(pr.x) || !aligned16(pr.y)) return LORA_EALIGN;
         if (pr.ldx % 8 != 0 || pr.ldy % 8 != 0) return LORA_EALIGN;
-        if (pr.ldx < d.h || pr.ldy < d.h || pr.ldx > INT32_MAX || pr.ldy > INT32_MAX)
-            return LORA_EINVAL;
         if (pr.layer < 0 || pr.layer >= d.num_layers || pr.proj < 0 || pr.proj >= d.num_proj)
+            return LORA_EINVAL;
+        if (pr.ldx < pool->d_in[pr.proj] || pr.ldy < pool->d_out[pr.proj] || pr.ldx > INT32_MAX ||
+            pr.ldy > INT32_MAX)
             return LORA_EINVAL;
     }
     return LORA_OK;
@@ -464,6 +484,27 @@ bool split_fits(const lora_pool_desc& d, int32_t nprob, int32_t T, size_t ws_byt
     return ws_bytes >= ws_layout(T, T).total + split_t_bytes(d, T);
 }
 
+template <bool W>
+lora_status launch_split(const SplitParams& prm, const DeviceInfo* di, cudaStream_t stream) {
+    const int grid = di->sm_count * 4;
+    const size_t xs_bytes = (size_t)kChunk * prm.pool.h * 2;   // the chunk's x rows
+    static thread_local int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        lora_status st = cuda_status(cudaFuncSetAttribute(split_shrink_kernel<W>,
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          (int)(kChunk * 8192 * 2)));   // h <= 8192
+        if (st != LORA_OK) return st;
+        attr_dev = dev;
+    }
+    split_shrink_kernel<W><<<grid, kSplitThreads, xs_bytes, stream>>>(prm);
+    lora_status st = cuda_status(cudaGetLastError());
+    if (st != LORA_OK) return st;
+    split_expand_kernel<W><<<grid, kSplitThreads, 0, stream>>>(prm);
+    return cuda_status(cudaGetLastError());
+}
+
 lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
                       cudaStream_t stream) {
     DeviceInfo* di = nullptr;
@@ -474,42 +515,24 @@ lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t 
     prm.pool = view_of(pool);
     prm.ws = reinterpret_cast<char*>(ws);
     prm.nprob = nprob;
+    prm.out_blocks = 1;
     for (int32_t i = 0; i < nprob; ++i) {
-        const lora_problem& pr = probs[i];
-        prm.probs[i].x = reinterpret_cast<const __nv_bfloat16*>(pr.x);
-        prm.probs[i].y = reinterpret_cast<__nv_bfloat16*>(pr.y);
-        prm.probs[i].ldx = (int32_t)pr.ldx;
-        prm.probs[i].ldy = (int32_t)pr.ldy;
-        prm.probs[i].blk = pr.layer * pool->d.num_proj + pr.proj;
+        prm.probs[i] = prob_desc(pool, probs[i]);
+        prm.out_blocks = std::max(prm.out_blocks, vec_pages(prm.probs[i].d_out, pool->d.h));
     }
-    const int grid = di->sm_count * 4;
-    const size_t xs_bytes = (size_t)kChunk * pool->d.h * 2;   // the chunk's x rows
-    static thread_local int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        st = cuda_status(cudaFuncSetAttribute(split_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)(kChunk * 8192 * 2)));   // h <= 8192
-        if (st != LORA_OK) return st;
-        attr_dev = dev;
-    }
-    split_shrink_kernel<<<grid, kSplitThreads, xs_bytes, stream>>>(prm);
-    st = cuda_status(cudaGetLastError());
-    if (st != LORA_OK) return st;
-    split_expand_kernel<<<grid, kSplitThreads, 0, stream>>>(prm);
-    return cuda_status(cudaGetLastError());
+    return pool->square ? launch_split<false>(prm, di, stream) : launch_split<true>(prm, di, stream);
 }
 
 // The delta launches after grouping: the CUDA-core kernel over the chunk list, then
 // (when the batch may hold tensor-core tiles) the tensor-core kernel over the tile list.
 lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
                       size_t ws_bytes, float* t_out, bool with_mma, cudaStream_t stream) {
-    lora_status st = check_problems(pool->d, probs, nprob);
+    lora_status st = check_problems(pool, probs, nprob);
     if (st != LORA_OK) return st;
     const int h8 = pool->d.h / 8;
     if (!with_mma && t_out == nullptr && split_fits(pool->d, nprob, T, ws_bytes))
         return run_split(pool, probs, nprob, ws, stream);
-    if (with_mma && mma_min_rows(pool->d) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
+    if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
         // one launch per batch of projections for both work classes
         if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
         if (h8 <= 512) return launch_fused<2, 8>(pool, probs, nprob, T, ws, stream);
@@ -517,7 +540,7 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     }
     st = run_delta_ring(pool, probs, nprob, ws, t_out, stream);
     if (st != LORA_OK) return st;
-    if (with_mma && mma_min_rows(pool->d) > 0) st = run_mma(pool, probs, nprob, T, ws, stream);
+    if (with_mma && mma_min_rows(pool) > 0) st = run_mma(pool, probs, nprob, T, ws, stream);
     return st;
 }
 
@@ -586,15 +609,39 @@ lora_status lora_pool_create(lora_pool** out, const lora_pool_desc* desc) {
     if (d.r_max > LORA_MAX_RANK || d.h > 8192) return LORA_ETOOBIG;
     if (d.num_pages > INT32_MAX || d.num_pages > INT64_MAX / d.h) return LORA_ETOOBIG;
     if ((int64_t)d.num_layers * d.num_proj > (1 << 20)) return LORA_ETOOBIG;
-    lora_pool* p = (lora_pool*)malloc(sizeof(lora_pool));
+    lora_pool* p = new (std::nothrow) lora_pool;
     if (p == nullptr) return LORA_EINVAL;
     p->d = d;
+    p->d.proj_dims = nullptr;
+    p->d_in.resize((size_t)d.num_proj);
+    p->d_out.resize((size_t)d.num_proj);
+    p->pre.resize((size_t)d.num_proj);
+    int64_t units = 0;
+    for (int32_t q = 0; q < d.num_proj; ++q) {
+        const int32_t di = d.proj_dims ? d.proj_dims[2 * q] : d.h;
+        const int32_t dq = d.proj_dims ? d.proj_dims[2 * q + 1] : d.h;
+        if (di <= 0 || dq <= 0 || di % 8 != 0 || dq % 8 != 0 ||
+            di > LORA_MAX_VEC_PAGES * d.h || dq > LORA_MAX_VEC_PAGES * d.h) {
+            delete p;
+            return (di <= 0 || dq <= 0 || di % 8 || dq % 8) ? LORA_EINVAL : LORA_ETOOBIG;
+        }
+        p->d_in[q] = di;
+        p->d_out[q] = dq;
+        p->pre[q] = (int32_t)units;
+        units += vec_pages(di, d.h) + vec_pages(dq, d.h);
+        p->square = p->square && di == d.h && dq == d.h;
+    }
+    if (units * d.num_layers > (1 << 26)) {
+        delete p;
+        return LORA_ETOOBIG;
+    }
+    p->units = (int32_t)units;
     *out = p;
     return LORA_OK;
 }
 
 lora_status lora_pool_destroy(lora_pool* pool) {
-    free(pool);
+    delete pool;
     return LORA_OK;
 }
 
@@ -654,7 +701,7 @@ static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start,
     sp.S = S;
     sp.Td = Td;
     sp.T = T;
-    sp.mma_min = mma_min_rows(pool->d);
+    sp.mma_min = mma_min_rows(pool);
     sp.mma_max_rank = kMmaMaxRank;
     sp.L_tokens = T;
     sp.L_segments = S + Td;
@@ -732,9 +779,10 @@ lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_byte
         return LORA_EINVAL;
     lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
     if (st != LORA_OK) return st;
+    const int32_t vec_units = vec_pages(pool->d_in[proj], pool->d.h) + vec_pages(pool->d_out[proj], pool->d.h);
     page_list_kernel<<<1, kSegThreads, 0, (cudaStream_t)stream>>>(
-        view_of(pool), reinterpret_cast<const char*>(ws), layer * pool->d.num_proj + proj, out_pages,
-        cap, count_dev);
+        view_of(pool), reinterpret_cast<const char*>(ws), layer * pool->units + pool->pre[proj], vec_units,
+        out_pages, cap, count_dev);
     return cuda_status(cudaGetLastError());
 }
 
@@ -789,7 +837,7 @@ lora_status lora_bgmv_noalloc(const lora_pool* pool, const lora_problem* probs, 
     if (pool == nullptr || T < 0 || nprob < 0) return LORA_EINVAL;
     if (T > LORA_NOALLOC_MAX_TOKENS) return LORA_ETOOBIG;
     if ((T > 0 && token_adapter == nullptr) || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
-    lora_status st = check_problems(pool->d, probs, nprob);
+    lora_status st = check_problems(pool, probs, nprob);
     if (st != LORA_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     void* ws = nullptr;

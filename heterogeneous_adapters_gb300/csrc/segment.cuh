@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
                     ok = false;
                 } else {
                     const long long off = P.pt_off[a];
-                    const long long need = (long long)P.num_layers * P.num_proj * 2 * r;
+                    const long long need = (long long)P.num_layers * P.units * r;
                     if (off < 0 || off + need > P.pt_len) {
                         errbits |= LORA_DERR_PTBLOCK;
                         ok = false;
@@ -307,10 +307,11 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
 }
 
 // Debug export of the page-table walk: for each group, its A-row pages then its
-// B-column pages for block `blk` (= layer * P + proj), packed in group order.
+// B-column pages for one problem, packed in group order.  blk: the A block's offset in
+// units of r (layer * U + pre(p)); vec_units: pages per A row plus pages per B column.
 __global__ void __launch_bounds__(kSegThreads)
-    page_list_kernel(const PoolView P, const char* ws, int32_t blk, int32_t* out, int64_t cap,
-                     int32_t* count_out) {
+    page_list_kernel(const PoolView P, const char* ws, int32_t blk, int32_t vec_units, int32_t* out,
+                     int64_t cap, int32_t* count_out) {
     __shared__ int scan_smem[33];
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     const WsLayout L = ws_layout(hdr->cap_tokens, hdr->cap_segments);
@@ -322,10 +323,10 @@ __global__ void __launch_bounds__(kSegThreads)
         const int a = g < G ? grp_adapter[g] : 0;
         const int r = g < G ? P.ranks[a] : 0;
         int tot;
-        const int base = block_exclusive_scan(2 * r, scan_smem, &tot) + carry;
+        const int base = block_exclusive_scan(vec_units * r, scan_smem, &tot) + carry;
         if (g < G) {
-            const long long src = P.pt_off[a] + (long long)blk * 2 * r;
-            for (int e = 0; e < 2 * r; ++e)
+            const long long src = P.pt_off[a] + (long long)blk * r;
+            for (int e = 0; e < vec_units * r; ++e)
                 if (base + e < cap) out[base + e] = P.pt[src + e];
         }
         carry += tot;

@@ -51,7 +51,7 @@ struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
     CUtensorMap x_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
     CUtensorMap y_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
     CUtensorMap y1_map[kMmaMaxProbs];        // {h, T}, box {64, 1}
-    int32_t blk[kMmaMaxProbs];               // layer * P + proj
+    int32_t blk[kMmaMaxProbs];               // A block offset in units of r (l * 2P + 2p)
     PoolView pool;
     char* ws;
     int32_t nprob;
@@ -118,7 +118,7 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
     it.pr = start + local % p.xgrp_size[p0];
     const int r = it.tile.rank;
     it.rp = mma_rpad(r);
-    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * 2 * r;
+    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * r;   // h x h pools only
     bool bad = false;
     for (int e = lane; e < 2 * r; e += 32) {
         const int page = p.pool.pt[it.blk + e];

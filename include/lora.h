@@ -69,6 +69,7 @@ extern "C" {
 #define LORA_MAX_PROBLEMS_PER_LAUNCH 256
 /* Maximum adapter "segments" of one call: prefill segments + decode tokens. */
 #define LORA_MAX_SEGMENTS 16384
+#define LORA_MAX_VEC_PAGES 16           /* pages one A row or B column may span */
 
 typedef enum {
     LORA_OK = 0,
@@ -105,18 +106,31 @@ typedef struct {
     const int64_t* adapter_pt_off; /* device int64 [num_adapters]                      */
     const int32_t* ranks;          /* device int32 [num_adapters]                      */
     const float* scales;           /* device f32   [num_adapters]                      */
+    /* host int32 [num_proj][2]: (d_in, d_out) of each projection, multiples of 8 and at
+     * most LORA_MAX_VEC_PAGES * h, copied at creation; NULL: every projection is h x h.
+     * "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "Worked example": the
+     * adapted projections of a model have different widths (grouped-query k/v, MLP).
+     * Page-table layout: a vector of length d takes ceil(d/h) pages (the last partly
+     * used); adapter a's block for (layer l, projection p, A or B) holds r_a * ceil(d/h)
+     * entries, page kb of every row (A) or column (B) and then page kb + 1; with
+     * u(p) = ceil(d_in/h) + ceil(d_out/h), U = sum of u over the projections and
+     * pre(p) = sum of u over the projections before p, the A block starts at entry
+     * adapter_pt_off[a] + r_a * (l * U + pre(p)) and the B block r_a * ceil(d_in/h) later
+     * (for h x h: (l * P + p) * 2 * r_a and r_a later).  Tensor-core tiles serve h x h
+     * pools only; other pools run on the CUDA-core kernels. */
+    const int32_t* proj_dims;
 } lora_pool_desc;
 
 typedef struct lora_pool lora_pool; /* opaque, host memory only */
 
-/* One projection instance: y (bf16 [T][ldy]) += delta computed from x (bf16 [T][ldx])
- * with the adapters' pages for (layer, proj).  All problems of one call share the
- * batch (the same tokens and adapter ids). */
+/* One projection instance: y (bf16 [T][ldy], d_out columns updated) += delta computed
+ * from x (bf16 [T][ldx], d_in columns read) with the adapters' pages for (layer, proj).
+ * All problems of one call share the batch (the same tokens and adapter ids). */
 typedef struct {
     const void* x;
     void* y;
-    int64_t ldx;                   /* elements, % 8 == 0, >= h                         */
-    int64_t ldy;
+    int64_t ldx;                   /* elements, % 8 == 0, >= d_in (h for h x h pools)  */
+    int64_t ldy;                   /* elements, % 8 == 0, >= d_out                     */
     int32_t layer;
     int32_t proj;
 } lora_problem;
@@ -193,9 +207,10 @@ lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs,
                                int32_t T, int32_t S, void* ws, size_t ws_bytes, void* stream);
 
 /* Debug export of the page-table walk (a2): for problem (layer, proj), for each group
- * g of the grouping in ws, the r_a A-row pages then the r_a B-column pages, packed in
- * group order into out_pages (device int32, capacity `cap`).  *count_dev receives the
- * number written (device int32). */
+ * g of the grouping in ws, the entries of its A block then of its B block as the
+ * page-table layout above orders them (r_a each for h x h pools; r_a * ceil(d/h) for a
+ * vector of length d), packed in group order into out_pages (device int32, capacity
+ * `cap`).  *count_dev receives the number written (device int32). */
 lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_bytes, int32_t layer,
                                  int32_t proj, int32_t* out_pages, int64_t cap, int32_t* count_dev,
                                  void* stream);

@@ -41,7 +41,7 @@ class GpuCase:
         p = wl.pool
         self.pool = lora.Pool(self.dev.pool, p.num_pages, p.h, self.dev.pt, p.pt.size,
                               self.dev.pt_off, self.dev.ranks, self.dev.scales, p.num_adapters,
-                              p.num_layers, p.num_proj, p.r_max)
+                              p.num_layers, p.num_proj, p.r_max, p.proj_dims)
         b = wl.batch
         self.T = b.num_tokens
         self.nseg = b.num_segments + b.num_decode

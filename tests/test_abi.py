@@ -48,7 +48,7 @@ def test_pool_create_host_checks(lib):
     def desc(**kw):
         d = dict(pages=fake, num_pages=16, h=256, num_adapters=2, num_layers=1, num_proj=1,
                  r_max=8, reserved=0, page_table=fake, page_table_len=32, adapter_pt_off=fake,
-                 ranks=fake, scales=fake)
+                 ranks=fake, scales=fake, proj_dims=None)
         d.update(kw)
         return lora_pool_desc(**d)
 
@@ -59,6 +59,15 @@ def test_pool_create_host_checks(lib):
     assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(pages=fake + 8))) == LORA_EALIGN
     assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(r_max=257))) == LORA_ETOOBIG
     assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(num_adapters=0))) == LORA_EINVAL
+    # projection widths: multiples of 8, at most LORA_MAX_VEC_PAGES pages
+    import numpy as np
+    for dims, want in (([256, 64], 0), ([256, 4096], 0), ([100, 256], LORA_EINVAL),
+                       ([256, 17 * 256], LORA_ETOOBIG), ([0, 256], LORA_EINVAL)):
+        arr = np.asarray(dims, np.int32)
+        st = lib.lora_pool_create(ctypes.byref(h), ctypes.byref(desc(proj_dims=arr.ctypes.data)))
+        assert st == want, (dims, st)
+        if st == 0:
+            assert lib.lora_pool_destroy(h) == 0
     assert lib.lora_pool_create(None, ctypes.byref(desc())) == LORA_EINVAL
 
 

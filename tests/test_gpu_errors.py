@@ -9,12 +9,14 @@ import heterogeneous_adapters_gb300 as lora
 from heterogeneous_adapters_gb300 import _binding as B
 
 from .harness import GpuCase, full_check
-from .test_gpu_parity import small_decode, small_prefill
+from .test_gpu_parity import _widths_case, small_decode, small_prefill
 
 pytestmark = pytest.mark.gpu
 
 
-def _wl():
+def _wl(wide=False):
+    if wide:   # projection 0 reads and writes vectors of 3 pages (the last partly used)
+        return _widths_case("decode", 72, 512, [(1280, 1040), (512, 512)], 6, [4, 8], T_dec=20)
     return small_decode(71, 512, 1, 2, 6, [4, 8], 20)
 
 
@@ -72,11 +74,13 @@ def test_bad_page_rank_and_block_bits(path, monkeypatch):
 
 @pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("ab", [0, 1])
-def test_bad_page_skips_that_adapter_in_that_projection_only(path, ab, monkeypatch):
-    """An out-of-range A-row (ab=0) or B-column (ab=1) page of adapter a in projection 0:
-    the page bit is set, a's rows of projection 0 keep their y, everything else is right."""
+@pytest.mark.parametrize("wide", [False, True])
+def test_bad_page_skips_that_adapter_in_that_projection_only(path, ab, wide, monkeypatch):
+    """An out-of-range A-row (ab=0) or B-column (ab=1) page of adapter a in projection 0
+    (for the wide pool, in the last page block of its vectors): the page bit is set, a's
+    rows of projection 0 keep their y, everything else is right."""
     monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
-    wl = _wl()
+    wl = _wl(wide)
     case = GpuCase(wl)
     try:
         ids = wl.batch.token_adapter()

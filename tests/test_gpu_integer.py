@@ -62,23 +62,34 @@ def test_grouping_bit_exact(name):
         case.close()
 
 
-@pytest.mark.parametrize("name", ["config0", "decode-zipf", "mixed"])
+def _widths_decode():
+    """Two layers of projections 256 -> 64, 256 -> 640 and 640 -> 256 on h = 256."""
+    rng = np.random.default_rng(67)
+    ranks = rng.choice(np.asarray([1, 3, 8, 16], np.int32), size=12)
+    pool = spec.make_pool_all_resident(rng, 256, 2, 3, ranks,
+                                       proj_dims=[(256, 64), (256, 640), (640, 256)])
+    ids = rng.integers(-1, 12, size=90).astype(np.int32)
+    batch = spec.Batch(np.zeros(1, np.int32), np.zeros(0, np.int32), ids)
+    return spec.Workload("decode-widths", 67, pool, batch, spec.all_problems(2, 3))
+
+
+@pytest.mark.parametrize("name", ["config0", "decode-zipf", "mixed", "decode-widths"])
 def test_page_list_bit_exact(name):
     import torch
-    wl = CASES[name]()
+    wl = _widths_decode() if name == "decode-widths" else CASES[name]()
     case = GpuCase(wl)
     try:
         _segment(case)
         _, _, ga, _ = _grouping_from_ws(case)
-        cap = int(2 * wl.pool.ranks.astype(np.int64)[ga].sum()) + 8
         for (l, p) in wl.problems:
+            want = oracle.page_list(wl.pool.pt, wl.pool.pt_off, wl.pool.ranks, wl.pool.num_proj,
+                                    l, p, ga, h=wl.h, proj_dims=wl.pool.proj_dims)
+            cap = want.size + 8
             out = torch.full((cap,), -7, dtype=torch.int32, device=case.device)
             cnt = torch.zeros(1, dtype=torch.int32, device=case.device)
             case.lora.debug_page_list(case.pool, case.ws, case.ws_bytes, l, p, out, cap, cnt,
                                       case.stream)
             assert case.error_bits() == 0
-            want = oracle.page_list(wl.pool.pt, wl.pool.pt_off, wl.pool.ranks, wl.pool.num_proj,
-                                    l, p, ga)
             n = int(cnt.item())
             assert n == want.size
             assert np.array_equal(out[:n].cpu().numpy(), want)

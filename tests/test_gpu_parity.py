@@ -302,3 +302,63 @@ def test_full_config(cfg, k):
                    strict=False)
     finally:
         case.close()
+
+
+def _widths_case(kind, seed, h, dims, N, ranks, T_dec=0, lens=()):
+    """One layer, one projection per (d_in, d_out) pair in dims, every adapter resident."""
+    rng = np.random.default_rng(seed)
+    P = len(dims)
+    ranks_a = rng.choice(np.asarray(ranks, np.int32), size=N)
+    pool = make_pool_all_resident(rng, h, 1, P, ranks_a, num_pages=None, proj_dims=dims)
+    lens = np.asarray(lens, np.int64)
+    ids = rng.choice(N, size=lens.size + T_dec, p=spec.zipf_probs(N, 1.0)).astype(np.int32)
+    ids[::7] = -1
+    seg_start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    batch = Batch(seg_start, ids[:lens.size], ids[lens.size:])
+    return Workload(f"{kind}-widths-h{h}", seed, pool, batch, all_problems(1, P))
+
+
+WIDTH_CASES = {
+    # narrower k/v outputs, a 2.5-page output and input, an output one page plus 8 columns
+    "h1024-mixed-widths": (1024, [(1024, 256), (1024, 2560), (2560, 1024), (1024, 1032),
+                                  (1024, 1024)]),
+    # Llama-3-8B shapes: q, k, v, o, gate, up, down
+    "h4096-llama3-8b": (4096, [(4096, 4096), (4096, 1024), (4096, 1024), (4096, 4096),
+                               (4096, 14336), (4096, 14336), (14336, 4096)]),
+    # the widest vector a pool allows (16 pages) on both sides
+    "h512-max-pages": (512, [(8192, 8), (8, 8192)]),
+}
+
+
+@pytest.mark.parametrize("case_name", list(WIDTH_CASES))
+@pytest.mark.parametrize("path", ["decode-split", "decode-ring", "prefill", "mixed"])
+def test_projection_widths(case_name, path, monkeypatch):
+    """Projections whose input and output widths differ from h (vectors spanning several
+    pool pages, the last one partly used).  x columns past a problem's d_in hold NaN and y
+    columns past its d_out must come back unchanged."""
+    h, dims = WIDTH_CASES[case_name]
+    if path == "decode-split":
+        monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", "8")
+    elif path == "decode-ring":
+        monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", "0")
+    kind = path.split("-")[0]
+    if kind == "decode":
+        wl = _widths_case(kind, 70, h, dims, 9, [1, 5, 8, 16, 64], T_dec=29)
+    elif kind == "prefill":
+        wl = _widths_case(kind, 71, h, dims, 6, [8, 16, 128], lens=[1, 130, 17, 64, 0, 5])
+    else:
+        wl = _widths_case(kind, 72, h, dims, 7, [4, 16, 32], T_dec=11, lens=[70, 3, 129])
+    case = GpuCase(wl)
+    try:
+        for i, (l, p) in enumerate(case.dev.problems):
+            d_in, d_out = wl.pool.dims(p)
+            case.dev.x[i, :, d_in:] = float("nan")
+        y_before = case.dev.y.clone()
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+        for i, (l, p) in enumerate(case.dev.problems):
+            d_out = wl.pool.dims(p)[1]
+            assert case.torch.equal(case.dev.y[i, :, d_out:].view(case.torch.int16),
+                                    y_before[i, :, d_out:].view(case.torch.int16)), (l, p)
+    finally:
+        case.close()

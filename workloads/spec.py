@@ -371,6 +371,20 @@ def config4(variant: str = "distinct") -> Workload:
                            layer_slices=True)
 
 
+# Llama-3-8B (h 4096, 8 KV heads of 128, MLP 14336): q, k, v, o, gate, up, down
+LLAMA3_8B_DIMS = [(4096, 4096), (4096, 1024), (4096, 1024), (4096, 4096),
+                  (4096, 14336), (4096, 14336), (14336, 4096)]
+
+
+def llama3_8b_decode(layers: int = 32) -> Workload:
+    """Decode batch of 64 tokens over 600 adapters of ranks {8..64} on a Llama-3-8B base,
+    every projection of every layer adapted at its own widths (about 105 GB of pool at
+    32 layers)."""
+    return decode_workload(f"llama3-8b-decode-bgmv-h4096-t64-a600-7proj-l{layers}", 1008, 4096,
+                           layers, 7, 600, [8, 16, 32, 64], 64, 1.0,
+                           proj_dims=LLAMA3_8B_DIMS)
+
+
 CONFIGS = {0: config0, 1: config1, 2: config2, 3: config3, 4: config4}
 
 
