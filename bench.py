@@ -39,7 +39,8 @@ def workload_for(cfg: str):
     """Configs 0-4 as named in the workload module; "1s" (4 layers, 300 adapters, ~2.4 GB
     pool), "2s" (2 layers x 2 projections, ~2 GB on the device) and "3s" (1 layer x 2
     projections) are small variants of configs 1, 2 and 3 for profiler captures; "8b" is a
-    Llama-3-8B decode batch over all seven projections at their own widths ("8bs": 1 layer)."""
+    Llama-3-8B decode batch over all seven projections at their own widths ("8bs": 1 layer);
+    "8bp" a Llama-3-8B prefill batch over 4 layers ("8bps": 1 layer)."""
     from workloads import spec
     if cfg == "1s":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
@@ -55,6 +56,10 @@ def workload_for(cfg: str):
         return spec.llama3_8b_decode()
     if cfg == "8bs":
         return spec.llama3_8b_decode(layers=1)
+    if cfg == "8bp":
+        return spec.llama3_8b_prefill()
+    if cfg == "8bps":
+        return spec.llama3_8b_prefill(layers=1)
     if cfg == "4d":
         return spec.config4("distinct")
     if cfg == "4z":

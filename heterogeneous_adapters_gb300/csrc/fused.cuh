@@ -21,6 +21,7 @@ struct FusedParams {
     RingParamsT<kMmaMaxProbs> ring;
     float ring_speed;   // bytes per CTA-second of the ring body / those of the tensor-core body
 };
+static_assert(sizeof(FusedParams) <= 32764, "kernel parameters are limited to 32,764 bytes");
 
 // CTAs given to the CUDA-core class out of G (0 if it has no work, G if the tensor-core
 // class has none; otherwise at least one each), so that both classes' CTAs need about the

@@ -31,6 +31,7 @@ struct lora_pool {
     std::vector<int32_t> pre;         // units before each projection in a layer
     int32_t units = 0;                // units of one layer
     bool square = true;               // every projection h x h
+    bool mma_widths = true;           // every d_in % 64 == 0 and d_out % 128 == 0 (tile shapes)
 };
 
 namespace {
@@ -222,10 +223,12 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
 
 // ---------------------------------------------------------------------------- tensor-core path
 // Segments of at least this many rows (and rank <= kMmaMaxRank) take the tensor-core
-// path when h is a multiple of 128; LORA_MMA_MIN_ROWS overrides it (0 disables).
+// path when h is a multiple of 128 and every projection's d_in is a multiple of 64 (the
+// shrink K chunk) and d_out one of 128 (the expand slice); LORA_MMA_MIN_ROWS overrides it
+// (0 disables).
 int mma_min_rows(const lora_pool* pool) {
     const lora_pool_desc& d = pool->d;
-    if (d.h % kMmaNTile != 0 || !pool->square) return 0;   // tensor-core tiles: h x h pools
+    if (d.h % kMmaNTile != 0 || !pool->mma_widths) return 0;
     const char* e = getenv("LORA_MMA_MIN_ROWS");
     // one-row (decode) segments always stay on the CUDA-core path
     if (e != nullptr) return atoi(e) > 0 ? std::max(2, atoi(e)) : 0;
@@ -305,13 +308,18 @@ lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* 
     if (st != LORA_OK) return st;
     for (int32_t i = 0; i < n; ++i) {
         const lora_problem& pr = probs[i];
-        st = make_map(&prm.x_map[i], pr.x, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldx, kMmaRowBlock);
+        const int32_t di = pool->d_in[pr.proj], dq = pool->d_out[pr.proj];
+        st = make_map(&prm.x_map[i], pr.x, (uint64_t)di, (uint64_t)T, (uint64_t)pr.ldx, kMmaRowBlock);
         if (st != LORA_OK) return st;
-        st = make_map(&prm.y_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, kMmaRowBlock);
+        st = make_map(&prm.y_map[i], pr.y, (uint64_t)dq, (uint64_t)T, (uint64_t)pr.ldy, kMmaRowBlock);
         if (st != LORA_OK) return st;
-        st = make_map(&prm.y1_map[i], pr.y, (uint64_t)d.h, (uint64_t)T, (uint64_t)pr.ldy, 1);
+        st = make_map(&prm.y1_map[i], pr.y, (uint64_t)dq, (uint64_t)T, (uint64_t)pr.ldy, 1);
         if (st != LORA_OK) return st;
         prm.blk[i] = pr.layer * pool->units + pool->pre[pr.proj];
+        prm.n_kc[i] = (int16_t)(di / kMmaKChunk);
+        prm.n_nt[i] = (int16_t)(dq / kMmaNTile);
+        prm.pv_in[i] = (uint8_t)vec_pages(di, d.h);
+        prm.pv_out[i] = (uint8_t)vec_pages(dq, d.h);
     }
     // runs of consecutive problems reading the same x form the item order's groups
     for (int32_t i = 0; i < n;) {
@@ -532,7 +540,7 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     const int h8 = pool->d.h / 8;
     if (!with_mma && t_out == nullptr && split_fits(pool->d, nprob, T, ws_bytes))
         return run_split(pool, probs, nprob, ws, stream);
-    if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
+    if (with_mma && mma_min_rows(pool) > 0 && pool->square && t_out == nullptr && h8 <= 640 && T > 0) {
         // one launch per batch of projections for both work classes
         if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
         if (h8 <= 512) return launch_fused<2, 8>(pool, probs, nprob, T, ws, stream);
@@ -630,6 +638,7 @@ lora_status lora_pool_create(lora_pool** out, const lora_pool_desc* desc) {
         p->pre[q] = (int32_t)units;
         units += vec_pages(di, d.h) + vec_pages(dq, d.h);
         p->square = p->square && di == d.h && dq == d.h;
+        p->mma_widths = p->mma_widths && di % kMmaKChunk == 0 && dq % kMmaNTile == 0;
     }
     if (units * d.num_layers > (1 << 26)) {
         delete p;

@@ -48,10 +48,14 @@ constexpr uint32_t kDerrTimeoutMma = LORA_DERR_TIMEOUT;
 
 struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
     CUtensorMap pool_map;                    // {h, num_pages}, box {64, 1}, 128B swizzle
-    CUtensorMap x_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
-    CUtensorMap y_map[kMmaMaxProbs];         // {h, T}, box {64, 32}
-    CUtensorMap y1_map[kMmaMaxProbs];        // {h, T}, box {64, 1}
-    int32_t blk[kMmaMaxProbs];               // A block offset in units of r (l * 2P + 2p)
+    CUtensorMap x_map[kMmaMaxProbs];         // {d_in, T}, box {64, 32}
+    CUtensorMap y_map[kMmaMaxProbs];         // {d_out, T}, box {64, 32}
+    CUtensorMap y1_map[kMmaMaxProbs];        // {d_out, T}, box {64, 1}
+    int32_t blk[kMmaMaxProbs];               // A block offset in units of r (l * U + pre(p))
+    int16_t n_kc[kMmaMaxProbs];              // shrink K chunks: d_in / 64
+    int16_t n_nt[kMmaMaxProbs];              // expand column slices: d_out / 128
+    uint8_t pv_in[kMmaMaxProbs];             // pages per A row: ceil(d_in / h)
+    uint8_t pv_out[kMmaMaxProbs];            // pages per B column: ceil(d_out / h)
     PoolView pool;
     char* ws;
     int32_t nprob;
@@ -98,7 +102,9 @@ struct MmaItem {
     Tile tile;
     int pr;
     int rp;
-    long long blk;    // first page-table entry of the A block (B block follows at +r)
+    int n_kc, n_nt;   // shrink K chunks and expand column slices of the projection
+    int pv_in;        // page blocks of an A row
+    long long blk;    // first page-table entry of the A block (B block follows at +r pv_in)
     bool ok;
 };
 
@@ -118,9 +124,13 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
     it.pr = start + local % p.xgrp_size[p0];
     const int r = it.tile.rank;
     it.rp = mma_rpad(r);
-    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * r;   // h x h pools only
+    it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * r;
+    it.n_kc = p.n_kc[it.pr];
+    it.n_nt = p.n_nt[it.pr];
+    it.pv_in = p.pv_in[it.pr];
     bool bad = false;
-    for (int e = lane; e < 2 * r; e += 32) {
+    const int n_ent = (it.pv_in + p.pv_out[it.pr]) * r;   // every page of the item
+    for (int e = lane; e < n_ent; e += 32) {
         const int page = p.pool.pt[it.blk + e];
         bad |= (page < 0 || page >= p.pool.num_pages);
     }
@@ -163,7 +173,9 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
     const int n_tiles = hdr->counts[3];
     const uint32_t total = (uint32_t)n_tiles * (uint32_t)p.nprob;
     const int h = p.pool.h;
-    const int n_kc = h / kMmaKChunk, n_nt = h / kMmaNTile;
+    // chunks and slices per page: a vector longer than a page continues on its next page
+    // block (page kb of every row, then kb + 1), so chunk kc reads page kc / kc_pg
+    const int kc_pg = h / kMmaKChunk, nt_pg = h / kMmaNTile;
     auto bar = [&](uint32_t off) { return smem_addr(base + off); };
 
     if (tid == 0) {
@@ -212,12 +224,16 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
             const void* xmap = &p.x_map[mi.pr];
             int pga[4];
+            for (int kc = 0; kc < mi.n_kc; ++kc) {
+                if (kc % kc_pg == 0) {   // page ids of the A rows' page block kc / kc_pg
+                    const long long b0 = mi.blk + (long long)(kc / kc_pg) * r;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = lane + 32 * q;
-                pga[q] = j < r ? p.pool.pt[mi.blk + j] : (int)p.pool.num_pages;
-            }
-            for (int kc = 0; kc < n_kc; ++kc) {
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = lane + 32 * q;
+                        pga[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
+                    }
+                }
+                const int kcol = (kc % kc_pg) * kMmaKChunk;   // column within the A page
                 const uint32_t s = it % S1;
                 if (!mbar_wait(bar(L.empty1 + s * 8), ((it / S1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
                 const uint32_t st = bar(L.ring1 + s * p.s1_bytes);
@@ -239,11 +255,10 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     if (j < rp) {
                         if ((j | 3) < r) {
                             if ((j & 3) == 0)
-                                tma_gather4(st + 16384 + j * 128, &p.pool_map, kc * kMmaKChunk, pga[q], p1, p2, p3,
+                                tma_gather4(st + 16384 + j * 128, &p.pool_map, kcol, pga[q], p1, p2, p3,
                                             bar(L.full1 + s * 8));
                         } else {
-                            tma_load_2d(st + 16384 + j * 128, &p.pool_map, kc * kMmaKChunk, pga[q],
-                                        bar(L.full1 + s * 8));
+                            tma_load_2d(st + 16384 + j * 128, &p.pool_map, kcol, pga[q], bar(L.full1 + s * 8));
                         }
                     }
                 }
@@ -263,12 +278,16 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             if (!mi.ok) continue;
             const int r = mi.tile.rank, rp = mi.rp;
             int pgb[4];
+            for (int nt = 0; nt < mi.n_nt; ++nt, ++it2) {
+                if (nt % nt_pg == 0) {   // page ids of the B columns' page block nt / nt_pg
+                    const long long b0 = mi.blk + (long long)(mi.pv_in + nt / nt_pg) * r;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = lane + 32 * q;
-                pgb[q] = j < r ? p.pool.pt[mi.blk + r + j] : (int)p.pool.num_pages;
-            }
-            for (int nt = 0; nt < n_nt; ++nt, ++it2) {
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = lane + 32 * q;
+                        pgb[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
+                    }
+                }
+                const int ncol = (nt % nt_pg) * kMmaNTile;   // column within the B page
                 // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
                 // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
                 const uint32_t s = it2 % S2;
@@ -286,13 +305,13 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                         const uint32_t dst = st + (j >> 3) * 2048 + (j & 7) * 128;
                         if ((j | 3) < r) {
                             if ((j & 3) == 0) {
-                                tma_gather4(dst, &p.pool_map, nt * kMmaNTile, pgb[q], p1, p2, p3, bar(L.full2 + s * 8));
-                                tma_gather4(dst + 1024, &p.pool_map, nt * kMmaNTile + 64, pgb[q], p1, p2, p3,
+                                tma_gather4(dst, &p.pool_map, ncol, pgb[q], p1, p2, p3, bar(L.full2 + s * 8));
+                                tma_gather4(dst + 1024, &p.pool_map, ncol + 64, pgb[q], p1, p2, p3,
                                             bar(L.full2 + s * 8));
                             }
                         } else {
-                            tma_load_2d(dst, &p.pool_map, nt * kMmaNTile, pgb[q], bar(L.full2 + s * 8));
-                            tma_load_2d(dst + 1024, &p.pool_map, nt * kMmaNTile + 64, pgb[q], bar(L.full2 + s * 8));
+                            tma_load_2d(dst, &p.pool_map, ncol, pgb[q], bar(L.full2 + s * 8));
+                            tma_load_2d(dst + 1024, &p.pool_map, ncol + 64, pgb[q], bar(L.full2 + s * 8));
                         }
                     }
                 }
@@ -312,7 +331,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             const int row0 = mi.tile.row0;
             const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
             const void* ymap = &p.y_map[mi.pr];
-            for (int nt = 0; nt < n_nt; ++nt, ++it3) {
+            for (int nt = 0; nt < mi.n_nt; ++nt, ++it3) {
                 // y tile: half hf (64 columns) at hf * 16 KB, 32-row block b at + b * 4 KB
                 const uint32_t s = it3 % S3;
                 if (!mbar_wait(bar(L.empty3 + s * 8), ((it3 / S3) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
@@ -340,7 +359,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         // shrink of the first tile
         if (item < total) {
             const uint32_t id_shrink = idesc_bf16(128, cur.rp, 0, 0);
-            for (int kc = 0; kc < n_kc && ok; ++kc, ++it1) {
+            for (int kc = 0; kc < cur.n_kc && ok; ++kc, ++it1) {
                 const uint32_t s = it1 % S1;
                 if (!mbar_wait(bar(L.full1 + s * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
@@ -364,7 +383,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             tc_fence_after();
             const int rp = cur.rp;
             const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
-            for (int nt = 0; nt < n_nt && ok; ++nt, ++g, ++it2) {
+            for (int nt = 0; nt < cur.n_nt && ok; ++nt, ++g, ++it2) {
                 const uint32_t s = it2 % S2;
                 const uint32_t b = g & 1;
                 if (!mbar_wait(bar(L.full2 + s * 8), (it2 / S2) & 1, kWaitLimitNs)) { ok = false; break; }
@@ -384,7 +403,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                 __syncwarp();
                 // the next tile's shrink chunks that have already landed (a test, not a
                 // wait: a suspending wait here would hold the expand back for the whole shrink)
-                while (has_next && kc_next < n_kc) {
+                while (has_next && kc_next < nxt.n_kc) {
                     const uint32_t s1 = it1 % S1;
                     if (!mbar_test_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) break;
                     tc_fence_after();
@@ -399,7 +418,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             }
             if (!ok || !has_next) break;
             // the rest of the next tile's shrink
-            for (; kc_next < n_kc && ok; ++kc_next, ++it1) {
+            for (; kc_next < nxt.n_kc && ok; ++kc_next, ++it1) {
                 const uint32_t s1 = it1 % S1;
                 if (!mbar_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
@@ -468,7 +487,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             if (lane == 0) mbar_arrive(bar(L.t_ready));
             ++tcount;
             // ---- expand epilogue over the column slices: y (in the y ring) += D2
-            for (int nt = 0; nt < n_nt; ++nt, ++g) {
+            for (int nt = 0; nt < mi.n_nt; ++nt, ++g) {
                 const uint32_t b = g & 1;
                 const uint32_t ys = g % S3;
                 if (!mbar_wait(bar(L.d2_full + b * 8), (g >> 1) & 1, kWaitLimitNs)) { ok = false; break; }

@@ -116,8 +116,9 @@ typedef struct {
      * u(p) = ceil(d_in/h) + ceil(d_out/h), U = sum of u over the projections and
      * pre(p) = sum of u over the projections before p, the A block starts at entry
      * adapter_pt_off[a] + r_a * (l * U + pre(p)) and the B block r_a * ceil(d_in/h) later
-     * (for h x h: (l * P + p) * 2 * r_a and r_a later).  Tensor-core tiles serve h x h
-     * pools only; other pools run on the CUDA-core kernels. */
+     * (for h x h: (l * P + p) * 2 * r_a and r_a later).  Tensor-core tiles serve pools
+     * whose d_in are multiples of 64 and d_out multiples of 128 (h a multiple of 128);
+     * other pools run prefill segments on the CUDA-core kernels. */
     const int32_t* proj_dims;
 } lora_pool_desc;
 

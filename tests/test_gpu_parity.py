@@ -362,3 +362,32 @@ def test_projection_widths(case_name, path, monkeypatch):
                                     y_before[i, :, d_out:].view(case.torch.int16)), (l, p)
     finally:
         case.close()
+
+
+@pytest.mark.parametrize("mma_min", ["1", "32", "0"])
+@pytest.mark.parametrize("kind", ["prefill", "mixed"])
+def test_projection_widths_tensor_core_tiles(mma_min, kind, monkeypatch):
+    """Prefill tiles of projections whose widths differ from h (d_in a multiple of 64, d_out
+    one of 128): the shrink K loop crosses into an A row's next page block and the expand's
+    column slices into a B column's next page block, the last block partly used.  Every
+    segment of >= 2 rows on the tensor cores (1), the default split (32), none (0)."""
+    monkeypatch.setenv("LORA_MMA_MIN_ROWS", mma_min)
+    dims = [(1024, 256), (1024, 2560), (2560, 1024), (1024, 1024), (3072, 640)]
+    lens = [1, 2, 127, 128, 129, 300, 33, 0, 9]
+    if kind == "prefill":
+        wl = _widths_case(kind, 73, 1024, dims, 8, [1, 8, 16, 32, 64, 128], lens=lens)
+    else:
+        wl = _widths_case(kind, 74, 1024, dims, 8, [3, 16, 64, 100], T_dec=23, lens=lens)
+    case = GpuCase(wl, y0_zero=True)
+    try:
+        for i, (l, p) in enumerate(case.dev.problems):
+            case.dev.x[i, :, wl.pool.dims(p)[0]:] = float("nan")
+        y_before = case.dev.y.clone()
+        assert case.run() == 0
+        full_check(wl, case, list(range(len(wl.problems))))
+        for i, (l, p) in enumerate(case.dev.problems):
+            d_out = wl.pool.dims(p)[1]
+            assert case.torch.equal(case.dev.y[i, :, d_out:].view(case.torch.int16),
+                                    y_before[i, :, d_out:].view(case.torch.int16)), (l, p)
+    finally:
+        case.close()

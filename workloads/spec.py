@@ -385,6 +385,24 @@ def llama3_8b_decode(layers: int = 32) -> Workload:
                            proj_dims=LLAMA3_8B_DIMS)
 
 
+def llama3_8b_prefill(layers: int = 4) -> Workload:
+    """Prefill batch of 32 prompts of lengths uniform in [64, 1024] over 600 adapters of
+    ranks {8..64} (Zipf 1.0) on a Llama-3-8B base, every projection adapted at its own
+    widths.  Four layers by default: every projection's x and y buffers are allocated at
+    the widest projection's width, so all 32 layers would not fit beside the pool."""
+    rng = np.random.default_rng(1009)
+    P = len(LLAMA3_8B_DIMS)
+    ranks = rng.choice(np.asarray([8, 16, 32, 64], np.int32), size=600)
+    lens = rng.integers(64, 1025, size=32)
+    ids = rng.choice(600, size=32, p=zipf_probs(600, 1.0))
+    pool = make_pool_all_resident(rng, 4096, layers, P, ranks, proj_dims=LLAMA3_8B_DIMS)
+    seg_start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    batch = Batch(seg_start=seg_start, seg_adapter=ids.astype(np.int32),
+                  dec_adapter=np.zeros(0, np.int32))
+    return Workload(f"llama3-8b-prefill-sgmv-h4096-s32-a600-7proj-l{layers}", 1009, pool, batch,
+                    all_problems(layers, P))
+
+
 CONFIGS = {0: config0, 1: config1, 2: config2, 3: config3, 4: config4}
 
 
