@@ -20,8 +20,12 @@ struct WsHeader {
     uint32_t work_counter2;  // second queue (tensor-core items)
     int32_t cap_tokens;      // layout of the arrays below the header (set by grouping)
     int32_t cap_segments;
-    unsigned long long weight[2];   // bytes one projection streams: CUDA-core, tensor-core class
-    uint32_t pad[50];
+    // per work class (0: CUDA-core chunks, 1: tensor-core tiles): adapted rows, and page
+    // rows (rank x items: an item reads its adapter's pages once); a projection of widths
+    // (d_in, d_out) streams (d_in + 2 d_out) bf16 per row and (d_in + d_out) per page row
+    unsigned long long rows[2];
+    unsigned long long page_rows[2];
+    uint32_t pad[46];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

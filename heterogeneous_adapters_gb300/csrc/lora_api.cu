@@ -379,10 +379,12 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
     static thread_local size_t attr_smem = 0;
     int dev = 0;
     cudaGetDevice(&dev);
+    auto kern = pool->square ? sgmv_mma_kernel<false> : sgmv_mma_kernel<true>;
     if (attr_dev != dev || attr_smem < c.smem) {
-        st = cuda_status(cudaFuncSetAttribute(sgmv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)c.smem));
-        if (st != LORA_OK) return st;
+        for (auto k : {sgmv_mma_kernel<false>, sgmv_mma_kernel<true>}) {
+            st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem));
+            if (st != LORA_OK) return st;
+        }
         attr_dev = dev;
         attr_smem = c.smem;
     }
@@ -391,7 +393,7 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
         const int32_t n = nprob - base < per ? nprob - base : per;
         st = fill_mma(prm, pool, probs + base, n, T, ws, c);
         if (st != LORA_OK) return st;
-        sgmv_mma_kernel<<<di->sm_count, kMmaThreads, c.smem, stream>>>(prm);
+        kern<<<di->sm_count, kMmaThreads, c.smem, stream>>>(prm);
         st = cuda_status(cudaGetLastError());
         if (st != LORA_OK) return st;
     }
@@ -402,7 +404,7 @@ constexpr float kFusedRingSpeed = 1.22f;
 
 // Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0); the
 // ring body takes the stage shape the stand-alone ring kernel would take.
-template <int NV, int CW, int RP>
+template <int NV, int CW, int RP, bool W>
 lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
                             void* ws, const DeviceInfo* di, const MmaConfig& c, const RingShape& sh,
                             cudaStream_t stream) {
@@ -417,7 +419,7 @@ lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, in
     static thread_local size_t attr_smem = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = delta_fused_kernel<NV, CW, RP>;
+    auto kern = delta_fused_kernel<NV, CW, RP, W>;
     lora_status st;
     if (attr_dev != dev || attr_smem < smem) {
         st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
@@ -432,6 +434,12 @@ lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, in
         if (st != LORA_OK) return st;
         fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, sh.stages, RP);
         prm.ring_speed = ring_speed;
+        prm.row_elems = prm.page_elems = 0;
+        for (int32_t i = base; i < base + n; ++i) {
+            const int64_t di = pool->d_in[probs[i].proj], dq = pool->d_out[probs[i].proj];
+            prm.row_elems += (unsigned long long)(di + 2 * dq);
+            prm.page_elems += (unsigned long long)(di + dq);
+        }
         kern<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
         st = cuda_status(cudaGetLastError());
         if (st != LORA_OK) return st;
@@ -450,9 +458,14 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     if (st != LORA_OK) return st;
     const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW);
     if (sh.stages < 2) return LORA_ETOOBIG;
+    if (!pool->square) {
+        if (sh.rp == kRingPagesLarge)
+            return launch_fused_rp<NV, CW, kRingPagesLarge, true>(pool, probs, nprob, T, ws, di, c, sh, stream);
+        return launch_fused_rp<NV, CW, kRingPagesSmall, true>(pool, probs, nprob, T, ws, di, c, sh, stream);
+    }
     if (sh.rp == kRingPagesLarge)
-        return launch_fused_rp<NV, CW, kRingPagesLarge>(pool, probs, nprob, T, ws, di, c, sh, stream);
-    return launch_fused_rp<NV, CW, kRingPagesSmall>(pool, probs, nprob, T, ws, di, c, sh, stream);
+        return launch_fused_rp<NV, CW, kRingPagesLarge, false>(pool, probs, nprob, T, ws, di, c, sh, stream);
+    return launch_fused_rp<NV, CW, kRingPagesSmall, false>(pool, probs, nprob, T, ws, di, c, sh, stream);
 }
 
 lora_status check_problems(const lora_pool* pool, const lora_problem* probs, int32_t nprob) {
@@ -540,7 +553,7 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     const int h8 = pool->d.h / 8;
     if (!with_mma && t_out == nullptr && split_fits(pool->d, nprob, T, ws_bytes))
         return run_split(pool, probs, nprob, ws, stream);
-    if (with_mma && mma_min_rows(pool) > 0 && pool->square && t_out == nullptr && h8 <= 640 && T > 0) {
+    if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
         // one launch per batch of projections for both work classes
         if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
         if (h8 <= 512) return launch_fused<2, 8>(pool, probs, nprob, T, ws, stream);

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     __shared__ int scan_smem[33];
     __shared__ long long key_tile[kKeyTile];
     __shared__ int n_adapted_s;
-    __shared__ unsigned long long weight_s[2];
+    __shared__ unsigned long long weight_s[4];   // rows[2], page_rows[2] of the header
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     const int n = p.S + p.Td;
     if (tid == 0) {
         n_adapted_s = 0;
-        weight_s[0] = weight_s[1] = 0;
+        weight_s[0] = weight_s[1] = weight_s[2] = weight_s[3] = 0;
     }
     __syncthreads();
     const int dec_base = p.S > 0 ? p.seg_start[p.S] : 0;
@@ -192,8 +192,10 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
                 gfirst[e_g] = q;
             }
             const int r = P.ranks[a];
-            if (ntile > 0)   // x read + y read and write, plus the pages once per tile
-                atomicAdd(&weight_s[1], (unsigned long long)P.h * 2 * (3ull * len + 2ull * r * ntile));
+            if (ntile > 0) {   // x read + y read and write, plus the pages once per tile
+                atomicAdd(&weight_s[1], (unsigned long long)len);
+                atomicAdd(&weight_s[3], (unsigned long long)r * ntile);
+            }
             for (int k = 0; k < ntile; ++k) {
                 Tile tl;
                 tl.adapter = a;
@@ -271,8 +273,10 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
             const int r = P.ranks[a];
             const float sc = P.scales[a];
             const long long ptb = P.pt_off[a];
-            if (nch > 0)     // rows read and written, plus the pages once per chunk
-                atomicAdd(&weight_s[0], (unsigned long long)P.h * 2 * (3ull * cnt + 2ull * r * nch));
+            if (nch > 0) {   // rows read and written, plus the pages once per chunk
+                atomicAdd(&weight_s[0], (unsigned long long)cnt);
+                atomicAdd(&weight_s[2], (unsigned long long)r * nch);
+            }
             for (int c = 0; c < nch; ++c) {
                 Chunk ch;
                 ch.adapter = a;
@@ -301,8 +305,10 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
     }
     __syncthreads();
     if (tid == 0) {
-        hdr->weight[0] = weight_s[0];
-        hdr->weight[1] = weight_s[1];
+        hdr->rows[0] = weight_s[0];
+        hdr->rows[1] = weight_s[1];
+        hdr->page_rows[0] = weight_s[2];
+        hdr->page_rows[1] = weight_s[3];
     }
 }
 

@@ -114,6 +114,9 @@ struct MmaItem {
 // time, and each x tile comes from DRAM once and from L2 for the others.  Across groups,
 // and for a projection alone in its group, items are projection-major, so consecutive
 // tiles of one segment (which read the same adapter pages) run side by side.
+// W: the launch has projections whose widths differ from h; W = false compiles the h x h
+// case (one page block per vector, h / 64 chunks and h / 128 slices per item).
+template <bool W>
 __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tiles, int n_tiles, uint32_t item,
                                             int lane) {
     MmaItem it;
@@ -125,11 +128,11 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
     const int r = it.tile.rank;
     it.rp = mma_rpad(r);
     it.blk = p.pool.pt_off[it.tile.adapter] + (long long)p.blk[it.pr] * r;
-    it.n_kc = p.n_kc[it.pr];
-    it.n_nt = p.n_nt[it.pr];
-    it.pv_in = p.pv_in[it.pr];
+    it.n_kc = W ? p.n_kc[it.pr] : p.pool.h / kMmaKChunk;
+    it.n_nt = W ? p.n_nt[it.pr] : p.pool.h / kMmaNTile;
+    it.pv_in = W ? p.pv_in[it.pr] : 1;
     bool bad = false;
-    const int n_ent = (it.pv_in + p.pv_out[it.pr]) * r;   // every page of the item
+    const int n_ent = W ? (it.pv_in + p.pv_out[it.pr]) * r : 2 * r;   // every page of the item
     for (int e = lane; e < n_ent; e += 32) {
         const int page = p.pool.pt[it.blk + e];
         bad |= (page < 0 || page >= p.pool.num_pages);
@@ -139,11 +142,12 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
 }
 
 // The next processable item at or after `item` (skipping items with bad pages), or total.
+template <bool W>
 __device__ __forceinline__ uint32_t mma_next_ok(const MmaParams& p, const Tile* tiles, int n_tiles,
                                                 uint32_t item, uint32_t total, uint32_t ncta, int lane,
                                                 MmaItem& mi) {
     for (; item < total; item += ncta) {
-        mi = mma_item(p, tiles, n_tiles, item, lane);
+        mi = mma_item<W>(p, tiles, n_tiles, item, lane);
         if (mi.ok) return item;
     }
     return total;
@@ -160,6 +164,7 @@ __device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t st, uin
 }
 
 // One CTA of the tensor-core kernel: CTA `cta` of `ncta` taking part (all kMmaThreads threads).
+template <bool W>
 __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_raw, uint32_t cta, uint32_t ncta) {
     // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
     unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -215,7 +220,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         if (lane == 0) prefetch_tmap(&p.pool_map);
         uint32_t it = 0;
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) {
                 if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
                 continue;
@@ -225,15 +230,15 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             const void* xmap = &p.x_map[mi.pr];
             int pga[4];
             for (int kc = 0; kc < mi.n_kc; ++kc) {
-                if (kc % kc_pg == 0) {   // page ids of the A rows' page block kc / kc_pg
-                    const long long b0 = mi.blk + (long long)(kc / kc_pg) * r;
+                if (W ? kc % kc_pg == 0 : kc == 0) {   // page ids of the A rows' page block kc / kc_pg
+                    const long long b0 = mi.blk + (W ? (long long)(kc / kc_pg) * r : 0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int j = lane + 32 * q;
                         pga[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
                     }
                 }
-                const int kcol = (kc % kc_pg) * kMmaKChunk;   // column within the A page
+                const int kcol = (W ? kc % kc_pg : kc) * kMmaKChunk;   // column within the A page
                 const uint32_t s = it % S1;
                 if (!mbar_wait(bar(L.empty1 + s * 8), ((it / S1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
                 const uint32_t st = bar(L.ring1 + s * p.s1_bytes);
@@ -274,20 +279,20 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         // ------------------------------------------------------------------ B^T producer
         uint32_t it2 = 0;
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
             const int r = mi.tile.rank, rp = mi.rp;
             int pgb[4];
             for (int nt = 0; nt < mi.n_nt; ++nt, ++it2) {
-                if (nt % nt_pg == 0) {   // page ids of the B columns' page block nt / nt_pg
-                    const long long b0 = mi.blk + (long long)(mi.pv_in + nt / nt_pg) * r;
+                if (W ? nt % nt_pg == 0 : nt == 0) {   // page ids of the B columns' page block nt / nt_pg
+                    const long long b0 = mi.blk + (W ? (long long)(mi.pv_in + nt / nt_pg) * r : (long long)r);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int j = lane + 32 * q;
                         pgb[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
                     }
                 }
-                const int ncol = (nt % nt_pg) * kMmaNTile;   // column within the B page
+                const int ncol = (W ? nt % nt_pg : nt) * kMmaNTile;   // column within the B page
                 // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
                 // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
                 const uint32_t s = it2 % S2;
@@ -326,7 +331,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         // ------------------------------------------------------------------ y producer
         uint32_t it3 = 0;
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
             const int row0 = mi.tile.row0;
             const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
@@ -354,7 +359,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         // ------------------------------------------------------------------ MMA issuer
         uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0;
         MmaItem cur, nxt;
-        uint32_t item = mma_next_ok(p, tiles, n_tiles, cta, total, ncta, lane, cur);
+        uint32_t item = mma_next_ok<W>(p, tiles, n_tiles, cta, total, ncta, lane, cur);
         int kc_next = 0;   // shrink chunks of `nxt` already issued
         // shrink of the first tile
         if (item < total) {
@@ -373,7 +378,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             __syncwarp();
         }
         while (item < total && ok) {
-            const uint32_t next_item = mma_next_ok(p, tiles, n_tiles, item + ncta, total, ncta, lane, nxt);
+            const uint32_t next_item = mma_next_ok<W>(p, tiles, n_tiles, item + ncta, total, ncta, lane, nxt);
             const bool has_next = next_item < total;
             const uint32_t id_next = has_next ? idesc_bf16(128, nxt.rp, 0, 0) : 0;
             kc_next = 0;
@@ -451,7 +456,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         uint32_t tcount = 0, g = 0;
         bool stored = false;
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
             const int rp = mi.rp, rows = mi.tile.rows, row0 = mi.tile.row0;
             const float scale = p.pool.scales[mi.tile.adapter];
@@ -551,9 +556,10 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool W>
 __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
-    mma_cta(p, mma_smem_raw, blockIdx.x, gridDim.x);
+    mma_cta<W>(p, mma_smem_raw, blockIdx.x, gridDim.x);
 }
 
 }  // namespace lora
