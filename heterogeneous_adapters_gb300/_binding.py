@@ -22,7 +22,7 @@ LORA_NOALLOC_MAX_TOKENS = 4096
 
 EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_workspace_size", "lora_workspace_init",
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
-            "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t",
+            "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t", "lora_debug_wait_limit",
             "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error",
             "lora_last_cuda_error", "lora_status_string",
             # host runtime (include/lora_runtime.h)
@@ -85,6 +85,7 @@ def lib():
             "lora_delta_grouped": [p, p, i32, i32, i32, p, sz, p],
             "lora_debug_page_list": [p, p, sz, i32, i32, p, i64, p, p],
             "lora_debug_delta_with_t": [p, ctypes.POINTER(lora_problem), p, sz, p, p],
+            "lora_debug_wait_limit": [p, sz, ctypes.c_uint64, p, p],
             "lora_stage_pages": [p, p, p, i32, p, p, p, i64, p],
             "lora_bgmv_noalloc": [p, p, i32, p, i32, p, p],
             "lora_get_device_error": [p, p, ctypes.POINTER(ctypes.c_uint32)],
@@ -230,6 +231,12 @@ def debug_delta_with_t(pool, problem, ws, ws_bytes, t_out, stream):
     arr, _ = problems_array([problem])
     _check(lib().lora_debug_delta_with_t(pool.handle, arr, _ptr(ws), ws_bytes, _ptr(t_out), stream),
            "lora_debug_delta_with_t")
+
+
+def debug_wait_limit(ws, ws_bytes, limit_ns, elapsed_ns, stream):
+    """elapsed_ns: device uint64 (int64 tensor of one element) or None."""
+    _check(lib().lora_debug_wait_limit(_ptr(ws), ws_bytes, limit_ns, _ptr(elapsed_ns), stream),
+           "lora_debug_wait_limit")
 
 
 def stage_pages(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_page, nupd, stream):

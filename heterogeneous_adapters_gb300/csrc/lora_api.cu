@@ -816,6 +816,32 @@ lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* p
     return run_delta(pool, prob, 1, 0, ws, ws_bytes, t_out, false, (cudaStream_t)stream);
 }
 
+namespace {
+// One thread waits, bounded, on a barrier nothing arrives at (the wait kernels use).
+__global__ void wait_limit_kernel(char* ws, uint64_t limit_ns, uint64_t* elapsed) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    const uint64_t t0 = global_timer_ns();
+    const bool done = mbar_wait(b, 0, limit_ns);
+    const uint64_t t1 = global_timer_ns();
+    if (!done) set_error(&reinterpret_cast<WsHeader*>(ws)->err, LORA_DERR_TIMEOUT);
+    if (elapsed != nullptr) *elapsed = t1 - t0;
+}
+}  // namespace
+
+lora_status lora_debug_wait_limit(void* ws, size_t ws_bytes, uint64_t limit_ns, uint64_t* elapsed_ns_dev,
+                                  void* stream) {
+    if (limit_ns < 1000000ull) return LORA_EINVAL;
+    if (limit_ns > 2000000000ull) return LORA_ETOOBIG;
+    lora_status st = check_ws(ws, ws_bytes, sizeof(WsHeader));
+    if (st != LORA_OK) return st;
+    wait_limit_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(reinterpret_cast<char*>(ws), limit_ns, elapsed_ns_dev);
+    return cuda_status(cudaGetLastError());
+}
+
 lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const int32_t* dst_pages,
                              int32_t npages, int32_t* page_table, const int64_t* upd_index,
                              const int32_t* upd_page, int64_t nupd, void* stream) {

@@ -222,6 +222,14 @@ lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_byte
 lora_status lora_debug_delta_with_t(const lora_pool* pool, const lora_problem* prob, void* ws,
                                     size_t ws_bytes, float* t_out, void* stream);
 
+/* Self-test of the bounded device waits every kernel uses: one thread waits on a
+ * shared-memory barrier that nothing completes, gives up after limit_ns nanoseconds
+ * (1 ms .. 2 s, else LORA_ETOOBIG / LORA_EINVAL) and sets LORA_DERR_TIMEOUT in the
+ * workspace's error word, exactly as a kernel whose wait ran out would; the context
+ * stays usable.  elapsed_ns_dev (device uint64, may be NULL) receives the time waited. */
+lora_status lora_debug_wait_limit(void* ws, size_t ws_bytes, uint64_t limit_ns, uint64_t* elapsed_ns_dev,
+                                  void* stream);
+
 /* Adapter staging from host memory (side-stream prefetch).
  * "S-LoRA: Serving Thousands of Concurrent LoRA Adapters", "Host memory for adapters":
  * adapters live in host memory and the ones a batch needs are copied to the GPU ahead

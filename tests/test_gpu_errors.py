@@ -148,3 +148,26 @@ def test_host_side_checks():
         assert case.error_bits() == 0
     finally:
         case.close()
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """The bounded device wait every kernel uses: a barrier nothing completes, a 5 ms limit;
+    the timeout bit comes back through the error word, the wait took about the limit, and
+    the context stays usable (a correct launch right after)."""
+    import torch
+    wl = _wl()
+    case = GpuCase(wl)
+    try:
+        el = torch.zeros(1, dtype=torch.int64, device=case.device)
+        lora.debug_wait_limit(case.ws, case.ws_bytes, 5_000_000, el, case.stream)
+        assert case.error_bits() == 0x20
+        waited = int(el.item())
+        assert 5_000_000 <= waited < 1_000_000_000, waited
+        with pytest.raises(lora.LoraError):
+            lora.debug_wait_limit(case.ws, case.ws_bytes, 3_000_000_000, None, case.stream)
+        with pytest.raises(lora.LoraError):
+            lora.debug_wait_limit(case.ws, case.ws_bytes, 10, None, case.stream)
+        assert case.run() == 0
+        full_check(wl, case, [0, 1])
+    finally:
+        case.close()
