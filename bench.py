@@ -97,11 +97,15 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the source files a kernel is built from (traffic figures taken on other
-    sources are not reused)."""
+    """Hash of the code of the source files a kernel is built from, comments and
+    whitespace removed (traffic figures taken on other code are not reused)."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(ROOT, "heterogeneous_adapters_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "heterogeneous_adapters_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -7,7 +7,10 @@
 // gathered from non-contiguous pages, mixed ranks without padding.
 //
 // Decode is HBM-bound: the work is streaming each distinct adapter's 2 r pages once
-// per projection.  One persistent CTA per SM:
+// per projection (r (ceil(d_in/h) + ceil(d_out/h)) for projections of other widths,
+// whose vectors span several pages: the item then streams, per input page block, the
+// x rows' block and that page of the A rows, and per output page block that page of the
+// B columns).  One persistent CTA per SM:
 //   warp 0 (producer)  takes work items (chunk of <= 4 rows of one adapter, projection)
 //                      in a static rank-sorted round-robin order, validates the item's page ids, and streams
 //                      into a ring of shared-memory stages with 1-D bulk copies

@@ -6,14 +6,16 @@
 // segment.  "S-LoRA: Serving Thousands of Concurrent LoRA Adapters": the prefill kernel
 // gathers the adapter from non-contiguous pages with mixed ranks.
 //
-// Per item (tile of <= 128 rows of one segment, adapter a of rank r <= 128, projection):
-//   shrink  D1[128 x r16] (TMEM, fp32) = X[128 x h] . A^T, K-loop over h in chunks of 64:
-//           X chunk by TMA (128-byte swizzle), the r A-row pages' chunks by TMA (one
-//           64-element row per request, rows r..r16-1 read out of range = zeros);
+// Per item (tile of <= 128 rows of one segment, adapter a of rank r <= 128, projection of
+// widths d_in x d_out; h x h in most models):
+//   shrink  D1[128 x r16] (TMEM, fp32) = X[128 x d_in] . A^T, K-loop over d_in in chunks of
+//           64: X chunk by TMA (128-byte swizzle), the r A-row pages' chunks by TMA (four
+//           rows per gather request, rows r..r16-1 read out of range = zeros); an A row
+//           longer than a page continues on its next page block (chunk kc on page kc / (h/64));
 //   convert the epilogue warps read D1, scale by s and split each fp32 value exactly into
 //           a bf16 pair t = hi + lo (|t - hi - lo| <= 2^-16 |t|), written back to TMEM
 //           as two K-major A operands;
-//   expand  for every 128-column slice of y: D2[128 x 128] = T_hi . B^T + T_lo . B^T with
+//   expand  for every 128-column slice of y's d_out: D2[128 x 128] = T_hi . B^T + T_lo . B^T with
 //           the B-column pages' slices as an MN-major operand (TMA, 128-byte swizzle),
 //           double-buffered in TMEM so the epilogue of one slice overlaps the MMA of the
 //           next; the epilogue adds D2 to y (fp32) and stores bf16 rows of the tile.
