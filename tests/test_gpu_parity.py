@@ -62,6 +62,9 @@ SMALL = {
                                                      [129, 257, 31, 32, 500, 128, 7, 64]),
     "mixed-h2048": lambda: _mixed(47, 2048, 2, 2, 30, [8, 16, 32, 64, 128], [5, 260, 131], 40, 5),
     "mixed-h5120": lambda: _mixed(48, 5120, 1, 2, 12, [8, 128], [300, 9], 17, 3),
+    # more projections than one launch takes (256 for the CUDA-core kernel, 64 for tiles)
+    "decode-320-projections": lambda: small_decode(67, 256, 80, 4, 9, [2, 8, 16], 21),
+    "mixed-320-projections": lambda: _mixed(68, 256, 80, 4, 9, [4, 16], [70, 2, 40], 11, 2),
 }
 
 
@@ -280,13 +283,17 @@ def _sample(n, k, seed):
     return sorted(rng.choice(n, size=min(k, n), replace=False).tolist())
 
 
-@pytest.mark.parametrize("cfg,k", [(1, 8), (2, 2), (3, 2), ("4d", 4), ("4z", 4)])
+@pytest.mark.parametrize("cfg,k", [(1, 8), (2, 2), (3, 2), ("4d", 4), ("4z", 4), ("8b", 7), ("8bp", 3)])
 def test_full_config(cfg, k):
     import torch
     if cfg == "4d":
         wl = spec.config4("distinct")
     elif cfg == "4z":
         wl = spec.config4("zipf")
+    elif cfg == "8b":
+        wl = spec.llama3_8b_decode()
+    elif cfg == "8bp":
+        wl = spec.llama3_8b_prefill()
     else:
         wl = spec.CONFIGS[cfg]()
     case = GpuCase(wl, nan_dummies=True)
