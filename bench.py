@@ -35,36 +35,30 @@ UNIT = "tokens/s"
 
 # ----------------------------------------------------------------------------- helpers
 
-def workload_for(cfg: str):
-    """Configs 0-4 as named in the workload module; "1s" (4 layers, 300 adapters, ~2.4 GB
-    pool), "2s" (2 layers x 2 projections, ~2 GB on the device) and "3s" (1 layer x 2
-    projections) are small variants of configs 1, 2 and 3 for profiler captures; "8b" is a
-    Llama-3-8B decode batch over all seven projections at their own widths ("8bs": 1 layer);
-    "8bp" a Llama-3-8B prefill batch over 4 layers ("8bps": 1 layer)."""
+def workload_for(name: str):
+    """A named workload of the workload module, or a small variant of one for profiler
+    captures: "decode-small" (4 layers, 300 adapters, ~2.4 GB pool), "prefill-small" (2
+    layers x 2 projections, ~2 GB on the device), "mixed-small" (1 layer x 2 projections),
+    "llama3-decode-small" and "llama3-prefill-small" (1 layer)."""
     from workloads import spec
-    if cfg == "1s":
+    if name == "decode-small":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
                                     300, [8, 16, 32, 64], 64, 1.0)
-    if cfg == "2s":
+    if name == "prefill-small":
         return spec.prefill_workload("llama7b-prefill-sgmv-h4096-s32-a1000-l2p2", 1002, 4096, 2, 2,
                                      1000, [8, 16, 32, 64], 32, 64, 1024, 1.0)
-    if cfg == "3s":
+    if name == "mixed-small":
         return spec.mixed_workload("13b-mixed-h5120-p8-d192-a2000-l1p2", 1003, 5120, 1, 2, 2000,
                                    [8, 16, 32, 64, 128], 8, 128, 2048, 192, 20, 0.8,
                                    pool_pages=1 << 18)
-    if cfg == "8b":
-        return spec.llama3_8b_decode()
-    if cfg == "8bs":
+    if name == "llama3-decode-small":
         return spec.llama3_8b_decode(layers=1)
-    if cfg == "8bp":
-        return spec.llama3_8b_prefill()
-    if cfg == "8bps":
+    if name == "llama3-prefill-small":
         return spec.llama3_8b_prefill(layers=1)
-    if cfg == "4d":
-        return spec.config4("distinct")
-    if cfg == "4z":
-        return spec.config4("zipf")
-    return spec.CONFIGS[int(cfg)]()
+    if name not in spec.WORKLOADS:
+        raise SystemExit(f"unknown workload {name!r}; choose from {sorted(spec.WORKLOADS)} or a "
+                         "-small variant")
+    return spec.WORKLOADS[name]()
 
 
 def cpu_model() -> str:
@@ -559,8 +553,8 @@ def run_ours(args, rank: int, world: int, local: int):
                   f"three device slots, copies of neighbouring steps overlapping the call"}
 
     staging = None
-    if args.config in ("4d", "4z") and args.stage_steps > 0:
-        variant = "distinct" if args.config == "4d" else "zipf"
+    if args.config in ("stress-distinct", "stress-zipf") and args.stage_steps > 0:
+        variant = args.config.split("-")[1]
         wl_steps = step_batches(wl, args.stage_steps, variant)
         staging = run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev)
 
@@ -596,7 +590,7 @@ def run_ours(args, rank: int, world: int, local: int):
 # ----------------------------------------------------------------------------- distinct-adapter sweep
 
 def run_sweep_distinct(args, local: int):
-    """Config 1's pool and projections; the 64 decode tokens spread round-robin over D
+    """The Llama-7B decode workload's pool and projections; the 64 decode tokens spread round-robin over D
     adapters drawn without replacement from the 2,000 (seed 7000 + D), D = 1, 2, 4, ..., 64.
     One JSON line per D: step time of the delta launch (CUDA events, K steps after W warm-up),
     adapted tokens/s and the fraction of the measured HBM peak."""
@@ -607,7 +601,7 @@ def run_sweep_distinct(args, local: int):
 
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    wl = workload_for("1")
+    wl = workload_for("decode")
     d = device_inputs(wl, device=dev, nan_dummies=False)
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
@@ -841,7 +835,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="1")
+    ap.add_argument("--config", default="decode",
+                    help="workload: tiny, decode, prefill, mixed, stress-distinct, stress-zipf, "
+                         "llama3-decode, llama3-prefill, or a -small variant")
     ap.add_argument("--graph-replays", type=int, default=50,
                     help="timed replays of the CUDA graph of one step")
     ap.add_argument("--e2e-slots", type=int, default=3, choices=[1, 2, 3, 4],
@@ -856,12 +852,12 @@ def main():
     ap.add_argument("--stage-capacity", type=int, default=1500,
                     help="resident adapter slices in the unified-pool stress workload")
     ap.add_argument("--stage-steps", type=int, default=20,
-                    help="steps of the staging scenario (configs 4d / 4z)")
+                    help="steps of the staging scenario (stress-distinct / stress-zipf)")
     ap.add_argument("--shared-x", action="store_true",
                     help="q, k and v of a layer read one x (as in a transformer), not one each")
     ap.add_argument("--sweep-distinct", action="store_true",
                     help="instead of the bench line: decode tokens/s against the number of "
-                         "distinct adapters in the batch (1..64) at config 1's shape")
+                         "distinct adapters in the batch (1..64) at the Llama-7B decode shape")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -34,7 +34,7 @@ def test_width_bytes_equal_the_arrays_a_step_reads_and_writes():
 
 
 def test_square_dims_match_the_h_by_h_model_and_adapter_size():
-    wl = spec.config0()
+    wl = spec.tiny_decode()
     p = wl.pool
     ids = wl.batch.token_adapter()
     a = costmodel.decode_step_bytes(p.ranks, ids, p.h, 3)

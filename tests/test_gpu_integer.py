@@ -37,7 +37,7 @@ def _segment(case):
 
 
 CASES = {
-    "config0": spec.config0,
+    "tiny": spec.tiny_decode,
     "decode-zipf": lambda: small_decode(61, 256, 1, 1, 50, [4], 300),
     "decode-base": lambda: small_decode(62, 256, 1, 1, 7, [4], 500, base=True),
     "decode-large": lambda: small_decode(63, 256, 1, 1, 3000, [4], 5000),
@@ -73,7 +73,7 @@ def _widths_decode():
     return spec.Workload("decode-widths", 67, pool, batch, spec.all_problems(2, 3))
 
 
-@pytest.mark.parametrize("name", ["config0", "decode-zipf", "mixed", "decode-widths"])
+@pytest.mark.parametrize("name", ["tiny", "decode-zipf", "mixed", "decode-widths"])
 def test_page_list_bit_exact(name):
     import torch
     wl = _widths_decode() if name == "decode-widths" else CASES[name]()
@@ -97,13 +97,13 @@ def test_page_list_bit_exact(name):
         case.close()
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, "4d"])
-def test_grouping_full_configs(cfg):
+@pytest.mark.parametrize("cfg", ["decode", "prefill", "mixed", "stress-distinct"])
+def test_grouping_full_workloads(cfg):
     """Grouping of the full-size batches (metadata only; a 1-page dummy pool suffices)."""
     import torch
 
     import heterogeneous_adapters_gb300 as lora
-    wl = spec.config4("distinct") if cfg == "4d" else spec.CONFIGS[cfg]()
+    wl = spec.WORKLOADS[cfg]()
     dev = "cuda:0"
     b = wl.batch
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)  # noqa: E731

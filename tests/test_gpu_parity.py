@@ -45,7 +45,7 @@ def _mixed(seed, h, L, P, N, ranks, lens, n_dec, n_base):
 
 
 SMALL = {
-    "config0": spec.config0,
+    "tiny": spec.tiny_decode,
     "decode-h512-ragged-ranks": lambda: small_decode(41, 512, 2, 4, 20, [1, 3, 8, 16, 64], 37),
     "decode-h5120": lambda: small_decode(43, 5120, 1, 2, 10, [8, 128], 20),
     "decode-h4096-r256": lambda: small_decode(44, 4096, 1, 1, 3, [256], 9),
@@ -276,26 +276,18 @@ def test_empty_and_all_base_batches():
         case.close()
 
 
-# ----------------------------------------------------------------------------- full-size configs
+# ----------------------------------------------------------------------------- full-size workloads
 
 def _sample(n, k, seed):
     rng = np.random.default_rng(seed)
     return sorted(rng.choice(n, size=min(k, n), replace=False).tolist())
 
 
-@pytest.mark.parametrize("cfg,k", [(1, 8), (2, 2), (3, 2), ("4d", 4), ("4z", 4), ("8b", 7), ("8bp", 3)])
-def test_full_config(cfg, k):
+@pytest.mark.parametrize("cfg,k", [("decode", 8), ("prefill", 2), ("mixed", 2), ("stress-distinct", 4),
+                                   ("stress-zipf", 4), ("llama3-decode", 7), ("llama3-prefill", 3)])
+def test_full_workload(cfg, k):
     import torch
-    if cfg == "4d":
-        wl = spec.config4("distinct")
-    elif cfg == "4z":
-        wl = spec.config4("zipf")
-    elif cfg == "8b":
-        wl = spec.llama3_8b_decode()
-    elif cfg == "8bp":
-        wl = spec.llama3_8b_prefill()
-    else:
-        wl = spec.CONFIGS[cfg]()
+    wl = spec.WORKLOADS[cfg]()
     case = GpuCase(wl, nan_dummies=True)
     try:
         assert case.run() == 0

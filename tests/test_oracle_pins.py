@@ -56,7 +56,7 @@ def small_multi(seed=7, h=64, L=2, P=3, N=5, T=24):
 
 # ----------------------------------------------------------------------------- formula pins
 
-@pytest.mark.parametrize("make", [spec.config0, small_multi])
+@pytest.mark.parametrize("make", [spec.tiny_decode, small_multi])
 def test_merge_identity(make):
     """x (W + s B A)^T == x W^T + s (x A^T) B^T (pofe.ai page, "The bottleneck": the merged
     weight W' = W + gamma B A; fdeinterviews S-LoRA page: the update to W is a low-rank
@@ -292,7 +292,7 @@ def test_batch_order_invariance():
 
 
 def test_oracle_rejects_bad_inputs():
-    wl = spec.config0()
+    wl = spec.tiny_decode()
     hi = host_inputs(wl)
     ids = wl.batch.token_adapter().copy()
     ids[0] = wl.pool.num_adapters

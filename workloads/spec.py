@@ -333,9 +333,9 @@ def mixed_workload(name: str, seed: int, h: int, L: int, P: int, num_adapters: i
     return Workload(name, seed, pool, batch, all_problems(L, P), notes)
 
 
-# ----------------------------------------------------------------------------- the five configs
+# ----------------------------------------------------------------------------- named workloads
 
-def config0() -> Workload:
+def tiny_decode() -> Workload:
     """Tiny check: h=256, 1 layer x 1 projection, ranks {4,8,8,16}, 16 tokens with
     ids uniform in {-1..3}, 256-page pool with the 72 adapter pages shuffled in."""
     rng = np.random.default_rng(1000)
@@ -346,23 +346,32 @@ def config0() -> Workload:
     return Workload("tiny-h256-r4-16-t16", 1000, pool, batch, [(0, 0)])
 
 
-def config1() -> Workload:
+def llama7b_decode() -> Workload:
+    """Llama-7B decode: 64 one-token requests, Zipf(1.0) over 2,000 adapters of ranks
+    {8..64}, 32 layers x q/k/v/o, every adapter resident."""
     return decode_workload("llama7b-decode-bgmv-h4096-t64-a2000", 1001, 4096, 32, 4, 2000,
                            [8, 16, 32, 64], 64, 1.0)
 
 
-def config2() -> Workload:
+def llama7b_prefill() -> Workload:
+    """Llama-7B prefill: 32 prompts of lengths uniform in [64, 1024], Zipf(1.0) over 1,000
+    adapters of ranks {8..64}, 32 layers x q/k/v/o."""
     return prefill_workload("llama7b-prefill-sgmv-h4096-s32-a1000", 1002, 4096, 32, 4, 1000,
                             [8, 16, 32, 64], 32, 64, 1024, 1.0)
 
 
-def config3() -> Workload:
+def mixed_13b() -> Workload:
+    """13B continuous-batching step: 8 prefill prompts of [128, 2048] tokens and 192 decode
+    tokens, 20 of the 200 requests base-only, Zipf(0.8) over 2,000 adapters of ranks
+    {8..128}, 40 layers x q/k/v/o, only the referenced adapters resident."""
     return mixed_workload("13b-mixed-h5120-p8-d192-a2000", 1003, 5120, 40, 4, 2000,
                           [8, 16, 32, 64, 128], 8, 128, 2048, 192, 20, 0.8,
                           pool_pages=1 << 22)
 
 
-def config4(variant: str = "distinct") -> Workload:
+def pool_stress(variant: str = "distinct") -> Workload:
+    """Unified-pool stress: 256 decode tokens with distinct adapters (or Zipf(1.2)) from
+    2,000, in a 2^20-page pool holding one layer's slice of each adapter."""
     assert variant in ("distinct", "zipf")
     return decode_workload(f"unified-pool-stress-{variant}-h4096-t256-a2000",
                            1004 if variant == "distinct" else 1014, 4096, 32, 4, 2000,
@@ -403,7 +412,16 @@ def llama3_8b_prefill(layers: int = 4) -> Workload:
                     all_problems(layers, P))
 
 
-CONFIGS = {0: config0, 1: config1, 2: config2, 3: config3, 4: config4}
+WORKLOADS = {
+    "tiny": tiny_decode,
+    "decode": llama7b_decode,
+    "prefill": llama7b_prefill,
+    "mixed": mixed_13b,
+    "stress-distinct": lambda: pool_stress("distinct"),
+    "stress-zipf": lambda: pool_stress("zipf"),
+    "llama3-decode": llama3_8b_decode,
+    "llama3-prefill": llama3_8b_prefill,
+}
 
 
 def shrink_problems(wl: Workload, problems: list) -> Workload:
