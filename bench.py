@@ -83,10 +83,9 @@ def measured_peaks() -> dict:
 
 
 KERNEL_SOURCES = {
-    "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh", "segment.cuh"],
-    "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh", "segment.cuh"],
-    "delta_fused_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh",
-                           "segment.cuh"],
+    "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh"],
+    "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
+    "delta_fused_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
 }
 
 

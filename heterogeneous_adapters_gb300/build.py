@@ -1,4 +1,5 @@
-"""Compile liblora.so in-tree for sm_103a (nvcc, no cmake)."""
+"""Compile liblora.so in-tree for sm_103a (nvcc, no cmake): one object per translation
+unit, compiled in parallel, then one link."""
 from __future__ import annotations
 
 import glob
@@ -9,8 +10,11 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SO = os.path.join(PKG, "liblora.so")
-MAIN = os.path.join(PKG, "csrc", "lora_api.cu")
-RUNTIME = os.path.join(PKG, "csrc", "runtime.cpp")   # host-only: adapter cache, scheduler
+OBJ_DIR = os.path.join(PKG, "_build")
+# the C ABI, the launch code of each kernel family, and the host runtime (adapter cache,
+# scheduler; host-only C++)
+SOURCES = [os.path.join(PKG, "csrc", f) for f in
+           ("lora_api.cu", "launch_ring.cu", "launch_tile.cu", "launch_split.cu", "runtime.cpp")]
 
 
 def nvcc() -> str:
@@ -20,10 +24,21 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def build_cmd(extra=()) -> list[str]:
-    return [nvcc(), "-O3", "-shared", "-Xcompiler", "-fPIC", "-std=c++17",
-            "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-            "-I", os.path.join(ROOT, "include"), *extra, "-o", SO, MAIN, RUNTIME]
+def _obj(src: str) -> str:
+    return os.path.join(OBJ_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+
+
+def compile_cmds(extra=()) -> list[list[str]]:
+    """One nvcc -c per translation unit (independent: run them in parallel)."""
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    return [[nvcc(), "-O3", "-Xcompiler", "-fPIC", "-std=c++17",
+             "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
+             "-I", os.path.join(ROOT, "include"), *extra, "-c", "-o", _obj(s), s] for s in SOURCES]
+
+
+def link_cmd() -> list[str]:
+    return [nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", SO,
+            *[_obj(s) for s in SOURCES]]
 
 
 def sources() -> list[str]:
@@ -38,7 +53,15 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(s) <= t for s in sources())
 
 
+def run_parallel(cmds: list[list[str]]) -> None:
+    procs = [subprocess.Popen(c) for c in cmds]
+    bad = [c for c, p in zip(cmds, procs) if p.wait() != 0]
+    if bad:
+        raise RuntimeError(f"build failed: {bad}")
+
+
 def build(force: bool = False) -> str:
     if force or not up_to_date():
-        subprocess.check_call(build_cmd())
+        run_parallel(compile_cmds())
+        subprocess.check_call(link_cmd())
     return SO

@@ -29,14 +29,12 @@
 #pragma once
 #include "common.cuh"
 #include "ptx.cuh"
-#include "segment.cuh"
 
 namespace lora {
 
 constexpr int kRingMaxConsumerWarps = 16;
 constexpr int kRingPagesSmall = 4;   // pages (or x rows) per stage: the two choices
 constexpr int kRingPagesLarge = 8;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint32_t kDerrTimeout = LORA_DERR_TIMEOUT;
 
 enum StageKind : int32_t { kStageX = 0, kStageA = 1, kStageB = 2, kStageStop = 3, kStageSkip = 4 };

@@ -20,7 +20,6 @@
 // are) and reported in the device error word.
 #pragma once
 #include "common.cuh"
-#include "segment.cuh"
 
 namespace lora {
 

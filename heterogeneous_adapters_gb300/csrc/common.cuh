@@ -9,6 +9,9 @@
 namespace lora {
 
 constexpr int kWarp = 32;
+constexpr int kChunk = 4;        // rows per CUDA-core work item
+constexpr int kTileRows = 128;   // rows per tensor-core tile
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 
 // ---------------------------------------------------------------------------- workspace
 // The workspace header lives at offset 0 of the caller's workspace.

@@ -1,0 +1,73 @@
+// Host-side launch plumbing shared by the translation units of liblora.so: the pool's
+// host record, device facts, kernel-parameter helpers, and the launch entry points of each
+// kernel family (launch_ring.cu: the CUDA-core ring kernel; launch_tile.cu: the
+// tensor-core tile kernel and the fused launch; launch_split.cu: the two-phase split
+// kernels).  The C ABI itself lives in lora_api.cu.
+#pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "common.cuh"
+#include "lora.h"
+
+struct lora_pool {
+    lora_pool_desc d;                 // proj_dims is not kept (a host array of the caller)
+    std::vector<int32_t> d_in, d_out; // widths of each projection
+    std::vector<int32_t> pre;         // units before each projection in a layer
+    int32_t units = 0;                // units of one layer
+    bool square = true;               // every projection h x h
+    bool mma_widths = true;           // every d_in % 64 == 0 and d_out % 128 == 0 (tile shapes)
+};
+
+namespace lora {
+namespace host {
+
+extern thread_local int g_last_cuda_error;
+lora_status cuda_status(cudaError_t e);
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Kernel views of the pool and of one problem.
+PoolView view_of(const lora_pool* pool);
+ProbDesc prob_desc(const lora_pool* pool, const lora_problem& pr);
+
+// Per-device launch facts, looked up once per device.
+struct DeviceInfo {
+    int sm_count = 0;
+    int smem_optin = 0;
+    bool ready = false;
+};
+constexpr int kMaxDevices = 64;
+lora_status device_info(DeviceInfo** out);
+
+// Shape of the ring for one launch: rows per stage, depth and the shared memory it takes.
+struct RingShape {
+    int rp, stages;
+    size_t smem;
+};
+RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps);
+
+// launch_ring.cu: the CUDA-core kernel over the chunk list (t_out: debug export of t).
+lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
+                           float* t_out, cudaStream_t stream);
+
+// launch_tile.cu: the tensor-core kernel over the tile list, and the fused launch of both
+// work classes (h <= 5120).
+int mma_min_rows(const lora_pool* pool);
+lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                    cudaStream_t stream);
+lora_status run_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                      cudaStream_t stream);
+
+// launch_split.cu: the two-phase CUDA-core path for launches of few projections.
+size_t split_t_bytes(const lora_pool_desc& d, int32_t max_tokens);
+bool split_fits(const lora_pool_desc& d, int32_t nprob, int32_t T, size_t ws_bytes);
+lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
+                      cudaStream_t stream);
+
+}  // namespace host
+}  // namespace lora

@@ -1,11 +1,9 @@
 // C ABI of liblora.so (declarations and contracts in include/lora.h).
 //
-// Host side: argument checks, workspace layout, launch configuration.  All compute runs in
-// the kernels of segment.cuh, bgmv_ring.cuh, sgmv_mma.cuh, fused.cuh and stage.cuh;
-// nothing here touches adapter or activation values.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_runtime.h>
+// Host side: argument checks, workspace layout, the grouping launch and the choice of
+// delta launches (launch_ring.cu, launch_tile.cu, launch_split.cu).  All compute runs in
+// the kernels of segment.cuh, bgmv_ring.cuh, bgmv_split.cuh, sgmv_mma.cuh, fused.cuh and
+// stage.cuh; nothing here touches adapter or activation values.
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -13,28 +11,18 @@
 #include <algorithm>
 #include <mutex>
 #include <new>
-#include <vector>
 
-#include "bgmv_ring.cuh"
 #include "bgmv_split.cuh"
-#include "common.cuh"
-#include "fused.cuh"
+#include "host.h"
 #include "segment.cuh"
 #include "sgmv_mma.cuh"
 #include "stage.cuh"
 
 using namespace lora;
+using namespace lora::host;
 
-struct lora_pool {
-    lora_pool_desc d;                 // proj_dims is not kept (a host array of the caller)
-    std::vector<int32_t> d_in, d_out; // widths of each projection
-    std::vector<int32_t> pre;         // units before each projection in a layer
-    int32_t units = 0;                // units of one layer
-    bool square = true;               // every projection h x h
-    bool mma_widths = true;           // every d_in % 64 == 0 and d_out % 128 == 0 (tile shapes)
-};
-
-namespace {
+namespace lora {
+namespace host {
 
 thread_local int g_last_cuda_error = 0;
 
@@ -43,8 +31,6 @@ lora_status cuda_status(cudaError_t e) {
     g_last_cuda_error = (int)e;
     return LORA_ECUDA;
 }
-
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 PoolView view_of(const lora_pool* pool) {
     const lora_pool_desc& d = pool->d;
@@ -80,13 +66,6 @@ ProbDesc prob_desc(const lora_pool* pool, const lora_problem& pr) {
     return o;
 }
 
-// Per-device launch facts, looked up once per device.
-struct DeviceInfo {
-    int sm_count = 0;
-    int smem_optin = 0;
-    bool ready = false;
-};
-constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
@@ -109,363 +88,15 @@ lora_status device_info(DeviceInfo** out) {
     return LORA_OK;
 }
 
+}  // namespace host
+}  // namespace lora
+
+namespace {
+
 lora_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
     if (ws == nullptr || ((uintptr_t)ws & 255u) != 0) return LORA_EWORKSPACE;
     if (ws_bytes < need) return LORA_EWORKSPACE;
     return LORA_OK;
-}
-
-// Ring depth that fits the opt-in shared memory of one CTA (at most 8 stages).
-int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* smem) {
-    for (int S = 8; S >= 2; --S) {
-        const size_t need = ring_smem_layout(S, stage_bytes, r_max, cwarps).total + 1024;
-        if (need <= (size_t)smem_optin) {
-            *smem = need;
-            return S;
-        }
-    }
-    return 0;
-}
-
-// Shape of the ring for one launch: rows per stage, depth and the shared memory it takes.
-struct RingShape {
-    int rp, stages;
-    size_t smem;
-};
-
-// Rows per stage: the larger stages when three of them fit (a bulk-copy ring streams
-// closer to the HBM read rate with fewer, larger stages), else the small ones.
-// LORA_RING_PAGES = 4 or 8 forces the choice where two such stages fit.
-RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps) {
-    const char* e = getenv("LORA_RING_PAGES");
-    const int force = e != nullptr ? atoi(e) : 0;
-    RingShape fallback{0, 0, 0};
-    for (int rp : {kRingPagesLarge, kRingPagesSmall}) {
-        size_t smem = 0;
-        const int S = ring_stages(smem_optin, rp * 2 * h, r_max, cwarps, &smem);
-        if (S < 2) continue;
-        const RingShape sh{rp, S, smem};
-        if (force == rp || (force == 0 && S >= 3)) return sh;
-        if (fallback.stages == 0) fallback = sh;
-    }
-    return fallback;
-}
-
-template <int NV, int CW, int RP, bool W>
-lora_status launch_ring_rp(RingParams& prm, const DeviceInfo* di, const RingShape& sh, cudaStream_t stream) {
-    static thread_local int attr_dev = -1;
-    static thread_local size_t attr_smem = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    prm.stage_bytes = RP * 2 * prm.pool.h;
-    prm.stages = sh.stages;
-    const size_t smem = sh.smem;
-    auto kern = bgmv_ring_kernel<NV, CW, RP, W>;
-    if (attr_dev != dev || attr_smem < smem) {
-        lora_status st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (st != LORA_OK) return st;
-        attr_dev = dev;
-        attr_smem = smem;
-    }
-    kern<<<di->sm_count, CW * 32 + 32, smem, stream>>>(prm);
-    return cuda_status(cudaGetLastError());
-}
-
-template <int NV, int CW, bool W>
-lora_status launch_ring_w(RingParams& prm, cudaStream_t stream) {
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW);
-    if (sh.stages < 2) return LORA_ETOOBIG;
-    if (sh.rp == kRingPagesLarge) return launch_ring_rp<NV, CW, kRingPagesLarge, W>(prm, di, sh, stream);
-    return launch_ring_rp<NV, CW, kRingPagesSmall, W>(prm, di, sh, stream);
-}
-
-// h x h pools take the kernels compiled for one page block per vector
-template <int NV, int CW>
-lora_status launch_ring(RingParams& prm, bool square, cudaStream_t stream) {
-    return square ? launch_ring_w<NV, CW, false>(prm, stream) : launch_ring_w<NV, CW, true>(prm, stream);
-}
-
-lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                           float* t_out, cudaStream_t stream) {
-    const lora_pool_desc& d = pool->d;
-    static thread_local RingParams prm;
-    for (int32_t base = 0; base < nprob; base += LORA_MAX_PROBLEMS_PER_LAUNCH) {
-        const int32_t n = nprob - base < LORA_MAX_PROBLEMS_PER_LAUNCH ? nprob - base
-                                                                         : LORA_MAX_PROBLEMS_PER_LAUNCH;
-        memset(&prm, 0, sizeof prm);
-        prm.pool = view_of(pool);
-        prm.ws = reinterpret_cast<char*>(ws);
-        prm.t_out = t_out;
-        prm.nprob = n;
-        for (int32_t i = 0; i < n; ++i) {
-            prm.probs[i] = prob_desc(pool, probs[base + i]);
-        }
-        // consumer warps x vectors per thread cover the h / 8 16-byte vectors of a row
-        const int h8 = d.h / 8;
-        lora_status st;
-        if (h8 <= 256)
-            st = launch_ring<1, 8>(prm, pool->square, stream);
-        else if (h8 <= 512)
-            st = launch_ring<2, 8>(prm, pool->square, stream);
-        else if (h8 <= 640)
-            st = launch_ring<2, 10>(prm, pool->square, stream);
-        else if (h8 <= 768)
-            st = launch_ring<2, 12>(prm, pool->square, stream);
-        else
-            st = launch_ring<2, 16>(prm, pool->square, stream);
-        if (st != LORA_OK) return st;
-    }
-    return LORA_OK;
-}
-
-// ---------------------------------------------------------------------------- tensor-core path
-// Segments of at least this many rows (and rank <= kMmaMaxRank) take the tensor-core
-// path when h is a multiple of 128 and every projection's d_in is a multiple of 64 (the
-// shrink K chunk) and d_out one of 128 (the expand slice); LORA_MMA_MIN_ROWS overrides it
-// (0 disables).
-int mma_min_rows(const lora_pool* pool) {
-    const lora_pool_desc& d = pool->d;
-    if (d.h % kMmaNTile != 0 || !pool->mma_widths) return 0;
-    const char* e = getenv("LORA_MMA_MIN_ROWS");
-    // one-row (decode) segments always stay on the CUDA-core path
-    if (e != nullptr) return atoi(e) > 0 ? std::max(2, atoi(e)) : 0;
-    return 32;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-lora_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (g_encode == nullptr) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        lora_status st = cuda_status(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                                      cudaEnableDefault, &q));
-        if (st != LORA_OK) return st;
-        if (fn == nullptr || q != cudaDriverEntryPointSuccess) return LORA_ECUDA;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    *out = g_encode;
-    return LORA_OK;
-}
-
-// 2-D bf16 tensor map {inner, rows} with row stride `ld` elements, box {64, box_rows},
-// 128-byte swizzle, out-of-range elements read as zero.
-lora_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld,
-                     uint32_t box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    lora_status st = encode_fn(&enc);
-    if (st != LORA_OK) return st;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {ld * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        g_last_cuda_error = 10000 + (int)r;
-        return LORA_ECUDA;
-    }
-    return LORA_OK;
-}
-
-// Shared-memory plan of the tensor-core kernel for this pool.
-struct MmaConfig {
-    int rp_max, s1, s2, s3, s1_bytes, s2_bytes;
-    size_t smem;
-};
-
-lora_status mma_config(const lora_pool_desc& d, int smem_optin, MmaConfig* c) {
-    c->rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
-    c->s1_bytes = (16384 + c->rp_max * 128 + 1023) / 1024 * 1024;   // x chunk + A chunk
-    c->s2_bytes = (c->rp_max * 256 + 1023) / 1024 * 1024;           // B^T slice
-    // the deepest y ring (<= 3) that leaves the shrink ring two stages, and the rest to
-    // the shrink ring (the next tile's shrink streams under this tile's expand and must
-    // end with it); B^T ring of 2.  On the Llama-7B prefill a 3-slot y ring with a 4-stage
-    // shrink ring beat both 4 + 2 (13% slower) and 2 + 6 (18% slower).
-    c->s2 = 2;
-    const char* ys = getenv("LORA_MMA_Y_STAGES");   // tuning override: 2..4
-    const int s3_max = ys != nullptr && atoi(ys) >= 2 && atoi(ys) <= 4 ? atoi(ys) : 3;
-    for (c->s3 = s3_max; c->s3 >= 2; --c->s3) {
-        for (c->s1 = kMmaMaxStages; c->s1 >= 2; --c->s1) {
-            c->smem = mma_smem_layout(c->s1, c->s1_bytes, c->s2, c->s2_bytes, c->s3).total + 1024;
-            if (c->smem <= (size_t)smem_optin) break;
-        }
-        if (c->s1 >= 2) break;
-    }
-    return c->s1 < 2 ? LORA_ETOOBIG : LORA_OK;
-}
-
-lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, int32_t T,
-                     void* ws, const MmaConfig& c) {
-    const lora_pool_desc& d = pool->d;
-    memset(&prm, 0, sizeof prm);
-    lora_status st = make_map(&prm.pool_map, d.pages, (uint64_t)d.h, (uint64_t)d.num_pages, (uint64_t)d.h, 1);
-    if (st != LORA_OK) return st;
-    for (int32_t i = 0; i < n; ++i) {
-        const lora_problem& pr = probs[i];
-        const int32_t di = pool->d_in[pr.proj], dq = pool->d_out[pr.proj];
-        st = make_map(&prm.x_map[i], pr.x, (uint64_t)di, (uint64_t)T, (uint64_t)pr.ldx, kMmaRowBlock);
-        if (st != LORA_OK) return st;
-        st = make_map(&prm.y_map[i], pr.y, (uint64_t)dq, (uint64_t)T, (uint64_t)pr.ldy, kMmaRowBlock);
-        if (st != LORA_OK) return st;
-        st = make_map(&prm.y1_map[i], pr.y, (uint64_t)dq, (uint64_t)T, (uint64_t)pr.ldy, 1);
-        if (st != LORA_OK) return st;
-        prm.blk[i] = pr.layer * pool->units + pool->pre[pr.proj];
-        prm.n_kc[i] = (int16_t)(di / kMmaKChunk);
-        prm.n_nt[i] = (int16_t)(dq / kMmaNTile);
-        prm.pv_in[i] = (uint8_t)vec_pages(di, d.h);
-        prm.pv_out[i] = (uint8_t)vec_pages(dq, d.h);
-    }
-    // runs of consecutive problems reading the same x form the item order's groups
-    for (int32_t i = 0; i < n;) {
-        int32_t j = i + 1;
-        while (j < n && probs[j].x == probs[i].x && probs[j].ldx == probs[i].ldx) ++j;
-        for (int32_t k = i; k < j; ++k) {
-            prm.xgrp_off[k] = (uint8_t)(k - i);
-            prm.xgrp_size[k] = (uint8_t)(j - i);
-        }
-        i = j;
-    }
-    prm.pool = view_of(pool);
-    prm.ws = reinterpret_cast<char*>(ws);
-    prm.nprob = n;
-    prm.s1 = c.s1;
-    prm.s2 = c.s2;
-    prm.s3 = c.s3;
-    prm.s1_bytes = c.s1_bytes;
-    prm.s2_bytes = c.s2_bytes;
-    prm.rp_max = c.rp_max;
-    return LORA_OK;
-}
-
-template <int MAXP>
-void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, void* ws,
-               float* t_out, int stages, int rows_per_stage) {
-    const lora_pool_desc& d = pool->d;
-    memset(&prm, 0, sizeof prm);
-    prm.pool = view_of(pool);
-    prm.ws = reinterpret_cast<char*>(ws);
-    prm.t_out = t_out;
-    prm.nprob = n;
-    prm.stages = stages;
-    prm.stage_bytes = rows_per_stage * 2 * d.h;
-    for (int32_t i = 0; i < n; ++i) {
-        prm.probs[i] = prob_desc(pool, probs[i]);
-    }
-}
-
-// Balanced batches of at most `cap` problems (no short last launch).
-int32_t batch_size(int32_t nprob, int32_t cap) {
-    const int32_t nb = (nprob + cap - 1) / cap;
-    return (nprob + nb - 1) / nb;
-}
-
-lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
-                    cudaStream_t stream) {
-    if (T <= 0 || nprob <= 0) return LORA_OK;
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    MmaConfig c;
-    st = mma_config(pool->d, di->smem_optin, &c);
-    if (st != LORA_OK) return st;
-    static thread_local MmaParams prm;
-    static thread_local int attr_dev = -1;
-    static thread_local size_t attr_smem = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    auto kern = pool->square ? sgmv_mma_kernel<false> : sgmv_mma_kernel<true>;
-    if (attr_dev != dev || attr_smem < c.smem) {
-        for (auto k : {sgmv_mma_kernel<false>, sgmv_mma_kernel<true>}) {
-            st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem));
-            if (st != LORA_OK) return st;
-        }
-        attr_dev = dev;
-        attr_smem = c.smem;
-    }
-    const int32_t per = batch_size(nprob, kMmaMaxProbs);
-    for (int32_t base = 0; base < nprob; base += per) {
-        const int32_t n = nprob - base < per ? nprob - base : per;
-        st = fill_mma(prm, pool, probs + base, n, T, ws, c);
-        if (st != LORA_OK) return st;
-        kern<<<di->sm_count, kMmaThreads, c.smem, stream>>>(prm);
-        st = cuda_status(cudaGetLastError());
-        if (st != LORA_OK) return st;
-    }
-    return LORA_OK;
-}
-
-constexpr float kFusedRingSpeed = 1.22f;
-
-// Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0); the
-// ring body takes the stage shape the stand-alone ring kernel would take.
-template <int NV, int CW, int RP, bool W>
-lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
-                            void* ws, const DeviceInfo* di, const MmaConfig& c, const RingShape& sh,
-                            cudaStream_t stream) {
-    const size_t smem = c.smem > sh.smem ? c.smem : sh.smem;
-    static thread_local FusedParams prm;
-    // per-CTA byte rate of the ring body relative to the tensor-core body, measured on the
-    // 13B mixed step (ring CTAs split by bytes alone ended 18% before the tensor-core ones);
-    // LORA_FUSED_RING_SPEED overrides it
-    const char* rs = getenv("LORA_FUSED_RING_SPEED");
-    const float ring_speed = rs != nullptr && atof(rs) > 0.1 && atof(rs) < 10.0 ? (float)atof(rs) : kFusedRingSpeed;
-    static thread_local int attr_dev = -1;
-    static thread_local size_t attr_smem = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    auto kern = delta_fused_kernel<NV, CW, RP, W>;
-    lora_status st;
-    if (attr_dev != dev || attr_smem < smem) {
-        st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (st != LORA_OK) return st;
-        attr_dev = dev;
-        attr_smem = smem;
-    }
-    const int32_t per = batch_size(nprob, kMmaMaxProbs);
-    for (int32_t base = 0; base < nprob; base += per) {
-        const int32_t n = nprob - base < per ? nprob - base : per;
-        st = fill_mma(prm.mma, pool, probs + base, n, T, ws, c);
-        if (st != LORA_OK) return st;
-        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, sh.stages, RP);
-        prm.ring_speed = ring_speed;
-        prm.row_elems = prm.page_elems = 0;
-        for (int32_t i = base; i < base + n; ++i) {
-            const int64_t di = pool->d_in[probs[i].proj], dq = pool->d_out[probs[i].proj];
-            prm.row_elems += (unsigned long long)(di + 2 * dq);
-            prm.page_elems += (unsigned long long)(di + dq);
-        }
-        kern<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
-        st = cuda_status(cudaGetLastError());
-        if (st != LORA_OK) return st;
-    }
-    return LORA_OK;
-}
-
-template <int NV, int CW>
-lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
-                         cudaStream_t stream) {
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    MmaConfig c;
-    st = mma_config(pool->d, di->smem_optin, &c);
-    if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW);
-    if (sh.stages < 2) return LORA_ETOOBIG;
-    if (!pool->square) {
-        if (sh.rp == kRingPagesLarge)
-            return launch_fused_rp<NV, CW, kRingPagesLarge, true>(pool, probs, nprob, T, ws, di, c, sh, stream);
-        return launch_fused_rp<NV, CW, kRingPagesSmall, true>(pool, probs, nprob, T, ws, di, c, sh, stream);
-    }
-    if (sh.rp == kRingPagesLarge)
-        return launch_fused_rp<NV, CW, kRingPagesLarge, false>(pool, probs, nprob, T, ws, di, c, sh, stream);
-    return launch_fused_rp<NV, CW, kRingPagesSmall, false>(pool, probs, nprob, T, ws, di, c, sh, stream);
 }
 
 lora_status check_problems(const lora_pool* pool, const lora_problem* probs, int32_t nprob) {
@@ -484,81 +115,17 @@ lora_status check_problems(const lora_pool* pool, const lora_problem* probs, int
     return LORA_OK;
 }
 
-
-
-// ---------------------------------------------------------------------------- split path
-// Workspace bytes the split path's t takes for batches of up to max_tokens rows (none
-// above kSplitMaxTokens: larger batches never take that path).
-size_t split_t_bytes(const lora_pool_desc& d, int32_t max_tokens) {
-    if (max_tokens > kSplitMaxTokens) return 0;
-    return (size_t)kSplitMaxProbs * (size_t)max_tokens * (size_t)d.r_max * sizeof(float);
-}
-
-// The two-phase CUDA-core path serves launches of few projections of a decode-sized batch
-// (a chunk of one projection per CTA would leave most SMs idle), when the workspace has
-// room for its t.  LORA_SPLIT_MAX_PROBS overrides the projection limit (0 turns it off).
-bool split_fits(const lora_pool_desc& d, int32_t nprob, int32_t T, size_t ws_bytes) {
-    const char* e = getenv("LORA_SPLIT_MAX_PROBS");
-    const int max_p = e != nullptr ? std::min(atoi(e), kSplitMaxProbs) : kSplitDefaultProbs;
-    if (nprob < 1 || nprob > max_p || T < 1 || T > kSplitMaxTokens) return false;
-    // the grouping laid the workspace out for (T, segments); decode segments number at most T
-    return ws_bytes >= ws_layout(T, T).total + split_t_bytes(d, T);
-}
-
-template <bool W>
-lora_status launch_split(const SplitParams& prm, const DeviceInfo* di, cudaStream_t stream) {
-    const int grid = di->sm_count * 4;
-    const size_t xs_bytes = (size_t)kChunk * prm.pool.h * 2;   // the chunk's x rows
-    static thread_local int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_dev != dev) {
-        lora_status st = cuda_status(cudaFuncSetAttribute(split_shrink_kernel<W>,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                          (int)(kChunk * 8192 * 2)));   // h <= 8192
-        if (st != LORA_OK) return st;
-        attr_dev = dev;
-    }
-    split_shrink_kernel<W><<<grid, kSplitThreads, xs_bytes, stream>>>(prm);
-    lora_status st = cuda_status(cudaGetLastError());
-    if (st != LORA_OK) return st;
-    split_expand_kernel<W><<<grid, kSplitThreads, 0, stream>>>(prm);
-    return cuda_status(cudaGetLastError());
-}
-
-lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                      cudaStream_t stream) {
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    static thread_local SplitParams prm;
-    memset(&prm, 0, sizeof prm);
-    prm.pool = view_of(pool);
-    prm.ws = reinterpret_cast<char*>(ws);
-    prm.nprob = nprob;
-    prm.out_blocks = 1;
-    for (int32_t i = 0; i < nprob; ++i) {
-        prm.probs[i] = prob_desc(pool, probs[i]);
-        prm.out_blocks = std::max(prm.out_blocks, vec_pages(prm.probs[i].d_out, pool->d.h));
-    }
-    return pool->square ? launch_split<false>(prm, di, stream) : launch_split<true>(prm, di, stream);
-}
-
 // The delta launches after grouping: the CUDA-core kernel over the chunk list, then
 // (when the batch may hold tensor-core tiles) the tensor-core kernel over the tile list.
 lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
                       size_t ws_bytes, float* t_out, bool with_mma, cudaStream_t stream) {
     lora_status st = check_problems(pool, probs, nprob);
     if (st != LORA_OK) return st;
-    const int h8 = pool->d.h / 8;
     if (!with_mma && t_out == nullptr && split_fits(pool->d, nprob, T, ws_bytes))
         return run_split(pool, probs, nprob, ws, stream);
-    if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && h8 <= 640 && T > 0) {
-        // one launch per batch of projections for both work classes
-        if (h8 <= 256) return launch_fused<1, 8>(pool, probs, nprob, T, ws, stream);
-        if (h8 <= 512) return launch_fused<2, 8>(pool, probs, nprob, T, ws, stream);
-        return launch_fused<2, 10>(pool, probs, nprob, T, ws, stream);
-    }
+    // one launch per batch of projections for both work classes
+    if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && pool->d.h / 8 <= 640 && T > 0)
+        return run_fused(pool, probs, nprob, T, ws, stream);
     st = run_delta_ring(pool, probs, nprob, ws, t_out, stream);
     if (st != LORA_OK) return st;
     if (with_mma && mma_min_rows(pool) > 0) st = run_mma(pool, probs, nprob, T, ws, stream);
@@ -575,6 +142,7 @@ constexpr size_t kNoallocWsBytes = ws_layout(LORA_NOALLOC_MAX_TOKENS, LORA_NOALL
 static __device__ __align__(256) unsigned char g_noalloc_ws[kNoallocWsBytes];
 
 void* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
 
 // First call on a device (that device current): find the array's device address and
 // zero its header.  Later calls reuse the cached address.
@@ -583,7 +151,7 @@ lora_status noalloc_workspace(void** out, cudaStream_t stream) {
     lora_status st = cuda_status(cudaGetDevice(&dev));
     if (st != LORA_OK) return st;
     if (dev < 0 || dev >= kMaxDevices) return LORA_ETOOBIG;
-    std::lock_guard<std::mutex> lk(g_dev_mu);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_addr[dev] == nullptr) {
         void* ptr = nullptr;
         st = cuda_status(cudaGetSymbolAddress(&ptr, g_noalloc_ws));

@@ -21,8 +21,6 @@
 
 namespace lora {
 
-constexpr int kChunk = 4;        // rows per CUDA-core work item
-constexpr int kTileRows = 128;   // rows per tensor-core tile
 constexpr int kSegThreads = 1024;
 constexpr int kKeyTile = 2048;
 

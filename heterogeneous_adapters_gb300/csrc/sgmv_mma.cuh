@@ -30,7 +30,6 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
-#include "segment.cuh"
 
 namespace lora {
 
