@@ -836,7 +836,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode",
                     help="workload: tiny, decode, prefill, mixed, stress-distinct, stress-zipf, "
-                         "llama3-decode, llama3-prefill, or a -small variant")
+                         "llama3-decode, llama3-prefill, llama3-mixed, or a -small variant")
     ap.add_argument("--graph-replays", type=int, default=50,
                     help="timed replays of the CUDA graph of one step")
     ap.add_argument("--e2e-slots", type=int, default=3, choices=[1, 2, 3, 4],

@@ -193,6 +193,11 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
 }
 
 constexpr float kFusedRingSpeed = 1.22f;
+// Pools with projections of other widths: the ring body streams multi-page vectors (an x
+// block and an A page per input page block), a slower byte rate per CTA; measured on the
+// Llama-3-8B mixed step (0.6 / 0.75 / 0.9 / 1.0 / 1.22 / 1.4: 1.96 / 1.84 / 1.82 / 1.95 /
+// 2.11 / 2.37 ms).
+constexpr float kFusedRingSpeedWide = 0.85f;
 
 // Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0); the
 // ring body takes the stage shape the stand-alone ring kernel would take.
@@ -206,7 +211,8 @@ lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, in
     // 13B mixed step (ring CTAs split by bytes alone ended 18% before the tensor-core ones);
     // LORA_FUSED_RING_SPEED overrides it
     const char* rs = getenv("LORA_FUSED_RING_SPEED");
-    const float ring_speed = rs != nullptr && atof(rs) > 0.1 && atof(rs) < 10.0 ? (float)atof(rs) : kFusedRingSpeed;
+    const float ring_speed = rs != nullptr && atof(rs) > 0.1 && atof(rs) < 10.0 ? (float)atof(rs)
+                             : (W ? kFusedRingSpeedWide : kFusedRingSpeed);
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
     int dev = 0;

@@ -284,7 +284,8 @@ def _sample(n, k, seed):
 
 
 @pytest.mark.parametrize("cfg,k", [("decode", 8), ("prefill", 2), ("mixed", 2), ("stress-distinct", 4),
-                                   ("stress-zipf", 4), ("llama3-decode", 7), ("llama3-prefill", 3)])
+                                   ("stress-zipf", 4), ("llama3-decode", 7), ("llama3-prefill", 3),
+                                   ("llama3-mixed", 3)])
 def test_full_workload(cfg, k):
     import torch
     wl = spec.WORKLOADS[cfg]()

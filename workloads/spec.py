@@ -412,6 +412,24 @@ def llama3_8b_prefill(layers: int = 4) -> Workload:
                     all_problems(layers, P))
 
 
+def llama3_8b_mixed(layers: int = 4) -> Workload:
+    """Continuous-batching step on a Llama-3-8B base: 8 prefill prompts of [128, 2048] tokens
+    and 192 decode tokens, 20 of the 200 requests base-only, Zipf(0.8) over 600 adapters of
+    ranks {8..64}, every projection adapted at its own widths, 4 layers by default."""
+    rng = np.random.default_rng(1010)
+    P = len(LLAMA3_8B_DIMS)
+    ranks = rng.choice(np.asarray([8, 16, 32, 64], np.int32), size=600)
+    lens = rng.integers(128, 2049, size=8)
+    ids = rng.choice(600, size=200, p=zipf_probs(600, 0.8))
+    ids[rng.choice(200, size=20, replace=False)] = -1
+    pool = make_pool_all_resident(rng, 4096, layers, P, ranks, proj_dims=LLAMA3_8B_DIMS)
+    seg_start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    batch = Batch(seg_start=seg_start, seg_adapter=ids[:8].astype(np.int32),
+                  dec_adapter=ids[8:].astype(np.int32))
+    return Workload(f"llama3-8b-mixed-h4096-p8-d192-a600-7proj-l{layers}", 1010, pool, batch,
+                    all_problems(layers, P))
+
+
 WORKLOADS = {
     "tiny": tiny_decode,
     "decode": llama7b_decode,
@@ -421,6 +439,7 @@ WORKLOADS = {
     "stress-zipf": lambda: pool_stress("zipf"),
     "llama3-decode": llama3_8b_decode,
     "llama3-prefill": llama3_8b_prefill,
+    "llama3-mixed": llama3_8b_mixed,
 }
 
 
