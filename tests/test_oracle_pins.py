@@ -360,6 +360,39 @@ def test_page_list_walks_the_layout():
         assert pos == pages.size
 
 
+def test_page_list_walks_the_layout_with_widths():
+    """Projections of other widths: the oracle's page list for (layer, proj) is, per group,
+    page kb of every A row for kb < ceil(d_in/h), then page q of every B column for
+    q < ceil(d_out/h), at the entries the layout fixes (U = sum of the projections' page
+    blocks, A block at r (l U + pre(p)), B block ceil(d_in/h) r later)."""
+    h, L = 256, 2
+    dims = [(256, 64), (256, 640), (640, 256), (1032, 8)]
+    rng = np.random.default_rng(38)
+    ranks = rng.choice(np.asarray([1, 3, 8], np.int32), size=5)
+    pool = spec.make_pool_all_resident(rng, h, L, len(dims), ranks, proj_dims=dims)
+    ids = rng.integers(-1, 5, size=30).astype(np.int32)
+    key_of = dict(zip(pool.page_ids.tolist(), pool.page_keys.tolist()))
+    _, _, ga = oracle.group_tokens(ids)
+    pv = [(-(-di // h), -(-do // h)) for di, do in dims]
+    U = sum(a + b for a, b in pv)
+    for l in range(L):
+        for p in range(len(dims)):
+            pre = sum(a + b for a, b in pv[:p])
+            pages = oracle.page_list(pool.pt, pool.pt_off, pool.ranks, pool.num_proj, l, p, ga,
+                                     h=h, proj_dims=pool.proj_dims)
+            pos = 0
+            for a in ga:
+                r = int(pool.ranks[a])
+                a0 = r * (l * U + pre)
+                for ab, nblk in ((0, pv[p][0]), (1, pv[p][1])):
+                    base = a0 + ab * pv[p][0] * r
+                    for kb in range(nblk):
+                        for j in range(r):
+                            assert key_of[int(pages[pos])] == int(spec.page_key(a, base + kb * r + j))
+                            pos += 1
+            assert pos == pages.size
+
+
 # ----------------------------------------------------------------------------- generator sanity
 
 def test_generator_moments():
