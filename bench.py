@@ -332,15 +332,19 @@ def graph_timing(capture_fn, tokens_step: int, dev, replays: int) -> dict:
 def step_model(wl, ids=None, problems=None) -> dict:
     """Algorithmic bytes and flops of one launch over the given problems (all of the
     workload's by default): each projection at its own widths, each distinct x buffer
-    read once."""
+    read once, each distinct physical page once (pools whose layers share a slice of
+    pages read those pages once per launch from DRAM)."""
     from heterogeneous_adapters_gb300 import costmodel
     p = wl.pool
     problems = wl.problems if problems is None else problems
     ids = wl.batch.token_adapter() if ids is None else ids
     dims = [p.dims(pj) for (_, pj) in problems]
     x_widths = [p.dims(pj)[0] for (_, pj) in {wl.x_source(l, pj) for (l, pj) in problems}]
+    U, pre, _, _ = p.layout_units()
+    blocks = [(l * U + pre[pj],) + p.dims(pj) for (l, pj) in problems]
+    phys, _ = costmodel.physical_page_bytes(p.pt, p.pt_off, p.ranks, ids, p.h, blocks)
     return costmodel.decode_step_bytes(p.ranks, ids, p.h, len(problems), dims=dims,
-                                       x_widths=x_widths)
+                                       x_widths=x_widths, page_bytes_physical=phys)
 
 
 def config_dict(wl, args) -> dict:
@@ -351,6 +355,8 @@ def config_dict(wl, args) -> dict:
             "adapters": p.num_adapters, "distinct_adapters": m["distinct_adapters"],
             "ranks": sorted(set(int(r) for r in np.unique(p.ranks))), "batch": wl.batch.kind,
             "seed": wl.seed, "shared_x": wl.shared_x, "bytes_per_step": m["bytes"],
+            "page_bytes_per_step": m["page_bytes"],
+            "page_bytes_logical_per_step": m["page_bytes_logical"],
             "l2": "inputs larger than L2: every step streams %.2f GB" % (m["bytes"] / 1e9),
             "parallelism": "replicas (weak scaling, no collective)"}
 
@@ -640,6 +646,84 @@ def run_sweep_distinct(args, local: int):
     pool.close()
 
 
+# ----------------------------------------------------------------------------- FMA / MMA threshold sweep
+
+def run_sweep_threshold(args, local: int):
+    """Where the tensor cores start to pay: prefill batches of T = 2,048 rows cut into
+    segments of n rows (n = 1, 2, 4 ... 128), every segment with its own adapter (so every
+    segment reads its pages once), all adapters of one rank r (8, 16, 64, 128), h = 4096,
+    2 layers x 4 projections per launch.  Each point runs once with every segment on the
+    CUDA-core kernels (tuning mma_min_rows = 0) and once with every segment of n >= 2 rows on
+    the tensor-core tiles (mma_min_rows = n).  One JSON line per (r, n, path)."""
+    import torch
+
+    import heterogeneous_adapters_gb300 as lora
+    from workloads import spec
+    from workloads.materialize import device_inputs
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks = measured_peaks()
+    h, L, P, T = 4096, 2, 4, 2048
+    ranks_swept = [int(r) for r in args.sweep_ranks.split(",")]
+    lengths = [int(n) for n in args.sweep_lengths.split(",")]
+    for r in ranks_swept:
+        rng = np.random.default_rng(8000 + r)
+        N = T
+        pool_d = spec.make_pool_all_resident(rng, h, L, P, np.full(N, r, np.int32))
+        order = rng.permutation(N).astype(np.int32)
+        batch = spec.Batch(np.asarray([0, T], np.int32), order[:1].copy(), np.zeros(0, np.int32))
+        wl = spec.Workload(f"threshold-h{h}-r{r}", 8000 + r, pool_d, batch, spec.all_problems(L, P))
+        d = device_inputs(wl, device=dev, nan_dummies=False)
+        pool = lora.Pool(d.pool, pool_d.num_pages, h, d.pt, pool_d.pt.size, d.pt_off, d.ranks,
+                         d.scales, N, L, P, pool_d.r_max)
+        probs = [(d.x[i], d.y[i], d.x.shape[2], d.y.shape[2], l, pj)
+                 for i, (l, pj) in enumerate(d.problems)]
+        stream_obj = torch.cuda.current_stream(dev)
+        stream = stream_obj.cuda_stream
+        for n in lengths:
+            S = T // n
+            seg_start = torch.arange(0, S * n + 1, n, dtype=torch.int32, device=dev)
+            seg_adapter = torch.from_numpy(order[:S].copy()).to(dev)
+            ids = np.repeat(order[:S], n)
+            nbytes = lora.workspace_size(pool, T, S)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            lora.workspace_init(ws, nbytes, stream)
+            m = step_model(dataclasses_replace_batch(wl, spec.Batch(seg_start.cpu().numpy(), order[:S].copy(),
+                                                                    np.zeros(0, np.int32))), ids=ids)
+            for path, mma_min in (("cuda-core", 0), ("tensor-core", max(2, n))):
+                if path == "tensor-core" and n < 2:
+                    continue
+                pool.set_tuning(mma_min_rows=mma_min)
+                for _ in range(max(3, args.warmup)):
+                    lora.sgmv(pool, probs, seg_start, seg_adapter, S, T, ws, nbytes, stream)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream_obj)
+                for _ in range(args.steps):
+                    lora.sgmv(pool, probs, seg_start, seg_adapter, S, T, ws, nbytes, stream)
+                e1.record(stream_obj)
+                torch.cuda.synchronize()
+                assert lora.get_device_error(ws, stream) == 0
+                ms = e0.elapsed_time(e1) / args.steps
+                gbs = m["bytes"] / (ms / 1e3) / 1e9
+                print(json.dumps({"sweep": "fma_mma_threshold", "rank": r, "segment_rows": n,
+                                  "segments": S, "path": path, "step_ms": ms,
+                                  "bytes_per_step": m["bytes"], "achieved_gbs": gbs,
+                                  "frac_of_peak": gbs / peaks["hbm_gbs"],
+                                  "tflops": m["flops"] / (ms / 1e3) / 1e12, "steps": args.steps}),
+                      flush=True)
+            del ws
+        pool.close()
+        del d
+        torch.cuda.empty_cache()
+
+
+def dataclasses_replace_batch(wl, batch):
+    import dataclasses
+    return dataclasses.replace(wl, batch=batch)
+
+
 # ----------------------------------------------------------------------------- staging scenario
 
 class SliceCache:
@@ -857,12 +941,19 @@ def main():
     ap.add_argument("--sweep-distinct", action="store_true",
                     help="instead of the bench line: decode tokens/s against the number of "
                          "distinct adapters in the batch (1..64) at the Llama-7B decode shape")
+    ap.add_argument("--sweep-threshold", action="store_true",
+                    help="instead of the bench line: CUDA-core against tensor-core step time "
+                         "over segment length x rank (the FMA / MMA crossover)")
+    ap.add_argument("--sweep-ranks", default="8,16,64,128")
+    ap.add_argument("--sweep-lengths", default="1,2,4,8,16,32,64,128")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)
     elif args.sweep_distinct:
         run_sweep_distinct(args, local)
+    elif args.sweep_threshold:
+        run_sweep_threshold(args, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -20,7 +20,8 @@ LORA_MAX_SEGMENTS = 16384
 LORA_MAX_RANK = 256
 LORA_NOALLOC_MAX_TOKENS = 4096
 
-EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_workspace_size", "lora_workspace_init",
+EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_pool_set_tuning", "lora_pool_get_tuning",
+            "lora_workspace_size", "lora_workspace_init",
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
             "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t", "lora_debug_wait_limit",
             "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error",
@@ -39,6 +40,17 @@ class lora_pool_desc(ctypes.Structure):
                 ("page_table_len", ctypes.c_int64), ("adapter_pt_off", ctypes.c_void_p),
                 ("ranks", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("proj_dims", ctypes.c_void_p)]
+
+
+class lora_tuning(ctypes.Structure):
+    _fields_ = [("ring_rows_per_stage", ctypes.c_int32), ("split_max_problems", ctypes.c_int32),
+                ("mma_min_rows", ctypes.c_int32), ("mma_y_stages", ctypes.c_int32),
+                ("fused_ring_speed", ctypes.c_float), ("reserved", ctypes.c_int32 * 3)]
+
+
+# lora_tuning fields and the value that keeps a field's default
+TUNING_KEEP = {"ring_rows_per_stage": 0, "split_max_problems": -1, "mma_min_rows": -1,
+               "mma_y_stages": 0, "fused_ring_speed": 0.0}
 
 
 class lora_problem(ctypes.Structure):
@@ -75,6 +87,8 @@ def lib():
         sig = {
             "lora_pool_create": [ctypes.POINTER(p), ctypes.POINTER(lora_pool_desc)],
             "lora_pool_destroy": [p],
+            "lora_pool_set_tuning": [p, ctypes.POINTER(lora_tuning)],
+            "lora_pool_get_tuning": [p, ctypes.POINTER(lora_tuning)],
             "lora_workspace_size": [p, i32, i32, ctypes.POINTER(sz)],
             "lora_workspace_init": [p, sz, p],
             "lora_segment": [p, p, p, i32, p, i32, i32, p, sz, p],
@@ -161,6 +175,20 @@ class Pool:
     @property
     def handle(self):
         return self._h
+
+    def set_tuning(self, **fields):
+        """Launch tuning (lora_pool_set_tuning): the named fields, every other one at its
+        default; no fields restores all the defaults."""
+        unknown = set(fields) - set(TUNING_KEEP)
+        if unknown:
+            raise ValueError(f"unknown tuning fields {sorted(unknown)}")
+        t = lora_tuning(**{k: fields.get(k, v) for k, v in TUNING_KEEP.items()})
+        _check(lib().lora_pool_set_tuning(self._h, ctypes.byref(t)), "lora_pool_set_tuning")
+
+    def get_tuning(self) -> dict:
+        t = lora_tuning()
+        _check(lib().lora_pool_get_tuning(self._h, ctypes.byref(t)), "lora_pool_get_tuning")
+        return {k: getattr(t, k) for k in TUNING_KEEP}
 
     def close(self):
         if self._h:

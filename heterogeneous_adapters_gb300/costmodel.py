@@ -38,15 +38,55 @@ def transfer_seconds(nbytes: float, bytes_per_s: float) -> float:
     return nbytes / bytes_per_s
 
 
+def physical_page_bytes(pt: np.ndarray, pt_off: np.ndarray, ranks_by_adapter: np.ndarray,
+                        token_adapter: np.ndarray, h: int, blocks) -> tuple[int, int]:
+    """Bytes of the distinct physical pool pages one launch reads, and of the logical
+    (adapter, projection) blocks it reads.  The two differ only where page tables of
+    different blocks point at the same pages (a pool that holds one layer's slice of each
+    adapter and maps every layer onto it): a page read twice by one launch is a DRAM read
+    once and an L2 hit after, so the roofline numerator counts it once.
+    blocks: per projection of the launch, (blk, d_in, d_out) with blk the A block's offset
+    in units of r_a page-table entries (l * U + pre(p)); only the used part of a partly
+    used last page counts."""
+    ids = np.asarray(token_adapter, dtype=np.int64)
+    distinct = np.unique(ids[ids >= 0])
+    pages, used = [], []
+    logical = 0
+    for a in distinct:
+        r = int(ranks_by_adapter[a])
+        off = int(pt_off[a])
+        for blk, d_in, d_out in blocks:
+            pv_in, pv_out = -(-d_in // h), -(-d_out // h)
+            start = off + r * blk
+            ent = np.arange(start, start + r * (pv_in + pv_out), dtype=np.int64)
+            kb = (ent - start) // r                     # page block of each entry
+            width = np.where(kb < pv_in, np.minimum(h, d_in - kb * h),
+                             np.minimum(h, d_out - (kb - pv_in) * h))
+            pages.append(pt[ent].astype(np.int64))
+            used.append(width.astype(np.int64) * BF16)
+            logical += int(width.sum()) * BF16
+    if not pages:
+        return 0, 0
+    pages, used = np.concatenate(pages), np.concatenate(used)
+    order = np.lexsort((-used, pages))                  # per page, its widest use first
+    first = np.ones(order.size, bool)
+    first[1:] = pages[order][1:] != pages[order][:-1]
+    return int(used[order][first].sum()), logical
+
+
 def decode_step_bytes(ranks_by_adapter: np.ndarray, token_adapter: np.ndarray, h: int,
-                      nprob: int, x_buffers: int | None = None, dims=None, x_widths=None) -> dict:
+                      nprob: int, x_buffers: int | None = None, dims=None, x_widths=None,
+                      page_bytes_physical: int | None = None) -> dict:
     """Algorithmic bytes and flops of one multi-problem launch over nprob projections,
     for a batch whose per-token adapter ids are token_adapter.
     dims: the projections' (d_in, d_out) widths; h x h each if None.  Only the d_in + d_out
     used elements of an adapter's vectors count, not the unused tail of their last page.
     x_widths: the widths of the distinct x buffers the launch reads (projections that
     share their input, as q, k and v of a layer do, read it once); one buffer per
-    projection of its d_in if None, or x_buffers buffers of width h when that is given."""
+    projection of its d_in if None, or x_buffers buffers of width h when that is given.
+    page_bytes_physical: the distinct physical page bytes of the launch
+    (physical_page_bytes); when given, it replaces the per-block page count in "bytes"
+    (the per-block count stays in "page_bytes_logical")."""
     ids = np.asarray(token_adapter, dtype=np.int64)
     adapted = ids[ids >= 0]
     distinct = np.unique(adapted)
@@ -62,7 +102,11 @@ def decode_step_bytes(ranks_by_adapter: np.ndarray, token_adapter: np.ndarray, h
     x_bytes = adapted.size * sum(x_widths) * BF16                      # x read
     y_bytes = adapted.size * 2 * sum(do for _, do in dims) * BF16      # y read and written
     flops = sum(2 * rt * (di + do) for di, do in dims)
+    logical = page_bytes
+    if page_bytes_physical is not None:
+        page_bytes = int(page_bytes_physical)
     return {"bytes": page_bytes + meta_bytes + x_bytes + y_bytes, "page_bytes": page_bytes,
+            "page_bytes_logical": logical,
             "xy_bytes": x_bytes + y_bytes, "meta_bytes": meta_bytes,
             "flops": flops, "adapted_tokens": int(adapted.size),
             "tokens": int(ids.size), "distinct_adapters": int(distinct.size)}

@@ -22,6 +22,7 @@ struct lora_pool {
     int32_t units = 0;                // units of one layer
     bool square = true;               // every projection h x h
     bool mma_widths = true;           // every d_in % 64 == 0 and d_out % 128 == 0 (tile shapes)
+    lora_tuning tune{};               // launch tuning, defaults resolved (lora_pool_set_tuning)
 };
 
 namespace lora {
@@ -49,7 +50,8 @@ struct RingShape {
     int rp, stages;
     size_t smem;
 };
-RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps);
+// force_rp: 4 or 8 rows per stage where two such stages fit; 0 = automatic.
+RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps, int force_rp);
 
 // launch_ring.cu: the CUDA-core kernel over the chunk list (t_out: debug export of t).
 lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
@@ -58,6 +60,7 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
 // launch_tile.cu: the tensor-core kernel over the tile list, and the fused launch of both
 // work classes (h <= 5120).
 int mma_min_rows(const lora_pool* pool);
+float default_fused_ring_speed(bool square);
 lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
                     cudaStream_t stream);
 lora_status run_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
@@ -65,7 +68,7 @@ lora_status run_fused(const lora_pool* pool, const lora_problem* probs, int32_t 
 
 // launch_split.cu: the two-phase CUDA-core path for launches of few projections.
 size_t split_t_bytes(const lora_pool_desc& d, int32_t max_tokens);
-bool split_fits(const lora_pool_desc& d, int32_t nprob, int32_t T, size_t ws_bytes);
+bool split_fits(const lora_pool* pool, int32_t nprob, int32_t T, size_t ws_bytes);
 lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
                       cudaStream_t stream);
 

@@ -1,6 +1,5 @@
 // Launches of the CUDA-core decode kernel (bgmv_ring.cuh): the ring's stage shape and the
 // kernel instantiation for h and for pools with or without projections of other widths.
-#include <stdlib.h>
 #include <string.h>
 
 #include "bgmv_ring.cuh"
@@ -23,10 +22,8 @@ int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* 
 
 // Rows per stage: the larger stages when three of them fit (a bulk-copy ring streams
 // closer to the HBM read rate with fewer, larger stages), else the small ones.
-// LORA_RING_PAGES = 4 or 8 forces the choice where two such stages fit.
-RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps) {
-    const char* e = getenv("LORA_RING_PAGES");
-    const int force = e != nullptr ? atoi(e) : 0;
+// force = 4 or 8 (the pool's tuning) forces the choice where two such stages fit.
+RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps, int force) {
     RingShape fallback{0, 0, 0};
     for (int rp : {kRingPagesLarge, kRingPagesSmall}) {
         size_t smem = 0;
@@ -60,11 +57,11 @@ lora_status launch_ring_rp(RingParams& prm, const DeviceInfo* di, const RingShap
 }
 
 template <int NV, int CW, bool W>
-lora_status launch_ring_w(RingParams& prm, cudaStream_t stream) {
+lora_status launch_ring_w(RingParams& prm, int force_rp, cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW);
+    const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW, force_rp);
     if (sh.stages < 2) return LORA_ETOOBIG;
     if (sh.rp == kRingPagesLarge) return launch_ring_rp<NV, CW, kRingPagesLarge, W>(prm, di, sh, stream);
     return launch_ring_rp<NV, CW, kRingPagesSmall, W>(prm, di, sh, stream);
@@ -72,8 +69,9 @@ lora_status launch_ring_w(RingParams& prm, cudaStream_t stream) {
 
 // h x h pools take the kernels compiled for one page block per vector
 template <int NV, int CW>
-lora_status launch_ring(RingParams& prm, bool square, cudaStream_t stream) {
-    return square ? launch_ring_w<NV, CW, false>(prm, stream) : launch_ring_w<NV, CW, true>(prm, stream);
+lora_status launch_ring(RingParams& prm, const lora_pool* pool, cudaStream_t stream) {
+    const int rp = pool->tune.ring_rows_per_stage;
+    return pool->square ? launch_ring_w<NV, CW, false>(prm, rp, stream) : launch_ring_w<NV, CW, true>(prm, rp, stream);
 }
 
 lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
@@ -95,15 +93,15 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
         const int h8 = d.h / 8;
         lora_status st;
         if (h8 <= 256)
-            st = launch_ring<1, 8>(prm, pool->square, stream);
+            st = launch_ring<1, 8>(prm, pool, stream);
         else if (h8 <= 512)
-            st = launch_ring<2, 8>(prm, pool->square, stream);
+            st = launch_ring<2, 8>(prm, pool, stream);
         else if (h8 <= 640)
-            st = launch_ring<2, 10>(prm, pool->square, stream);
+            st = launch_ring<2, 10>(prm, pool, stream);
         else if (h8 <= 768)
-            st = launch_ring<2, 12>(prm, pool->square, stream);
+            st = launch_ring<2, 12>(prm, pool, stream);
         else
-            st = launch_ring<2, 16>(prm, pool->square, stream);
+            st = launch_ring<2, 16>(prm, pool, stream);
         if (st != LORA_OK) return st;
     }
     return LORA_OK;

@@ -1,6 +1,5 @@
 // Launches of the two-phase CUDA-core kernels (bgmv_split.cuh) for launches of few
 // projections of a decode-sized batch.
-#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -20,13 +19,12 @@ size_t split_t_bytes(const lora_pool_desc& d, int32_t max_tokens) {
 
 // The two-phase CUDA-core path serves launches of few projections of a decode-sized batch
 // (a chunk of one projection per CTA would leave most SMs idle), when the workspace has
-// room for its t.  LORA_SPLIT_MAX_PROBS overrides the projection limit (0 turns it off).
-bool split_fits(const lora_pool_desc& d, int32_t nprob, int32_t T, size_t ws_bytes) {
-    const char* e = getenv("LORA_SPLIT_MAX_PROBS");
-    const int max_p = e != nullptr ? std::min(atoi(e), kSplitMaxProbs) : kSplitDefaultProbs;
+// room for its t.  The pool's tuning sets the projection limit (0 turns the path off).
+bool split_fits(const lora_pool* pool, int32_t nprob, int32_t T, size_t ws_bytes) {
+    const int max_p = std::min(pool->tune.split_max_problems, kSplitMaxProbs);
     if (nprob < 1 || nprob > max_p || T < 1 || T > kSplitMaxTokens) return false;
     // the grouping laid the workspace out for (T, segments); decode segments number at most T
-    return ws_bytes >= ws_layout(T, T).total + split_t_bytes(d, T);
+    return ws_bytes >= ws_layout(T, T).total + split_t_bytes(pool->d, T);
 }
 
 template <bool W>

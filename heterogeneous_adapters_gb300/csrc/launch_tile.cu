@@ -1,6 +1,5 @@
 // Launches of the tensor-core tile kernel (sgmv_mma.cuh) and of the fused launch of both
 // work classes (fused.cuh): tensor maps, shared-memory plan, CTA split weights.
-#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -14,15 +13,12 @@ namespace host {
 
 // Segments of at least this many rows (and rank <= kMmaMaxRank) take the tensor-core
 // path when h is a multiple of 128 and every projection's d_in is a multiple of 64 (the
-// shrink K chunk) and d_out one of 128 (the expand slice); LORA_MMA_MIN_ROWS overrides it
-// (0 disables).
+// shrink K chunk) and d_out one of 128 (the expand slice); the pool's tuning sets the
+// row count (0 disables the path; one-row segments always stay on the CUDA-core path).
 int mma_min_rows(const lora_pool* pool) {
     const lora_pool_desc& d = pool->d;
     if (d.h % kMmaNTile != 0 || !pool->mma_widths) return 0;
-    const char* e = getenv("LORA_MMA_MIN_ROWS");
-    // one-row (decode) segments always stay on the CUDA-core path
-    if (e != nullptr) return atoi(e) > 0 ? std::max(2, atoi(e)) : 0;
-    return 32;
+    return pool->tune.mma_min_rows;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -71,7 +67,8 @@ struct MmaConfig {
     size_t smem;
 };
 
-lora_status mma_config(const lora_pool_desc& d, int smem_optin, MmaConfig* c) {
+lora_status mma_config(const lora_pool* pool, int smem_optin, MmaConfig* c) {
+    const lora_pool_desc& d = pool->d;
     c->rp_max = mma_rpad(d.r_max < kMmaMaxRank ? d.r_max : kMmaMaxRank);
     c->s1_bytes = (16384 + c->rp_max * 128 + 1023) / 1024 * 1024;   // x chunk + A chunk
     c->s2_bytes = (c->rp_max * 256 + 1023) / 1024 * 1024;           // B^T slice
@@ -80,8 +77,7 @@ lora_status mma_config(const lora_pool_desc& d, int smem_optin, MmaConfig* c) {
     // end with it); B^T ring of 2.  On the Llama-7B prefill a 3-slot y ring with a 4-stage
     // shrink ring beat both 4 + 2 (13% slower) and 2 + 6 (18% slower).
     c->s2 = 2;
-    const char* ys = getenv("LORA_MMA_Y_STAGES");   // tuning override: 2..4
-    const int s3_max = ys != nullptr && atoi(ys) >= 2 && atoi(ys) <= 4 ? atoi(ys) : 3;
+    const int s3_max = pool->tune.mma_y_stages;   // 3 unless the pool's tuning says otherwise
     for (c->s3 = s3_max; c->s3 >= 2; --c->s3) {
         for (c->s1 = kMmaMaxStages; c->s1 >= 2; --c->s1) {
             c->smem = mma_smem_layout(c->s1, c->s1_bytes, c->s2, c->s2_bytes, c->s3).total + 1024;
@@ -164,7 +160,7 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
     MmaConfig c;
-    st = mma_config(pool->d, di->smem_optin, &c);
+    st = mma_config(pool, di->smem_optin, &c);
     if (st != LORA_OK) return st;
     static thread_local MmaParams prm;
     static thread_local int attr_dev = -1;
@@ -192,12 +188,14 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
     return LORA_OK;
 }
 
-constexpr float kFusedRingSpeed = 1.22f;
+// Per-CTA byte rate of the ring body relative to the tensor-core body in the fused launch,
+// measured on the 13B mixed step (ring CTAs split by bytes alone ended 18% before the
+// tensor-core ones; 1.0 / 1.1 / 1.22 / 1.35 / 1.5: 11.67 / 11.29 / 11.18 / 11.42 / 12.95 ms).
 // Pools with projections of other widths: the ring body streams multi-page vectors (an x
 // block and an A page per input page block), a slower byte rate per CTA; measured on the
 // Llama-3-8B mixed step (0.6 / 0.75 / 0.9 / 1.0 / 1.22 / 1.4: 1.96 / 1.84 / 1.82 / 1.95 /
 // 2.11 / 2.37 ms).
-constexpr float kFusedRingSpeedWide = 0.85f;
+float default_fused_ring_speed(bool square) { return square ? 1.22f : 0.85f; }
 
 // Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0); the
 // ring body takes the stage shape the stand-alone ring kernel would take.
@@ -207,12 +205,7 @@ lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, in
                             cudaStream_t stream) {
     const size_t smem = c.smem > sh.smem ? c.smem : sh.smem;
     static thread_local FusedParams prm;
-    // per-CTA byte rate of the ring body relative to the tensor-core body, measured on the
-    // 13B mixed step (ring CTAs split by bytes alone ended 18% before the tensor-core ones);
-    // LORA_FUSED_RING_SPEED overrides it
-    const char* rs = getenv("LORA_FUSED_RING_SPEED");
-    const float ring_speed = rs != nullptr && atof(rs) > 0.1 && atof(rs) < 10.0 ? (float)atof(rs)
-                             : (W ? kFusedRingSpeedWide : kFusedRingSpeed);
+    const float ring_speed = pool->tune.fused_ring_speed;   // see default_fused_ring_speed
     static thread_local int attr_dev = -1;
     static thread_local size_t attr_smem = 0;
     int dev = 0;
@@ -252,9 +245,9 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
     MmaConfig c;
-    st = mma_config(pool->d, di->smem_optin, &c);
+    st = mma_config(pool, di->smem_optin, &c);
     if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW);
+    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW, pool->tune.ring_rows_per_stage);
     if (sh.stages < 2) return LORA_ETOOBIG;
     if (!pool->square) {
         if (sh.rp == kRingPagesLarge)

@@ -93,6 +93,17 @@ lora_status device_info(DeviceInfo** out) {
 
 namespace {
 
+// The measured defaults of a pool's launch tuning: stage rows chosen by shared memory,
+// the split path up to 2 projections, tensor-core tiles from 32 rows, a 3-slot y ring.
+void default_tuning(const lora_pool* pool, lora_tuning* t) {
+    memset(t, 0, sizeof *t);
+    t->ring_rows_per_stage = 0;
+    t->split_max_problems = kSplitDefaultProbs;
+    t->mma_min_rows = kMmaDefaultMinRows;
+    t->mma_y_stages = 3;
+    t->fused_ring_speed = default_fused_ring_speed(pool->square);
+}
+
 lora_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
     if (ws == nullptr || ((uintptr_t)ws & 255u) != 0) return LORA_EWORKSPACE;
     if (ws_bytes < need) return LORA_EWORKSPACE;
@@ -121,7 +132,7 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
                       size_t ws_bytes, float* t_out, bool with_mma, cudaStream_t stream) {
     lora_status st = check_problems(pool, probs, nprob);
     if (st != LORA_OK) return st;
-    if (!with_mma && t_out == nullptr && split_fits(pool->d, nprob, T, ws_bytes))
+    if (!with_mma && t_out == nullptr && split_fits(pool, nprob, T, ws_bytes))
         return run_split(pool, probs, nprob, ws, stream);
     // one launch per batch of projections for both work classes
     if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && pool->d.h / 8 <= 640 && T > 0)
@@ -226,12 +237,42 @@ lora_status lora_pool_create(lora_pool** out, const lora_pool_desc* desc) {
         return LORA_ETOOBIG;
     }
     p->units = (int32_t)units;
+    default_tuning(p, &p->tune);
     *out = p;
     return LORA_OK;
 }
 
 lora_status lora_pool_destroy(lora_pool* pool) {
     delete pool;
+    return LORA_OK;
+}
+
+lora_status lora_pool_set_tuning(lora_pool* pool, const lora_tuning* t) {
+    if (pool == nullptr) return LORA_EINVAL;
+    lora_tuning v;
+    default_tuning(pool, &v);
+    if (t != nullptr) {
+        if (t->reserved[0] != 0 || t->reserved[1] != 0 || t->reserved[2] != 0) return LORA_EINVAL;
+        if (t->ring_rows_per_stage != 0 && t->ring_rows_per_stage != 4 && t->ring_rows_per_stage != 8)
+            return LORA_EINVAL;
+        if (t->split_max_problems < -1 || t->split_max_problems > kSplitMaxProbs) return LORA_EINVAL;
+        if (t->mma_min_rows < -1 || t->mma_min_rows == 1) return LORA_EINVAL;
+        if (t->mma_y_stages != 0 && (t->mma_y_stages < 2 || t->mma_y_stages > 4)) return LORA_EINVAL;
+        if (t->fused_ring_speed != 0.f && !(t->fused_ring_speed >= 0.1f && t->fused_ring_speed <= 10.f))
+            return LORA_EINVAL;
+        v.ring_rows_per_stage = t->ring_rows_per_stage;
+        if (t->split_max_problems >= 0) v.split_max_problems = t->split_max_problems;
+        if (t->mma_min_rows >= 0) v.mma_min_rows = t->mma_min_rows;
+        if (t->mma_y_stages != 0) v.mma_y_stages = t->mma_y_stages;
+        if (t->fused_ring_speed != 0.f) v.fused_ring_speed = t->fused_ring_speed;
+    }
+    pool->tune = v;
+    return LORA_OK;
+}
+
+lora_status lora_pool_get_tuning(const lora_pool* pool, lora_tuning* out) {
+    if (pool == nullptr || out == nullptr) return LORA_EINVAL;
+    *out = pool->tune;
     return LORA_OK;
 }
 
@@ -267,8 +308,9 @@ lora_status lora_workspace_view(const lora_pool* pool, void* ws, size_t ws_bytes
 }
 
 // The grouping launch.  with_split_room: the workspace must also hold the split path's t
-// (the size lora_workspace_size reports); the allocation-free entry point, whose fixed
-// scratch has no such room and which never takes that path, passes false.
+// (the size lora_workspace_size reports); the allocation-free entry point passes false:
+// its fixed scratch holds the split path's t only for small batches, and run_delta then
+// takes that path only when split_fits finds the room.
 static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
                          int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
                          size_t ws_bytes, bool with_split_room, void* stream) {

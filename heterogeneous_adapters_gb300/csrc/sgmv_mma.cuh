@@ -37,6 +37,7 @@ constexpr int kMmaThreads = 384;
 constexpr int kMmaEpiWarps = 8;
 constexpr int kMmaMaxProbs = 64;            // problems per launch (3 tensor maps each)
 constexpr int kMmaMaxRank = 128;
+constexpr int kMmaDefaultMinRows = 32;      // segments of at least this many rows take the tiles
 constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 bytes)
 constexpr int kMmaNTile = 128;              // y columns per expand slice
 constexpr int kMmaRowBlock = 32;            // rows per x / y TMA box

@@ -50,9 +50,9 @@
  * is still computed.  No kernel traps or spins without a bound: every wait inside a
  * kernel gives up after a time limit and reports LORA_DERR_TIMEOUT.
  *
- * Threading: a pool handle is read-only after creation and may be shared by calls
- * on different streams.  A workspace must not be used by two calls that may run
- * concurrently on the GPU.
+ * Threading: a pool handle is read-only after creation (lora_pool_set_tuning aside) and
+ * may be shared by calls on different streams.  A workspace must not be used by two
+ * calls that may run concurrently on the GPU.
  */
 #ifndef LORA_GB300_H
 #define LORA_GB300_H
@@ -143,6 +143,33 @@ typedef struct {
 lora_status lora_pool_create(lora_pool** out, const lora_pool_desc* desc);
 lora_status lora_pool_destroy(lora_pool* pool);
 
+/* Launch tuning of a pool: which kernel serves which work and the shape of its stages.
+ * Every field has a measured default, which lora_pool_create installs; a field given
+ * its "default" value below takes that default.  The results never depend on these
+ * choices beyond the rounding order of the fp32 sums: they exist for measurement and
+ * tests.  The library reads no environment variable.  Set the tuning before the pool
+ * is shared between threads (calls read it from the handle). */
+typedef struct {
+    int32_t ring_rows_per_stage; /* CUDA-core ring: rows (pages) per shared-memory stage,
+                                    4 or 8; 0 = 8 where three stages fit, else 4        */
+    int32_t split_max_problems;  /* launches of at most this many projections (and at
+                                    most 1,024 rows) run the two-phase split kernels;
+                                    0 = never, 1..8; -1 = default (2)                   */
+    int32_t mma_min_rows;        /* prefill segments of at least this many rows take the
+                                    tensor-core tiles; 0 = never, >= 2; -1 = default    */
+    int32_t mma_y_stages;        /* depth of the tensor-core kernel's y ring, 2..4;
+                                    0 = default (3)                                     */
+    float fused_ring_speed;      /* mixed launch: per-CTA byte rate of the CUDA-core body
+                                    over the tensor-core body's (0.1 .. 10); 0 = default */
+    int32_t reserved[3];         /* must be 0                                           */
+} lora_tuning;
+
+/* t == NULL restores the defaults.  Returns LORA_EINVAL for a value outside the ranges
+ * above (the pool keeps its previous tuning). */
+lora_status lora_pool_set_tuning(lora_pool* pool, const lora_tuning* t);
+/* The effective values (defaults resolved). */
+lora_status lora_pool_get_tuning(const lora_pool* pool, lora_tuning* out);
+
 /* Bytes of device workspace needed by a call over at most max_tokens rows and at
  * most max_segments segments (prefill segments + decode tokens).  The workspace
  * holds the grouping of the batch, the work queue, the device error word and, for
@@ -157,6 +184,12 @@ lora_status lora_workspace_size(const lora_pool* pool, int32_t max_tokens, int32
 lora_status lora_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Scheduler step: groups the batch by adapter, on the device.
+ *   "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels work":
+ *   SGMV groups tokens into contiguous segments that share an adapter, and the engine
+ *   computes, per step, an index from each token to its adapter; "S-LoRA: Serving
+ *   Thousands of Concurrent Adapters in 2026", "The Three Core Pillars": the kernel
+ *   groups token slices by adapter id with no CPU involvement -- here one CTA sorts the
+ *   segments by (adapter, position) with no host synchronisation.
  * Rows [seg_start[s], seg_start[s+1]) form prefill segment s (adapter seg_adapter[s]),
  * for s < S, and rows seg_start[S] + d, d < Td, are decode tokens (adapter
  * dec_adapter[d]).  S may be 0 (decode only; seg_start may then be NULL and decode
@@ -193,7 +226,12 @@ lora_status lora_sgmv(const lora_pool* pool, const lora_problem* probs, int32_t 
                       void* ws, size_t ws_bytes, void* stream);
 
 /* Mixed continuous-batching step: S prefill segments followed by Td decode tokens
- * (rows seg_start[S] + d), one grouping and one delta launch per problem batch. */
+ * (rows seg_start[S] + d), one grouping and one delta launch per problem batch.
+ *   "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "What the engine does each
+ *   step": a step's batch holds requests in prefill and in decode, and every LoRA target
+ *   of every layer applies shrink then expand to all of them; "How the kernels work":
+ *   SGMV suits the prefill segments and BGMV the decode tokens.  Both work classes run in
+ *   the same persistent launch, its CTAs split between them by the bytes each streams. */
 lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
                              const int32_t* seg_start, const int32_t* seg_adapter, int32_t S,
                              const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
@@ -247,20 +285,27 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
                              const int32_t* upd_page, int64_t nupd, void* stream);
 
 /* Allocation-free BGMV.  The pages this library follows have no counterpart of this
- * call; it exists for callers that cannot allocate device memory: code running inside
- * a CUDA graph being captured, allocators that forbid extra device allocations (a
- * serving engine that has carved the GPU into a fixed pool), or plugins that are handed
- * only their inputs and outputs.  It computes exactly what lora_bgmv computes, with the
- * grouping and work lists kept in a fixed-size array inside the library instead of a
- * caller workspace, and calls no cudaMalloc, cudaFree or allocating routine.
+ * call.  It is for callers that have no way to obtain device memory for a workspace:
+ * a serving engine that reserves all of the GPU's memory for its own pools at start-up
+ * (any later cudaMalloc fails or eats into the KV cache), a plugin or operator that a
+ * host framework hands only its input and output buffers, or a step loop in which a
+ * cudaMalloc -- which may synchronise the device -- is not allowed.  It computes what
+ * lora_bgmv computes (the same grouping and delta kernels, chosen by the same rules),
+ * with the grouping, the work lists and, where it runs, the split path's fp32 t kept
+ * in a fixed array inside the library instead of a caller workspace, and it calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  *   - T must be <= LORA_NOALLOC_MAX_TOKENS (decode rows); larger batches return
- *     LORA_ETOOBIG and launch nothing.
+ *     LORA_ETOOBIG and launch nothing.  Launches of one or two projections take the
+ *     split path only when its t fits in the array beside the grouping (small T).
  *   - The array is shared by every call in the process on a given GPU and keeps the
- *     last call's contents: calls whose kernels may overlap on the GPU (different
- *     streams without ordering, or several host threads) race with each other; order
- *     them on one stream.
+ *     last call's contents (the call clears what must start at zero): calls whose
+ *     kernels may overlap on the GPU (different streams without ordering, or several
+ *     host threads) race with each other; order them on one stream.
  *   - The first call on each device (that device current) looks up the array's device
- *     address and zeroes its header; make that first call before capturing a stream.
+ *     address (cudaGetSymbolAddress) and zeroes its header; make that first call before
+ *     any stream capture begins.  The address is kept for the life of the process: it
+ *     does not survive cudaDeviceReset or a reset of the primary context, after which
+ *     this entry point must not be called again in the process.
  *   - error_bits (a device uint32, may be NULL) receives this call's device error bits
  *     (LORA_DERR_*), copied on `stream` after the kernels.
  * Every GPU that loads this library holds the array (about 0.5 MB) until the process

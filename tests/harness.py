@@ -26,7 +26,9 @@ T_ACC = 2e-5
 class GpuCase:
     """Device buffers, pool handle and workspace of one workload."""
 
-    def __init__(self, wl, problems=None, y0_zero=False, nan_dummies=True, device="cuda:0"):
+    def __init__(self, wl, problems=None, y0_zero=False, nan_dummies=True, device="cuda:0",
+                 tuning=None):
+        """tuning: lora_pool_set_tuning fields for the pool (kernel choice, stage shapes)."""
         import torch
         import heterogeneous_adapters_gb300 as lora
         self.torch = torch
@@ -42,6 +44,8 @@ class GpuCase:
         self.pool = lora.Pool(self.dev.pool, p.num_pages, p.h, self.dev.pt, p.pt.size,
                               self.dev.pt_off, self.dev.ranks, self.dev.scales, p.num_adapters,
                               p.num_layers, p.num_proj, p.r_max, p.proj_dims)
+        if tuning:
+            self.pool.set_tuning(**tuning)
         b = wl.batch
         self.T = b.num_tokens
         self.nseg = b.num_segments + b.num_decode

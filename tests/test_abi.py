@@ -119,3 +119,39 @@ def test_stage_pages_host_checks(lib):
     assert lib.lora_stage_pages(h, None, None, 0, c(other), c(idx), c(pg), 2, None) == LORA_EINVAL
     assert lib.lora_stage_pages(h, None, None, 0, None, None, None, 0, None) == 0
     lib.lora_pool_destroy(h)
+
+
+def test_pool_tuning_defaults_overrides_and_checks(lib):
+    """Launch tuning lives in the pool handle (no environment variable is read): the
+    defaults, a partial override that keeps the other fields, range checks that leave the
+    tuning unchanged, and NULL restoring the defaults."""
+    from heterogeneous_adapters_gb300._binding import LORA_EINVAL, lora_tuning, lora_pool_desc
+    h = ctypes.c_void_p()
+    d = lora_pool_desc(1 << 20, 16, 256, 2, 1, 1, 8, 0, 1 << 20, 32, 1 << 20, 1 << 20, 1 << 20)
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(d)) == 0
+
+    def get():
+        t = lora_tuning()
+        assert lib.lora_pool_get_tuning(h, ctypes.byref(t)) == 0
+        return (t.ring_rows_per_stage, t.split_max_problems, t.mma_min_rows, t.mma_y_stages,
+                round(t.fused_ring_speed, 4))
+
+    default = get()
+    assert default == (0, 2, 32, 3, 1.22)
+
+    def set_(**kw):
+        f = dict(ring_rows_per_stage=0, split_max_problems=-1, mma_min_rows=-1, mma_y_stages=0,
+                 fused_ring_speed=0.0)
+        f.update(kw)
+        t = lora_tuning(**f)
+        return lib.lora_pool_set_tuning(h, ctypes.byref(t))
+
+    assert set_(split_max_problems=0, mma_min_rows=64) == 0
+    assert get() == (0, 0, 64, 3, 1.22)
+    for bad in (dict(ring_rows_per_stage=5), dict(split_max_problems=9), dict(mma_min_rows=1),
+                dict(mma_y_stages=5), dict(fused_ring_speed=20.0), dict(reserved=(ctypes.c_int32 * 3)(1, 0, 0))):
+        assert set_(**bad) == LORA_EINVAL, bad
+        assert get() == (0, 0, 64, 3, 1.22)
+    assert lib.lora_pool_set_tuning(h, None) == 0
+    assert get() == default
+    lib.lora_pool_destroy(h)

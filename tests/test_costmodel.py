@@ -56,3 +56,47 @@ def test_llama3_8b_worked_example():
     n = costmodel.adapter_params(32, dims, 16)
     assert round(n / 1e6, 1) == 41.9 and round(2 * n / 1e6, 1) == 83.9
     assert round(32 * sum(a * b for a, b in dims) / 1e9, 2) == 6.98
+
+
+def test_physical_page_bytes_count_shared_pages_once():
+    """A pool whose layers map onto one shared slice of pages (the unified-pool stress
+    layout): the physical count is the set of page ids the launch's page-table entries
+    hold, each counted once at its widest use; the logical count is per block."""
+    h = 256
+    rng = np.random.default_rng(11)
+    ranks = np.asarray([2, 4, 4], np.int64)
+    L, P = 3, 2
+    U = 2 * P
+    pt_off = np.concatenate([[0], np.cumsum(L * U * ranks)[:-1]])
+    pt = np.zeros(int((L * U * ranks).sum()), np.int32)
+    # every adapter owns U * r physical pages; layer l maps onto them through a permutation
+    # of the adapter's slice entries, so the 3 layers read the same pages
+    base = 0
+    for a, r in enumerate(ranks):
+        slice_pages = base + np.arange(U * r)
+        base += U * r
+        for l in range(L):
+            perm = rng.permutation(U * r)
+            pt[pt_off[a] + l * U * r: pt_off[a] + (l + 1) * U * r] = slice_pages[perm]
+    ids = np.asarray([0, 2, 2, -1, 0], np.int32)
+    blocks = [(l * U + 2 * p, h, h) for l in range(L) for p in range(P)]
+    phys, logical = costmodel.physical_page_bytes(pt, pt_off, ranks, ids, h, blocks)
+    read = set()
+    for a in (0, 2):
+        r = int(ranks[a])
+        for blk, _, _ in blocks:
+            read |= set(pt[pt_off[a] + r * blk: pt_off[a] + r * blk + 2 * r].tolist())
+    assert phys == len(read) * h * 2
+    assert logical == len(blocks) * 2 * (2 + 4) * h * 2
+    assert phys == (U * (2 + 4)) * h * 2 < logical
+    # a pool where every block owns its pages: the two counts agree, and agree with the
+    # per-block model of decode_step_bytes
+    wl = spec.tiny_decode()
+    p = wl.pool
+    Up, pre, _, _ = p.layout_units()
+    blocks = [(l * Up + pre[pj],) + p.dims(pj) for (l, pj) in wl.problems]
+    phys, logical = costmodel.physical_page_bytes(p.pt, p.pt_off, p.ranks, wl.batch.token_adapter(),
+                                                  p.h, blocks)
+    m = costmodel.decode_step_bytes(p.ranks, wl.batch.token_adapter(), p.h, len(wl.problems),
+                                    page_bytes_physical=phys)
+    assert phys == logical == m["page_bytes_logical"] == m["page_bytes"]

@@ -22,15 +22,14 @@ def _wl(wide=False):
 
 # the decode batches here have 2 projections: the split path by default, the ring kernel
 # when the split path is turned off
-PATHS = {"split": "8", "ring": "0"}
+PATHS = {"split": 8, "ring": 0}
 
 
 @pytest.mark.parametrize("path", list(PATHS))
-def test_bad_adapter_id_sets_bit_and_skips_only_that_token(path, monkeypatch):
+def test_bad_adapter_id_sets_bit_and_skips_only_that_token(path):
     import torch
-    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
     wl = _wl()
-    case = GpuCase(wl)
+    case = GpuCase(wl, tuning={"split_max_problems": PATHS[path]})
     try:
         ids = wl.batch.token_adapter().copy()
         victim = int(np.nonzero(ids >= 0)[0][0])
@@ -49,11 +48,10 @@ def test_bad_adapter_id_sets_bit_and_skips_only_that_token(path, monkeypatch):
 
 
 @pytest.mark.parametrize("path", list(PATHS))
-def test_bad_page_rank_and_block_bits(path, monkeypatch):
+def test_bad_page_rank_and_block_bits(path):
     import torch
-    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
     wl = _wl()
-    case = GpuCase(wl)
+    case = GpuCase(wl, tuning={"split_max_problems": PATHS[path]})
     try:
         ids = wl.batch.token_adapter()
         a = int(ids[ids >= 0][0])
@@ -75,13 +73,12 @@ def test_bad_page_rank_and_block_bits(path, monkeypatch):
 @pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("ab", [0, 1])
 @pytest.mark.parametrize("wide", [False, True])
-def test_bad_page_skips_that_adapter_in_that_projection_only(path, ab, wide, monkeypatch):
+def test_bad_page_skips_that_adapter_in_that_projection_only(path, ab, wide):
     """An out-of-range A-row (ab=0) or B-column (ab=1) page of adapter a in projection 0
     (for the wide pool, in the last page block of its vectors): the page bit is set, a's
     rows of projection 0 keep their y, everything else is right."""
-    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", PATHS[path])
     wl = _wl(wide)
-    case = GpuCase(wl)
+    case = GpuCase(wl, tuning={"split_max_problems": PATHS[path]})
     try:
         ids = wl.batch.token_adapter()
         a = int(ids[ids >= 0][0])

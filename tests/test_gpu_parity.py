@@ -80,13 +80,12 @@ def test_small_parity(name, y0_zero):
         case.close()
 
 
-@pytest.mark.parametrize("mma_min", ["0", "1", "128"])
-def test_prefill_size_classes(mma_min, monkeypatch):
-    """The same prefill batch with every segment on the CUDA-core path (0), every segment on
-    the tensor-core path (1), and only full-tile segments on it (128)."""
-    monkeypatch.setenv("LORA_MMA_MIN_ROWS", mma_min)
+@pytest.mark.parametrize("mma_min", [0, 2, 128])
+def test_prefill_size_classes(mma_min):
+    """The same prefill batch with every segment on the CUDA-core path (0), every segment of
+    more than one row on the tensor-core path (2), and only full-tile segments on it (128)."""
     wl = small_prefill(57, 1024, 2, 2, 10, [8, 16, 32, 64, 128], [1, 2, 127, 128, 129, 300, 64, 0, 9])
-    case = GpuCase(wl, y0_zero=True)
+    case = GpuCase(wl, y0_zero=True, tuning={"mma_min_rows": mma_min})
     try:
         assert case.run() == 0
         full_check(wl, case, list(range(len(wl.problems))))
@@ -94,14 +93,13 @@ def test_prefill_size_classes(mma_min, monkeypatch):
         case.close()
 
 
-@pytest.mark.parametrize("pages", ["4", "8"])
-def test_decode_ring_stage_shapes(pages, monkeypatch):
+@pytest.mark.parametrize("pages", [4, 8])
+def test_decode_ring_stage_shapes(pages):
     """The decode ring with 4 and with 8 rows per stage on the same batch: ranks that are
     not multiples of either and chunks of 1 to 4 rows (a skewed adapter mix)."""
-    monkeypatch.setenv("LORA_RING_PAGES", pages)
-    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", "0")   # the ring kernel, not the split path
     wl = small_decode(65, 2048, 1, 3, 12, [1, 3, 5, 8, 13, 64, 100], 57, zipf=1.3)
-    case = GpuCase(wl)
+    # the ring kernel, not the split path
+    case = GpuCase(wl, tuning={"ring_rows_per_stage": pages, "split_max_problems": 0})
     try:
         assert case.run() == 0
         full_check(wl, case, list(range(len(wl.problems))))
@@ -109,16 +107,15 @@ def test_decode_ring_stage_shapes(pages, monkeypatch):
         case.close()
 
 
-@pytest.mark.parametrize("split", ["0", "8"])
+@pytest.mark.parametrize("split", [0, 8])
 @pytest.mark.parametrize("h", [512, 4096, 5120])
-def test_decode_split_and_ring_paths(split, h, monkeypatch):
+def test_decode_split_and_ring_paths(split, h):
     """The same few-projection decode batch through the two-phase split kernels (up to 8
     projections) and through the ring kernel: ranks not multiples of 8 rows, chunks of 1
     to 4 rows, base-only rows, ranks up to 128."""
-    monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", split)
     wl = small_decode(66, h, 2, 3, 10, [1, 5, 8, 16, 64, 128], 47, zipf=1.2)
     wl.batch.dec_adapter[::9] = -1
-    case = GpuCase(wl)
+    case = GpuCase(wl, tuning={"split_max_problems": split})
     try:
         assert case.run() == 0
         full_check(wl, case, list(range(len(wl.problems))))
@@ -332,15 +329,13 @@ WIDTH_CASES = {
 
 @pytest.mark.parametrize("case_name", list(WIDTH_CASES))
 @pytest.mark.parametrize("path", ["decode-split", "decode-ring", "prefill", "mixed"])
-def test_projection_widths(case_name, path, monkeypatch):
+def test_projection_widths(case_name, path):
     """Projections whose input and output widths differ from h (vectors spanning several
     pool pages, the last one partly used).  x columns past a problem's d_in hold NaN and y
     columns past its d_out must come back unchanged."""
     h, dims = WIDTH_CASES[case_name]
-    if path == "decode-split":
-        monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", "8")
-    elif path == "decode-ring":
-        monkeypatch.setenv("LORA_SPLIT_MAX_PROBS", "0")
+    tuning = {"decode-split": {"split_max_problems": 8},
+              "decode-ring": {"split_max_problems": 0}}.get(path)
     kind = path.split("-")[0]
     if kind == "decode":
         wl = _widths_case(kind, 70, h, dims, 9, [1, 5, 8, 16, 64], T_dec=29)
@@ -348,7 +343,7 @@ def test_projection_widths(case_name, path, monkeypatch):
         wl = _widths_case(kind, 71, h, dims, 6, [8, 16, 128], lens=[1, 130, 17, 64, 0, 5])
     else:
         wl = _widths_case(kind, 72, h, dims, 7, [4, 16, 32], T_dec=11, lens=[70, 3, 129])
-    case = GpuCase(wl)
+    case = GpuCase(wl, tuning=tuning)
     try:
         for i, (l, p) in enumerate(case.dev.problems):
             d_in, d_out = wl.pool.dims(p)
@@ -364,21 +359,20 @@ def test_projection_widths(case_name, path, monkeypatch):
         case.close()
 
 
-@pytest.mark.parametrize("mma_min", ["1", "32", "0"])
+@pytest.mark.parametrize("mma_min", [2, 32, 0])
 @pytest.mark.parametrize("kind", ["prefill", "mixed"])
-def test_projection_widths_tensor_core_tiles(mma_min, kind, monkeypatch):
+def test_projection_widths_tensor_core_tiles(mma_min, kind):
     """Prefill tiles of projections whose widths differ from h (d_in a multiple of 64, d_out
     one of 128): the shrink K loop crosses into an A row's next page block and the expand's
     column slices into a B column's next page block, the last block partly used.  Every
-    segment of >= 2 rows on the tensor cores (1), the default split (32), none (0)."""
-    monkeypatch.setenv("LORA_MMA_MIN_ROWS", mma_min)
+    segment of >= 2 rows on the tensor cores (2), the default split (32), none (0)."""
     dims = [(1024, 256), (1024, 2560), (2560, 1024), (1024, 1024), (3072, 640)]
     lens = [1, 2, 127, 128, 129, 300, 33, 0, 9]
     if kind == "prefill":
         wl = _widths_case(kind, 73, 1024, dims, 8, [1, 8, 16, 32, 64, 128], lens=lens)
     else:
         wl = _widths_case(kind, 74, 1024, dims, 8, [3, 16, 64, 100], T_dec=23, lens=lens)
-    case = GpuCase(wl, y0_zero=True)
+    case = GpuCase(wl, y0_zero=True, tuning={"mma_min_rows": mma_min})
     try:
         for i, (l, p) in enumerate(case.dev.problems):
             case.dev.x[i, :, wl.pool.dims(p)[0]:] = float("nan")
