@@ -86,7 +86,6 @@ KERNEL_SOURCES = {
     "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh"],
     "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
     "delta_fused_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
-    "delta_decode_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
 }
 
 
@@ -272,21 +271,6 @@ def selected_workload(args):
     return wl
 
 
-def tuning_args(args) -> dict:
-    """--tuning k=v,k=v: lora_pool_set_tuning fields (kernel choice and stage shapes)."""
-    out = {}
-    for kv in filter(None, (args.tuning or "").split(",")):
-        k, v = kv.split("=")
-        out[k.strip()] = float(v) if k.strip() == "fused_ring_speed" else int(v)
-    return out
-
-
-def apply_tuning(pool, args):
-    t = tuning_args(args)
-    if t:
-        pool.set_tuning(**t)
-
-
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
@@ -390,7 +374,6 @@ def run_ours(args, rank: int, world: int, local: int):
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
                      p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
-    apply_tuning(pool, args)
     b = wl.batch
     T, S, Td = b.num_tokens, b.num_segments, b.num_decode
     nbytes = lora.workspace_size(pool, T, S + Td)
@@ -418,14 +401,8 @@ def run_ours(args, rank: int, world: int, local: int):
     # launch), else the CUDA-core kernel followed by the tensor-core one (64 a launch)
     ceil = lambda a, c: -(-a // c)  # noqa: E731
     nprob = len(probs)
-    mma_shapes = p.h % 128 == 0 and all(p.dims(j)[0] % 64 == 0 and p.dims(j)[1] % 128 == 0
-                                        for j in range(p.num_proj))
     if b.kind == "decode":
-        # the decode launch (CUDA-core ring beside gathered tensor-core tiles) where the pool's
-        # shapes allow tiles, else the ring kernel alone; up to 256 projections a launch
-        gathered = mma_shapes and p.h // 8 <= 640 and pool.get_tuning()["gather_min_rows"] > 0
-        kname = "delta_decode_kernel" if gathered else "bgmv_ring_kernel"
-        delta_launches = ceil(nprob, lora.LORA_MAX_PROBLEMS_PER_LAUNCH)
+        kname, delta_launches = "bgmv_ring_kernel", ceil(nprob, lora.LORA_MAX_PROBLEMS_PER_LAUNCH)
     elif p.h % 128 == 0 and p.h // 8 <= 640:
         kname, delta_launches = "delta_fused_kernel", ceil(nprob, 64)
     else:
@@ -608,8 +585,7 @@ def run_ours(args, rank: int, world: int, local: int):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config_dict(wl, args), "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "graph": graph, "clocks": clk.summary(), "impl": "ours",
-                "tuning": pool.get_tuning()}
+                "graph": graph, "clocks": clk.summary(), "impl": "ours"}
         if staging is not None:
             line["staging"] = staging
         print(json.dumps(line), flush=True)
@@ -635,7 +611,6 @@ def run_sweep_distinct(args, local: int):
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
                      p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
-    apply_tuning(pool, args)
     T = wl.batch.num_tokens
     nbytes = lora.workspace_size(pool, T, T)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -719,7 +694,7 @@ def run_sweep_threshold(args, local: int):
             for path, mma_min in (("cuda-core", 0), ("tensor-core", max(2, n))):
                 if path == "tensor-core" and n < 2:
                     continue
-                pool.set_tuning(**dict(tuning_args(args), mma_min_rows=mma_min))
+                pool.set_tuning(mma_min_rows=mma_min)
                 for _ in range(max(3, args.warmup)):
                     lora.sgmv(pool, probs, seg_start, seg_adapter, S, T, ws, nbytes, stream)
                 torch.cuda.synchronize()
@@ -969,10 +944,6 @@ def main():
     ap.add_argument("--sweep-threshold", action="store_true",
                     help="instead of the bench line: CUDA-core against tensor-core step time "
                          "over segment length x rank (the FMA / MMA crossover)")
-    ap.add_argument("--tuning", default="",
-                    help="launch tuning of the pool, k=v,...: ring_rows_per_stage, "
-                         "split_max_problems, mma_min_rows, mma_y_stages, fused_ring_speed, "
-                         "gather_min_rows (the defaults otherwise)")
     ap.add_argument("--sweep-ranks", default="8,16,64,128")
     ap.add_argument("--sweep-lengths", default="1,2,4,8,16,32,64,128")
     args = ap.parse_args()

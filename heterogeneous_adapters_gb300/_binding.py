@@ -45,13 +45,12 @@ class lora_pool_desc(ctypes.Structure):
 class lora_tuning(ctypes.Structure):
     _fields_ = [("ring_rows_per_stage", ctypes.c_int32), ("split_max_problems", ctypes.c_int32),
                 ("mma_min_rows", ctypes.c_int32), ("mma_y_stages", ctypes.c_int32),
-                ("fused_ring_speed", ctypes.c_float), ("gather_min_rows", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("fused_ring_speed", ctypes.c_float), ("reserved", ctypes.c_int32 * 3)]
 
 
-# lora_tuning fields and the value that selects a field's default
+# lora_tuning fields and the value that keeps a field's default
 TUNING_KEEP = {"ring_rows_per_stage": 0, "split_max_problems": -1, "mma_min_rows": -1,
-               "mma_y_stages": 0, "fused_ring_speed": 0.0, "gather_min_rows": -1}
+               "mma_y_stages": 0, "fused_ring_speed": 0.0}
 
 
 class lora_problem(ctypes.Structure):

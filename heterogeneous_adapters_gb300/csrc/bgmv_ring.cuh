@@ -60,8 +60,7 @@ struct RingParamsT {
     int32_t nprob;
     int32_t stages;        // ring depth
     int32_t stage_bytes;   // RP * 2h
-    int32_t all_chunks;    // 1: every group's chunks (the launch serves every adapted row);
-                           // 0: only the groups left to the CUDA-core class
+    int32_t pad;
     ProbDesc probs[MAXP];
 };
 using RingParams = RingParamsT<LORA_MAX_PROBLEMS_PER_LAUNCH>;
@@ -322,7 +321,7 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
         const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
         const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
         int32_t* pgbuf = reinterpret_cast<int32_t*>(base + L.pgbuf);
-        const uint32_t total = (uint32_t)(p.all_chunks ? hdr->chunks_all : hdr->counts[2]) * (uint32_t)p.nprob;
+        const uint32_t total = (uint32_t)hdr->counts[2] * (uint32_t)p.nprob;
         const uint32_t row_bytes = (uint32_t)PV.h * 2;
         const uint32_t G = ncta;
         constexpr int kPg = 2 * LORA_MAX_RANK / 32;   // page ids per lane

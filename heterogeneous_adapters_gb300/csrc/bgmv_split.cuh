@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_shrink_kernel(const __gri
     const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
     const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
     float* tbuf = split_t(p, hdr);
-    const int n_chunks = hdr->chunks_all;   // the split path serves every group
+    const int n_chunks = hdr->counts[2];
     const int T = hdr->cap_tokens;
     const PoolView& P = p.pool;
     const int h8 = P.h >> 3, r_max = P.r_max;
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_expand_kernel(const __gri
     const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
     const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
     const float* tbuf = split_t(p, hdr);
-    const int n_chunks = hdr->chunks_all;   // the split path serves every group
+    const int n_chunks = hdr->counts[2];
     const int T = hdr->cap_tokens;
     const PoolView& P = p.pool;
     const int h8 = P.h >> 3, r_max = P.r_max;

@@ -28,11 +28,7 @@ struct WsHeader {
     // (d_in, d_out) streams (d_in + 2 d_out) bf16 per row and (d_in + d_out) per page row
     unsigned long long rows[2];
     unsigned long long page_rows[2];
-    // chunks of every group: the CUDA-core class's counts[2] first, then the chunks of the
-    // groups served as gathered tensor-core tiles (for launches that run every group on the
-    // CUDA-core kernels)
-    int32_t chunks_all;
-    uint32_t pad[45];
+    uint32_t pad[46];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

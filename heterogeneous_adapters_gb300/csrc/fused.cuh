@@ -26,22 +26,10 @@ struct FusedParams {
 };
 static_assert(sizeof(FusedParams) <= 32764, "kernel parameters are limited to 32,764 bytes");
 
-// Decode batches: the CUDA-core ring over the small groups' chunks and the tensor-core body
-// over the gathered tiles of the groups with many tokens (one adapter's rows anywhere in
-// the batch), in one launch of up to 256 projections.
-struct DecodeParams {
-    GatherParams mma;
-    RingParams ring;
-    float ring_speed;
-    unsigned long long row_elems, page_elems;
-};
-static_assert(sizeof(DecodeParams) <= 32764, "kernel parameters are limited to 32,764 bytes");
-
 // CTAs given to the CUDA-core class out of G (0 if it has no work, G if the tensor-core
 // class has none; otherwise at least one each), so that both classes' CTAs need about the
 // same time: G * (wf / speed) / (wf / speed + wm), w the bytes each class streams.
-template <class P>
-__device__ __forceinline__ uint32_t fused_split(const WsHeader* hdr, const P& p, uint32_t G) {
+__device__ __forceinline__ uint32_t fused_split(const WsHeader* hdr, const FusedParams& p, uint32_t G) {
     const float ring_speed = p.ring_speed;
     const unsigned long long wf = hdr->rows[0] * p.row_elems + hdr->page_rows[0] * p.page_elems;
     const unsigned long long wm = hdr->rows[1] * p.row_elems + hdr->page_rows[1] * p.page_elems;
@@ -63,18 +51,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) delta_fused_kernel(const __gri
     if (blockIdx.x < gf)
         ring_cta<NV, CW, RP, W>(p.ring, fused_smem_raw, blockIdx.x, gf);
     else
-        mma_cta<W, false>(p.mma, fused_smem_raw, blockIdx.x - gf, gridDim.x - gf);
-}
-
-template <int NV, int CW, int RP, bool W>
-__global__ void __launch_bounds__(kMmaThreads, 1) delta_decode_kernel(const __grid_constant__ DecodeParams p) {
-    static_assert(CW * 32 + 32 <= kMmaThreads, "ring body must fit the fused CTA");
-    extern __shared__ __align__(1024) unsigned char decode_smem_raw[];
-    const uint32_t gf = fused_split(reinterpret_cast<const WsHeader*>(p.mma.ws), p, gridDim.x);
-    if (blockIdx.x < gf)
-        ring_cta<NV, CW, RP, W>(p.ring, decode_smem_raw, blockIdx.x, gf);
-    else
-        mma_cta<W, true>(p.mma, decode_smem_raw, blockIdx.x - gf, gridDim.x - gf);
+        mma_cta<W>(p.mma, fused_smem_raw, blockIdx.x - gf, gridDim.x - gf);
 }
 
 }  // namespace lora

@@ -61,11 +61,6 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
 // work classes (h <= 5120).
 int mma_min_rows(const lora_pool* pool);
 float default_fused_ring_speed(bool square);
-// decode batches: groups of at least this many rows become gathered tensor-core tiles
-// (0: the pool's shapes or tuning rule them out)
-int gather_min_rows(const lora_pool* pool);
-lora_status run_decode(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                       cudaStream_t stream);
 lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
                     cudaStream_t stream);
 lora_status run_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,

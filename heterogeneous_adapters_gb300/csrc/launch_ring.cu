@@ -86,7 +86,6 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
         prm.ws = reinterpret_cast<char*>(ws);
         prm.t_out = t_out;
         prm.nprob = n;
-        prm.all_chunks = 1;   // alone, this launch serves every group's rows
         for (int32_t i = 0; i < n; ++i) {
             prm.probs[i] = prob_desc(pool, probs[base + i]);
         }

@@ -21,15 +21,6 @@ int mma_min_rows(const lora_pool* pool) {
     return pool->tune.mma_min_rows;
 }
 
-// Decode groups of at least this many rows become gathered tensor-core tiles, served by
-// the decode launch (its CUDA-core body must fit the 384-thread CTA: h <= 5120), under the
-// same shape rules as prefill tiles.
-int gather_min_rows(const lora_pool* pool) {
-    const lora_pool_desc& d = pool->d;
-    if (d.h % kMmaNTile != 0 || !pool->mma_widths || d.h / 8 > 640) return 0;
-    return pool->tune.gather_min_rows;
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 std::mutex g_encode_mu;
@@ -140,56 +131,15 @@ lora_status fill_mma(MmaParams& prm, const lora_pool* pool, const lora_problem* 
     return LORA_OK;
 }
 
-// The gathered-tile body's parameters for problems probs[0..n).
-lora_status fill_gather(GatherParams& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, void* ws,
-                        const MmaConfig& c) {
-    const lora_pool_desc& d = pool->d;
-    memset(&prm, 0, sizeof prm);
-    lora_status st = make_map(&prm.pool_map, d.pages, (uint64_t)d.h, (uint64_t)d.num_pages, (uint64_t)d.h, 1);
-    if (st != LORA_OK) return st;
-    for (int32_t i = 0; i < n; ++i) {
-        const lora_problem& pr = probs[i];
-        const int32_t di = pool->d_in[pr.proj], dq = pool->d_out[pr.proj];
-        prm.probs[i] = prob_desc(pool, pr);
-        prm.blk[i] = pr.layer * pool->units + pool->pre[pr.proj];
-        prm.n_kc[i] = (int16_t)(di / kMmaKChunk);
-        prm.n_nt[i] = (int16_t)(dq / kMmaNTile);
-        prm.pv_in[i] = (uint8_t)vec_pages(di, d.h);
-        prm.pv_out[i] = (uint8_t)vec_pages(dq, d.h);
-    }
-    for (int32_t i = 0; i < n;) {   // runs of problems reading the same x
-        int32_t j = i + 1;
-        while (j < n && probs[j].x == probs[i].x && probs[j].ldx == probs[i].ldx) ++j;
-        for (int32_t k = i; k < j; ++k) {
-            prm.xgrp_off[k] = (uint16_t)(k - i);
-            prm.xgrp_size[k] = (uint16_t)(j - i);
-        }
-        i = j;
-    }
-    prm.pool = view_of(pool);
-    prm.ws = reinterpret_cast<char*>(ws);
-    prm.nprob = n;
-    prm.s1 = c.s1;
-    prm.s2 = c.s2;
-    prm.s3 = c.s3;
-    prm.s1_bytes = c.s1_bytes;
-    prm.s2_bytes = c.s2_bytes;
-    prm.rp_max = c.rp_max;
-    return LORA_OK;
-}
-
-// all_chunks: 1 when the ring body serves every group, 0 when it shares the launch with
-// the tensor-core body (only the CUDA-core class's chunks).
 template <int MAXP>
 void fill_ring(RingParamsT<MAXP>& prm, const lora_pool* pool, const lora_problem* probs, int32_t n, void* ws,
-               float* t_out, int stages, int rows_per_stage, int all_chunks) {
+               float* t_out, int stages, int rows_per_stage) {
     const lora_pool_desc& d = pool->d;
     memset(&prm, 0, sizeof prm);
     prm.pool = view_of(pool);
     prm.ws = reinterpret_cast<char*>(ws);
     prm.t_out = t_out;
     prm.nprob = n;
-    prm.all_chunks = all_chunks;
     prm.stages = stages;
     prm.stage_bytes = rows_per_stage * 2 * d.h;
     for (int32_t i = 0; i < n; ++i) {
@@ -273,7 +223,7 @@ lora_status launch_fused_rp(const lora_pool* pool, const lora_problem* probs, in
         const int32_t n = nprob - base < per ? nprob - base : per;
         st = fill_mma(prm.mma, pool, probs + base, n, T, ws, c);
         if (st != LORA_OK) return st;
-        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, sh.stages, RP, 0);
+        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, sh.stages, RP);
         prm.ring_speed = ring_speed;
         prm.row_elems = prm.page_elems = 0;
         for (int32_t i = base; i < base + n; ++i) {
@@ -307,74 +257,6 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     if (sh.rp == kRingPagesLarge)
         return launch_fused_rp<NV, CW, kRingPagesLarge, false>(pool, probs, nprob, T, ws, di, c, sh, stream);
     return launch_fused_rp<NV, CW, kRingPagesSmall, false>(pool, probs, nprob, T, ws, di, c, sh, stream);
-}
-
-// Decode batches: one launch per batch of up to 256 projections, the ring body over the
-// chunks of the small groups and the tensor-core body over the gathered tiles.
-template <int NV, int CW, int RP, bool W>
-lora_status launch_decode_rp(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                             const DeviceInfo* di, const MmaConfig& c, const RingShape& sh, cudaStream_t stream) {
-    const size_t smem = c.smem > sh.smem ? c.smem : sh.smem;
-    static thread_local DecodeParams prm;
-    static thread_local int attr_dev = -1;
-    static thread_local size_t attr_smem = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    auto kern = delta_decode_kernel<NV, CW, RP, W>;
-    lora_status st;
-    if (attr_dev != dev || attr_smem < smem) {
-        st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (st != LORA_OK) return st;
-        attr_dev = dev;
-        attr_smem = smem;
-    }
-    const int32_t per = batch_size(nprob, kGatherMaxProbs);
-    for (int32_t base = 0; base < nprob; base += per) {
-        const int32_t n = nprob - base < per ? nprob - base : per;
-        st = fill_gather(prm.mma, pool, probs + base, n, ws, c);
-        if (st != LORA_OK) return st;
-        fill_ring(prm.ring, pool, probs + base, n, ws, nullptr, sh.stages, RP, 0);
-        prm.ring_speed = pool->tune.fused_ring_speed;
-        prm.row_elems = prm.page_elems = 0;
-        for (int32_t i = base; i < base + n; ++i) {
-            const int64_t di_ = pool->d_in[probs[i].proj], dq = pool->d_out[probs[i].proj];
-            prm.row_elems += (unsigned long long)(di_ + 2 * dq);
-            prm.page_elems += (unsigned long long)(di_ + dq);
-        }
-        kern<<<di->sm_count, kMmaThreads, smem, stream>>>(prm);
-        st = cuda_status(cudaGetLastError());
-        if (st != LORA_OK) return st;
-    }
-    return LORA_OK;
-}
-
-template <int NV, int CW>
-lora_status launch_decode(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                          cudaStream_t stream) {
-    DeviceInfo* di = nullptr;
-    lora_status st = device_info(&di);
-    if (st != LORA_OK) return st;
-    MmaConfig c;
-    st = mma_config(pool, di->smem_optin, &c);
-    if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW, pool->tune.ring_rows_per_stage);
-    if (sh.stages < 2) return LORA_ETOOBIG;
-    if (!pool->square) {
-        if (sh.rp == kRingPagesLarge)
-            return launch_decode_rp<NV, CW, kRingPagesLarge, true>(pool, probs, nprob, ws, di, c, sh, stream);
-        return launch_decode_rp<NV, CW, kRingPagesSmall, true>(pool, probs, nprob, ws, di, c, sh, stream);
-    }
-    if (sh.rp == kRingPagesLarge)
-        return launch_decode_rp<NV, CW, kRingPagesLarge, false>(pool, probs, nprob, ws, di, c, sh, stream);
-    return launch_decode_rp<NV, CW, kRingPagesSmall, false>(pool, probs, nprob, ws, di, c, sh, stream);
-}
-
-lora_status run_decode(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                       cudaStream_t stream) {
-    const int h8 = pool->d.h / 8;
-    if (h8 <= 256) return launch_decode<1, 8>(pool, probs, nprob, ws, stream);
-    if (h8 <= 512) return launch_decode<2, 8>(pool, probs, nprob, ws, stream);
-    return launch_decode<2, 10>(pool, probs, nprob, ws, stream);
 }
 
 // One launch per batch of projections for both work classes (h <= 5120).

@@ -102,7 +102,6 @@ void default_tuning(const lora_pool* pool, lora_tuning* t) {
     t->mma_min_rows = kMmaDefaultMinRows;
     t->mma_y_stages = 3;
     t->fused_ring_speed = default_fused_ring_speed(pool->square);
-    t->gather_min_rows = kGatherDefaultMinRows;
 }
 
 lora_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
@@ -135,10 +134,6 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     if (st != LORA_OK) return st;
     if (!with_mma && t_out == nullptr && split_fits(pool, nprob, T, ws_bytes))
         return run_split(pool, probs, nprob, ws, stream);
-    // decode batches: the ring over the small groups and tensor-core tiles over the gathered
-    // rows of the adapters with many tokens, in one launch
-    if (!with_mma && t_out == nullptr && gather_min_rows(pool) > 0 && T > 0)
-        return run_decode(pool, probs, nprob, ws, stream);
     // one launch per batch of projections for both work classes
     if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && pool->d.h / 8 <= 640 && T > 0)
         return run_fused(pool, probs, nprob, T, ws, stream);
@@ -257,7 +252,7 @@ lora_status lora_pool_set_tuning(lora_pool* pool, const lora_tuning* t) {
     lora_tuning v;
     default_tuning(pool, &v);
     if (t != nullptr) {
-        if (t->reserved[0] != 0 || t->reserved[1] != 0) return LORA_EINVAL;
+        if (t->reserved[0] != 0 || t->reserved[1] != 0 || t->reserved[2] != 0) return LORA_EINVAL;
         if (t->ring_rows_per_stage != 0 && t->ring_rows_per_stage != 4 && t->ring_rows_per_stage != 8)
             return LORA_EINVAL;
         if (t->split_max_problems < -1 || t->split_max_problems > kSplitMaxProbs) return LORA_EINVAL;
@@ -265,13 +260,11 @@ lora_status lora_pool_set_tuning(lora_pool* pool, const lora_tuning* t) {
         if (t->mma_y_stages != 0 && (t->mma_y_stages < 2 || t->mma_y_stages > 4)) return LORA_EINVAL;
         if (t->fused_ring_speed != 0.f && !(t->fused_ring_speed >= 0.1f && t->fused_ring_speed <= 10.f))
             return LORA_EINVAL;
-        if (t->gather_min_rows < -1 || t->gather_min_rows == 1) return LORA_EINVAL;
         v.ring_rows_per_stage = t->ring_rows_per_stage;
         if (t->split_max_problems >= 0) v.split_max_problems = t->split_max_problems;
         if (t->mma_min_rows >= 0) v.mma_min_rows = t->mma_min_rows;
         if (t->mma_y_stages != 0) v.mma_y_stages = t->mma_y_stages;
         if (t->fused_ring_speed != 0.f) v.fused_ring_speed = t->fused_ring_speed;
-        if (t->gather_min_rows >= 0) v.gather_min_rows = t->gather_min_rows;
     }
     pool->tune = v;
     return LORA_OK;
@@ -341,9 +334,6 @@ static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start,
     sp.Td = Td;
     sp.T = T;
     sp.mma_min = mma_min_rows(pool);
-    // decode batches may list gathered tensor-core tiles (the delta launch decides with the
-    // same rule whether to serve them; a launch that does not serves every chunk instead)
-    sp.gmin = S == 0 ? gather_min_rows(pool) : 0;
     sp.mma_max_rank = kMmaMaxRank;
     sp.L_tokens = T;
     sp.L_segments = S + Td;

@@ -259,22 +259,3 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 }  // namespace lora
-
-namespace lora {
-
-// ---------------------------------------------------------------------------- cp.async (16 bytes)
-// Per-thread asynchronous copy global -> shared of 16 bytes (both addresses 16-byte aligned),
-// cached in L2 only.  Completion is tracked per thread in commit groups; the data written are
-// generic-proxy writes, so a reader in the async proxy (the tensor cores) needs the copies
-// waited (cp_async_wait) and a fence.proxy.async by the writing thread first.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits until at most N of this thread's committed groups are still pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-}  // namespace lora

@@ -15,12 +15,7 @@
 // Outputs (workspace): perm / grp_start / grp_adapter (the grouping), the row list
 // and chunk list of the CUDA-core path (segments shorter than mma_min, at most kChunk
 // rows of one adapter per chunk) and the tile list of the tensor-core path (segments
-// of at least mma_min rows, 128 rows per tile).  With gmin > 0 (decode batches), a group
-// whose CUDA-core rows number at least gmin is also listed as gathered tiles of up to 128
-// of those rows (an adapter serving many tokens of a decode batch is a small dense GEMM:
-// "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels work", SGMV
-// reuses an adapter's weights across its tokens); its chunks then follow every other
-// group's chunks, for launches that serve all rows on the CUDA-core kernels.
+// of at least mma_min rows, 128 rows per tile).
 #pragma once
 #include "common.cuh"
 
@@ -44,8 +39,7 @@ struct SegParams {
     int32_t L_tokens;  // the (max_tokens, max_segments) that L was computed from
     int32_t L_segments;
     int32_t smem_segs; // > 0: the per-segment scratch arrays live in dynamic shared memory
-    int32_t gmin;      // > 0: groups of at least this many CUDA-core rows (and rank <=
-                       // mma_max_rank) also become gathered tensor-core tiles; 0: none
+    int32_t pad;
 };
 
 // Dynamic shared memory of the grouping kernel when the per-segment arrays fit there
@@ -260,71 +254,46 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
         if (g < G) gorder[rank] = g;
     }
     __syncthreads();
-    // Pass A: the chunks of the groups left to the CUDA-core class, and the gathered tiles
-    // of the groups with at least gmin CUDA-core rows (row0 = the tile's first position in
-    // the CUDA-core row list), listed after the contiguous tiles.  Pass B: the chunks of the
-    // gathered groups too, after all the others, for launches that serve every group on the
-    // CUDA-core kernels.
-    auto gathered = [&](int cnt, int r) { return p.gmin > 0 && cnt >= p.gmin && r <= p.mma_max_rank; };
     int carry_c = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int i0 = 0; i0 < G; i0 += nthr) {
-            const int i = i0 + tid;
-            const int g = i < G ? gorder[i] : 0;
-            int first = 0, cnt = 0, a = 0, r = 0;
-            if (i < G) {
-                first = fpos[gfirst[g]];
-                cnt = fpos[gfirst[g + 1]] - first;
-                a = grp_adapter[g];
-                r = P.ranks[a];
-            }
-            const bool gat = i < G && gathered(cnt, r);
-            const int nch = (pass == 0) != gat ? (cnt + kChunk - 1) / kChunk : 0;
-            const int ngt = pass == 0 && gat ? (cnt + kTileRows - 1) / kTileRows : 0;
-            int tot, tot_t;
-            const int base = block_exclusive_scan(nch, scan_smem, &tot) + carry_c;
-            const int tbase = block_exclusive_scan(ngt, scan_smem, &tot_t) + carry_t;
-            if (i < G) {
-                const float sc = P.scales[a];
-                const long long ptb = P.pt_off[a];
-                if (nch > 0 && pass == 0) {   // rows read and written, plus the pages once per chunk
-                    atomicAdd(&weight_s[0], (unsigned long long)cnt);
-                    atomicAdd(&weight_s[2], (unsigned long long)r * nch);
-                }
-                for (int c = 0; c < nch; ++c) {
-                    Chunk ch;
-                    ch.adapter = a;
-                    ch.begin = first + c * kChunk;
-                    ch.count = min(kChunk, cnt - c * kChunk);
-                    ch.rank = r;
-                    ch.scale = sc;
-                    ch.pt_base = ptb;
-                    ch.pad = 0;
-                    for (int t = 0; t < kChunk; ++t) ch.rows[t] = t < ch.count ? fma_rows[ch.begin + t] : 0;
-                    chunks[base + c] = ch;
-                }
-                if (ngt > 0) {   // x read + y read and written, plus the pages once per tile
-                    atomicAdd(&weight_s[1], (unsigned long long)cnt);
-                    atomicAdd(&weight_s[3], (unsigned long long)r * ngt);
-                }
-                for (int k = 0; k < ngt; ++k) {
-                    Tile tl;
-                    tl.adapter = a;
-                    tl.row0 = first + k * kTileRows;
-                    tl.rows = min(kTileRows, cnt - k * kTileRows);
-                    tl.rank = r;
-                    tiles[tbase + k] = tl;
-                }
-            }
-            carry_c += tot;
-            carry_t += tot_t;
+    for (int i0 = 0; i0 < G; i0 += nthr) {
+        const int i = i0 + tid;
+        const int g = i < G ? gorder[i] : 0;
+        int first = 0, cnt = 0;
+        if (i < G) {
+            first = fpos[gfirst[g]];
+            cnt = fpos[gfirst[g + 1]] - first;
         }
-        if (pass == 0 && tid == 0) hdr->counts[2] = carry_c;
+        const int nch = (cnt + kChunk - 1) / kChunk;
+        int tot;
+        const int base = block_exclusive_scan(nch, scan_smem, &tot) + carry_c;
+        if (i < G) {
+            const int a = grp_adapter[g];
+            const int r = P.ranks[a];
+            const float sc = P.scales[a];
+            const long long ptb = P.pt_off[a];
+            if (nch > 0) {   // rows read and written, plus the pages once per chunk
+                atomicAdd(&weight_s[0], (unsigned long long)cnt);
+                atomicAdd(&weight_s[2], (unsigned long long)r * nch);
+            }
+            for (int c = 0; c < nch; ++c) {
+                Chunk ch;
+                ch.adapter = a;
+                ch.begin = first + c * kChunk;
+                ch.count = min(kChunk, cnt - c * kChunk);
+                ch.rank = r;
+                ch.scale = sc;
+                ch.pt_base = ptb;
+                ch.pad = 0;
+                for (int t = 0; t < kChunk; ++t) ch.rows[t] = t < ch.count ? fma_rows[ch.begin + t] : 0;
+                chunks[base + c] = ch;
+            }
+        }
+        carry_c += tot;
     }
     if (tid == 0) {
         hdr->counts[0] = carry_pos;
         hdr->counts[1] = G;
-        hdr->chunks_all = carry_c;
+        hdr->counts[2] = carry_c;
         hdr->counts[3] = carry_t;
         hdr->work_counter = 0;
         hdr->work_counter2 = 0;

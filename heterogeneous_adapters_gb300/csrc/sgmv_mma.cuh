@@ -38,12 +38,10 @@ constexpr int kMmaEpiWarps = 8;
 constexpr int kMmaMaxProbs = 64;            // problems per launch (3 tensor maps each)
 constexpr int kMmaMaxRank = 128;
 constexpr int kMmaDefaultMinRows = 32;      // segments of at least this many rows take the tiles
-constexpr int kGatherDefaultMinRows = 8;    // decode adapters with at least this many tokens too
 constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 bytes)
 constexpr int kMmaNTile = 128;              // y columns per expand slice
 constexpr int kMmaRowBlock = 32;            // rows per x / y TMA box
 constexpr int kMmaMaxStages = 8;
-constexpr int kMmaYSlot = 32768;            // bytes of one y stage (128 rows x 128 columns)
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: D1 (shrink, fp32) 0..127, D2 (expand, fp32, two buffers) 128..383,
 // T_hi and T_lo (bf16 pairs, K / 2 columns each) 384..447 and 448..511.
@@ -71,29 +69,6 @@ struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
     uint8_t xgrp_size[kMmaMaxProbs];         // size of that group
 };
 
-// The tensor-core body over gathered tiles (decode groups: the rows of one adapter anywhere
-// in the batch).  No x / y tensor maps: the rows are copied through the problems' pointers,
-// so a launch takes as many projections as the CUDA-core ring kernel.
-constexpr int kGatherMaxProbs = LORA_MAX_PROBLEMS_PER_LAUNCH;
-struct GatherParams {
-    CUtensorMap pool_map;                    // {h, num_pages}, box {64, 1}, 128B swizzle
-    ProbDesc probs[kGatherMaxProbs];         // x, y and their strides
-    int32_t blk[kGatherMaxProbs];
-    int16_t n_kc[kGatherMaxProbs];
-    int16_t n_nt[kGatherMaxProbs];
-    uint8_t pv_in[kGatherMaxProbs];
-    uint8_t pv_out[kGatherMaxProbs];
-    uint16_t xgrp_off[kGatherMaxProbs];
-    uint16_t xgrp_size[kGatherMaxProbs];
-    PoolView pool;
-    char* ws;
-    int32_t nprob;
-    int32_t s1, s2, s3;
-    int32_t s1_bytes, s2_bytes;
-    int32_t rp_max;
-    int32_t pad;
-};
-
 struct MmaSmem {
     uint32_t ring1, ring2, ring3, full1, empty1, full2, empty2, full3, empty3, d1_full, t_ready, d2_full,
         d2_empty, final_bar, tmem_slot, total;
@@ -104,7 +79,7 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int s1, int s1_bytes, int s2,
     uint32_t o = 0;
     L.ring1 = o;     o += (uint32_t)s1 * s1_bytes;
     L.ring2 = o;     o += (uint32_t)s2 * s2_bytes;
-    L.ring3 = o;     o += (uint32_t)s3 * kMmaYSlot;
+    L.ring3 = o;     o += (uint32_t)s3 * 32768;
     L.full1 = o;     o += kMmaMaxStages * 8;
     L.empty1 = o;    o += kMmaMaxStages * 8;
     L.full2 = o;     o += kMmaMaxStages * 8;
@@ -133,15 +108,6 @@ struct MmaItem {
     int pv_in;        // page blocks of an A row
     long long blk;    // first page-table entry of the A block (B block follows at +r pv_in)
     bool ok;
-    // Staging.  A small tile packs several shrink K chunks, B^T slices or y slices into one
-    // ring stage, so that the same bytes travel in fewer round trips (a tile of a few rows
-    // is bound by the latency of its 64-column chunks and 128-column slices, not by bytes).
-    int xb;           // x bytes of one shrink chunk: rows rounded up to whole row blocks
-    int cb;           // bytes of one shrink chunk in a stage: its x rows, then its A rows
-    int cps;          // shrink chunks per stage
-    int sps;          // B^T slices per stage
-    int yb;           // bytes of one y slice in a stage (two 64-column halves of xb each)
-    int yps;          // y slices per stage
 };
 
 // Item order.  Projections that read the same x (consecutive problems with the same input,
@@ -152,11 +118,8 @@ struct MmaItem {
 // tiles of one segment (which read the same adapter pages) run side by side.
 // W: the launch has projections whose widths differ from h; W = false compiles the h x h
 // case (one page block per vector, h / 64 chunks and h / 128 slices per item).
-// G: the tiles are gathered rows (row0 indexes the grouping's row list; rows are x / y rows
-// anywhere in the batch), whose x and y rows are copied row by row; otherwise a tile is
-// rows [row0, row0 + rows) of the batch, moved in 32-row tensor-map boxes.
-template <bool W, bool G, class P>
-__device__ __forceinline__ MmaItem mma_item(const P& p, const Tile* tiles, int n_tiles, uint32_t item,
+template <bool W>
+__device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tiles, int n_tiles, uint32_t item,
                                             int lane) {
     MmaItem it;
     const uint32_t p0 = item / (uint32_t)n_tiles;          // projection-major position
@@ -177,86 +140,34 @@ __device__ __forceinline__ MmaItem mma_item(const P& p, const Tile* tiles, int n
         bad |= (page < 0 || page >= p.pool.num_pages);
     }
     it.ok = !__any_sync(0xffffffffu, bad);
-    // x rows held per chunk: whole 8-row swizzle atoms (gathered) or 32-row boxes
-    const int xrows = G ? (it.tile.rows + 7) / 8 * 8
-                        : (it.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock * kMmaRowBlock;
-    it.xb = xrows * 128;
-    it.cb = it.xb + it.rp * 128;
-    it.cps = max(1, p.s1_bytes / it.cb);
-    it.sps = max(1, p.s2_bytes / (it.rp * 256));
-    it.yb = xrows * 256;
-    it.yps = max(1, kMmaYSlot / it.yb);
     return it;
 }
 
 // The next processable item at or after `item` (skipping items with bad pages), or total.
-template <bool W, bool G, class P>
-__device__ __forceinline__ uint32_t mma_next_ok(const P& p, const Tile* tiles, int n_tiles, uint32_t item,
-                                                uint32_t total, uint32_t ncta, int lane, MmaItem& mi) {
+template <bool W>
+__device__ __forceinline__ uint32_t mma_next_ok(const MmaParams& p, const Tile* tiles, int n_tiles,
+                                                uint32_t item, uint32_t total, uint32_t ncta, int lane,
+                                                MmaItem& mi) {
     for (; item < total; item += ncta) {
-        mi = mma_item<W, G>(p, tiles, n_tiles, item, lane);
+        mi = mma_item<W>(p, tiles, n_tiles, item, lane);
         if (mi.ok) return item;
     }
     return total;
 }
 
-// Issue the four shrink MMAs of one K chunk (x rows at shared address xa, A rows at aa) into D1.
-__device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t xa, uint32_t aa, uint32_t idesc, int kc) {
+// Issue the four shrink MMAs of one K chunk (stage at shared address st) into D1.
+__device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t st, uint32_t idesc, int kc) {
 #pragma unroll
     for (int kk = 0; kk < kMmaKChunk / 16; ++kk) {
-        const uint64_t da = smem_desc(xa + kk * 32, 16, 1024, 2);
-        const uint64_t db = smem_desc(aa + kk * 32, 16, 1024, 2);
+        const uint64_t da = smem_desc(st + kk * 32, 16, 1024, 2);
+        const uint64_t db = smem_desc(st + 16384 + kk * 32, 16, 1024, 2);
         tc_mma_f16(tmem + kD1Col, da, db, idesc, (kc | kk) != 0);
     }
 }
 
-// The shrink MMAs of one stage: chunks kc0 .. kc0 + nch - 1 of item mi.
-__device__ __forceinline__ void mma_shrink_stage(uint32_t tmem, uint32_t st, const MmaItem& mi, uint32_t idesc,
-                                                 int kc0) {
-    const int nch = min(mi.cps, mi.n_kc - kc0);
-    for (int c = 0; c < nch; ++c)
-        mma_shrink_chunk(tmem, st + c * mi.cb, st + c * mi.cb + mi.xb, idesc, kc0 + c);
-}
-
-// Rows of a gathered tile held by lane `lane`: rows lane, lane + 32, lane + 64, lane + 96.
-__device__ __forceinline__ void gather_rows(const int32_t* rowlist, const Tile& t, int lane, int (&rid)[4]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int i = lane + 32 * q;
-        rid[q] = i < t.rows ? rowlist[t.row0 + i] : 0;
-    }
-}
-
-// Signal the oldest stage whose row copies this warp has issued once at most `lag` newer
-// ones are pending: the copies are waited, then made visible to the tensor cores' proxy
-// (fence_async) and announced on that stage's full barrier.
-template <int LAG, bool FENCE>
-__device__ __forceinline__ void gather_signal(uint32_t full_base, uint32_t it, uint32_t S, int& pend, int lane) {
-    cp_async_commit();
-    ++pend;
-    if (pend > LAG) {
-        cp_async_wait<LAG>();
-        if (FENCE) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_base + ((it - LAG) % S) * 8);
-        --pend;
-    }
-}
-
-// Every pending stage of this warp: wait all its copies and announce them.
-template <bool FENCE>
-__device__ __forceinline__ void gather_flush(uint32_t full_base, uint32_t it, uint32_t S, int& pend, int lane) {
-    cp_async_wait<0>();
-    if (FENCE) fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0)
-        for (uint32_t k = it - pend; k < it; ++k) mbar_arrive(full_base + (k % S) * 8);
-    pend = 0;
-}
-
 // One CTA of the tensor-core kernel: CTA `cta` of `ncta` taking part (all kMmaThreads threads).
-template <bool W, bool G, class P>
-__device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uint32_t cta, uint32_t ncta) {
+template <bool W>
+__device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_raw, uint32_t cta, uint32_t ncta) {
     // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -266,7 +177,6 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
     const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
     const Tile* tiles = reinterpret_cast<const Tile*>(p.ws + WL.tiles);
-    const int32_t* rowlist = reinterpret_cast<const int32_t*>(p.ws + WL.fma_rows);   // gathered tiles
     const int n_tiles = hdr->counts[3];
     const uint32_t total = (uint32_t)n_tiles * (uint32_t)p.nprob;
     const int h = p.pool.h;
@@ -277,8 +187,7 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
 
     if (tid == 0) {
         for (uint32_t s = 0; s < S1; ++s) {
-            // gathered tiles: the A rows' bytes (expect_tx) and the x rows' copies (one arrive)
-            mbar_init(bar(L.full1 + s * 8), G ? 2 : 1);
+            mbar_init(bar(L.full1 + s * 8), 1);
             mbar_init(bar(L.empty1 + s * 8), 1);
         }
         for (uint32_t s = 0; s < S2; ++s) {
@@ -312,88 +221,57 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
         // ------------------------------------------------------------------ shrink producer
         if (lane == 0) prefetch_tmap(&p.pool_map);
         uint32_t it = 0;
-        int pend = 0;   // gathered tiles: stages whose x copies are not yet announced
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W, G>(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) {
                 if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
                 continue;
             }
-            const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0, rows = mi.tile.rows;
-            const int nblk = (rows + kMmaRowBlock - 1) / kMmaRowBlock;
-            int rid[4];
-            if (G) gather_rows(rowlist, mi.tile, lane, rid);
+            const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
+            const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
+            const void* xmap = &p.x_map[mi.pr];
             int pga[4];
-            for (int kc0 = 0; kc0 < mi.n_kc; kc0 += mi.cps) {
-                const int nch = min(mi.cps, mi.n_kc - kc0);
+            for (int kc = 0; kc < mi.n_kc; ++kc) {
+                if (W ? kc % kc_pg == 0 : kc == 0) {   // page ids of the A rows' page block kc / kc_pg
+                    const long long b0 = mi.blk + (W ? (long long)(kc / kc_pg) * r : 0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = lane + 32 * q;
+                        pga[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
+                    }
+                }
+                const int kcol = (W ? kc % kc_pg : kc) * kMmaKChunk;   // column within the A page
                 const uint32_t s = it % S1;
                 if (!mbar_wait(bar(L.empty1 + s * 8), ((it / S1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
                 const uint32_t st = bar(L.ring1 + s * p.s1_bytes);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(bar(L.full1 + s * 8),
-                                          (uint32_t)nch * (G ? rp * 128 : nblk * kMmaRowBlock * 128 + rp * 128));
+                    mbar_arrive_expect_tx(bar(L.full1 + s * 8), nblk * kMmaRowBlock * 128 + rp * 128);
                 __syncwarp();
-                for (int c = 0; c < nch; ++c) {
-                    const int kc = kc0 + c;
-                    if (W ? kc % kc_pg == 0 : kc == 0) {   // page ids of the A rows' page block kc / kc_pg
-                        const long long b0 = mi.blk + (W ? (long long)(kc / kc_pg) * r : 0);
+                if (lane < nblk)
+                    tma_load_2d(st + lane * kMmaRowBlock * 128, xmap, kc * kMmaKChunk, row0 + lane * kMmaRowBlock,
+                                bar(L.full1 + s * 8));
+                // A rows: groups of four real rows with one gather (lane 4k issues rows
+                // 4k..4k+3, page ids taken from the next three lanes); padding rows (>= r)
+                // and a ragged last group one row each, read out of range (zeros)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int j = lane + 32 * q;
-                            pga[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
+                for (int q = 0; q < 4; ++q) {
+                    const int j = lane + 32 * q;
+                    const int p1 = __shfl_down_sync(0xffffffffu, pga[q], 1);
+                    const int p2 = __shfl_down_sync(0xffffffffu, pga[q], 2);
+                    const int p3 = __shfl_down_sync(0xffffffffu, pga[q], 3);
+                    if (j < rp) {
+                        if ((j | 3) < r) {
+                            if ((j & 3) == 0)
+                                tma_gather4(st + 16384 + j * 128, &p.pool_map, kcol, pga[q], p1, p2, p3,
+                                            bar(L.full1 + s * 8));
+                        } else {
+                            tma_load_2d(st + 16384 + j * 128, &p.pool_map, kcol, pga[q], bar(L.full1 + s * 8));
                         }
                     }
-                    const int kcol = (W ? kc % kc_pg : kc) * kMmaKChunk;   // column within the A page
-                    const uint32_t cst = st + c * mi.cb;
-                    if constexpr (G) {
-                        // x rows: 8 pieces of 16 bytes per row; piece e = lane + 32 j is piece
-                        // e % 8 of row e / 8, written where the 128-byte swizzle puts it
-                        const ProbDesc& pd = p.probs[mi.pr];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            for (int jj = 0; jj < 8; ++jj) {
-                                const int e = lane + 32 * (8 * q + jj);
-                                if (32 * (8 * q + jj) >= rows * 8) break;
-                                const int i = e >> 3, u = e & 7;
-                                const int src = __shfl_sync(0xffffffffu, rid[q], i & 31);
-                                if (i < rows)
-                                    cp_async16(cst + i * 128 + ((u ^ (i & 7)) << 4),
-                                               pd.x + (long long)src * pd.ldx + kc * kMmaKChunk + u * 8);
-                            }
-                        }
-                    } else {
-                        if (lane < nblk)
-                            tma_load_2d(cst + lane * kMmaRowBlock * 128, &p.x_map[mi.pr], kc * kMmaKChunk,
-                                        row0 + lane * kMmaRowBlock, bar(L.full1 + s * 8));
-                    }
-                    // A rows: groups of four real rows with one gather (lane 4k issues rows
-                    // 4k..4k+3, page ids taken from the next three lanes); padding rows (>= r)
-                    // and a ragged last group one row each, read out of range (zeros)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int j = lane + 32 * q;
-                        const int p1 = __shfl_down_sync(0xffffffffu, pga[q], 1);
-                        const int p2 = __shfl_down_sync(0xffffffffu, pga[q], 2);
-                        const int p3 = __shfl_down_sync(0xffffffffu, pga[q], 3);
-                        if (j < rp) {
-                            if ((j | 3) < r) {
-                                if ((j & 3) == 0)
-                                    tma_gather4(cst + mi.xb + j * 128, &p.pool_map, kcol, pga[q], p1, p2, p3,
-                                                bar(L.full1 + s * 8));
-                            } else {
-                                tma_load_2d(cst + mi.xb + j * 128, &p.pool_map, kcol, pga[q], bar(L.full1 + s * 8));
-                            }
-                        }
-                    }
-                }
-                if constexpr (G) {
-                    if (S1 >= 3) gather_signal<2, true>(bar(L.full1), it, S1, pend, lane);
-                    else gather_signal<1, true>(bar(L.full1), it, S1, pend, lane);
                 }
                 ++it;
             }
         }
-        if (G) gather_flush<true>(bar(L.full1), it, S1, pend, lane);
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
         if (lane == 0) {   // let every stage this warp filled land before the CTA can exit
             for (uint32_t k = it > S1 ? it - S1 : 0; k < it; ++k)
@@ -403,54 +281,47 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
         // ------------------------------------------------------------------ B^T producer
         uint32_t it2 = 0;
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W, G>(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
             const int r = mi.tile.rank, rp = mi.rp;
             int pgb[4];
-            for (int nt0 = 0; nt0 < mi.n_nt; nt0 += mi.sps) {
-                const int nsl = min(mi.sps, mi.n_nt - nt0);
-                // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
-                // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8);
-                // the stage holds nsl slices of rp * 256 bytes
-                const uint32_t s = it2 % S2;
-                if (!mbar_wait(bar(L.empty2 + s * 8), ((it2 / S2) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                const uint32_t st = bar(L.ring2 + s * p.s2_bytes);
-                if (lane == 0) mbar_arrive_expect_tx(bar(L.full2 + s * 8), (uint32_t)nsl * rp * 256);
-                __syncwarp();
-                for (int c = 0; c < nsl; ++c) {
-                    const int nt = nt0 + c;
-                    if (W ? nt % nt_pg == 0 : nt == 0) {   // page ids of the B columns' page block nt / nt_pg
-                        const long long b0 = mi.blk + (W ? (long long)(mi.pv_in + nt / nt_pg) * r : (long long)r);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int j = lane + 32 * q;
-                            pgb[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
-                        }
-                    }
-                    const int ncol = (W ? nt % nt_pg : nt) * kMmaNTile;   // column within the B page
-                    const uint32_t sst = st + c * rp * 256;
+            for (int nt = 0; nt < mi.n_nt; ++nt, ++it2) {
+                if (W ? nt % nt_pg == 0 : nt == 0) {   // page ids of the B columns' page block nt / nt_pg
+                    const long long b0 = mi.blk + (W ? (long long)(mi.pv_in + nt / nt_pg) * r : (long long)r);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int j = lane + 32 * q;
-                        const int p1 = __shfl_down_sync(0xffffffffu, pgb[q], 1);
-                        const int p2 = __shfl_down_sync(0xffffffffu, pgb[q], 2);
-                        const int p3 = __shfl_down_sync(0xffffffffu, pgb[q], 3);
-                        if (j < rp) {
-                            const uint32_t dst = sst + (j >> 3) * 2048 + (j & 7) * 128;
-                            if ((j | 3) < r) {
-                                if ((j & 3) == 0) {
-                                    tma_gather4(dst, &p.pool_map, ncol, pgb[q], p1, p2, p3, bar(L.full2 + s * 8));
-                                    tma_gather4(dst + 1024, &p.pool_map, ncol + 64, pgb[q], p1, p2, p3,
-                                                bar(L.full2 + s * 8));
-                                }
-                            } else {
-                                tma_load_2d(dst, &p.pool_map, ncol, pgb[q], bar(L.full2 + s * 8));
-                                tma_load_2d(dst + 1024, &p.pool_map, ncol + 64, pgb[q], bar(L.full2 + s * 8));
+                        pgb[q] = j < r ? p.pool.pt[b0 + j] : (int)p.pool.num_pages;
+                    }
+                }
+                const int ncol = (W ? nt % nt_pg : nt) * kMmaNTile;   // column within the B page
+                // B^T slice: K rows = pages j, N = 128 columns as two 64-column atoms;
+                // atom (j / 8, nb) at (j / 8) * 2048 + nb * 1024, row j % 8 at +128 (j % 8)
+                const uint32_t s = it2 % S2;
+                if (!mbar_wait(bar(L.empty2 + s * 8), ((it2 / S2) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
+                const uint32_t st = bar(L.ring2 + s * p.s2_bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar(L.full2 + s * 8), rp * 256);
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = lane + 32 * q;
+                    const int p1 = __shfl_down_sync(0xffffffffu, pgb[q], 1);
+                    const int p2 = __shfl_down_sync(0xffffffffu, pgb[q], 2);
+                    const int p3 = __shfl_down_sync(0xffffffffu, pgb[q], 3);
+                    if (j < rp) {
+                        const uint32_t dst = st + (j >> 3) * 2048 + (j & 7) * 128;
+                        if ((j | 3) < r) {
+                            if ((j & 3) == 0) {
+                                tma_gather4(dst, &p.pool_map, ncol, pgb[q], p1, p2, p3, bar(L.full2 + s * 8));
+                                tma_gather4(dst + 1024, &p.pool_map, ncol + 64, pgb[q], p1, p2, p3,
+                                            bar(L.full2 + s * 8));
                             }
+                        } else {
+                            tma_load_2d(dst, &p.pool_map, ncol, pgb[q], bar(L.full2 + s * 8));
+                            tma_load_2d(dst + 1024, &p.pool_map, ncol + 64, pgb[q], bar(L.full2 + s * 8));
                         }
                     }
                 }
-                ++it2;
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
@@ -461,59 +332,26 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
     } else if (warp == 3) {
         // ------------------------------------------------------------------ y producer
         uint32_t it3 = 0;
-        int pend = 0;   // gathered tiles: stages whose y copies are not yet announced
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W, G>(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
-            const int row0 = mi.tile.row0, rows = mi.tile.rows;
-            const int nblk = (rows + kMmaRowBlock - 1) / kMmaRowBlock;
-            int rid[4];
-            if (G) gather_rows(rowlist, mi.tile, lane, rid);
-            for (int nt0 = 0; nt0 < mi.n_nt; nt0 += mi.yps) {
-                const int nsl = min(mi.yps, mi.n_nt - nt0);
-                // y slice: half hf (64 columns) at hf * yb / 2, row m at + m * 128 (128-byte
-                // swizzle); the stage holds nsl slices of yb bytes
+            const int row0 = mi.tile.row0;
+            const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
+            const void* ymap = &p.y_map[mi.pr];
+            for (int nt = 0; nt < mi.n_nt; ++nt, ++it3) {
+                // y tile: half hf (64 columns) at hf * 16 KB, 32-row block b at + b * 4 KB
                 const uint32_t s = it3 % S3;
                 if (!mbar_wait(bar(L.empty3 + s * 8), ((it3 / S3) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
-                const uint32_t st = bar(L.ring3 + s * kMmaYSlot);
-                if constexpr (G) {
-                    const ProbDesc& pd = p.probs[mi.pr];
-                    for (int c = 0; c < nsl; ++c) {
-                        const int col = (nt0 + c) * kMmaNTile;
-                        // 16 pieces of 16 bytes per row: piece e = lane + 32 j is piece e % 8 of
-                        // half (e / 8) % 2 of row e / 16
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            for (int jj = 0; jj < 16; ++jj) {
-                                const int e = lane + 32 * (16 * q + jj);
-                                if (32 * (16 * q + jj) >= rows * 16) break;
-                                const int i = e >> 4, hf = (e >> 3) & 1, u = e & 7;
-                                const int src = __shfl_sync(0xffffffffu, rid[q], i & 31);
-                                if (i < rows)
-                                    cp_async16(st + c * mi.yb + hf * (mi.yb / 2) + i * 128 + ((u ^ (i & 7)) << 4),
-                                               pd.y + (long long)src * pd.ldy + col + hf * 64 + u * 8);
-                            }
-                        }
-                    }
-                    // the epilogue reads the rows with ordinary loads: no proxy fence
-                    if (S3 >= 3) gather_signal<2, false>(bar(L.full3), it3, S3, pend, lane);
-                    else gather_signal<1, false>(bar(L.full3), it3, S3, pend, lane);
-                } else {
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(bar(L.full3 + s * 8), (uint32_t)nsl * 2 * nblk * kMmaRowBlock * 128);
-                    __syncwarp();
-                    for (int c = 0; c < nsl; ++c) {
-                        if (lane < 2 * nblk) {
-                            const int hf = lane & 1, b = lane >> 1;
-                            tma_load_2d(st + c * mi.yb + hf * (mi.yb / 2) + b * kMmaRowBlock * 128, &p.y_map[mi.pr],
-                                        (nt0 + c) * kMmaNTile + hf * 64, row0 + b * kMmaRowBlock, bar(L.full3 + s * 8));
-                        }
-                    }
+                const uint32_t st = bar(L.ring3 + s * 32768);
+                if (lane == 0) mbar_arrive_expect_tx(bar(L.full3 + s * 8), 2 * nblk * kMmaRowBlock * 128);
+                __syncwarp();
+                if (lane < 2 * nblk) {
+                    const int hf = lane & 1, b = lane >> 1;
+                    tma_load_2d(st + hf * 16384 + b * kMmaRowBlock * 128, ymap, nt * kMmaNTile + hf * 64,
+                                row0 + b * kMmaRowBlock, bar(L.full3 + s * 8));
                 }
-                ++it3;
             }
         }
-        if (G) gather_flush<false>(bar(L.full3), it3, S3, pend, lane);
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
         if (lane == 0) {
             for (uint32_t k = it3 > S3 ? it3 - S3 : 0; k < it3; ++k)
@@ -523,17 +361,17 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
         // ------------------------------------------------------------------ MMA issuer
         uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0;
         MmaItem cur, nxt;
-        uint32_t item = mma_next_ok<W, G>(p, tiles, n_tiles, cta, total, ncta, lane, cur);
+        uint32_t item = mma_next_ok<W>(p, tiles, n_tiles, cta, total, ncta, lane, cur);
         int kc_next = 0;   // shrink chunks of `nxt` already issued
         // shrink of the first tile
         if (item < total) {
             const uint32_t id_shrink = idesc_bf16(128, cur.rp, 0, 0);
-            for (int kc0 = 0; kc0 < cur.n_kc && ok; kc0 += cur.cps, ++it1) {
+            for (int kc = 0; kc < cur.n_kc && ok; ++kc, ++it1) {
                 const uint32_t s = it1 % S1;
                 if (!mbar_wait(bar(L.full1 + s * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    mma_shrink_stage(tmem, bar(L.ring1 + s * p.s1_bytes), cur, id_shrink, kc0);
+                    mma_shrink_chunk(tmem, bar(L.ring1 + s * p.s1_bytes), id_shrink, kc);
                     tc_commit(bar(L.empty1 + s * 8));
                 }
                 __syncwarp();
@@ -542,7 +380,7 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
             __syncwarp();
         }
         while (item < total && ok) {
-            const uint32_t next_item = mma_next_ok<W, G>(p, tiles, n_tiles, item + ncta, total, ncta, lane, nxt);
+            const uint32_t next_item = mma_next_ok<W>(p, tiles, n_tiles, item + ncta, total, ncta, lane, nxt);
             const bool has_next = next_item < total;
             const uint32_t id_next = has_next ? idesc_bf16(128, nxt.rp, 0, 0) : 0;
             kc_next = 0;
@@ -552,50 +390,47 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
             tc_fence_after();
             const int rp = cur.rp;
             const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
-            for (int nt = 0; nt < cur.n_nt && ok; ++nt, ++g) {
-                const int c2 = nt % cur.sps;
-                const bool last2 = c2 == cur.sps - 1 || nt == cur.n_nt - 1;
+            for (int nt = 0; nt < cur.n_nt && ok; ++nt, ++g, ++it2) {
                 const uint32_t s = it2 % S2;
                 const uint32_t b = g & 1;
-                if (c2 == 0 && !mbar_wait(bar(L.full2 + s * 8), (it2 / S2) & 1, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(bar(L.full2 + s * 8), (it2 / S2) & 1, kWaitLimitNs)) { ok = false; break; }
                 if (!mbar_wait(bar(L.d2_empty + b * 8), ((g >> 1) & 1) ^ 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t st = bar(L.ring2 + s * p.s2_bytes) + c2 * rp * 256;
+                    const uint32_t st = bar(L.ring2 + s * p.s2_bytes);
                     const uint32_t d2 = tmem + kD2Col + b * kMmaNTile;
                     for (int ks = 0; ks < rp / 16; ++ks) {
                         const uint64_t dbt = smem_desc(st + ks * 4096, 1024, 2048, 2);
                         tc_mma_f16_ts(d2, tmem + kThiCol + ks * 8, dbt, id_expand, ks != 0);
                         tc_mma_f16_ts(d2, tmem + kTloCol + ks * 8, dbt, id_expand, 1);
                     }
-                    if (last2) tc_commit(bar(L.empty2 + s * 8));
+                    tc_commit(bar(L.empty2 + s * 8));
                     tc_commit(bar(L.d2_full + b * 8));
                 }
                 __syncwarp();
-                if (last2) ++it2;
-                // the next tile's shrink stages that have already landed (a test, not a
+                // the next tile's shrink chunks that have already landed (a test, not a
                 // wait: a suspending wait here would hold the expand back for the whole shrink)
                 while (has_next && kc_next < nxt.n_kc) {
                     const uint32_t s1 = it1 % S1;
                     if (!mbar_test_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) break;
                     tc_fence_after();
                     if (lane == 0) {
-                        mma_shrink_stage(tmem, bar(L.ring1 + s1 * p.s1_bytes), nxt, id_next, kc_next);
+                        mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
                         tc_commit(bar(L.empty1 + s1 * 8));
                     }
                     __syncwarp();
-                    kc_next += nxt.cps;
+                    ++kc_next;
                     ++it1;
                 }
             }
             if (!ok || !has_next) break;
             // the rest of the next tile's shrink
-            for (; kc_next < nxt.n_kc && ok; kc_next += nxt.cps, ++it1) {
+            for (; kc_next < nxt.n_kc && ok; ++kc_next, ++it1) {
                 const uint32_t s1 = it1 % S1;
                 if (!mbar_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    mma_shrink_stage(tmem, bar(L.ring1 + s1 * p.s1_bytes), nxt, id_next, kc_next);
+                    mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
                     tc_commit(bar(L.empty1 + s1 * 8));
                 }
                 __syncwarp();
@@ -620,22 +455,16 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
         const int half = e >> 2;                // column half of each slice
         const int m = quad * 32 + lane;         // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        uint32_t tcount = 0, g = 0, it3 = 0;
+        uint32_t tcount = 0, g = 0;
         bool stored = false;
         for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W, G>(p, tiles, n_tiles, item, lane);
+            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
             if (!mi.ok) continue;
             const int rp = mi.rp, rows = mi.tile.rows, row0 = mi.tile.row0;
             const float scale = p.pool.scales[mi.tile.adapter];
             const bool live = m < rows;
             const bool block_full = quad * kMmaRowBlock + kMmaRowBlock <= rows;
             const bool block_part = !block_full && quad * kMmaRowBlock < rows;
-            // gathered tiles: this thread's y row
-            __nv_bfloat16* yrow_g = nullptr;
-            if constexpr (G) {
-                const ProbDesc& pd = p.probs[mi.pr];
-                if (live) yrow_g = pd.y + (long long)rowlist[row0 + m] * pd.ldy + half * 64;
-            }
             // ---- convert D1 -> T_hi, T_lo in TMEM (bf16 pairs, column c / 2 holds k = c, c + 1)
             if (!mbar_wait(bar(L.d1_full), tcount & 1, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
@@ -666,10 +495,8 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
             ++tcount;
             // ---- expand epilogue over the column slices: y (in the y ring) += D2
             for (int nt = 0; nt < mi.n_nt; ++nt, ++g) {
-                const int c3 = nt % mi.yps;
-                const bool last3 = c3 == mi.yps - 1 || nt == mi.n_nt - 1;
                 const uint32_t b = g & 1;
-                const uint32_t ys = it3 % S3;
+                const uint32_t ys = g % S3;
                 if (!mbar_wait(bar(L.d2_full + b * 8), (g >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 float acc[64];
@@ -684,10 +511,9 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L.d2_empty + b * 8));
-                if (c3 == 0 && !mbar_wait(bar(L.full3 + ys * 8), (it3 / S3) & 1, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(bar(L.full3 + ys * 8), (g / S3) & 1, kWaitLimitNs)) { ok = false; break; }
                 // this warp's box: rows 32 quad .. +31 of column half `half` (128-byte swizzle)
-                const uint32_t half_off = ys * kMmaYSlot + c3 * mi.yb + half * (mi.yb / 2);
-                unsigned char* yrow = base + L.ring3 + half_off + m * 128;
+                unsigned char* yrow = base + L.ring3 + ys * 32768 + half * 16384 + m * 128;
                 if (live) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -699,43 +525,28 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
                         o.y = pack2(y8[2] + acc[8 * c + 2], y8[3] + acc[8 * c + 3]);
                         o.z = pack2(y8[4] + acc[8 * c + 4], y8[5] + acc[8 * c + 5]);
                         o.w = pack2(y8[6] + acc[8 * c + 6], y8[7] + acc[8 * c + 7]);
-                        if constexpr (G)
-                            st16(yrow_g + nt * kMmaNTile + c * 8, o);
-                        else
-                            *ptr = o;
+                        *ptr = o;
                     }
                 }
-                if constexpr (G) {
-                    // the stage's rows were read into registers: release it at once
-                    if (last3) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(L.empty3 + ys * 8));
-                        ++it3;
-                    }
-                } else {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    const int col = nt * kMmaNTile + half * 64;
-                    if (block_full) {
-                        if (lane == 0) {
-                            tma_store_2d(&p.y_map[mi.pr], col, row0 + quad * kMmaRowBlock,
-                                         smem_addr(base + L.ring3 + half_off + quad * 4096));
-                            stored = true;
-                        }
-                    } else if (block_part && live) {
-                        tma_store_2d(&p.y1_map[mi.pr], col, row0 + m, smem_addr(yrow));
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int col = nt * kMmaNTile + half * 64;
+                if (block_full) {
+                    if (lane == 0) {
+                        tma_store_2d(&p.y_map[mi.pr], col, row0 + quad * kMmaRowBlock,
+                                     smem_addr(base + L.ring3 + ys * 32768 + half * 16384 + quad * 4096));
                         stored = true;
                     }
-                    // one commit group per y stage; the previous stage's slot is released once
-                    // its stores have read shared memory, so the stores overlap the next stage
-                    if (last3) {
-                        bulk_commit();
-                        bulk_wait_read1();
-                        __syncwarp();
-                        if (lane == 0 && it3 > 0) mbar_arrive(bar(L.empty3 + ((it3 - 1) % S3) * 8));
-                        ++it3;
-                    }
+                } else if (block_part && live) {
+                    tma_store_2d(&p.y1_map[mi.pr], col, row0 + m, smem_addr(yrow));
+                    stored = true;
                 }
+                // one commit group per slice; the slot of the previous slice is released
+                // once its stores have read shared memory, so a store overlaps the next slice
+                bulk_commit();
+                bulk_wait_read1();
+                __syncwarp();
+                if (lane == 0 && g > 0) mbar_arrive(bar(L.empty3 + ((g - 1) % S3) * 8));
             }
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
@@ -750,7 +561,7 @@ __device__ __forceinline__ void mma_cta(const P& p, unsigned char* smem_raw, uin
 template <bool W>
 __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
-    mma_cta<W, false>(p, mma_smem_raw, blockIdx.x, gridDim.x);
+    mma_cta<W>(p, mma_smem_raw, blockIdx.x, gridDim.x);
 }
 
 }  // namespace lora

@@ -126,9 +126,7 @@ typedef struct lora_pool lora_pool; /* opaque, host memory only */
 
 /* One projection instance: y (bf16 [T][ldy], d_out columns updated) += delta computed
  * from x (bf16 [T][ldx], d_in columns read) with the adapters' pages for (layer, proj).
- * All problems of one call share the batch (the same tokens and adapter ids).  Problems
- * may share x, but their y elements must not overlap: each problem's y is read and
- * rewritten in place by work items that run at the same time. */
+ * All problems of one call share the batch (the same tokens and adapter ids). */
 typedef struct {
     const void* x;
     void* y;
@@ -163,10 +161,7 @@ typedef struct {
                                     0 = default (3)                                     */
     float fused_ring_speed;      /* mixed launch: per-CTA byte rate of the CUDA-core body
                                     over the tensor-core body's (0.1 .. 10); 0 = default */
-    int32_t gather_min_rows;     /* decode batches: an adapter with at least this many
-                                    tokens is served by tensor-core tiles of its gathered
-                                    rows; 0 = never, >= 2; -1 = default                 */
-    int32_t reserved[2];         /* must be 0                                           */
+    int32_t reserved[3];         /* must be 0                                           */
 } lora_tuning;
 
 /* t == NULL restores the defaults.  Returns LORA_EINVAL for a value outside the ranges

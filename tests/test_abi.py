@@ -134,25 +134,24 @@ def test_pool_tuning_defaults_overrides_and_checks(lib):
         t = lora_tuning()
         assert lib.lora_pool_get_tuning(h, ctypes.byref(t)) == 0
         return (t.ring_rows_per_stage, t.split_max_problems, t.mma_min_rows, t.mma_y_stages,
-                round(t.fused_ring_speed, 4), t.gather_min_rows)
+                round(t.fused_ring_speed, 4))
 
     default = get()
-    assert default == (0, 2, 32, 3, 1.22, 8)
+    assert default == (0, 2, 32, 3, 1.22)
 
     def set_(**kw):
         f = dict(ring_rows_per_stage=0, split_max_problems=-1, mma_min_rows=-1, mma_y_stages=0,
-                 fused_ring_speed=0.0, gather_min_rows=-1)
+                 fused_ring_speed=0.0)
         f.update(kw)
         t = lora_tuning(**f)
         return lib.lora_pool_set_tuning(h, ctypes.byref(t))
 
-    assert set_(split_max_problems=0, mma_min_rows=64, gather_min_rows=0) == 0
-    assert get() == (0, 0, 64, 3, 1.22, 0)
+    assert set_(split_max_problems=0, mma_min_rows=64) == 0
+    assert get() == (0, 0, 64, 3, 1.22)
     for bad in (dict(ring_rows_per_stage=5), dict(split_max_problems=9), dict(mma_min_rows=1),
-                dict(mma_y_stages=5), dict(fused_ring_speed=20.0), dict(gather_min_rows=1),
-                dict(reserved=(ctypes.c_int32 * 2)(1, 0))):
+                dict(mma_y_stages=5), dict(fused_ring_speed=20.0), dict(reserved=(ctypes.c_int32 * 3)(1, 0, 0))):
         assert set_(**bad) == LORA_EINVAL, bad
-        assert get() == (0, 0, 64, 3, 1.22, 0)
+        assert get() == (0, 0, 64, 3, 1.22)
     assert lib.lora_pool_set_tuning(h, None) == 0
     assert get() == default
     lib.lora_pool_destroy(h)
