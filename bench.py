@@ -271,6 +271,21 @@ def selected_workload(args):
     return wl
 
 
+def tuning_args(args) -> dict:
+    """--tuning k=v,k=v: lora_pool_set_tuning fields (kernel choice and stage shapes)."""
+    out = {}
+    for kv in filter(None, (args.tuning or "").split(",")):
+        k, v = kv.split("=")
+        out[k.strip()] = float(v) if k.strip() == "fused_ring_speed" else int(v)
+    return out
+
+
+def apply_tuning(pool, args):
+    t = tuning_args(args)
+    if t:
+        pool.set_tuning(**t)
+
+
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
@@ -374,6 +389,7 @@ def run_ours(args, rank: int, world: int, local: int):
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
                      p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
+    apply_tuning(pool, args)
     b = wl.batch
     T, S, Td = b.num_tokens, b.num_segments, b.num_decode
     nbytes = lora.workspace_size(pool, T, S + Td)
@@ -585,7 +601,8 @@ def run_ours(args, rank: int, world: int, local: int):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config_dict(wl, args), "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "graph": graph, "clocks": clk.summary(), "impl": "ours"}
+                "graph": graph, "clocks": clk.summary(), "impl": "ours",
+                "tuning": pool.get_tuning()}
         if staging is not None:
             line["staging"] = staging
         print(json.dumps(line), flush=True)
@@ -611,6 +628,7 @@ def run_sweep_distinct(args, local: int):
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
                      p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
+    apply_tuning(pool, args)
     T = wl.batch.num_tokens
     nbytes = lora.workspace_size(pool, T, T)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -694,7 +712,7 @@ def run_sweep_threshold(args, local: int):
             for path, mma_min in (("cuda-core", 0), ("tensor-core", max(2, n))):
                 if path == "tensor-core" and n < 2:
                     continue
-                pool.set_tuning(mma_min_rows=mma_min)
+                pool.set_tuning(**dict(tuning_args(args), mma_min_rows=mma_min))
                 for _ in range(max(3, args.warmup)):
                     lora.sgmv(pool, probs, seg_start, seg_adapter, S, T, ws, nbytes, stream)
                 torch.cuda.synchronize()
@@ -944,6 +962,10 @@ def main():
     ap.add_argument("--sweep-threshold", action="store_true",
                     help="instead of the bench line: CUDA-core against tensor-core step time "
                          "over segment length x rank (the FMA / MMA crossover)")
+    ap.add_argument("--tuning", default="",
+                    help="launch tuning of the pool, k=v,...: ring_rows_per_stage, "
+                         "split_max_problems, mma_min_rows, mma_y_stages, fused_ring_speed "
+                         "(the defaults otherwise)")
     ap.add_argument("--sweep-ranks", default="8,16,64,128")
     ap.add_argument("--sweep-lengths", default="1,2,4,8,16,32,64,128")
     args = ap.parse_args()

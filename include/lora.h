@@ -126,7 +126,9 @@ typedef struct lora_pool lora_pool; /* opaque, host memory only */
 
 /* One projection instance: y (bf16 [T][ldy], d_out columns updated) += delta computed
  * from x (bf16 [T][ldx], d_in columns read) with the adapters' pages for (layer, proj).
- * All problems of one call share the batch (the same tokens and adapter ids). */
+ * All problems of one call share the batch (the same tokens and adapter ids).  Problems
+ * may share x, but their y elements must not overlap: each problem's y is read and
+ * rewritten in place by work items that run at the same time. */
 typedef struct {
     const void* x;
     void* y;
