@@ -664,6 +664,61 @@ def run_sweep_distinct(args, local: int):
     pool.close()
 
 
+# ----------------------------------------------------------------------------- few-projection launches
+
+def run_sweep_few(args, local: int):
+    """Launches of 1 .. 8 projections of the Llama-7B decode batch (the shape of a serving
+    loop that applies each projection's delta next to its base GEMM): per launch time of the
+    cluster kernel and the ring kernel, each launch on the next
+    projections of the step (no launch re-reads the previous one's x, y or pages from L2).
+    One JSON line per (projections, kernel)."""
+    import torch
+
+    import heterogeneous_adapters_gb300 as lora
+    from workloads.materialize import device_inputs
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    wl = workload_for("decode")
+    d = device_inputs(wl, device=dev, nan_dummies=False)
+    p = wl.pool
+    pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
+                     p.num_adapters, p.num_layers, p.num_proj, p.r_max, p.proj_dims)
+    T = wl.batch.num_tokens
+    nbytes = lora.workspace_size(pool, T, T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream_obj = torch.cuda.current_stream(dev)
+    stream = stream_obj.cuda_stream
+    lora.workspace_init(ws, nbytes, stream)
+    probs = [(d.x[i], d.y[i], d.x.shape[2], d.y.shape[2], l, pj) for i, (l, pj) in enumerate(d.problems)]
+    peaks = measured_peaks()
+    lora.segment(pool, None, None, 0, d.token_adapter, T, T, ws, nbytes, stream)
+    kernels = {"cluster": dict(split_max_problems=8), "ring": dict(split_max_problems=0)}
+    for n in (1, 2, 3, 4, 6, 8):
+        groups = [probs[i:i + n] for i in range(0, len(probs) - n + 1, n)]
+        m = step_model(wl, problems=wl.problems[:n])
+        for name, tun in kernels.items():
+            pool.set_tuning(**tun)
+            for g in groups[:4]:
+                lora.delta_grouped(pool, g, T, 0, ws, nbytes, stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            launches = max(len(groups), args.steps)
+            e0.record(stream_obj)
+            for k in range(launches):
+                lora.delta_grouped(pool, groups[k % len(groups)], T, 0, ws, nbytes, stream)
+            e1.record(stream_obj)
+            torch.cuda.synchronize()
+            assert lora.get_device_error(ws, stream) == 0
+            ms = e0.elapsed_time(e1) / launches
+            gbs = m["bytes"] / (ms / 1e3) / 1e9
+            print(json.dumps({"sweep": "few_projections", "projections": n, "kernel": name,
+                              "launch_ms": ms, "bytes_per_launch": m["bytes"], "achieved_gbs": gbs,
+                              "frac_of_peak": gbs / peaks["hbm_gbs"], "launches": launches}), flush=True)
+    pool.set_tuning()
+    pool.close()
+
+
 # ----------------------------------------------------------------------------- FMA / MMA threshold sweep
 
 def run_sweep_threshold(args, local: int):
@@ -966,6 +1021,9 @@ def main():
                     help="launch tuning of the pool, k=v,...: ring_rows_per_stage, "
                          "split_max_problems, mma_min_rows, mma_y_stages, fused_ring_speed "
                          "(the defaults otherwise)")
+    ap.add_argument("--sweep-few", action="store_true",
+                    help="instead of the bench line: launches of 1 .. 8 projections of the decode "
+                         "batch through the cluster and ring kernels")
     ap.add_argument("--sweep-ranks", default="8,16,64,128")
     ap.add_argument("--sweep-lengths", default="1,2,4,8,16,32,64,128")
     args = ap.parse_args()
@@ -976,6 +1034,8 @@ def main():
         run_sweep_distinct(args, local)
     elif args.sweep_threshold:
         run_sweep_threshold(args, local)
+    elif args.sweep_few:
+        run_sweep_few(args, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -14,7 +14,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 # the C ABI, the launch code of each kernel family, and the host runtime (adapter cache,
 # scheduler; host-only C++)
 SOURCES = [os.path.join(PKG, "csrc", f) for f in
-           ("lora_api.cu", "launch_ring.cu", "launch_tile.cu", "launch_split.cu", "runtime.cpp")]
+           ("lora_api.cu", "launch_ring.cu", "launch_tile.cu", "launch_cluster.cu", "runtime.cpp")]
 
 
 def nvcc() -> str:

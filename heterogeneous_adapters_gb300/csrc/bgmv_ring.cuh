@@ -108,17 +108,8 @@ __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, in
                 const int vi = c + v * (CW * 32);
                 if (vi < h8) {
                     const uint4 a = *reinterpret_cast<const uint4*>(stage + jj * stage_row_bytes + vi * 16);
-                    float a8[8];
-                    unpack8(a, a8);
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        float x8[8];
-                        unpack8(xv[t][v], x8);
-                        float s = vals[jj * kChunk + t];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) s = fmaf(x8[e], a8[e], s);
-                        vals[jj * kChunk + t] = s;
-                    }
+                    for (int t = 0; t < NT; ++t) vals[jj * kChunk + t] = dot8_bf16(xv[t][v], a, vals[jj * kChunk + t]);
                 }
             }
         }

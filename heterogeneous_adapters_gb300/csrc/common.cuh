@@ -129,6 +129,29 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
 }
 
+// s + x.lo * a.lo + x.hi * a.hi for two packed bf16 pairs, accumulated in fp32 in that
+// order with the mixed-precision FMA (bf16 inputs, fp32 addend and result): the products
+// are exact and each FMA rounds once, as fmaf on the widened values does, but the bf16
+// halves feed the FMA directly instead of being widened first.
+__device__ __forceinline__ float fma_bf16x2(uint32_t x, uint32_t a, float s) {
+    asm("{\n\t.reg .b16 xl, xh, al, ah;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, xl, al, %0;\n\t"
+        "fma.rn.f32.bf16 %0, xh, ah, %0;\n\t}"
+        : "+f"(s)
+        : "r"(x), "r"(a));
+    return s;
+}
+
+// s + the dot product of eight bf16 pairs (x, a), element by element in order.
+__device__ __forceinline__ float dot8_bf16(const uint4& x, const uint4& a, float s) {
+    s = fma_bf16x2(x.x, a.x, s);
+    s = fma_bf16x2(x.y, a.y, s);
+    s = fma_bf16x2(x.z, a.z, s);
+    return fma_bf16x2(x.w, a.w, s);
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&b);

@@ -1,8 +1,8 @@
 // Host-side launch plumbing shared by the translation units of liblora.so: the pool's
 // host record, device facts, kernel-parameter helpers, and the launch entry points of each
 // kernel family (launch_ring.cu: the CUDA-core ring kernel; launch_tile.cu: the
-// tensor-core tile kernel and the fused launch; launch_split.cu: the two-phase split
-// kernels).  The C ABI itself lives in lora_api.cu.
+// tensor-core tile kernel and the fused launch; launch_cluster.cu: the cluster kernel for
+// launches of few projections).  The C ABI itself lives in lora_api.cu.
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -66,11 +66,11 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
 lora_status run_fused(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
                       cudaStream_t stream);
 
-// launch_split.cu: the two-phase CUDA-core path for launches of few projections.
-size_t split_t_bytes(const lora_pool_desc& d, int32_t max_tokens);
-bool split_fits(const lora_pool* pool, int32_t nprob, int32_t T, size_t ws_bytes);
-lora_status run_split(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
-                      cudaStream_t stream);
+// launch_cluster.cu: the cluster kernel for launches of few projections (no workspace
+// beyond the grouping).
+bool cluster_fits(const lora_pool* pool, int32_t nprob);
+lora_status run_cluster(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
+                        cudaStream_t stream);
 
 }  // namespace host
 }  // namespace lora

@@ -1,8 +1,8 @@
 // C ABI of liblora.so (declarations and contracts in include/lora.h).
 //
 // Host side: argument checks, workspace layout, the grouping launch and the choice of
-// delta launches (launch_ring.cu, launch_tile.cu, launch_split.cu).  All compute runs in
-// the kernels of segment.cuh, bgmv_ring.cuh, bgmv_split.cuh, sgmv_mma.cuh, fused.cuh and
+// delta launches (launch_ring.cu, launch_tile.cu, launch_cluster.cu).  All compute runs in
+// the kernels of segment.cuh, bgmv_ring.cuh, bgmv_cluster.cuh, sgmv_mma.cuh, fused.cuh and
 // stage.cuh; nothing here touches adapter or activation values.
 #include <stdint.h>
 #include <stdlib.h>
@@ -12,7 +12,7 @@
 #include <mutex>
 #include <new>
 
-#include "bgmv_split.cuh"
+#include "bgmv_cluster.cuh"
 #include "host.h"
 #include "segment.cuh"
 #include "sgmv_mma.cuh"
@@ -94,11 +94,11 @@ lora_status device_info(DeviceInfo** out) {
 namespace {
 
 // The measured defaults of a pool's launch tuning: stage rows chosen by shared memory,
-// the split path up to 2 projections, tensor-core tiles from 32 rows, a 3-slot y ring.
+// the cluster kernel up to 2 projections, tensor-core tiles from 32 rows, a 3-slot y ring.
 void default_tuning(const lora_pool* pool, lora_tuning* t) {
     memset(t, 0, sizeof *t);
     t->ring_rows_per_stage = 0;
-    t->split_max_problems = kSplitDefaultProbs;
+    t->split_max_problems = kClusterDefaultProbs;
     t->mma_min_rows = kMmaDefaultMinRows;
     t->mma_y_stages = 3;
     t->fused_ring_speed = default_fused_ring_speed(pool->square);
@@ -132,8 +132,9 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
                       size_t ws_bytes, float* t_out, bool with_mma, cudaStream_t stream) {
     lora_status st = check_problems(pool, probs, nprob);
     if (st != LORA_OK) return st;
-    if (!with_mma && t_out == nullptr && split_fits(pool, nprob, T, ws_bytes))
-        return run_split(pool, probs, nprob, ws, stream);
+    // launches of few projections: a chunk's work is spread over a cluster of CTAs
+    if (!with_mma && t_out == nullptr && cluster_fits(pool, nprob))
+        return run_cluster(pool, probs, nprob, ws, stream);
     // one launch per batch of projections for both work classes
     if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && pool->d.h / 8 <= 640 && T > 0)
         return run_fused(pool, probs, nprob, T, ws, stream);
@@ -255,7 +256,7 @@ lora_status lora_pool_set_tuning(lora_pool* pool, const lora_tuning* t) {
         if (t->reserved[0] != 0 || t->reserved[1] != 0 || t->reserved[2] != 0) return LORA_EINVAL;
         if (t->ring_rows_per_stage != 0 && t->ring_rows_per_stage != 4 && t->ring_rows_per_stage != 8)
             return LORA_EINVAL;
-        if (t->split_max_problems < -1 || t->split_max_problems > kSplitMaxProbs) return LORA_EINVAL;
+        if (t->split_max_problems < -1 || t->split_max_problems > kClusterMaxProbs) return LORA_EINVAL;
         if (t->mma_min_rows < -1 || t->mma_min_rows == 1) return LORA_EINVAL;
         if (t->mma_y_stages != 0 && (t->mma_y_stages < 2 || t->mma_y_stages > 4)) return LORA_EINVAL;
         if (t->fused_ring_speed != 0.f && !(t->fused_ring_speed >= 0.1f && t->fused_ring_speed <= 10.f))
@@ -281,7 +282,7 @@ lora_status lora_workspace_size(const lora_pool* pool, int32_t max_tokens, int32
     if (pool == nullptr || bytes == nullptr || max_tokens < 0 || max_segments < 0)
         return LORA_EINVAL;
     if (max_segments > LORA_MAX_SEGMENTS || max_tokens > (1 << 28)) return LORA_ETOOBIG;
-    *bytes = ws_layout(max_tokens, max_segments).total + split_t_bytes(pool->d, max_tokens);
+    *bytes = ws_layout(max_tokens, max_segments).total;
     return LORA_OK;
 }
 
@@ -307,20 +308,17 @@ lora_status lora_workspace_view(const lora_pool* pool, void* ws, size_t ws_bytes
     return LORA_OK;
 }
 
-// The grouping launch.  with_split_room: the workspace must also hold the split path's t
-// (the size lora_workspace_size reports); the allocation-free entry point passes false:
-// its fixed scratch holds the split path's t only for small batches, and run_delta then
-// takes that path only when split_fits finds the room.
+// The grouping launch.
 static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
                          int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
-                         size_t ws_bytes, bool with_split_room, void* stream) {
+                         size_t ws_bytes, void* stream) {
     if (pool == nullptr || S < 0 || Td < 0 || T < 0) return LORA_EINVAL;
     if ((int64_t)S + Td > LORA_MAX_SEGMENTS || T > (1 << 28)) return LORA_ETOOBIG;
     if (S > 0 && (seg_start == nullptr || seg_adapter == nullptr)) return LORA_EINVAL;
     if (Td > 0 && dec_adapter == nullptr) return LORA_EINVAL;
     if (S == 0 && Td > T) return LORA_EINVAL;
     const WsLayout L = ws_layout(T, S + Td);
-    lora_status st = check_ws(ws, ws_bytes, L.total + (with_split_room ? split_t_bytes(pool->d, T) : 0));
+    lora_status st = check_ws(ws, ws_bytes, L.total);
     if (st != LORA_OK) return st;
     SegParams sp;
     memset(&sp, 0, sizeof sp);
@@ -359,7 +357,7 @@ static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start,
 lora_status lora_segment(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
                          int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
                          size_t ws_bytes, void* stream) {
-    return segment_impl(pool, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes, true, stream);
+    return segment_impl(pool, seg_start, seg_adapter, S, dec_adapter, Td, T, ws, ws_bytes, stream);
 }
 
 lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
@@ -505,7 +503,7 @@ lora_status lora_bgmv_noalloc(const lora_pool* pool, const lora_problem* probs, 
     // the error word is per call; the grouping kernel re-initialises everything else
     st = cuda_status(cudaMemsetAsync(&hdr->err, 0, sizeof(uint32_t), s));
     if (st != LORA_OK) return st;
-    st = segment_impl(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, kNoallocWsBytes, false, stream);
+    st = segment_impl(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, kNoallocWsBytes, stream);
     if (st != LORA_OK) return st;
     if (nprob > 0) {
         st = run_delta(pool, probs, nprob, T, ws, kNoallocWsBytes, nullptr, false, s);

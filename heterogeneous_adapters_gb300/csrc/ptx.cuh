@@ -259,3 +259,13 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 }  // namespace lora
+
+namespace lora {
+
+// Prefetch `bytes` (a multiple of 16, at a 16-byte aligned address) of global memory into
+// L2 with one bulk operation.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+}  // namespace lora

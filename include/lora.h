@@ -154,8 +154,8 @@ lora_status lora_pool_destroy(lora_pool* pool);
 typedef struct {
     int32_t ring_rows_per_stage; /* CUDA-core ring: rows (pages) per shared-memory stage,
                                     4 or 8; 0 = 8 where three stages fit, else 4        */
-    int32_t split_max_problems;  /* launches of at most this many projections (and at
-                                    most 1,024 rows) run the two-phase split kernels;
+    int32_t split_max_problems;  /* decode launches of at most this many projections run
+                                    the cluster kernel (each chunk split over 8 CTAs);
                                     0 = never, 1..8; -1 = default (2)                   */
     int32_t mma_min_rows;        /* prefill segments of at least this many rows take the
                                     tensor-core tiles; 0 = never, >= 2; -1 = default    */
@@ -174,10 +174,8 @@ lora_status lora_pool_get_tuning(const lora_pool* pool, lora_tuning* out);
 
 /* Bytes of device workspace needed by a call over at most max_tokens rows and at
  * most max_segments segments (prefill segments + decode tokens).  The workspace
- * holds the grouping of the batch, the work queue, the device error word and, for
- * batches of up to 1024 rows, the fp32 t of launches of up to 8 projections
- * (8 * max_tokens * r_max * 4 bytes), which such launches compute in a first phase
- * and expand in a second so that a few projections still fill the GPU. */
+ * holds the grouping of the batch, the work lists and the device error word; no
+ * kernel keeps intermediate values (t) in it. */
 lora_status lora_workspace_size(const lora_pool* pool, int32_t max_tokens, int32_t max_segments,
                                 size_t* bytes);
 
@@ -293,12 +291,11 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
  * host framework hands only its input and output buffers, or a step loop in which a
  * cudaMalloc -- which may synchronise the device -- is not allowed.  It computes what
  * lora_bgmv computes (the same grouping and delta kernels, chosen by the same rules),
- * with the grouping, the work lists and, where it runs, the split path's fp32 t kept
- * in a fixed array inside the library instead of a caller workspace, and it calls no
- * cudaMalloc, cudaFree or other allocating routine.
+ * with the grouping and the work lists kept in a fixed array inside the library
+ * instead of a caller workspace, and it calls no cudaMalloc, cudaFree or other
+ * allocating routine.
  *   - T must be <= LORA_NOALLOC_MAX_TOKENS (decode rows); larger batches return
- *     LORA_ETOOBIG and launch nothing.  Launches of one or two projections take the
- *     split path only when its t fits in the array beside the grouping (small T).
+ *     LORA_ETOOBIG and launch nothing.
  *   - The array is shared by every call in the process on a given GPU and keeps the
  *     last call's contents (the call clears what must start at zero): calls whose
  *     kernels may overlap on the GPU (different streams without ordering, or several

@@ -20,16 +20,16 @@ def _wl(wide=False):
     return small_decode(71, 512, 1, 2, 6, [4, 8], 20)
 
 
-# the decode batches here have 2 projections: the split path by default, the ring kernel
-# when the split path is turned off
-PATHS = {"split": 8, "ring": 0}
+# the decode batches here have 2 projections: the cluster kernel by default, the ring
+# kernel when the cluster kernel is turned off
+PATHS = {"cluster": {"split_max_problems": 8}, "ring": {"split_max_problems": 0}}
 
 
 @pytest.mark.parametrize("path", list(PATHS))
 def test_bad_adapter_id_sets_bit_and_skips_only_that_token(path):
     import torch
     wl = _wl()
-    case = GpuCase(wl, tuning={"split_max_problems": PATHS[path]})
+    case = GpuCase(wl, tuning=PATHS[path])
     try:
         ids = wl.batch.token_adapter().copy()
         victim = int(np.nonzero(ids >= 0)[0][0])
@@ -51,7 +51,7 @@ def test_bad_adapter_id_sets_bit_and_skips_only_that_token(path):
 def test_bad_page_rank_and_block_bits(path):
     import torch
     wl = _wl()
-    case = GpuCase(wl, tuning={"split_max_problems": PATHS[path]})
+    case = GpuCase(wl, tuning=PATHS[path])
     try:
         ids = wl.batch.token_adapter()
         a = int(ids[ids >= 0][0])
@@ -78,7 +78,7 @@ def test_bad_page_skips_that_adapter_in_that_projection_only(path, ab, wide):
     (for the wide pool, in the last page block of its vectors): the page bit is set, a's
     rows of projection 0 keep their y, everything else is right."""
     wl = _wl(wide)
-    case = GpuCase(wl, tuning={"split_max_problems": PATHS[path]})
+    case = GpuCase(wl, tuning=PATHS[path])
     try:
         ids = wl.batch.token_adapter()
         a = int(ids[ids >= 0][0])

@@ -49,13 +49,13 @@ HOT = {
 }
 
 
-@pytest.mark.parametrize("path", ["ring", "split"])
+@pytest.mark.parametrize("path", ["ring", "cluster"])
 @pytest.mark.parametrize("name", list(HOT))
 def test_hot_adapter_decode(name, path):
     """Adapters with 5 .. 257 tokens of one decode batch, through the ring kernel and through
-    the two-phase split kernels (every projection of the batch in one split launch)."""
+    the few-projection kernels (every projection of the batch in one launch)."""
     wl = HOT[name]()
-    tuning = {"split_max_problems": 0 if path == "ring" else 8}
+    tuning = {"ring": {"split_max_problems": 0}, "cluster": {"split_max_problems": 8}}[path]
     case = GpuCase(wl, y0_zero=True, tuning=tuning)
     try:
         assert case.run() == 0

@@ -98,7 +98,7 @@ def test_decode_ring_stage_shapes(pages):
     """The decode ring with 4 and with 8 rows per stage on the same batch: ranks that are
     not multiples of either and chunks of 1 to 4 rows (a skewed adapter mix)."""
     wl = small_decode(65, 2048, 1, 3, 12, [1, 3, 5, 8, 13, 64, 100], 57, zipf=1.3)
-    # the ring kernel, not the split path
+    # the ring kernel, not the cluster kernel
     case = GpuCase(wl, tuning={"ring_rows_per_stage": pages, "split_max_problems": 0})
     try:
         assert case.run() == 0
@@ -107,15 +107,16 @@ def test_decode_ring_stage_shapes(pages):
         case.close()
 
 
-@pytest.mark.parametrize("split", [0, 8])
-@pytest.mark.parametrize("h", [512, 4096, 5120])
-def test_decode_split_and_ring_paths(split, h):
-    """The same few-projection decode batch through the two-phase split kernels (up to 8
-    projections) and through the ring kernel: ranks not multiples of 8 rows, chunks of 1
-    to 4 rows, base-only rows, ranks up to 128."""
+@pytest.mark.parametrize("path", ["ring", "cluster"])
+@pytest.mark.parametrize("h", [512, 4096, 5120, 8192])
+def test_decode_cluster_and_ring_paths(path, h):
+    """The same few-projection decode batch through the cluster kernel (each chunk split over
+    8 CTAs) and the ring kernel (6 projections in one launch): ranks not multiples of 8 rows,
+    chunks of 1 to 4 rows, base-only rows, ranks up to 128."""
     wl = small_decode(66, h, 2, 3, 10, [1, 5, 8, 16, 64, 128], 47, zipf=1.2)
     wl.batch.dec_adapter[::9] = -1
-    case = GpuCase(wl, tuning={"split_max_problems": split})
+    tuning = {"ring": {"split_max_problems": 0}, "cluster": {"split_max_problems": 8}}[path]
+    case = GpuCase(wl, tuning=tuning)
     try:
         assert case.run() == 0
         full_check(wl, case, list(range(len(wl.problems))))
@@ -328,13 +329,13 @@ WIDTH_CASES = {
 
 
 @pytest.mark.parametrize("case_name", list(WIDTH_CASES))
-@pytest.mark.parametrize("path", ["decode-split", "decode-ring", "prefill", "mixed"])
+@pytest.mark.parametrize("path", ["decode-cluster", "decode-ring", "prefill", "mixed"])
 def test_projection_widths(case_name, path):
     """Projections whose input and output widths differ from h (vectors spanning several
     pool pages, the last one partly used).  x columns past a problem's d_in hold NaN and y
     columns past its d_out must come back unchanged."""
     h, dims = WIDTH_CASES[case_name]
-    tuning = {"decode-split": {"split_max_problems": 8},
+    tuning = {"decode-cluster": {"split_max_problems": 8},
               "decode-ring": {"split_max_problems": 0}}.get(path)
     kind = path.split("-")[0]
     if kind == "decode":

@@ -22,12 +22,12 @@ from .harness import GpuCase, full_check
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("nprob,path", [(4, "ring"), (1, "split")])
+@pytest.mark.parametrize("nprob,path", [(4, "ring"), (1, "cluster")])
 def test_noalloc_matches_workspace_bgmv_on_two_calls(nprob, path):
     """Four projections run the ring kernel; one projection of a 96-row batch runs the
-    two-phase split kernels, whose fp32 t then sits in the library's array after the
-    grouping.  Two calls in a row, each from the same y0: bit-identical to lora_bgmv, and
-    within the parity gate of the oracle (with y0 = 0, the strict delta-only bound too)."""
+    cluster kernel.  Two calls in a row, each from the same y0: bit-identical to lora_bgmv,
+    and within the parity gate of the oracle (with y0 = 0, the strict delta-only bound
+    too)."""
     import torch
     L, P = (2, 2) if nprob == 4 else (1, 1)
     wl = spec.decode_workload(f"noalloc-h2048-t96-{path}", 91, 2048, L, P, 30, [4, 8, 16, 64], 96, 1.0)
