@@ -14,7 +14,8 @@ namespace host {
 // Segments of at least this many rows (and rank <= kMmaMaxRank) take the tensor-core
 // path when h is a multiple of 128 and every projection's d_in is a multiple of 64 (the
 // shrink K chunk) and d_out one of 128 (the expand slice); the pool's tuning sets the
-// row count (0 disables the path; one-row segments always stay on the CUDA-core path).
+// row count, or -1 for the rank rule mma_min_rows_for_rank (0 disables the path; one-row
+// segments always stay on the CUDA-core path).
 int mma_min_rows(const lora_pool* pool) {
     const lora_pool_desc& d = pool->d;
     if (d.h % kMmaNTile != 0 || !pool->mma_widths) return 0;

@@ -94,12 +94,12 @@ lora_status device_info(DeviceInfo** out) {
 namespace {
 
 // The measured defaults of a pool's launch tuning: stage rows chosen by shared memory,
-// the cluster kernel up to 2 projections, tensor-core tiles from 32 rows, a 3-slot y ring.
+// the cluster kernel up to 2 projections, tensor-core tiles by the rank rule, a 3-slot y ring.
 void default_tuning(const lora_pool* pool, lora_tuning* t) {
     memset(t, 0, sizeof *t);
     t->ring_rows_per_stage = 0;
     t->split_max_problems = kClusterDefaultProbs;
-    t->mma_min_rows = kMmaDefaultMinRows;
+    t->mma_min_rows = kMmaMinRowsByRank;
     t->mma_y_stages = 3;
     t->fused_ring_speed = default_fused_ring_speed(pool->square);
 }
@@ -136,11 +136,11 @@ lora_status run_delta(const lora_pool* pool, const lora_problem* probs, int32_t 
     if (!with_mma && t_out == nullptr && cluster_fits(pool, nprob))
         return run_cluster(pool, probs, nprob, ws, stream);
     // one launch per batch of projections for both work classes
-    if (with_mma && mma_min_rows(pool) > 0 && t_out == nullptr && pool->d.h / 8 <= 640 && T > 0)
+    if (with_mma && mma_min_rows(pool) != 0 && t_out == nullptr && pool->d.h / 8 <= 640 && T > 0)
         return run_fused(pool, probs, nprob, T, ws, stream);
     st = run_delta_ring(pool, probs, nprob, ws, t_out, stream);
     if (st != LORA_OK) return st;
-    if (with_mma && mma_min_rows(pool) > 0) st = run_mma(pool, probs, nprob, T, ws, stream);
+    if (with_mma && mma_min_rows(pool) != 0) st = run_mma(pool, probs, nprob, T, ws, stream);
     return st;
 }
 

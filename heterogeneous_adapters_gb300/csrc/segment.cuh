@@ -18,6 +18,7 @@
 // of at least mma_min rows, 128 rows per tile).
 #pragma once
 #include "common.cuh"
+#include "sgmv_mma.cuh"
 
 namespace lora {
 
@@ -34,7 +35,9 @@ struct SegParams {
     int32_t S;
     int32_t Td;
     int32_t T;
-    int32_t mma_min;   // 0: every segment goes to the CUDA-core path
+    int32_t mma_min;   // 0: every segment goes to the CUDA-core path; > 0: segments of at
+                       // least this many rows take the tensor-core tiles; -1: the rank rule
+                       // mma_min_rows_for_rank
     int32_t mma_max_rank;   // segments whose adapter rank exceeds this use the CUDA-core path
     int32_t L_tokens;  // the (max_tokens, max_segments) that L was computed from
     int32_t L_segments;
@@ -46,6 +49,12 @@ struct SegParams {
 // (key 8 B + six int arrays per segment).
 constexpr int kSegSmemMax = 1536;
 __host__ __device__ constexpr size_t seg_smem_bytes(int n) { return (size_t)(n + 1) * 32 + 64; }
+
+// Whether a segment of len rows of an adapter of rank r takes the tensor-core tiles.
+__device__ __forceinline__ bool mma_tile(const SegParams& p, int len, int r) {
+    if (p.mma_min == 0 || r > p.mma_max_rank) return false;
+    return len >= (p.mma_min > 0 ? p.mma_min : mma_min_rows_for_rank(r));
+}
 
 __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p) {
     __shared__ int scan_smem[33];
@@ -173,7 +182,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
         const int len = valid ? slen[seg] : 0;
         const int prev_a = (valid && q > 0) ? (int)(key[sorted[q - 1]] >> 32) : -1;
         const int flag = (valid && (q == 0 || a != prev_a)) ? 1 : 0;
-        const bool is_mma = valid && p.mma_min > 0 && len >= p.mma_min && P.ranks[a] <= p.mma_max_rank;
+        const bool is_mma = valid && mma_tile(p, len, P.ranks[a]);
         const int flen = (valid && !is_mma) ? len : 0;
         const int ntile = is_mma ? (len + kTileRows - 1) / kTileRows : 0;
         int tot_pos, tot_g, tot_f, tot_t;
@@ -222,7 +231,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_kernel(const SegParams p)
         const int seg = sorted[q];
         const int b = sbeg[seg], len = slen[seg];
         const int a = (int)(key[seg] >> 32);
-        const bool is_mma = p.mma_min > 0 && len >= p.mma_min && P.ranks[a] <= p.mma_max_rank;
+        const bool is_mma = mma_tile(p, len, P.ranks[a]);
         const int pq = pos[q], fq = fpos[q];
         for (int t = lane; t < len; t += 32) {
             perm[pq + t] = b + t;

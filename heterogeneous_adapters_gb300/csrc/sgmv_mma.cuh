@@ -37,7 +37,12 @@ constexpr int kMmaThreads = 384;
 constexpr int kMmaEpiWarps = 8;
 constexpr int kMmaMaxProbs = 64;            // problems per launch (3 tensor maps each)
 constexpr int kMmaMaxRank = 128;
-constexpr int kMmaDefaultMinRows = 32;      // segments of at least this many rows take the tiles
+// Segments of at least this many rows take the tensor-core tiles by default: the measured
+// crossover of the CUDA-core and tensor-core paths (h = 4096, every segment with its own
+// adapter, 2,048 rows) is 64 rows at rank 8, 32 at rank 16 and 16 from rank 32 up.  A few
+// rows of low rank carry too few flops per page byte for the tile's fixed latency to pay.
+__host__ __device__ constexpr int mma_min_rows_for_rank(int r) { return r >= 32 ? 16 : 512 / (r > 0 ? r : 1); }
+constexpr int kMmaMinRowsByRank = -1;       // the tuning value that selects the rule above
 constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 bytes)
 constexpr int kMmaNTile = 128;              // y columns per expand slice
 constexpr int kMmaRowBlock = 32;            // rows per x / y TMA box

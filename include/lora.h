@@ -158,7 +158,9 @@ typedef struct {
                                     the cluster kernel (each chunk split over 8 CTAs);
                                     0 = never, 1..8; -1 = default (2)                   */
     int32_t mma_min_rows;        /* prefill segments of at least this many rows take the
-                                    tensor-core tiles; 0 = never, >= 2; -1 = default    */
+                                    tensor-core tiles; 0 = never, >= 2; -1 = default:
+                                    by rank, 512 / r rows under rank 32, 16 from rank
+                                    32 up (the measured crossover of the two paths)     */
     int32_t mma_y_stages;        /* depth of the tensor-core kernel's y ring, 2..4;
                                     0 = default (3)                                     */
     float fused_ring_speed;      /* mixed launch: per-CTA byte rate of the CUDA-core body
