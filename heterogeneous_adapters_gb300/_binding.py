@@ -24,7 +24,8 @@ EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_pool_set_tuning", "lo
             "lora_workspace_size", "lora_workspace_init",
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
             "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t", "lora_debug_wait_limit",
-            "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error",
+            "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error", "lora_shrink",
+            "lora_expand",
             "lora_last_cuda_error", "lora_status_string",
             # host runtime (include/lora_runtime.h)
             "lora_cache_create", "lora_cache_destroy", "lora_cache_acquire", "lora_cache_loaded",
@@ -102,6 +103,8 @@ def lib():
             "lora_debug_wait_limit": [p, sz, ctypes.c_uint64, p, p],
             "lora_stage_pages": [p, p, p, i32, p, p, p, i64, p],
             "lora_bgmv_noalloc": [p, p, i32, p, i32, p, p],
+            "lora_shrink": [p, p, i32, p, i32, p, sz, p, p],
+            "lora_expand": [p, p, i32, i32, p, sz, p, p],
             "lora_get_device_error": [p, p, ctypes.POINTER(ctypes.c_uint32)],
             "lora_last_cuda_error": [],
             "lora_status_string": [ctypes.c_int],
@@ -279,6 +282,19 @@ def bgmv_noalloc(pool, problems, token_adapter, T, error_bits, stream):
     arr, n = problems_array(problems)
     _check(lib().lora_bgmv_noalloc(pool.handle, arr, n, _ptr(token_adapter), T, _ptr(error_bits),
                                    stream), "lora_bgmv_noalloc")
+
+
+def shrink(pool, problems, token_adapter, T, ws, ws_bytes, t, stream):
+    """t[p][row][j] = s * x_p[row] . A_j (fp32 [nprob][T][r_max]); groups the batch into ws."""
+    arr, n = problems_array(problems)
+    _check(lib().lora_shrink(pool.handle, arr, n, _ptr(token_adapter), T, _ptr(ws), ws_bytes, _ptr(t),
+                             stream), "lora_shrink")
+
+
+def expand(pool, problems, T, ws, ws_bytes, t, stream):
+    """y_p[row] += t[p][row] . B^T with the grouping lora_shrink left in ws."""
+    arr, n = problems_array(problems)
+    _check(lib().lora_expand(pool.handle, arr, n, T, _ptr(ws), ws_bytes, _ptr(t), stream), "lora_expand")
 
 
 def get_device_error(ws, stream) -> int:

@@ -71,6 +71,10 @@ lora_status run_fused(const lora_pool* pool, const lora_problem* probs, int32_t 
 bool cluster_fits(const lora_pool* pool, int32_t nprob);
 lora_status run_cluster(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,
                         cudaStream_t stream);
+// The separate shrink (expand = false: t = s * x A^T into t) or expand (y += t B^T) over the
+// CUDA-core chunks of the grouping in ws; t is fp32 [nprob][T][r_max].
+lora_status run_shrink_expand(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T,
+                              void* ws, float* t, bool expand, cudaStream_t stream);
 
 }  // namespace host
 }  // namespace lora

@@ -309,9 +309,11 @@ lora_status lora_workspace_view(const lora_pool* pool, void* ws, size_t ws_bytes
 }
 
 // The grouping launch.
+// allow_tiles = false: every row goes to the CUDA-core chunks (the separate shrink and
+// expand serve chunks only).
 static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start, const int32_t* seg_adapter,
                          int32_t S, const int32_t* dec_adapter, int32_t Td, int32_t T, void* ws,
-                         size_t ws_bytes, void* stream) {
+                         size_t ws_bytes, void* stream, bool allow_tiles = true) {
     if (pool == nullptr || S < 0 || Td < 0 || T < 0) return LORA_EINVAL;
     if ((int64_t)S + Td > LORA_MAX_SEGMENTS || T > (1 << 28)) return LORA_ETOOBIG;
     if (S > 0 && (seg_start == nullptr || seg_adapter == nullptr)) return LORA_EINVAL;
@@ -331,7 +333,7 @@ static lora_status segment_impl(const lora_pool* pool, const int32_t* seg_start,
     sp.S = S;
     sp.Td = Td;
     sp.T = T;
-    sp.mma_min = mma_min_rows(pool);
+    sp.mma_min = allow_tiles ? mma_min_rows(pool) : 0;
     sp.mma_max_rank = kMmaMaxRank;
     sp.L_tokens = T;
     sp.L_segments = S + Td;
@@ -399,6 +401,31 @@ lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, i
                                   stream);
     if (st != LORA_OK) return st;
     return lora_delta_grouped(pool, probs, nprob, T, S, ws, ws_bytes, stream);
+}
+
+lora_status lora_shrink(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                        const int32_t* token_adapter, int32_t T, void* ws, size_t ws_bytes, float* t,
+                        void* stream) {
+    if (pool == nullptr || nprob < 0 || T < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
+    if (T > 0 && (token_adapter == nullptr || t == nullptr)) return LORA_EINVAL;
+    if (((uintptr_t)t & 15u) != 0) return LORA_EALIGN;
+    lora_status st = check_problems(pool, probs, nprob);
+    if (st != LORA_OK) return st;
+    st = segment_impl(pool, nullptr, nullptr, 0, token_adapter, T, T, ws, ws_bytes, stream, false);
+    if (st != LORA_OK || nprob == 0 || T == 0) return st;
+    return run_shrink_expand(pool, probs, nprob, T, ws, t, false, (cudaStream_t)stream);
+}
+
+lora_status lora_expand(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                        size_t ws_bytes, const float* t, void* stream) {
+    if (pool == nullptr || nprob < 0 || T < 0 || (nprob > 0 && probs == nullptr)) return LORA_EINVAL;
+    if (T > 0 && t == nullptr) return LORA_EINVAL;
+    if (((uintptr_t)t & 15u) != 0) return LORA_EALIGN;
+    lora_status st = check_ws(ws, ws_bytes, ws_layout(T, T).total);
+    if (st != LORA_OK) return st;
+    st = check_problems(pool, probs, nprob);
+    if (st != LORA_OK || nprob == 0 || T == 0) return st;
+    return run_shrink_expand(pool, probs, nprob, T, ws, const_cast<float*>(t), true, (cudaStream_t)stream);
 }
 
 lora_status lora_debug_page_list(const lora_pool* pool, void* ws, size_t ws_bytes, int32_t layer,

@@ -247,6 +247,28 @@ lora_status lora_apply_mixed(const lora_pool* pool, const lora_problem* probs, i
 lora_status lora_delta_grouped(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
                                int32_t T, int32_t S, void* ws, size_t ws_bytes, void* stream);
 
+/* Shrink alone: groups the batch (token_adapter[T], -1 = base only) into ws, then writes
+ *     t[p][row][j] = s_a * sum_k x_p[row, k] A_a[j, k]        (fp32, j < r_a)
+ * for every problem p and every adapted row, into t (device f32 [nprob][T][r_max],
+ * 16-byte aligned; entries of base-only rows and entries j >= r_a are not written).
+ * Expand alone: with the grouping lora_shrink left in ws (same batch, same T),
+ *     y_p[row, n] = bf16_rn(y_p[row, n] + sum_j t[p][row][j] B_a[n, j]).
+ * lora_shrink followed by lora_expand computes what lora_bgmv computes, up to the fp32
+ * summation order.  Between the two a caller may combine t: the sum over tensor-parallel
+ * shards of their partial t (an all-reduce) is the t of the whole projection.
+ *   "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "What the engine does each
+ *   step": per LoRA target, v = shrink(x, A_pool[proj], idx), y += expand(v, B_pool[proj],
+ *   idx, scaling).  "S-LoRA: Serving Thousands of Concurrent LoRA Adapters", "Kernels and
+ *   tensor parallelism": a partition of the adapters aligned with Megatron-LM's partition
+ *   of the base model, whose LoRA terms add a small exchange of the B x r intermediate.
+ * Both run on the CUDA-core kernels (up to 8 projections per launch; more take several
+ * launches); they serve decode and prefill rows alike (no tensor-core tiles). */
+lora_status lora_shrink(const lora_pool* pool, const lora_problem* probs, int32_t nprob,
+                        const int32_t* token_adapter, int32_t T, void* ws, size_t ws_bytes, float* t,
+                        void* stream);
+lora_status lora_expand(const lora_pool* pool, const lora_problem* probs, int32_t nprob, int32_t T, void* ws,
+                        size_t ws_bytes, const float* t, void* stream);
+
 /* Debug export of the page-table walk (a2): for problem (layer, proj), for each group
  * g of the grouping in ws, the entries of its A block then of its B block as the
  * page-table layout above orders them (r_a each for h x h pools; r_a * ceil(d/h) for a

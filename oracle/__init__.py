@@ -6,7 +6,7 @@ bench.py's CPU-baseline / reference legs may use it; it shares no code with the
 CUDA path (heterogeneous_adapters_gb300) and neither imports the other.
 """
 from .oracle import (ERRORS, OracleError, build, group_tokens, lora_delta,
-                     page_list)
+                     lora_expand, page_list)
 
 __all__ = ["ERRORS", "OracleError", "build", "group_tokens",
-           "lora_delta", "page_list"]
+           "lora_delta", "lora_expand", "page_list"]

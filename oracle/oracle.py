@@ -101,6 +101,43 @@ def lora_delta(pool: np.ndarray, pt: np.ndarray, pt_off: np.ndarray, ranks: np.n
     return y, t, int(madds.value)
 
 
+def lora_expand(pool: np.ndarray, pt: np.ndarray, pt_off: np.ndarray, ranks: np.ndarray,
+                scales: np.ndarray, num_layers: int, num_proj: int, layer: int, proj: int,
+                t: np.ndarray, y0: np.ndarray, token_adapter: np.ndarray, proj_dims=None) -> np.ndarray:
+    """The expand step alone, in float64: y[i, n] = y0[i, n] + s_a * sum_j t[i, j] B_a[n, j]
+    for every token i with adapter a >= 0 (base-only rows are y0 unchanged).
+
+    "Multi-LoRA serving: S-LoRA, Punica and adapter batching", "How the kernels work":
+    expand y_i += gamma B_{a(i)} v_i after the shrink v_i = A_{a(i)} x_i; "What the engine
+    does each step": the two are separate steps with v between them.  t is the unscaled
+    shrink (lora_delta's t, or a sum of partial t); B column j of (layer, proj) is read from
+    its pages by walking the page table (page q of column j at the B block's entry q r + j).
+    pool: uint16 [num_pages, h] bf16 bits; t: float64 [T, >= r_max]; y0: float64 [T, d_out]."""
+    pool = np.asarray(pool, dtype=np.uint16)
+    h = pool.shape[1]
+    U, pre, pv_in, pv_out = block_units(num_proj, h, proj_dims)
+    d_out = h if proj_dims is None else int(np.asarray(proj_dims).reshape(-1, 2)[proj][1])
+    y = np.array(y0, dtype=np.float64, copy=True)
+    ids = np.asarray(token_adapter, dtype=np.int64)
+    for i in range(ids.size):
+        a = int(ids[i])
+        if a < 0:
+            continue
+        r = int(ranks[a])
+        b0 = int(pt_off[a]) + r * (layer * U + pre[proj] + pv_in[proj])   # first B-block entry
+        acc = np.zeros(d_out, dtype=np.float64)
+        for j in range(r):
+            col = np.concatenate([_bf16_to_f64(pool[int(pt[b0 + q * r + j])]) for q in range(pv_out[proj])])
+            acc += float(t[i, j]) * col[:d_out]
+        y[i] += float(scales[a]) * acc
+    return y
+
+
+def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) widened exactly to float64."""
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def group_tokens(token_adapter: np.ndarray):
     """Stable grouping of the adapted tokens by adapter id.
 

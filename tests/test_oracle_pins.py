@@ -438,3 +438,78 @@ def test_zipf_batches_match_pages_simulation():
                 lru.popitem(last=False)
     frac = misses / (arrivals.size - 20_000)
     assert abs(frac - g["miss_fraction_at_64_slots_zipf_1"]) < 0.08
+
+
+# ----------------------------------------------------------------------------- the expand step alone
+
+def test_expand_matches_dense_B():
+    """The expand alone: y0 + s B t with B assembled from the generator keys (not through
+    the page table), for t = the oracle's shrink; B's orientation and page walk pinned."""
+    wl = small_multi(seed=23)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    p = wl.pool
+    for (l, pj) in wl.problems:
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, pj)])
+        _, t, _ = run_oracle(wl, hi, l, pj, want_t=True)
+        got = oracle.lora_expand(hi.pool, hi.pt, p.pt_off, p.ranks, p.scales, p.num_layers, p.num_proj,
+                                 l, pj, t, y0, ids)
+        for i, a in enumerate(ids):
+            if a < 0:
+                assert np.array_equal(got[i], y0[i])
+                continue
+            _, B = dense_adapter(wl, a, l, pj)
+            want = y0[i] + float(p.scales[a]) * (B @ t[i, :B.shape[1]])
+            np.testing.assert_allclose(got[i], want, rtol=1e-13, atol=1e-13)
+
+
+def test_shrink_then_expand_is_the_delta():
+    """The two steps composed (shrink of the C oracle, expand of the Python one) give the
+    whole delta of the C oracle; the expand is linear in t."""
+    wl = small_multi(seed=29)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    p = wl.pool
+    rng = np.random.default_rng(3)
+    for (l, pj) in wl.problems:
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, pj)])
+        y_ref, t, _ = run_oracle(wl, hi, l, pj, want_t=True)
+        args = (hi.pool, hi.pt, p.pt_off, p.ranks, p.scales, p.num_layers, p.num_proj, l, pj)
+        np.testing.assert_allclose(oracle.lora_expand(*args, t, y0, ids), y_ref, rtol=1e-12, atol=1e-12)
+        t2 = rng.standard_normal(t.shape)
+        lhs = oracle.lora_expand(*args, t + t2, y0, ids)
+        rhs = oracle.lora_expand(*args, t, y0, ids) + oracle.lora_expand(*args, t2, np.zeros_like(y0), ids)
+        np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("n_shards", [2, 4])
+def test_tensor_parallel_partition_identity(n_shards):
+    """"S-LoRA: Serving Thousands of Concurrent LoRA Adapters", "Kernels and tensor
+    parallelism": the adapters partitioned as the base model is.  Shard k holds columns
+    [k h/N, (k+1) h/N) of every page: the sum over shards of their shrinks (each over its
+    input columns) is the whole shrink, and each shard's expand with that sum gives its
+    output columns of the whole delta."""
+    from heterogeneous_adapters_gb300 import tp
+    wl = small_multi(seed=31, h=64)
+    hi = host_inputs(wl)
+    ids = wl.batch.token_adapter()
+    p = wl.pool
+    h = p.h
+    for (l, pj) in wl.problems:
+        y0 = vg.bf16_bits_to_f64(hi.y0[(l, pj)])
+        y_ref, t_ref, _ = run_oracle(wl, hi, l, pj, want_t=True)
+        parts = []
+        for k in range(n_shards):
+            lo, hi_ = tp.shard_range(h, n_shards, k)
+            _, tk, _ = oracle.lora_delta(np.ascontiguousarray(hi.pool[:, lo:hi_]), hi.pt, p.pt_off, p.ranks,
+                                         p.scales, p.num_layers, p.num_proj, l, pj,
+                                         np.ascontiguousarray(hi.x[(l, pj)][:, lo:hi_]),
+                                         np.zeros((ids.size, hi_ - lo)), ids, want_t=True)
+            parts.append(tk)
+        t_sum = np.sum(parts, axis=0)
+        np.testing.assert_allclose(t_sum, t_ref, rtol=1e-12, atol=1e-12)
+        for k in range(n_shards):
+            lo, hi_ = tp.shard_range(h, n_shards, k)
+            yk = oracle.lora_expand(np.ascontiguousarray(hi.pool[:, lo:hi_]), hi.pt, p.pt_off, p.ranks, p.scales,
+                                    p.num_layers, p.num_proj, l, pj, t_sum, y0[:, lo:hi_], ids)
+            np.testing.assert_allclose(yk, y_ref[:, lo:hi_], rtol=1e-12, atol=1e-12)
