@@ -799,47 +799,36 @@ def dataclasses_replace_batch(wl, batch):
 
 # ----------------------------------------------------------------------------- staging scenario
 
-class SliceCache:
-    """Host side of adapter staging for the unified-pool stress workload: an LRU over
-    adapter slices (one layer's pages of one adapter) with a fixed capacity; misses are
-    copied from a pinned host copy into free pool pages, and every page-table entry that
-    points into the slice is rewritten (one lora_stage_pages call per step)."""
+class SliceUnits:
+    """The unified-pool stress workload's slices as units of the library's adapter cache
+    (lora_cache_*): unit s is slice s (one layer's pages of one adapter, P * 2 * r_s pages,
+    listed in the pool description slice by slice), read by every page-table entry that
+    points into it.  Holds the fixed maps page-table entry -> (slice, position in the
+    slice), the slices a batch reads, and the pinned host copy of every slice (the host
+    tier the misses are staged from)."""
 
-    def __init__(self, wl, pool_t, capacity: int):
+    def __init__(self, wl, pool_t):
         p = wl.pool
         self.wl = wl
-        self.capacity = capacity
-        n_slices = p.num_adapters
-        self.spp = p.num_proj * 2 * p.ranks.astype(np.int64)          # pages per slice
+        n = p.num_adapters
+        self.spp = (p.num_proj * 2 * p.ranks.astype(np.int64)).astype(np.int32)   # pages per slice
         self.slice_off = np.concatenate([[0], np.cumsum(self.spp)[:-1]])
-        # pages are listed slice by slice in the pool description
-        owner = np.repeat(np.arange(n_slices), self.spp)
+        owner = np.repeat(np.arange(n), self.spp)
         page_slice = np.full(p.num_pages, -1, np.int64)
         page_slice[p.page_ids] = owner
         page_pos = np.full(p.num_pages, -1, np.int64)
         page_pos[p.page_ids] = np.arange(p.page_ids.size) - self.slice_off[owner]
-        # fixed maps: page-table entry -> (slice, position inside the slice)
         self.ent_slice = page_slice[p.pt]
         self.ent_pos = page_pos[p.pt]
         order = np.argsort(self.ent_slice, kind="stable")
-        counts = np.bincount(self.ent_slice, minlength=n_slices)
+        counts = np.bincount(self.ent_slice, minlength=n)
         self.ent_off = np.concatenate([[0], np.cumsum(counts)])
         self.ent_sorted = order.astype(np.int64)
-        self.slice_pages = [p.page_ids[self.slice_off[s]:self.slice_off[s] + self.spp[s]].copy()
-                            for s in range(n_slices)]
-        # pinned host copy of every slice (the host tier), rows in slice order
         self.host = None
         if pool_t is not None:
             import torch
             allp = torch.from_numpy(p.page_ids.astype(np.int64)).to(pool_t.device)
             self.host = pool_t[allp].cpu().pin_memory()
-        # initial residency: the first `capacity` slices; every other page is free
-        self.lru = {s: 0 for s in range(min(capacity, n_slices))}
-        self.clock = 0
-        used = np.zeros(p.num_pages, bool)
-        for s in self.lru:
-            used[self.slice_pages[s]] = True
-        self.free = np.nonzero(~used)[0].astype(np.int32).tolist()
 
     def needed(self, token_adapter) -> np.ndarray:
         """Slices read by a batch: every slice its adapters' page-table blocks point into."""
@@ -849,37 +838,31 @@ class SliceCache:
                                         int(p.ranks[a])) for a in ids])
         return np.unique(self.ent_slice[ent])
 
-    def plan(self, need: np.ndarray, keep: np.ndarray):
-        """Stage the missing slices of `need`; never evict a slice in `keep` or `need`."""
-        self.clock += 1
-        miss = [int(v) for v in need if int(v) not in self.lru]
-        for v in need:
-            if int(v) in self.lru:
-                self.lru[int(v)] = self.clock
-        protect = set(int(v) for v in need) | set(int(v) for v in keep)
-        rows, dst, upd_i, upd_p = [], [], [], []
-        for sl in miss:
-            while len(self.lru) >= self.capacity:
-                cands = [v for v in self.lru if v not in protect]
-                if not cands:      # everything resident is in use: run over capacity
-                    break
-                victim = min(cands, key=self.lru.get)
-                del self.lru[victim]
-                self.free.extend(self.slice_pages[victim].tolist())
-            n = int(self.spp[sl])
-            new = np.array(self.free[-n:], np.int32)
-            del self.free[-n:]
-            self.slice_pages[sl] = new.astype(np.int64)
-            rows.append(np.arange(self.slice_off[sl], self.slice_off[sl] + n))
-            dst.append(new)
-            ent = self.ent_sorted[self.ent_off[sl]:self.ent_off[sl + 1]]
-            upd_i.append(ent)
-            upd_p.append(new[self.ent_pos[ent]])
-            self.lru[sl] = self.clock
-        if not miss:
+    def rewrite(self, s: int, pages: np.ndarray):
+        """Page-table entries of slice s and the pages they take once s sits in `pages`."""
+        ent = self.ent_sorted[self.ent_off[s]:self.ent_off[s + 1]]
+        return ent, pages[self.ent_pos[ent]]
+
+    def plan(self, cache, need):
+        """Acquire every slice of `need` in the adapter cache (one more user each): the
+        misses' host rows, destination pages and page-table rewrites, and the slices that
+        became LOADING (None when every slice was resident)."""
+        rows, dst, ui, up, loading = [], [], [], [], []
+        for s in need:
+            got = cache.try_acquire(int(s))
+            if got is None:
+                raise SystemExit("adapter cache full: every resident slice is in use (raise --stage-headroom)")
+            loaded, pages, _ = got
+            if loaded:
+                rows.append(np.arange(self.slice_off[s], self.slice_off[s] + self.spp[s]))
+                dst.append(pages)
+                ent, new = self.rewrite(int(s), pages.astype(np.int64))
+                ui.append(ent)
+                up.append(new)
+                loading.append(int(s))
+        if not loading:
             return None
-        return (np.concatenate(rows), np.concatenate(dst), np.concatenate(upd_i),
-                np.concatenate(upd_p), len(miss))
+        return np.concatenate(rows), np.concatenate(dst), np.concatenate(ui), np.concatenate(up), loading
 
 
 def step_batches(wl, n: int, variant: str):
@@ -902,87 +885,151 @@ def step_batches(wl, n: int, variant: str):
 
 
 def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
-    """Unified-pool stress with staging: every step has its own batch; the misses of step
-    k+1 are staged on a side stream while step k's delta runs."""
+    """Unified-pool stress with staging, driven by the library's host runtime: each step's
+    requests go through the batch scheduler (lora_sched_*), the adapter cache (lora_cache_*)
+    keeps the slices resident in a fixed share of the pool's pages (least recently used
+    slices no running request reads are evicted), and the misses of step k+1 are staged
+    during step k on a side stream through the copy engines (lora_stage_pages_ce: one host
+    to device copy into a staging buffer, then one small kernel moving the rows into their
+    pages and rewriting the page table).  Reported: the decode kernel's time per step with
+    and without staging running beside it, and the staged bytes over the copy's duration."""
     import torch
 
     import heterogeneous_adapters_gb300 as lora
     wl0 = wl_steps[0]
-    cache = SliceCache(wl0, d.pool, args.stage_capacity)
-    side = torch.cuda.Stream(device=dev)
     p = wl0.pool
+    units = SliceUnits(wl0, d.pool)
+    # The cache's pages: the pages the slices occupy now plus stage_headroom of them taken
+    # from the pool's other pages (the rest stands for KV-cache blocks).  Under this
+    # workload's reading a step reads nearly every slice (each of its adapters reads a
+    # different slice in each of the 32 layers), so the cache must hold about all of them;
+    # the headroom is what lets the slices a step newly needs come in while the ones it
+    # no longer reads leave.
+    n_slice_pages = p.page_ids.size
+    extra = int(n_slice_pages * args.stage_headroom)
+    spare = np.setdiff1d(np.arange(p.num_pages), p.page_ids)[:extra]
+    managed = np.concatenate([p.page_ids, spare]).astype(np.int32)
+    cache = lora.AdapterCache(managed, units.spp)
+    sched = lora.Scheduler(None)
+    side = torch.cuda.Stream(device=dev)
     probs = [(d.x[i], d.y[i], d.x.shape[2], d.y.shape[2], l, pj) for i, (l, pj) in enumerate(d.problems)]
-    ids_dev = [torch.from_numpy(w.batch.token_adapter()).to(dev) for w in wl_steps]
-    needs = [cache.needed(w.batch.token_adapter()) for w in wl_steps]
-    stage_ms, stage_bytes, misses, kern_ms = [], [], [], []
-    pending = []
-    # stage what step 0 needs, synchronously
-    plan = cache.plan(needs[0], np.zeros(0, np.int64))
-    staged_ev = None
+    # room for every slice: the first step stages everything it reads
+    staging = torch.empty(int(units.spp.sum()) * p.h * 2, dtype=torch.uint8, device=dev)
+    T = wl0.batch.num_tokens
+    keep = []   # host buffers of staging calls in flight
 
-    def launch_stage(plan_):
-        rows, dst, ui, up, nmiss = plan_
-        src = cache.host[torch.from_numpy(rows)].pin_memory()
-        dst_t = torch.from_numpy(dst).pin_memory()
+    def batch_of(k):
+        """Step k's requests through the scheduler: one decode token per request."""
+        ids = wl_steps[k].batch.token_adapter()
+        for i, a in enumerate(ids):
+            sched.enqueue(k * T + i, int(a), 1)
+        _, ads, _ = sched.pick(T, T)
+        return ads.astype(np.int32)
+
+    def plan(need):
+        return units.plan(cache, need)
+
+    def launch_stage(plan_, stream):
+        rows, dst, ui, up, loading = plan_
+        src = units.host[torch.from_numpy(rows)].pin_memory()
+        dst_t = torch.from_numpy(dst.astype(np.int32)).pin_memory()
         ui_t = torch.from_numpy(ui.astype(np.int64)).pin_memory()
         up_t = torch.from_numpy(up.astype(np.int32)).pin_memory()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(side):
-            e0.record(side)
-            lora.stage_pages(pool, src, dst_t, dst.size, d.pt, ui_t, up_t, ui.size, side.cuda_stream)
-            e1.record(side)
-        pending.append((src, dst_t, ui_t, up_t))
-        return e0, e1, dst.size * p.h * 2, nmiss
+        assert dst.size * p.h * 2 <= staging.numel(), "staging buffer too small for one step's misses"
+        e0, e_copy, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e_copy.record(stream)   # creates the event; the library records it again after the copy
+        e0.record(stream)
+        lora.stage_pages_ce(pool, src, staging, staging.numel(), dst_t, dst.size, d.pt, ui_t, up_t, ui.size,
+                            stream.cuda_stream, copied_event=e_copy)
+        e1.record(stream)
+        keep.append((src, dst_t, ui_t, up_t))
+        return e0, e_copy, e1, dst.size * p.h * 2, loading
 
-    if plan is not None:
-        e0, e1, nb, nm = launch_stage(plan)
+    # step 0's slices, staged before the loop
+    ads0 = batch_of(0)
+    need = units.needed(ads0)
+    pl = plan(need)
+    if pl is not None:
+        _, _, _, _, loading = launch_stage(pl, stream_obj)
         torch.cuda.synchronize()
+        for s in loading:
+            cache.loaded(s)
+    kern_ms, copy_ms, stage_ms, stage_bytes, misses = [], [], [], [], []
+    staged = None
+    ads = ads0
     for k in range(len(wl_steps)):
-        if staged_ev is not None:
-            stream_obj.wait_event(staged_ev[1])
-            staged_ev[1].synchronize()
-            stage_ms.append(staged_ev[0].elapsed_time(staged_ev[1]))
-            stage_bytes.append(staged_ev[2])
-            misses.append(staged_ev[3])
-            staged_ev = None
+        if staged is not None:   # step k's misses, staged during step k-1
+            stream_obj.wait_event(staged[2])
+            staged[2].synchronize()
+            copy_ms.append(staged[0].elapsed_time(staged[1]))
+            stage_ms.append(staged[0].elapsed_time(staged[2]))
+            stage_bytes.append(staged[3])
+            misses.append(len(staged[4]))
+            for s in staged[4]:
+                cache.loaded(s)
+            staged = None
+        tok = torch.from_numpy(ads).to(dev)
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         k0.record(stream_obj)
-        T = wl_steps[k].batch.num_tokens
-        lora.bgmv(pool, probs, ids_dev[k], T, ws, nbytes, stream_obj.cuda_stream)
+        lora.bgmv(pool, probs, tok, T, ws, nbytes, stream_obj.cuda_stream)
         k1.record(stream_obj)
+        nxt_ads, nxt_need = None, None
         if k + 1 < len(wl_steps):
-            plan = cache.plan(needs[k + 1], needs[k])
-            if plan is not None:
-                staged_ev = launch_stage(plan)
+            nxt_ads = batch_of(k + 1)
+            nxt_need = units.needed(nxt_ads)
+            pl = plan(nxt_need)   # step k's slices have users: they are never evicted
+            if pl is not None:
+                with torch.cuda.stream(side):
+                    staged = launch_stage(pl, side)
         k1.synchronize()
         kern_ms.append(k0.elapsed_time(k1))
+        for s in need:   # step k is done with its slices
+            cache.release(int(s))
+        keep[:] = keep[-2:]
+        ads, need = nxt_ads, nxt_need
     torch.cuda.synchronize()
     err = lora.get_device_error(ws, stream_obj.cuda_stream)
-    # the same copy path with nothing else running: stage 64 resident slices into free pages
-    iso = None
-    victims = [v for v in list(cache.lru)[:64]]
-    if victims and cache.host is not None:
-        rows = np.concatenate([np.arange(cache.slice_off[v], cache.slice_off[v] + cache.spp[v]) for v in victims])
-        free = np.array(cache.free[-rows.size:], np.int32) if len(cache.free) >= rows.size else None
-        if free is not None:
-            src = cache.host[torch.from_numpy(rows)].pin_memory()
-            dst_t = torch.from_numpy(free).pin_memory()
+    # the same decode step with nothing staged beside it
+    tok = torch.from_numpy(wl_steps[-1].batch.token_adapter()).to(dev)
+    alone = []
+    for _ in range(5):
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream_obj)
+        lora.bgmv(pool, probs, tok, T, ws, nbytes, stream_obj.cuda_stream)
+        k1.record(stream_obj)
+        k1.synchronize()
+        alone.append(k0.elapsed_time(k1))
+    # the copy alone: the median step's bytes (and 4x as many) with nothing else running
+    alone_copy = {}
+    for mult in (1, 4):
+        nbytes_c = int(min(staging.numel(), (statistics.median(stage_bytes) if stage_bytes else 0) * mult))
+        if nbytes_c <= 0:
+            break
+        src = torch.empty(nbytes_c, dtype=torch.uint8).pin_memory()
+        ms = []
+        for _ in range(5):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            for rep in range(3):
-                e0.record(side)
-                lora.stage_pages(pool, src, dst_t, free.size, None, None, None, 0, side.cuda_stream)
-                e1.record(side)
-                e1.synchronize()
-            iso = {"bytes": int(free.size) * p.h * 2, "ms": e0.elapsed_time(e1),
-                   "gbs": free.size * p.h * 2 / (e0.elapsed_time(e1) * 1e6)}
-    return {"steps": len(wl_steps), "kernel_ms_median": statistics.median(kern_ms),
-            "isolated_stage": iso,
-            "stage_ms_median": statistics.median(stage_ms) if stage_ms else 0.0,
-            "stage_bytes_median": statistics.median(stage_bytes) if stage_bytes else 0,
-            "stage_gbs_median": (statistics.median([b / (t * 1e6) for b, t in zip(stage_bytes, stage_ms)])
-                                 if stage_ms else None),
-            "slices_staged_median": statistics.median(misses) if misses else 0,
-            "capacity_slices": cache.capacity, "device_error": err}
+            e0.record(side)
+            with torch.cuda.stream(side):
+                staging[:nbytes_c].copy_(src, non_blocking=True)
+            e1.record(side)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        alone_copy[f"{nbytes_c}"] = {"ms": statistics.median(ms), "gbs": nbytes_c / (statistics.median(ms) * 1e6)}
+    st = cache.stats()
+    cache.close()
+    sched.close()
+    med = statistics.median
+    return {"steps": len(wl_steps), "runtime": "lora_cache_* (slices as units), lora_sched_*, lora_stage_pages_ce",
+            "kernel_ms_median": med(kern_ms), "kernel_ms_alone_median": med(alone),
+            "kernel_slowdown": med(kern_ms) / med(alone) - 1.0,
+            "copy_ms_median": med(copy_ms) if copy_ms else 0.0,
+            "stage_ms_median": med(stage_ms) if stage_ms else 0.0,
+            "stage_bytes_median": med(stage_bytes) if stage_bytes else 0,
+            "copy_gbs_median": (med([b / (t * 1e6) for b, t in zip(stage_bytes, copy_ms)]) if copy_ms else None),
+            "copy_alone": alone_copy,
+            "slices_staged_median": med(misses) if misses else 0, "cache_pages": int(managed.size),
+            "cache": st, "device_error": err}
 
 
 def main():
@@ -1005,8 +1052,9 @@ def main():
     ap.add_argument("--ref-problems", type=int, default=16,
                     help="projections whose host inputs the oracle prepares")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--stage-capacity", type=int, default=1500,
-                    help="resident adapter slices in the unified-pool stress workload")
+    ap.add_argument("--stage-headroom", type=float, default=0.05,
+                    help="unified-pool stress: pages the adapter cache holds beyond the slices' own, "
+                         "as a fraction of them")
     ap.add_argument("--stage-steps", type=int, default=20,
                     help="steps of the staging scenario (stress-distinct / stress-zipf)")
     ap.add_argument("--shared-x", action="store_true",

@@ -10,12 +10,13 @@ from ._binding import (DERR, LORA_ENOSPACE, LORA_MAX_PROBLEMS_PER_LAUNCH, LORA_M
                        LORA_UNIT_READY, AdapterCache, LoraError, Pool, Scheduler, apply_mixed, bgmv,
                        bgmv_noalloc, debug_delta_with_t, debug_page_list, debug_wait_limit, delta_grouped,
                        expand, get_device_error, shrink,
-                       lib, segment, sgmv, stage_pages, workspace_init, workspace_size, workspace_view)
+                       lib, segment, sgmv, stage_pages, stage_pages_ce, workspace_init, workspace_size,
+                       workspace_view)
 
 __all__ = ["costmodel", "DERR", "LORA_ENOSPACE", "LORA_MAX_PROBLEMS_PER_LAUNCH", "LORA_MAX_RANK",
            "LORA_MAX_SEGMENTS", "LORA_NOALLOC_MAX_TOKENS", "LORA_UNIT_ABSENT", "LORA_UNIT_LOADING",
            "LORA_UNIT_READY", "AdapterCache", "LoraError", "Pool", "Scheduler", "apply_mixed",
            "bgmv", "bgmv_noalloc", "debug_delta_with_t", "debug_page_list", "debug_wait_limit",
            "delta_grouped", "expand", "shrink",
-           "get_device_error", "lib", "segment", "sgmv", "stage_pages", "workspace_init",
+           "get_device_error", "lib", "segment", "sgmv", "stage_pages", "stage_pages_ce", "workspace_init",
            "workspace_size", "workspace_view"]

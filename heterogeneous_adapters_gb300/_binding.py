@@ -25,7 +25,7 @@ EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_pool_set_tuning", "lo
             "lora_segment", "lora_workspace_view", "lora_bgmv", "lora_sgmv", "lora_apply_mixed",
             "lora_delta_grouped", "lora_debug_page_list", "lora_debug_delta_with_t", "lora_debug_wait_limit",
             "lora_stage_pages", "lora_bgmv_noalloc", "lora_get_device_error", "lora_shrink",
-            "lora_expand",
+            "lora_expand", "lora_stage_pages_ce",
             "lora_last_cuda_error", "lora_status_string",
             # host runtime (include/lora_runtime.h)
             "lora_cache_create", "lora_cache_destroy", "lora_cache_acquire", "lora_cache_loaded",
@@ -102,6 +102,7 @@ def lib():
             "lora_debug_delta_with_t": [p, ctypes.POINTER(lora_problem), p, sz, p, p],
             "lora_debug_wait_limit": [p, sz, ctypes.c_uint64, p, p],
             "lora_stage_pages": [p, p, p, i32, p, p, p, i64, p],
+            "lora_stage_pages_ce": [p, p, p, sz, p, i32, p, p, p, i64, p, p],
             "lora_bgmv_noalloc": [p, p, i32, p, i32, p, p],
             "lora_shrink": [p, p, i32, p, i32, p, sz, p, p],
             "lora_expand": [p, p, i32, i32, p, sz, p, p],
@@ -275,6 +276,20 @@ def stage_pages(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_p
     _check(lib().lora_stage_pages(pool.handle, _ptr(host_rows), _ptr(dst_pages), npages,
                                   _ptr(page_table), _ptr(upd_index), _ptr(upd_page), nupd, stream),
            "lora_stage_pages")
+
+
+def stage_pages_ce(pool, host_rows, staging, staging_bytes, dst_pages, npages, page_table, upd_index, upd_page,
+                   nupd, stream, copied_event=None):
+    """Staging through the copy engines: host rows -> device staging buffer (one copy), then
+    staging rows -> pool pages and the page-table rewrite (one kernel).  host_rows, dst_pages,
+    upd_index, upd_page: pinned host tensors; staging: a device buffer of npages * 2h bytes;
+    copied_event: a torch.cuda.Event (or raw handle) recorded right after the copy."""
+    ev = None
+    if copied_event is not None:
+        ev = copied_event.cuda_event if hasattr(copied_event, "cuda_event") else copied_event
+    _check(lib().lora_stage_pages_ce(pool.handle, _ptr(host_rows), _ptr(staging), staging_bytes,
+                                     _ptr(dst_pages), npages, _ptr(page_table), _ptr(upd_index),
+                                     _ptr(upd_page), nupd, ev, stream), "lora_stage_pages_ce")
 
 
 def bgmv_noalloc(pool, problems, token_adapter, T, error_bits, stream):

@@ -477,41 +477,78 @@ lora_status lora_debug_wait_limit(void* ws, size_t ws_bytes, uint64_t limit_ns, 
     return cuda_status(cudaGetLastError());
 }
 
-lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const int32_t* dst_pages,
-                             int32_t npages, int32_t* page_table, const int64_t* upd_index,
-                             const int32_t* upd_page, int64_t nupd, void* stream) {
+// Host-side checks of a staging call (the index arrays are host memory).
+static lora_status check_stage(const lora_pool* pool, const void* rows, const int32_t* dst_pages, int32_t npages,
+                               int32_t* page_table, const int64_t* upd_index, const int32_t* upd_page, int64_t nupd) {
     if (pool == nullptr || npages < 0 || nupd < 0) return LORA_EINVAL;
     const lora_pool_desc& d = pool->d;
-    if (npages > 0 && (host_rows == nullptr || dst_pages == nullptr)) return LORA_EINVAL;
-    if (nupd > 0 && (page_table == nullptr || upd_index == nullptr || upd_page == nullptr))
-        return LORA_EINVAL;
+    if (npages > 0 && (rows == nullptr || dst_pages == nullptr)) return LORA_EINVAL;
+    if (nupd > 0 && (page_table == nullptr || upd_index == nullptr || upd_page == nullptr)) return LORA_EINVAL;
     if (nupd > 0 && page_table != d.page_table) return LORA_EINVAL;
-    if (npages > 0 && !aligned16(host_rows)) return LORA_EALIGN;
+    if (npages > 0 && !aligned16(rows)) return LORA_EALIGN;
     for (int32_t i = 0; i < npages; ++i)
         if (dst_pages[i] < 0 || dst_pages[i] >= d.num_pages) return LORA_EINVAL;
     for (int64_t k = 0; k < nupd; ++k) {
         if (upd_index[k] < 0 || upd_index[k] >= d.page_table_len) return LORA_EINVAL;
         if (upd_page[k] < 0 || upd_page[k] >= d.num_pages) return LORA_EINVAL;
     }
-    if (npages == 0 && nupd == 0) return LORA_OK;
+    return LORA_OK;
+}
+
+// The staging kernel: rows (host memory read through its mapping, or device memory) into
+// pool pages, then the page-table rewrite.
+static lora_status launch_stage(const lora_pool* pool, const void* rows, const int32_t* dst_pages, int32_t npages,
+                                int32_t* page_table, const int64_t* upd_index, const int32_t* upd_page, int64_t nupd,
+                                cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
     StageParams sp;
-    sp.host_rows = reinterpret_cast<const uint4*>(host_rows);
+    sp.host_rows = reinterpret_cast<const uint4*>(rows);
     sp.dst_pages = dst_pages;
-    sp.pages = reinterpret_cast<__nv_bfloat16*>(d.pages);
+    sp.pages = reinterpret_cast<__nv_bfloat16*>(pool->d.pages);
     sp.pt = page_table;
     sp.upd_index = upd_index;
     sp.upd_page = upd_page;
     sp.nupd = nupd;
     sp.npages = npages;
-    sp.vec_per_row = d.h / 8;
+    sp.vec_per_row = pool->d.h / 8;
     int grid = di->sm_count * 4;
     if (npages > 0 && npages < grid) grid = npages;
     if (grid < 1) grid = 1;
-    stage_kernel<<<grid, kStageThreads, 0, (cudaStream_t)stream>>>(sp);
+    stage_kernel<<<grid, kStageThreads, 0, stream>>>(sp);
     return cuda_status(cudaGetLastError());
+}
+
+lora_status lora_stage_pages_ce(const lora_pool* pool, const void* host_rows, void* staging, size_t staging_bytes,
+                                const int32_t* dst_pages, int32_t npages, int32_t* page_table,
+                                const int64_t* upd_index, const int32_t* upd_page, int64_t nupd, void* copied,
+                                void* stream) {
+    lora_status st = check_stage(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_page, nupd);
+    if (st != LORA_OK) return st;
+    const size_t bytes = (size_t)npages * (size_t)pool->d.h * 2;
+    if (npages > 0 && (staging == nullptr || !aligned16(staging) || staging_bytes < bytes)) return LORA_EINVAL;
+    if (npages == 0 && nupd == 0) return LORA_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (npages > 0) {
+        st = cuda_status(cudaMemcpyAsync(staging, host_rows, bytes, cudaMemcpyHostToDevice, s));
+        if (st != LORA_OK) return st;
+    }
+    if (copied != nullptr) {
+        st = cuda_status(cudaEventRecord((cudaEvent_t)copied, s));
+        if (st != LORA_OK) return st;
+    }
+    return launch_stage(pool, staging, dst_pages, npages, page_table, upd_index, upd_page, nupd, s);
+}
+
+lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const int32_t* dst_pages,
+                             int32_t npages, int32_t* page_table, const int64_t* upd_index,
+                             const int32_t* upd_page, int64_t nupd, void* stream) {
+    lora_status st = check_stage(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_page, nupd);
+    if (st != LORA_OK) return st;
+    if (npages == 0 && nupd == 0) return LORA_OK;
+    return launch_stage(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_page, nupd,
+                        (cudaStream_t)stream);
 }
 
 lora_status lora_bgmv_noalloc(const lora_pool* pool, const lora_problem* probs, int32_t nprob,

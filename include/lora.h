@@ -308,6 +308,25 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
                              int32_t npages, int32_t* page_table, const int64_t* upd_index,
                              const int32_t* upd_page, int64_t nupd, void* stream);
 
+/* Adapter staging through the copy engines: one cudaMemcpyAsync on `stream` copies the
+ * npages rows (host_rows, pinned host memory, row i = h bf16 values, 16-byte aligned)
+ * into `staging` (caller-owned device memory of at least npages * 2h bytes, 16-byte
+ * aligned); the copy uses the host link's copy engine and no SM, so it proceeds at the
+ * link's rate while kernels hold every SM.  Then one kernel on `stream` moves staging row
+ * i into pool page dst_pages[i] (device to device) and sets page_table[upd_index[k]] =
+ * upd_page[k], as lora_stage_pages does.  dst_pages, upd_index and upd_page are pinned
+ * host memory, validated on the host before anything is launched.  The caller keeps
+ * host_rows, staging and the index arrays alive until the work on `stream` has finished,
+ * orders consumers after it with an event, and must not stage into pages that a running
+ * kernel reads.  The page moves and the page-table rewrite need an SM: while a persistent
+ * kernel holds them all, that small kernel starts when it ends.  copied (a cudaEvent_t
+ * passed as void*, may be NULL) is recorded on `stream` right after the copy: once it
+ * has completed, host_rows may be reused. */
+lora_status lora_stage_pages_ce(const lora_pool* pool, const void* host_rows, void* staging,
+                                size_t staging_bytes, const int32_t* dst_pages, int32_t npages,
+                                int32_t* page_table, const int64_t* upd_index, const int32_t* upd_page,
+                                int64_t nupd, void* copied, void* stream);
+
 /* Allocation-free BGMV.  The pages this library follows have no counterpart of this
  * call.  It is for callers that have no way to obtain device memory for a workspace:
  * a serving engine that reserves all of the GPU's memory for its own pools at start-up

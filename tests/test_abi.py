@@ -112,12 +112,12 @@ def test_stage_pages_host_checks(lib):
     bad_idx = np.array([0, 32], np.int64)
     pg = np.array([1, 2], np.int32)
     c = lambda a: a.ctypes.data  # noqa: E731
-    assert lib.lora_stage_pages(h, c(rows), c(bad), 2, None, None, None, 0, None) == LORA_EINVAL
-    assert lib.lora_stage_pages(h, c(rows) + 2, c(good), 2, None, None, None, 0, None) == LORA_EALIGN
+    assert lib.lora_stage_pages(h, c(rows), c(bad), 2, None, None, None, 0, None, None) == LORA_EINVAL
+    assert lib.lora_stage_pages(h, c(rows) + 2, c(good), 2, None, None, None, 0, None, None) == LORA_EALIGN
     assert lib.lora_stage_pages(h, None, None, 0, c(pt), c(bad_idx), c(pg), 2, None) == LORA_EINVAL
     other = np.zeros(32, np.int32)
     assert lib.lora_stage_pages(h, None, None, 0, c(other), c(idx), c(pg), 2, None) == LORA_EINVAL
-    assert lib.lora_stage_pages(h, None, None, 0, None, None, None, 0, None) == 0
+    assert lib.lora_stage_pages(h, None, None, 0, None, None, None, 0, None, None) == 0
     lib.lora_pool_destroy(h)
 
 
@@ -154,4 +154,32 @@ def test_pool_tuning_defaults_overrides_and_checks(lib):
         assert get() == (0, 0, 64, 3, 1.22)
     assert lib.lora_pool_set_tuning(h, None) == 0
     assert get() == default
+    lib.lora_pool_destroy(h)
+
+
+def test_stage_pages_ce_host_checks(lib):
+    """The copy-engine staging validates its index arrays and its staging buffer before
+    launching or copying anything."""
+    import numpy as np
+
+    from heterogeneous_adapters_gb300._binding import LORA_EALIGN, LORA_EINVAL, lora_pool_desc
+    h = ctypes.c_void_p()
+    pt = np.zeros(32, np.int32)
+    d = lora_pool_desc(1 << 20, 16, 256, 2, 1, 1, 8, 0, pt.ctypes.data, 32, 1 << 20, 1 << 20, 1 << 20)
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(d)) == 0
+    rows = np.zeros((2, 256), np.uint16)
+    good = np.array([3, 4], np.int32)
+    c = lambda a: a.ctypes.data  # noqa: E731
+    stage = 1 << 20          # a device address stand-in: never used, the checks fail first
+    assert lib.lora_stage_pages_ce(h, c(rows), stage, 2 * 512, c(np.array([3, 16], np.int32)), 2,
+                                   None, None, None, 0, None, None) == LORA_EINVAL          # page out of range
+    assert lib.lora_stage_pages_ce(h, c(rows), stage, 2 * 512 - 16, c(good), 2, None, None, None, 0,
+                                   None, None) == LORA_EINVAL                               # staging too small
+    assert lib.lora_stage_pages_ce(h, c(rows), None, 2 * 512, c(good), 2, None, None, None, 0,
+                                   None, None) == LORA_EINVAL                               # no staging buffer
+    assert lib.lora_stage_pages_ce(h, c(rows), stage + 8, 2 * 512, c(good), 2, None, None, None, 0,
+                                   None, None) == LORA_EINVAL                               # misaligned staging
+    assert lib.lora_stage_pages_ce(h, c(rows) + 2, stage, 2 * 512, c(good), 2, None, None, None, 0,
+                                   None, None) == LORA_EALIGN                               # misaligned rows
+    assert lib.lora_stage_pages_ce(h, None, None, 0, None, 0, None, None, None, 0, None, None) == 0
     lib.lora_pool_destroy(h)

@@ -1,7 +1,8 @@
 """A miniature serving loop on the GPU: requests arrive for adapters held in host memory,
 the adapter cache (include/lora_runtime.h) gives each missing adapter pool pages (evicting
-least recently used adapters nobody uses), lora_stage_pages copies its rows in and points
-its page-table entries at them, the scheduler picks each step's batch under a token cap and
+least recently used adapters nobody uses), lora_stage_pages (a kernel reading the host rows
+through their mapping) or lora_stage_pages_ce (the copy engines into a staging buffer, then a
+kernel) copies its rows in and points its page-table entries at them, the scheduler picks each step's batch under a token cap and
 a distinct-adapter cap, lora_bgmv applies the deltas, and every step is checked against the
 fp64 oracle.  Pages freed by evictions are reused, so a stale page-table entry or a missed
 copy shows up as a wrong (or NaN) row.
@@ -21,7 +22,8 @@ from .harness import check_gate
 pytestmark = pytest.mark.gpu
 
 
-def test_serving_loop_with_cache_scheduler_and_staging():
+@pytest.mark.parametrize("path", ["mapped", "copy_engine"])
+def test_serving_loop_with_cache_scheduler_and_staging(path):
     import torch
 
     import heterogeneous_adapters_gb300 as lora
@@ -54,12 +56,18 @@ def test_serving_loop_with_cache_scheduler_and_staging():
     rng = np.random.default_rng(11)
     probs_lp = spec.all_problems(L, P)
 
+    staging = torch.empty(int(n_pages.max()) * h * 2, dtype=torch.uint8, device=dev)
+
     def stage(a, dst):
         ent = np.arange(src.pt_off[a], src.pt_off[a] + n_pages[a], dtype=np.int64)
         dst_t = torch.from_numpy(dst.astype(np.int32)).pin_memory()
         ui = torch.from_numpy(ent).pin_memory()
         up = torch.from_numpy(dst.astype(np.int32)).pin_memory()
-        lora.stage_pages(pool, host[a], dst_t, dst.size, pt, ui, up, ent.size, stream)
+        if path == "mapped":
+            lora.stage_pages(pool, host[a], dst_t, dst.size, pt, ui, up, ent.size, stream)
+        else:
+            lora.stage_pages_ce(pool, host[a], staging, staging.numel(), dst_t, dst.size, pt, ui, up, ent.size,
+                                stream)
         torch.cuda.synchronize()        # the copy is done: the adapter becomes ready
         cache.loaded(a)
 

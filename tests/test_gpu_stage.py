@@ -1,6 +1,8 @@
-"""Adapter staging from pinned host memory: pages land bit-exact in their new pool
-slots, the page table is rewritten in the same kernel, and a delta launch ordered
-after it (event on a side stream) reads the moved adapter correctly."""
+"""Adapter staging from pinned host memory, by the kernel that reads the host rows
+through their mapping (lora_stage_pages) and through the copy engines into a device
+staging buffer (lora_stage_pages_ce): pages land bit-exact in their new pool slots, the
+page table is rewritten, and a delta launch ordered after it (event on a side stream)
+reads the moved adapter correctly."""
 import numpy as np
 import pytest
 
@@ -11,7 +13,8 @@ from .harness import GpuCase, full_check
 pytestmark = pytest.mark.gpu
 
 
-def test_stage_moves_adapters_to_free_pages():
+@pytest.mark.parametrize("path", ["mapped", "copy_engine"])
+def test_stage_moves_adapters_to_free_pages(path):
     import torch
 
     import heterogeneous_adapters_gb300 as lora
@@ -37,9 +40,14 @@ def test_stage_moves_adapters_to_free_pages():
         upd_index = torch.from_numpy(entries.astype(np.int64)).pin_memory()
         upd_page = torch.from_numpy(new_pages).pin_memory()
         side = torch.cuda.Stream(device=case.device)
+        staging = torch.empty(entries.size * wl.pool.h * 2, dtype=torch.uint8, device=case.device)
         with torch.cuda.stream(side):
-            lora.stage_pages(case.pool, host_rows, dst, entries.size, dev.pt, upd_index, upd_page,
-                             entries.size, side.cuda_stream)
+            if path == "mapped":
+                lora.stage_pages(case.pool, host_rows, dst, entries.size, dev.pt, upd_index, upd_page,
+                                 entries.size, side.cuda_stream)
+            else:
+                lora.stage_pages_ce(case.pool, host_rows, staging, staging.numel(), dst, entries.size, dev.pt,
+                                    upd_index, upd_page, entries.size, side.cuda_stream)
             done = torch.cuda.Event()
             done.record(side)
         torch.cuda.current_stream(case.device).wait_event(done)
