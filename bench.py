@@ -679,7 +679,7 @@ def run_sweep_few(args, local: int):
 
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    wl = workload_for("decode")
+    wl = workload_for(args.config)   # the Llama-7B decode batch unless --config names another
     d = device_inputs(wl, device=dev, nan_dummies=False)
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
@@ -696,6 +696,8 @@ def run_sweep_few(args, local: int):
     kernels = {"cluster": dict(split_max_problems=8), "ring": dict(split_max_problems=0)}
     for n in (1, 2, 3, 4, 6, 8):
         groups = [probs[i:i + n] for i in range(0, len(probs) - n + 1, n)]
+        if not groups:
+            continue
         m = step_model(wl, problems=wl.problems[:n])
         for name, tun in kernels.items():
             pool.set_tuning(**tun)
