@@ -37,13 +37,17 @@ UNIT = "tokens/s"
 
 def workload_for(name: str):
     """A named workload of the workload module, or a small variant of one for profiler
-    captures: "decode-small" (4 layers, 300 adapters, ~2.4 GB pool), "prefill-small" (2
+    captures: "decode-small" (4 layers, 300 adapters, ~2.4 GB pool), "decode-l12" (12 layers,
+    100 adapters, ~2.4 GB: enough projections per launch for a sweep), "prefill-small" (2
     layers x 2 projections, ~2 GB on the device), "mixed-small" (1 layer x 2 projections),
     "llama3-decode-small" and "llama3-prefill-small" (1 layer)."""
     from workloads import spec
     if name == "decode-small":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a300-l4", 1001, 4096, 4, 4,
                                     300, [8, 16, 32, 64], 64, 1.0)
+    if name == "decode-l12":
+        return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a100-l12", 1001, 4096, 12, 4,
+                                    100, [8, 16, 32, 64], 64, 1.0)
     if name == "prefill-small":
         return spec.prefill_workload("llama7b-prefill-sgmv-h4096-s32-a1000-l2p2", 1002, 4096, 2, 2,
                                      1000, [8, 16, 32, 64], 32, 64, 1024, 1.0)
@@ -612,8 +616,10 @@ def run_ours(args, rank: int, world: int, local: int):
 # ----------------------------------------------------------------------------- distinct-adapter sweep
 
 def run_sweep_distinct(args, local: int):
-    """The Llama-7B decode workload's pool and projections; the 64 decode tokens spread round-robin over D
-    adapters drawn without replacement from the 2,000 (seed 7000 + D), D = 1, 2, 4, ..., 64.
+    """The decode workload's pool and projections (--config; the Llama-7B decode workload by
+    default); its decode tokens spread round-robin over D adapters drawn without replacement
+    from its adapters (seed 7000 + D), D = 1, 2, 4, ..., 64
+    (--sweep-counts).
     One JSON line per D: step time of the delta launch (CUDA events, K steps after W warm-up),
     adapted tokens/s and the fraction of the measured HBM peak."""
     import torch
@@ -623,7 +629,7 @@ def run_sweep_distinct(args, local: int):
 
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    wl = workload_for("decode")
+    wl = workload_for(args.config)
     d = device_inputs(wl, device=dev, nan_dummies=False)
     p = wl.pool
     pool = lora.Pool(d.pool, p.num_pages, p.h, d.pt, p.pt.size, d.pt_off, d.ranks, d.scales,
@@ -637,7 +643,7 @@ def run_sweep_distinct(args, local: int):
     lora.workspace_init(ws, nbytes, stream)
     probs = [(d.x[i], d.y[i], d.x.shape[2], d.y.shape[2], l, pj) for i, (l, pj) in enumerate(d.problems)]
     peaks = measured_peaks()
-    for D in (1, 2, 4, 8, 16, 32, 64):
+    for D in (int(v) for v in args.sweep_counts.split(",")):
         rng = np.random.default_rng(7000 + D)
         chosen = rng.choice(p.num_adapters, size=D, replace=False)
         ids = chosen[np.arange(T) % D].astype(np.int32)
@@ -892,9 +898,11 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
     keeps the slices resident in a fixed share of the pool's pages (least recently used
     slices no running request reads are evicted), and the misses of step k+1 are staged
     during step k on a side stream through the copy engines (lora_stage_pages_ce: one host
-    to device copy into a staging buffer, then one small kernel moving the rows into their
-    pages and rewriting the page table).  Reported: the decode kernel's time per step with
-    and without staging running beside it, and the staged bytes over the copy's duration."""
+    to device copy per run of consecutive destination pages straight into the pool -- the
+    cache hands a slice's pages out of its free list in a run -- then one small kernel
+    rewriting the page table).  Reported: the decode kernel's time per step with staging
+    running beside it and, for the same steps' batches, without; the staged bytes over the
+    copies' duration."""
     import torch
 
     import heterogeneous_adapters_gb300 as lora
@@ -956,7 +964,7 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
         torch.cuda.synchronize()
         for s in loading:
             cache.loaded(s)
-    kern_ms, copy_ms, stage_ms, stage_bytes, misses = [], [], [], [], []
+    kern_ms, copy_ms, stage_ms, stage_bytes, misses, step_ads = [], [], [], [], [], []
     staged = None
     ads = ads0
     for k in range(len(wl_steps)):
@@ -971,6 +979,7 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
                 cache.loaded(s)
             staged = None
         tok = torch.from_numpy(ads).to(dev)
+        step_ads.append(ads)
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         k0.record(stream_obj)
         lora.bgmv(pool, probs, tok, T, ws, nbytes, stream_obj.cuda_stream)
@@ -991,10 +1000,10 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
         ads, need = nxt_ads, nxt_need
     torch.cuda.synchronize()
     err = lora.get_device_error(ws, stream_obj.cuda_stream)
-    # the same decode step with nothing staged beside it
-    tok = torch.from_numpy(wl_steps[-1].batch.token_adapter()).to(dev)
+    # the same decode steps (each step's batch, every slice resident) with nothing staged beside them
     alone = []
-    for _ in range(5):
+    for ads_k in step_ads:
+        tok = torch.from_numpy(ads_k).to(dev)
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         k0.record(stream_obj)
         lora.bgmv(pool, probs, tok, T, ws, nbytes, stream_obj.cuda_stream)
@@ -1025,6 +1034,7 @@ def run_staging(args, wl_steps, pool, d, ws, nbytes, stream_obj, dev):
     return {"steps": len(wl_steps), "runtime": "lora_cache_* (slices as units), lora_sched_*, lora_stage_pages_ce",
             "kernel_ms_median": med(kern_ms), "kernel_ms_alone_median": med(alone),
             "kernel_slowdown": med(kern_ms) / med(alone) - 1.0,
+            "kernel_slowdown_per_step_median": med([a / b - 1.0 for a, b in zip(kern_ms, alone)]),
             "copy_ms_median": med(copy_ms) if copy_ms else 0.0,
             "stage_ms_median": med(stage_ms) if stage_ms else 0.0,
             "stage_bytes_median": med(stage_bytes) if stage_bytes else 0,
@@ -1076,6 +1086,8 @@ def main():
                          "batch through the cluster and ring kernels")
     ap.add_argument("--sweep-ranks", default="8,16,64,128")
     ap.add_argument("--sweep-lengths", default="1,2,4,8,16,32,64,128")
+    ap.add_argument("--sweep-counts", default="1,2,4,8,16,32,64",
+                    help="distinct-adapter counts of --sweep-distinct")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

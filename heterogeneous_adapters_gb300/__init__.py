@@ -6,7 +6,8 @@ the sources (csrc/), the in-tree build, the ctypes binding and the byte/flop mod
 to report throughput against the HBM roofline."""
 from . import costmodel
 from ._binding import (DERR, LORA_ENOSPACE, LORA_MAX_PROBLEMS_PER_LAUNCH, LORA_MAX_RANK,
-                       LORA_MAX_SEGMENTS, LORA_NOALLOC_MAX_TOKENS, LORA_UNIT_ABSENT, LORA_UNIT_LOADING,
+                       LORA_MAX_SEGMENTS, LORA_NOALLOC_MAX_TOKENS, LORA_STAGE_MAX_RUNS, LORA_UNIT_ABSENT,
+                       LORA_UNIT_LOADING,
                        LORA_UNIT_READY, AdapterCache, LoraError, Pool, Scheduler, apply_mixed, bgmv,
                        bgmv_noalloc, debug_delta_with_t, debug_page_list, debug_wait_limit, delta_grouped,
                        expand, get_device_error, shrink,
@@ -14,7 +15,8 @@ from ._binding import (DERR, LORA_ENOSPACE, LORA_MAX_PROBLEMS_PER_LAUNCH, LORA_M
                        workspace_view)
 
 __all__ = ["costmodel", "DERR", "LORA_ENOSPACE", "LORA_MAX_PROBLEMS_PER_LAUNCH", "LORA_MAX_RANK",
-           "LORA_MAX_SEGMENTS", "LORA_NOALLOC_MAX_TOKENS", "LORA_UNIT_ABSENT", "LORA_UNIT_LOADING",
+           "LORA_MAX_SEGMENTS", "LORA_NOALLOC_MAX_TOKENS", "LORA_STAGE_MAX_RUNS", "LORA_UNIT_ABSENT",
+           "LORA_UNIT_LOADING",
            "LORA_UNIT_READY", "AdapterCache", "LoraError", "Pool", "Scheduler", "apply_mixed",
            "bgmv", "bgmv_noalloc", "debug_delta_with_t", "debug_page_list", "debug_wait_limit",
            "delta_grouped", "expand", "shrink",

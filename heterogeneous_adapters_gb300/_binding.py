@@ -19,6 +19,7 @@ LORA_MAX_PROBLEMS_PER_LAUNCH = 256
 LORA_MAX_SEGMENTS = 16384
 LORA_MAX_RANK = 256
 LORA_NOALLOC_MAX_TOKENS = 4096
+LORA_STAGE_MAX_RUNS = 64
 
 EXPORTED = ["lora_pool_create", "lora_pool_destroy", "lora_pool_set_tuning", "lora_pool_get_tuning",
             "lora_workspace_size", "lora_workspace_init",
@@ -280,10 +281,12 @@ def stage_pages(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_p
 
 def stage_pages_ce(pool, host_rows, staging, staging_bytes, dst_pages, npages, page_table, upd_index, upd_page,
                    nupd, stream, copied_event=None):
-    """Staging through the copy engines: host rows -> device staging buffer (one copy), then
-    staging rows -> pool pages and the page-table rewrite (one kernel).  host_rows, dst_pages,
-    upd_index, upd_page: pinned host tensors; staging: a device buffer of npages * 2h bytes;
-    copied_event: a torch.cuda.Event (or raw handle) recorded right after the copy."""
+    """Staging through the copy engines: each run of consecutive destination pages copied
+    straight into the pool (at most LORA_STAGE_MAX_RUNS runs), else host rows -> device
+    staging buffer (one copy) -> pool pages (one kernel); then the page-table rewrite.
+    host_rows, dst_pages, upd_index, upd_page: pinned host tensors; staging: a device buffer of
+    npages * 2h bytes, or None when the pages form at most LORA_STAGE_MAX_RUNS runs;
+    copied_event: a torch.cuda.Event (or raw handle) recorded right after the copies."""
     ev = None
     if copied_event is not None:
         ev = copied_event.cuda_event if hasattr(copied_event, "cuda_event") else copied_event

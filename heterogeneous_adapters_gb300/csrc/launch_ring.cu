@@ -95,7 +95,7 @@ lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int
         if (h8 <= 256)
             st = launch_ring<1, 8>(prm, pool, stream);
         else if (h8 <= 512)
-            st = launch_ring<2, 8>(prm, pool, stream);
+            st = launch_ring<1, 16>(prm, pool, stream);
         else if (h8 <= 640)
             st = launch_ring<2, 10>(prm, pool, stream);
         else if (h8 <= 768)

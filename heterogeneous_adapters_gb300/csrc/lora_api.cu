@@ -515,6 +515,7 @@ static lora_status launch_stage(const lora_pool* pool, const void* rows, const i
     sp.vec_per_row = pool->d.h / 8;
     int grid = di->sm_count * 4;
     if (npages > 0 && npages < grid) grid = npages;
+    if (npages == 0) grid = (int)std::min<int64_t>(grid, (nupd + kStageThreads - 1) / kStageThreads);
     if (grid < 1) grid = 1;
     stage_kernel<<<grid, kStageThreads, 0, stream>>>(sp);
     return cuda_status(cudaGetLastError());
@@ -526,17 +527,40 @@ lora_status lora_stage_pages_ce(const lora_pool* pool, const void* host_rows, vo
                                 void* stream) {
     lora_status st = check_stage(pool, host_rows, dst_pages, npages, page_table, upd_index, upd_page, nupd);
     if (st != LORA_OK) return st;
-    const size_t bytes = (size_t)npages * (size_t)pool->d.h * 2;
-    if (npages > 0 && (staging == nullptr || !aligned16(staging) || staging_bytes < bytes)) return LORA_EINVAL;
+    const size_t row_bytes = (size_t)pool->d.h * 2;
+    const size_t bytes = (size_t)npages * row_bytes;
+    if (staging != nullptr && (!aligned16(staging) || staging_bytes < bytes)) return LORA_EINVAL;
+    // runs of consecutive destination pages (a cache that hands out a unit's pages from a
+    // free list gives one run per unit): each run is one copy straight into the pool
+    int32_t runs = 0;
+    for (int32_t i = 0; i < npages; ++i)
+        if (i == 0 || dst_pages[i] != dst_pages[i - 1] + 1) ++runs;
+    const bool direct = runs <= LORA_STAGE_MAX_RUNS;
+    if (npages > 0 && !direct && staging == nullptr) return LORA_EINVAL;
     if (npages == 0 && nupd == 0) return LORA_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    if (npages > 0) {
+    const char* src = static_cast<const char*>(host_rows);
+    if (direct) {
+        char* pages = static_cast<char*>(pool->d.pages);
+        for (int32_t i0 = 0; i0 < npages;) {
+            int32_t i1 = i0 + 1;
+            while (i1 < npages && dst_pages[i1] == dst_pages[i1 - 1] + 1) ++i1;
+            st = cuda_status(cudaMemcpyAsync(pages + (size_t)dst_pages[i0] * row_bytes, src + (size_t)i0 * row_bytes,
+                                             (size_t)(i1 - i0) * row_bytes, cudaMemcpyHostToDevice, s));
+            if (st != LORA_OK) return st;
+            i0 = i1;
+        }
+    } else {
         st = cuda_status(cudaMemcpyAsync(staging, host_rows, bytes, cudaMemcpyHostToDevice, s));
         if (st != LORA_OK) return st;
     }
     if (copied != nullptr) {
         st = cuda_status(cudaEventRecord((cudaEvent_t)copied, s));
         if (st != LORA_OK) return st;
+    }
+    if (direct) {   // the pages are in place: only the page-table rewrite is left
+        if (nupd == 0) return LORA_OK;
+        return launch_stage(pool, nullptr, nullptr, 0, page_table, upd_index, upd_page, nupd, s);
     }
     return launch_stage(pool, staging, dst_pages, npages, page_table, upd_index, upd_page, nupd, s);
 }

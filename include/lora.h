@@ -308,20 +308,26 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
                              int32_t npages, int32_t* page_table, const int64_t* upd_index,
                              const int32_t* upd_page, int64_t nupd, void* stream);
 
-/* Adapter staging through the copy engines: one cudaMemcpyAsync on `stream` copies the
- * npages rows (host_rows, pinned host memory, row i = h bf16 values, 16-byte aligned)
- * into `staging` (caller-owned device memory of at least npages * 2h bytes, 16-byte
- * aligned); the copy uses the host link's copy engine and no SM, so it proceeds at the
- * link's rate while kernels hold every SM.  Then one kernel on `stream` moves staging row
- * i into pool page dst_pages[i] (device to device) and sets page_table[upd_index[k]] =
- * upd_page[k], as lora_stage_pages does.  dst_pages, upd_index and upd_page are pinned
- * host memory, validated on the host before anything is launched.  The caller keeps
- * host_rows, staging and the index arrays alive until the work on `stream` has finished,
- * orders consumers after it with an event, and must not stage into pages that a running
- * kernel reads.  The page moves and the page-table rewrite need an SM: while a persistent
- * kernel holds them all, that small kernel starts when it ends.  copied (a cudaEvent_t
- * passed as void*, may be NULL) is recorded on `stream` right after the copy: once it
- * has completed, host_rows may be reused. */
+/* Adapter staging through the copy engines (the host link's DMA engines, no SM), on
+ * `stream`.  host_rows: pinned host memory, row i = h bf16 values for pool page
+ * dst_pages[i], 16-byte aligned.  Destination pages that form runs of consecutive ids
+ * (dst_pages[i + 1] = dst_pages[i] + 1) are copied straight into the pool, one
+ * cudaMemcpyAsync per run, when the call has at most LORA_STAGE_MAX_RUNS runs; otherwise
+ * one cudaMemcpyAsync copies all rows into `staging` (caller-owned device memory of at
+ * least npages * 2h bytes, 16-byte aligned) and one kernel moves staging row i into pool
+ * page dst_pages[i].  Either way a kernel on `stream` then sets page_table[upd_index[k]] =
+ * upd_page[k], k < nupd, as lora_stage_pages does (no kernel if nupd = 0 and every row
+ * went straight into the pool).  staging may be NULL (staging_bytes ignored) when the
+ * rows form at most LORA_STAGE_MAX_RUNS runs; a non-NULL staging is always checked.
+ * dst_pages, upd_index and upd_page are pinned host memory, validated on the host before
+ * anything is copied or launched (LORA_EINVAL: a page id or entry out of range, staging
+ * missing when needed, too small or misaligned; LORA_EALIGN: host_rows misaligned).
+ * The caller keeps host_rows, staging and the index arrays alive until the work on
+ * `stream` has finished, orders consumers after it with an event, and must not stage
+ * into pages that a running kernel reads.  copied (a cudaEvent_t passed as void*, may be
+ * NULL) is recorded on `stream` right after the copies: once it has completed, host_rows
+ * may be reused. */
+#define LORA_STAGE_MAX_RUNS 64
 lora_status lora_stage_pages_ce(const lora_pool* pool, const void* host_rows, void* staging,
                                 size_t staging_bytes, const int32_t* dst_pages, int32_t npages,
                                 int32_t* page_table, const int64_t* upd_index, const int32_t* upd_page,

@@ -159,7 +159,8 @@ def test_pool_tuning_defaults_overrides_and_checks(lib):
 
 def test_stage_pages_ce_host_checks(lib):
     """The copy-engine staging validates its index arrays and its staging buffer before
-    launching or copying anything."""
+    launching or copying anything (a staging buffer is needed only when the destination
+    pages form more than LORA_STAGE_MAX_RUNS runs, and is checked whenever one is given)."""
     import numpy as np
 
     from heterogeneous_adapters_gb300._binding import LORA_EALIGN, LORA_EINVAL, lora_pool_desc
@@ -175,7 +176,11 @@ def test_stage_pages_ce_host_checks(lib):
                                    None, None, None, 0, None, None) == LORA_EINVAL          # page out of range
     assert lib.lora_stage_pages_ce(h, c(rows), stage, 2 * 512 - 16, c(good), 2, None, None, None, 0,
                                    None, None) == LORA_EINVAL                               # staging too small
-    assert lib.lora_stage_pages_ce(h, c(rows), None, 2 * 512, c(good), 2, None, None, None, 0,
+    # more runs of consecutive pages than LORA_STAGE_MAX_RUNS (every other page): the rows go
+    # through the staging buffer, which is then required
+    many = np.zeros((65, 256), np.uint16)
+    spread = (2 * np.arange(65)).astype(np.int32)
+    assert lib.lora_stage_pages_ce(h, c(many), None, 0, c(spread), 65, None, None, None, 0,
                                    None, None) == LORA_EINVAL                               # no staging buffer
     assert lib.lora_stage_pages_ce(h, c(rows), stage + 8, 2 * 512, c(good), 2, None, None, None, 0,
                                    None, None) == LORA_EINVAL                               # misaligned staging

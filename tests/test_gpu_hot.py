@@ -41,7 +41,7 @@ HOT = {
     # a group longer than one tile (130 and 257 tokens: two and three tiles, ragged)
     "h2048-multi-tile-groups": lambda: hot_decode(83, 2048, 2, 2, [(130, 16), (257, 64), (8, 24)],
                                                   20, 10, [4, 16]),
-    # rank 256 groups stay on the CUDA-core path beside gathered ones
+    # a rank-256 group (above the tensor-core limit) beside rank-128 and rank-8 groups
     "h5120-rank256-and-gathered": lambda: hot_decode(84, 5120, 1, 2, [(20, 256), (20, 128), (12, 8)],
                                                      9, 5, [16]),
     # a narrow pool (one 16-byte vector per thread in the ring body)

@@ -1,8 +1,9 @@
 """A miniature serving loop on the GPU: requests arrive for adapters held in host memory,
 the adapter cache (include/lora_runtime.h) gives each missing adapter pool pages (evicting
 least recently used adapters nobody uses), lora_stage_pages (a kernel reading the host rows
-through their mapping) or lora_stage_pages_ce (the copy engines into a staging buffer, then a
-kernel) copies its rows in and points its page-table entries at them, the scheduler picks each step's batch under a token cap and
+through their mapping) or lora_stage_pages_ce (the copy engines: straight into the pool for
+runs of consecutive pages, else into a staging buffer and then a kernel) copies its rows in
+and points its page-table entries at them, the scheduler picks each step's batch under a token cap and
 a distinct-adapter cap, lora_bgmv applies the deltas, and every step is checked against the
 fp64 oracle.  Pages freed by evictions are reused, so a stale page-table entry or a missed
 copy shows up as a wrong (or NaN) row.

@@ -1,8 +1,9 @@
 """Adapter staging from pinned host memory, by the kernel that reads the host rows
-through their mapping (lora_stage_pages) and through the copy engines into a device
-staging buffer (lora_stage_pages_ce): pages land bit-exact in their new pool slots, the
-page table is rewritten, and a delta launch ordered after it (event on a side stream)
-reads the moved adapter correctly."""
+through their mapping (lora_stage_pages) and through the copy engines (lora_stage_pages_ce:
+runs of consecutive destination pages copied straight into the pool, or, with more runs
+than LORA_STAGE_MAX_RUNS, one copy into a device staging buffer and a kernel moving the
+rows): pages land bit-exact in their new pool slots, the page table is rewritten, and a
+delta launch ordered after it (event on a side stream) reads the moved adapter correctly."""
 import numpy as np
 import pytest
 
@@ -13,7 +14,7 @@ from .harness import GpuCase, full_check
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("path", ["mapped", "copy_engine"])
+@pytest.mark.parametrize("path", ["mapped", "copy_engine", "copy_engine_staged"])
 def test_stage_moves_adapters_to_free_pages(path):
     import torch
 
@@ -33,6 +34,10 @@ def test_stage_moves_adapters_to_free_pages(path):
                                             pool.num_proj * 2 * pool.ranks[a]) for a in movers])
         old_pages = pool.pt[entries].astype(np.int64)
         new_pages = (pool.num_pages - extra + np.arange(entries.size)).astype(np.int32)
+        if path == "copy_engine_staged":   # scattered destinations: more runs than direct copies take
+            new_pages = np.random.default_rng(5).permutation(new_pages).astype(np.int32)
+            runs = 1 + int(np.count_nonzero(np.diff(new_pages) != 1))
+            assert runs > lora.LORA_STAGE_MAX_RUNS
         # host copy of the rows (the staging source), then poison the old pages
         host_rows = dev.pool[torch.from_numpy(old_pages).to(case.device)].cpu().pin_memory()
         dev.pool[torch.from_numpy(old_pages).to(case.device)] = float("nan")
@@ -45,6 +50,9 @@ def test_stage_moves_adapters_to_free_pages(path):
             if path == "mapped":
                 lora.stage_pages(case.pool, host_rows, dst, entries.size, dev.pt, upd_index, upd_page,
                                  entries.size, side.cuda_stream)
+            elif path == "copy_engine":   # one run of consecutive pages: no staging buffer needed
+                lora.stage_pages_ce(case.pool, host_rows, None, 0, dst, entries.size, dev.pt,
+                                    upd_index, upd_page, entries.size, side.cuda_stream)
             else:
                 lora.stage_pages_ce(case.pool, host_rows, staging, staging.numel(), dst, entries.size, dev.pt,
                                     upd_index, upd_page, entries.size, side.cuda_stream)
