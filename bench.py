@@ -86,10 +86,10 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {
-    "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh"],
-    "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
-    "delta_fused_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh"],
+KERNEL_SOURCES = {   # the kernel's code and the launch file that picks its instantiation
+    "bgmv_ring_kernel": ["bgmv_ring.cuh", "common.cuh", "ptx.cuh", "launch_ring.cu"],
+    "sgmv_mma_kernel": ["sgmv_mma.cuh", "common.cuh", "ptx.cuh", "launch_tile.cu"],
+    "delta_fused_kernel": ["fused.cuh", "bgmv_ring.cuh", "sgmv_mma.cuh", "common.cuh", "ptx.cuh", "launch_tile.cu"],
 }
 
 

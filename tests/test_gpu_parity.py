@@ -302,6 +302,23 @@ def test_full_workload(cfg, k):
         case.close()
 
 
+@pytest.mark.parametrize("cfg,k", [("decode", 3), ("prefill", 1), ("mixed", 1), ("stress-distinct", 2),
+                                   ("stress-zipf", 2), ("llama3-decode", 3), ("llama3-prefill", 2),
+                                   ("llama3-mixed", 2)])
+def test_full_workload_delta_only(cfg, k):
+    """The full workloads with y0 = 0, so that y holds the delta alone (|delta| is ~0.05 of
+    |y0| otherwise, where the gate could hide a dropped rank term): every sampled
+    projection within the strict delta-only bound, in the launch configuration the bench
+    times."""
+    wl = spec.WORKLOADS[cfg]()
+    case = GpuCase(wl, y0_zero=True, nan_dummies=True)
+    try:
+        assert case.run() == 0
+        full_check(wl, case, _sample(len(wl.problems), k, seed=7 + sum(map(ord, str(cfg)))), strict=True)
+    finally:
+        case.close()
+
+
 def _widths_case(kind, seed, h, dims, N, ranks, T_dec=0, lens=()):
     """One layer, one projection per (d_in, d_out) pair in dims, every adapter resident."""
     rng = np.random.default_rng(seed)
