@@ -67,10 +67,13 @@ using RingParams = RingParamsT<LORA_MAX_PROBLEMS_PER_LAUNCH>;
 
 // Dynamic shared memory layout (offsets from a 1024-byte aligned base).
 struct RingSmem {
-    uint32_t ring, full, empty, cbar, meta, red, ts, pgbuf, total;
+    uint32_t ring, full, empty, cbar, meta, red, ts, pgbuf, probs, total;
 };
 
-__host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes, int r_max, int cwarps) {
+// nprob: problem descriptors copied into shared memory (the last region, so that the other
+// offsets do not depend on it and a host may size for more problems than a launch has).
+__host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes, int r_max, int cwarps,
+                                                     int nprob) {
     RingSmem L;
     const int rp = (r_max + 7) / 8 * 8;
     uint32_t o = 0;
@@ -82,7 +85,8 @@ __host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes
     o = (o + 15) & ~15u;
     L.red = o;   o += cwarps * rp * kChunk * 4;
     L.ts = o;    o += rp * kChunk * 4;
-    L.pgbuf = o; o += 2 * LORA_MAX_RANK * 4;
+    L.pgbuf = o; o += 2 * 2 * LORA_MAX_RANK * 4;   // page ids of two items
+    L.probs = o; o += (uint32_t)nprob * sizeof(ProbDesc);
     L.total = o;
     return L;
 }
@@ -120,6 +124,50 @@ __device__ __forceinline__ void ring_shrink_stage(const unsigned char* stage, in
     if (lane % kRep == 0) {   // index jj*kChunk + t; the same lane owns it in every block
         float* dst = red_w + j0 * kChunk + lane / kRep;
         *dst = accumulate ? *dst + sum : sum;
+    }
+}
+
+// The shrink of one A stage on the tensor cores (warp-level mma.sync, m16n8k16, bf16 x bf16
+// into fp32), for pools whose h splits into kXf groups of four 16-byte vectors per consumer
+// warp.  Warp w takes the columns [w h / CW, (w + 1) h / CW) of the chunk's rows and of the
+// stage's pages: the tile is rows (16, of which the chunk's <= 4 are real) x pages (8) x
+// those columns.  The sum over k is order-free, so lane (g, q) feeds the k slots {2q, 2q+1,
+// 2q+8, 2q+9} of two consecutive k steps from one 16-byte vector (its vector q + 4j of the
+// warp's columns) -- of x row g for the A operand and of page g for the B operand, the same
+// columns on both sides -- and no operand needs a shared-memory shuffle.  Accumulator lane
+// (g, q) then holds the warp's partial sums for row g and pages 2q, 2q+1.
+constexpr int kMmaXf = 8;   // 16-byte vectors of a row per lane, at most (h = 4096 over 16 warps)
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+template <int XF>
+__device__ __forceinline__ void ring_shrink_stage_mma(const unsigned char* stage, int stage_row_bytes, int npages,
+                                                      int warp_vec0, int lane, const uint4 (&xf)[kMmaXf],
+                                                      float* red_w, int j0, bool accumulate) {
+    const int g = lane >> 2, q = lane & 3;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const unsigned char* pg = stage + (size_t)g * stage_row_bytes + (size_t)warp_vec0 * 16;
+#pragma unroll
+    for (int j = 0; j < XF; ++j) {
+        const uint4 b = g < npages ? *reinterpret_cast<const uint4*>(pg + (q + 4 * j) * 16) : make_uint4(0, 0, 0, 0);
+        mma_bf16_16816(c, xf[j].x, xf[j].y, b.x, b.y);
+        mma_bf16_16816(c, xf[j].z, xf[j].w, b.z, b.w);
+    }
+    if (g < kChunk) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int page = 2 * q + e;
+            if (page < npages) {
+                float* dst = red_w + (j0 + page) * kChunk + g;
+                *dst = accumulate ? *dst + c[e] : c[e];
+            }
+        }
     }
 }
 
@@ -176,11 +224,49 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
     float* red_w = red + warp * rp * kChunk;
     float* ts = reinterpret_cast<float*>(base + L.ts);
     const int r = mx.rank;
-    const ProbDesc pd = p.probs[mx.pr];
+    const ProbDesc& pd = reinterpret_cast<const ProbDesc*>(base + L.probs)[mx.pr];
 
     // for each page block kb of the input: the x rows' block (the first one's stage was
     // waited by the caller), then page kb of the A rows; partial sums add up over blocks
     const int pv_in = W ? vec_pages(pd.d_in, h) : 1, pv_out = W ? vec_pages(pd.d_out, h) : 1;
+    // tensor-core shrink: one vector per thread (NV = 1), h x h pages, and the row's vectors
+    // split into groups of four per warp (h = 1024, 2048, 4096 with 8 or 16 warps)
+    constexpr bool kMmaShape = (NV == 1 && !W && RP == 8);
+    const int warp_vecs = h8 / CW;
+    const int xgroups = warp_vecs / 4;   // k-step pairs of a warp: 1, 2, 4 or 8
+    if (kMmaShape && h8 % (CW * 4) == 0 && (xgroups == 1 || xgroups == 2 || xgroups == 4 || xgroups == 8)) {
+        const int g = lane >> 2, q = lane & 3;
+        uint4 xf[kMmaXf];
+        {
+            const unsigned char* st = base + L.ring + (size_t)(it % S) * p.stage_bytes;
+#pragma unroll
+            for (int j = 0; j < kMmaXf; ++j)
+                xf[j] = (g < mx.count && j < xgroups)
+                            ? *reinterpret_cast<const uint4*>(st + g * row_bytes + (warp * warp_vecs + q + 4 * j) * 16)
+                            : make_uint4(0, 0, 0, 0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(base + L.empty + (it % S) * 8));
+            ++it;
+        }
+        for (int j0 = 0; j0 < r; j0 += RP) {
+            const uint32_t s = it % S;
+            if (!mbar_wait(smem_addr(base + L.full + s * 8), (it / S) & 1, kWaitLimitNs)) return false;
+            const int np = min(RP, r - j0);
+            const unsigned char* st = base + L.ring + (size_t)s * p.stage_bytes;
+            // exactly the warp's groups: a wider loop would read other warps' columns
+            if (xgroups == 8)
+                ring_shrink_stage_mma<8>(st, row_bytes, np, warp * warp_vecs, lane, xf, red_w, j0, false);
+            else if (xgroups == 4)
+                ring_shrink_stage_mma<4>(st, row_bytes, np, warp * warp_vecs, lane, xf, red_w, j0, false);
+            else if (xgroups == 2)
+                ring_shrink_stage_mma<2>(st, row_bytes, np, warp * warp_vecs, lane, xf, red_w, j0, false);
+            else
+                ring_shrink_stage_mma<1>(st, row_bytes, np, warp * warp_vecs, lane, xf, red_w, j0, false);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(base + L.empty + s * 8));
+            ++it;
+        }
+    } else
     for (int kb = 0; kb < pv_in; ++kb) {
         const int w8 = W ? min(h8, (pd.d_in - kb * h) >> 3) : h8;   // used vectors of this block
         if (kb > 0 && !mbar_wait(smem_addr(base + L.full + (it % S) * 8), (it / S) & 1, kWaitLimitNs))
@@ -285,11 +371,23 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
 // or less); RP: rows per stage (stage_bytes = RP * 2h).
 template <int NV, int CW, int RP, bool W, class P>
 __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32_t cta, uint32_t ncta) {
-    const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max, CW);
+    const RingSmem L = ring_smem_layout(p.stages, p.stage_bytes, p.pool.r_max, CW, p.nprob);
     const int S = p.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws);
     StageMeta* meta = reinterpret_cast<StageMeta*>(base + L.meta);
+    // The problem descriptors, copied once into shared memory: read from the kernel
+    // parameters by problem index, they go through the constant cache, which misses on
+    // most items (about a microsecond each on the producer's path, as long as a small
+    // item takes to stream).
+    const ProbDesc* sprobs = reinterpret_cast<const ProbDesc*>(base + L.probs);
+    {
+        static_assert(sizeof(ProbDesc) % 8 == 0, "descriptor copy in 8-byte words");
+        const unsigned long long* src = reinterpret_cast<const unsigned long long*>(p.probs);
+        unsigned long long* dst = reinterpret_cast<unsigned long long*>(base + L.probs);
+        const int words = p.nprob * (int)(sizeof(ProbDesc) / 8);
+        for (int w = tid; w < words; w += blockDim.x) dst[w] = src[w];
+    }
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -307,11 +405,14 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
         // over the CTAs (chunks are listed by descending rank, so every CTA gets a similar
         // mix and the last round is made of the smallest items).  The metadata of the next
         // items is loaded while the current one streams: the chunk two items ahead, the
-        // page ids one item ahead.
+        // page ids one item ahead.  Each item is prepared (page ids checked and written to
+        // one of two id buffers, its stage metadata built) while the previous item's x and
+        // A stages are in flight, before that item's B stages wait for a free stage: the
+        // B stages of item k need the consumers to finish item k - 1, and the x stage of
+        // item k + 1 then follows them at once.
         const PoolView& PV = p.pool;
         const WsLayout WL = ws_layout(hdr->cap_tokens, hdr->cap_segments);
         const Chunk* chunks = reinterpret_cast<const Chunk*>(p.ws + WL.chunks);
-        int32_t* pgbuf = reinterpret_cast<int32_t*>(base + L.pgbuf);
         const uint32_t total = (uint32_t)hdr->counts[2] * (uint32_t)p.nprob;
         const uint32_t row_bytes = (uint32_t)PV.h * 2;
         const uint32_t G = ncta;
@@ -325,7 +426,7 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
         };
         // page ids of an item's first A block and first B block (all of them for h x h pools)
         auto load_pages = [&](const Chunk& c, uint32_t itm, int32_t (&pg)[kPg]) {
-            const ProbDesc& pd = p.probs[itm % p.nprob];
+            const ProbDesc& pd = sprobs[itm % p.nprob];
             const long long a0 = c.pt_base + (long long)pd.blk * c.rank;
             const long long b0 = a0 + (long long)(W ? vec_pages(pd.d_in, PV.h) : 1) * c.rank;
 #pragma unroll
@@ -334,76 +435,82 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
                 pg[k] = e < c.rank ? PV.pt[a0 + e] : (e < 2 * c.rank ? PV.pt[b0 + e - c.rank] : 0);
             }
         };
-        uint32_t item = cta;
+        struct Cur {
+            Chunk ch;
+            long long a0, b0;   // first A-block and B-block entries
+            int pr, pv_in, pv_out;
+            bool bad;
+        };
         Chunk c_next, c_next2;
         int32_t pg_next[kPg];
-        if (item < total) {
-            c_next = chunks[item / p.nprob];
-            load_pages(c_next, item, pg_next);
-        }
-        if (item + G < total) c_next2 = chunks[(item + G) / p.nprob];
-        for (; item < total; item += G) {
-            const Chunk ch = c_next;
-            const int pr = item % p.nprob;
+        // item `itm`: rotate the metadata pipeline, check its page ids into id buffer `buf`
+        auto prepare = [&](uint32_t itm, int buf, Cur& cu) {
+            cu.ch = c_next;
             int32_t pg[kPg];
 #pragma unroll
             for (int k = 0; k < kPg; ++k) pg[k] = pg_next[k];
-            if (item + G < total) {
+            if (itm + G < total) {
                 c_next = c_next2;
-                load_pages(c_next, item + G, pg_next);
+                load_pages(c_next, itm + G, pg_next);
             }
-            if (item + 2 * G < total) c_next2 = chunks[(item + 2 * G) / p.nprob];
-
-            const int r = ch.rank;
-            const ProbDesc& pd = p.probs[pr];
-            const int pv_in = W ? vec_pages(pd.d_in, PV.h) : 1, pv_out = W ? vec_pages(pd.d_out, PV.h) : 1;
-            const long long a0 = ch.pt_base + (long long)pd.blk * r;   // first A-block entry
-            const long long b0 = a0 + (long long)pv_in * r;            // first B-block entry
+            if (itm + 2 * G < total) c_next2 = chunks[(itm + 2 * G) / p.nprob];
+            const int r = cu.ch.rank;
+            cu.pr = itm % p.nprob;
+            const ProbDesc& pd = sprobs[cu.pr];
+            cu.pv_in = W ? vec_pages(pd.d_in, PV.h) : 1;
+            cu.pv_out = W ? vec_pages(pd.d_out, PV.h) : 1;
+            cu.a0 = cu.ch.pt_base + (long long)pd.blk * r;
+            cu.b0 = cu.a0 + (long long)cu.pv_in * r;
+            int32_t* ids = reinterpret_cast<int32_t*>(base + L.pgbuf) + buf * 2 * LORA_MAX_RANK;
             bool bad = false;
 #pragma unroll
             for (int k = 0; k < kPg; ++k) {
                 const int e = lane + 32 * k;
                 if (e < 2 * r) {
                     bad |= (pg[k] < 0 || pg[k] >= PV.num_pages);
-                    pgbuf[e] = pg[k];
+                    ids[e] = pg[k];
                 }
             }
             // vectors longer than a page: the item's other page blocks are checked too
             if (W) {
-                for (long long e = lane; e < (long long)(pv_in - 1) * r; e += 32) {
-                    const int q = PV.pt[a0 + r + e];
+                for (long long e = lane; e < (long long)(cu.pv_in - 1) * r; e += 32) {
+                    const int q = PV.pt[cu.a0 + r + e];
                     bad |= (q < 0 || q >= PV.num_pages);
                 }
-                for (long long e = lane; e < (long long)(pv_out - 1) * r; e += 32) {
-                    const int q = PV.pt[b0 + r + e];
+                for (long long e = lane; e < (long long)(cu.pv_out - 1) * r; e += 32) {
+                    const int q = PV.pt[cu.b0 + r + e];
                     bad |= (q < 0 || q >= PV.num_pages);
                 }
             }
-            bad = __any_sync(0xffffffffu, bad);
+            cu.bad = __any_sync(0xffffffffu, bad);
             __syncwarp();
+            if (cu.bad && lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
+        };
+        uint32_t item = cta;
+        if (item < total) {
+            c_next = chunks[item / p.nprob];
+            load_pages(c_next, item, pg_next);
+        }
+        if (item + G < total) c_next2 = chunks[(item + G) / p.nprob];
+        Cur cur;
+        int buf = 0;
+        if (item < total) prepare(item, buf, cur);
+        while (item < total) {
+            const Chunk& ch = cur.ch;
+            const int r = ch.rank;
+            const ProbDesc& pd = sprobs[cur.pr];
+            int32_t* pgbuf = reinterpret_cast<int32_t*>(base + L.pgbuf) + buf * 2 * LORA_MAX_RANK;
             StageMeta m;
-            m.kind = bad ? kStageSkip : kStageX;
+            m.kind = cur.bad ? kStageSkip : kStageX;
             m.npages = ch.count;
             m.j0 = 0;
-            m.pr = pr;
+            m.pr = cur.pr;
             m.count = ch.count;
             m.rank = r;
             m.scale = ch.scale;
 #pragma unroll
             for (int t = 0; t < kChunk; ++t) m.rows[t] = ch.rows[t];
             m.blk = 0;
-            if (bad && lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
-            if (bad) {   // a skip marker in place of the item
-                const int s = claim();
-                if (s < 0) { ok = false; break; }
-                if (lane == 0) {
-                    meta[s] = m;
-                    mbar_arrive(smem_addr(base + L.full + s * 8));
-                }
-                __syncwarp();
-                ++it;
-                continue;
-            }
             // Stages of the item: for each page block kb of the input, the x rows' block
             // kb then page kb of the A rows; then, for each page block q of the output,
             // page q of the B columns.  Only the used part of a partly used page is copied.
@@ -438,31 +545,55 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
                 for (int e = lane; e < r; e += 32) pgbuf[off + e] = PV.pt[first + e];
                 __syncwarp();
             };
-            for (int kb = 0; kb < pv_in && ok; ++kb) {
-                const uint32_t bytes = W ? (uint32_t)min(PV.h, pd.d_in - kb * PV.h) * 2 : row_bytes;
+            if (cur.bad) {   // a skip marker in place of the item
                 const int s = claim();
                 if (s < 0) { ok = false; break; }
                 if (lane == 0) {
-                    StageMeta mx = m;
-                    mx.blk = kb;
-                    meta[s] = mx;
-                    mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), bytes * ch.count);
+                    meta[s] = m;
+                    mbar_arrive(smem_addr(base + L.full + s * 8));
                 }
                 __syncwarp();
-                if (lane < ch.count)
-                    bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
-                             pd.x + (long long)ch.rows[lane] * pd.ldx + (long long)kb * PV.h, bytes,
-                             smem_addr(base + L.full + s * 8));
                 ++it;
-                if (kb > 0) fetch_block(a0 + (long long)kb * r, 0);
-                if (!emit_pages(kStageA, kb, 0, bytes)) ok = false;
-            }
-            for (int q = 0; q < pv_out && ok; ++q) {
-                const uint32_t bytes = W ? (uint32_t)min(PV.h, pd.d_out - q * PV.h) * 2 : row_bytes;
-                if (q > 0) fetch_block(b0 + (long long)q * r, r);
-                if (!emit_pages(kStageB, q, r, bytes)) ok = false;
+            } else {
+                for (int kb = 0; kb < cur.pv_in && ok; ++kb) {
+                    const uint32_t bytes = W ? (uint32_t)min(PV.h, pd.d_in - kb * PV.h) * 2 : row_bytes;
+                    const int s = claim();
+                    if (s < 0) { ok = false; break; }
+                    if (lane == 0) {
+                        StageMeta mx = m;
+                        mx.blk = kb;
+                        meta[s] = mx;
+                        mbar_arrive_expect_tx(smem_addr(base + L.full + s * 8), bytes * ch.count);
+                    }
+                    __syncwarp();
+                    if (lane < ch.count)
+                        bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
+                                 pd.x + (long long)ch.rows[lane] * pd.ldx + (long long)kb * PV.h, bytes,
+                                 smem_addr(base + L.full + s * 8));
+                    ++it;
+                    if (kb > 0) fetch_block(cur.a0 + (long long)kb * r, 0);
+                    if (!emit_pages(kStageA, kb, 0, bytes)) ok = false;
+                }
             }
             if (!ok) break;
+            // the next item, prepared while this one's x and A stages land (after its B
+            // stages for pools with vectors of several pages, whose longer checks would
+            // otherwise keep both items' state in registers across the B stages)
+            const uint32_t nxt = item + G;
+            Cur nx;
+            if (!W && nxt < total) prepare(nxt, buf ^ 1, nx);
+            if (!cur.bad) {
+                for (int q = 0; q < cur.pv_out && ok; ++q) {
+                    const uint32_t bytes = W ? (uint32_t)min(PV.h, pd.d_out - q * PV.h) * 2 : row_bytes;
+                    if (q > 0) fetch_block(cur.b0 + (long long)q * r, r);
+                    if (!emit_pages(kStageB, q, r, bytes)) ok = false;
+                }
+            }
+            if (!ok) break;
+            if (W && nxt < total) prepare(nxt, buf ^ 1, nx);
+            item = nxt;
+            if (item < total) cur = nx;
+            buf ^= 1;
         }
         if (ok) {
             // stop marker for the consumers

@@ -50,8 +50,9 @@ struct RingShape {
     int rp, stages;
     size_t smem;
 };
-// force_rp: 4 or 8 rows per stage where two such stages fit; 0 = automatic.
-RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps, int force_rp);
+// force_rp: 4 or 8 rows per stage where two such stages fit; 0 = automatic.  nprob: the
+// most problem descriptors a launch copies into shared memory.
+RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps, int force_rp, int nprob);
 
 // launch_ring.cu: the CUDA-core kernel over the chunk list (t_out: debug export of t).
 lora_status run_delta_ring(const lora_pool* pool, const lora_problem* probs, int32_t nprob, void* ws,

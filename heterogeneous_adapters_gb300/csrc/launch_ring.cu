@@ -9,9 +9,9 @@ namespace lora {
 namespace host {
 
 // Ring depth that fits the opt-in shared memory of one CTA (at most 8 stages).
-int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* smem) {
+int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, int nprob, size_t* smem) {
     for (int S = 8; S >= 2; --S) {
-        const size_t need = ring_smem_layout(S, stage_bytes, r_max, cwarps).total + 1024;
+        const size_t need = ring_smem_layout(S, stage_bytes, r_max, cwarps, nprob).total + 1024;
         if (need <= (size_t)smem_optin) {
             *smem = need;
             return S;
@@ -23,11 +23,11 @@ int ring_stages(int smem_optin, int stage_bytes, int r_max, int cwarps, size_t* 
 // Rows per stage: the larger stages when three of them fit (a bulk-copy ring streams
 // closer to the HBM read rate with fewer, larger stages), else the small ones.
 // force = 4 or 8 (the pool's tuning) forces the choice where two such stages fit.
-RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps, int force) {
+RingShape ring_shape(int h, int r_max, int smem_optin, int cwarps, int force, int nprob) {
     RingShape fallback{0, 0, 0};
     for (int rp : {kRingPagesLarge, kRingPagesSmall}) {
         size_t smem = 0;
-        const int S = ring_stages(smem_optin, rp * 2 * h, r_max, cwarps, &smem);
+        const int S = ring_stages(smem_optin, rp * 2 * h, r_max, cwarps, nprob, &smem);
         if (S < 2) continue;
         const RingShape sh{rp, S, smem};
         if (force == rp || (force == 0 && S >= 3)) return sh;
@@ -61,7 +61,7 @@ lora_status launch_ring_w(RingParams& prm, int force_rp, cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW, force_rp);
+    const RingShape sh = ring_shape(prm.pool.h, prm.pool.r_max, di->smem_optin, CW, force_rp, prm.nprob);
     if (sh.stages < 2) return LORA_ETOOBIG;
     if (sh.rp == kRingPagesLarge) return launch_ring_rp<NV, CW, kRingPagesLarge, W>(prm, di, sh, stream);
     return launch_ring_rp<NV, CW, kRingPagesSmall, W>(prm, di, sh, stream);

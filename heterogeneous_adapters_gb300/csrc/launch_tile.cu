@@ -248,7 +248,8 @@ lora_status launch_fused(const lora_pool* pool, const lora_problem* probs, int32
     MmaConfig c;
     st = mma_config(pool, di->smem_optin, &c);
     if (st != LORA_OK) return st;
-    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW, pool->tune.ring_rows_per_stage);
+    const RingShape sh = ring_shape(pool->d.h, pool->d.r_max, di->smem_optin, CW, pool->tune.ring_rows_per_stage,
+                                    kMmaMaxProbs);
     if (sh.stages < 2) return LORA_ETOOBIG;
     if (!pool->square) {
         if (sh.rp == kRingPagesLarge)
