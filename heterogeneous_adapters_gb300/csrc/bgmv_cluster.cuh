@@ -28,7 +28,7 @@ namespace lora {
 constexpr int kClusterCtas = 8;          // CTAs of one cluster (the portable maximum)
 constexpr int kClusterThreads = 256;
 constexpr int kClusterMaxProbs = 8;      // projections of one launch at most
-constexpr int kClusterDefaultProbs = 2;  // the default limit (measured against the ring kernel)
+constexpr int kClusterDefaultProbs = 1;  // the default limit (measured against the ring kernel)
 constexpr int kClusterExpandVecs = 64;   // 16-byte column vectors per expand pass
 constexpr int kClusterPg = 4;            // A rows a warp loads at once in the shrink
 
@@ -171,7 +171,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterT
         const int nv = v_hi - v_lo;
         for (int e = tid; e < ch.count * nv; e += kClusterThreads) {
             const int t = e / nv, v = e % nv;
-            xs[t * p.ni + v] = ld16(pd.x + (long long)ch.rows[t] * pd.ldx + (long long)(v_lo + v) * 8);
+            xs[t * p.ni + v] = ld16(pd.x + (long long)row_of(ch.rows, t) * pd.ldx + (long long)(v_lo + v) * 8);
         }
         if (__syncthreads_or(bad)) {
             if (tid == 0 && crank == 0) set_error(&hdr->err, LORA_DERR_PAGE);
@@ -196,7 +196,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterT
                                      (uint32_t)(s1 - s0) * 16);
                 }
             } else if (o_hi > o_lo) {
-                bulk_prefetch_l2(pd.y + (long long)ch.rows[e - r] * pd.ldy + (long long)o_lo * 8,
+                bulk_prefetch_l2(pd.y + (long long)row_of(ch.rows, e - r) * pd.ldy + (long long)o_lo * 8,
                                  (uint32_t)(o_hi - o_lo) * 16);
             }
         }
@@ -282,7 +282,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterT
             uint4 yv[kChunk];
 #pragma unroll
             for (int t = 0; t < kChunk; ++t)
-                yv[t] = (g == 0 && live && t < ch.count) ? ld16(pd.y + (long long)ch.rows[t] * pd.ldy + (long long)ov * 8)
+                yv[t] = (g == 0 && live && t < ch.count) ? ld16(pd.y + (long long)row_of(ch.rows, t) * pd.ldy + (long long)ov * 8)
                                                          : make_uint4(0, 0, 0, 0);
             float acc[kChunk][8];
 #pragma unroll
@@ -329,7 +329,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterT
                     o.y = pack2(s8[2], s8[3]);
                     o.z = pack2(s8[4], s8[5]);
                     o.w = pack2(s8[6], s8[7]);
-                    st16(pd.y + (long long)ch.rows[t] * pd.ldy + (long long)ov * 8, o);
+                    st16(pd.y + (long long)row_of(ch.rows, t) * pd.ldy + (long long)ov * 8, o);
                 }
             }
             __syncthreads();   // red is reused by the next pass

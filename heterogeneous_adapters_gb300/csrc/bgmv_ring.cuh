@@ -213,7 +213,7 @@ __device__ __forceinline__ bool consumer_barrier(unsigned char* base, const Ring
 // W: the pool has projections whose widths differ from h (vectors of several page blocks,
 // a partly used last page); W = false compiles the h x h case with one block each.
 template <int NV, int NT, int CW, int RP, bool W, class P>
-__device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSmem& L,
+__device__ __forceinline__ bool ring_consume_item(const P& p, unsigned char* base, const RingSmem& L,
                                   uint32_t& it, uint32_t& bphase, const StageMeta& mx, int c) {
     const int h = p.pool.h, h8 = h >> 3;
     const int row_bytes = h * 2;
@@ -311,7 +311,7 @@ __device__ bool ring_consume_item(const P& p, unsigned char* base, const RingSme
         for (int w = 0; w < CW; ++w) a += red[w * rp * kChunk + idx];
         ts[idx] = a * mx.scale;
         if (p.t_out != nullptr && t < mx.count)
-            p.t_out[(long long)mx.rows[t] * p.pool.r_max + j] = a * mx.scale;
+            p.t_out[(long long)row_of(mx.rows, t) * p.pool.r_max + j] = a * mx.scale;
     }
     if (!consumer_barrier(base, L, bphase)) return false;
     // for each page block q of the output: y's block q (loaded while its B pages stream
@@ -568,7 +568,7 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
                     __syncwarp();
                     if (lane < ch.count)
                         bulk_g2s(smem_addr(base + L.ring + (size_t)s * p.stage_bytes + lane * row_bytes),
-                                 pd.x + (long long)ch.rows[lane] * pd.ldx + (long long)kb * PV.h, bytes,
+                                 pd.x + (long long)row_of(ch.rows, lane) * pd.ldx + (long long)kb * PV.h, bytes,
                                  smem_addr(base + L.full + s * 8));
                     ++it;
                     if (kb > 0) fetch_block(cur.a0 + (long long)kb * r, 0);

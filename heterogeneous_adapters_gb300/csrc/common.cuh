@@ -112,6 +112,13 @@ struct ProbDesc {
     int32_t pad;
 };
 
+// rows[i] for a run-time i < kChunk, by selection: an array indexed by a run-time value
+// would be placed in local memory, and with it every other field of its struct.
+__device__ __forceinline__ int32_t row_of(const int32_t (&rows)[kChunk], int i) {
+    static_assert(kChunk == 4, "selection over four rows");
+    return i == 0 ? rows[0] : i == 1 ? rows[1] : i == 2 ? rows[2] : rows[3];
+}
+
 // Pages one vector of length d spans on pages of h values.
 __host__ __device__ __forceinline__ int vec_pages(int d, int h) { return (d + h - 1) / h; }
 

@@ -94,7 +94,7 @@ lora_status device_info(DeviceInfo** out) {
 namespace {
 
 // The measured defaults of a pool's launch tuning: stage rows chosen by shared memory,
-// the cluster kernel up to 2 projections, tensor-core tiles by the rank rule, a 3-slot y ring.
+// the cluster kernel for one projection, tensor-core tiles by the rank rule, a 3-slot y ring.
 void default_tuning(const lora_pool* pool, lora_tuning* t) {
     memset(t, 0, sizeof *t);
     t->ring_rows_per_stage = 0;

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kSxThreads) lora_shrink_kernel(const __grid_co
                 if (v0 == 0) {   // the x rows' block kb, while the A loads are in flight
                     for (int e = threadIdx.x; e < ch.count * w8; e += blockDim.x) {
                         const int t = e / w8, v = e % w8;
-                        xs[t * h8 + v] = ld16(pd.x + (long long)ch.rows[t] * pd.ldx + (long long)kb * P.h + v * 8);
+                        xs[t * h8 + v] = ld16(pd.x + (long long)row_of(ch.rows, t) * pd.ldx + (long long)kb * P.h + v * 8);
                     }
                     __syncthreads();
                 }
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kSxThreads) lora_shrink_kernel(const __grid_co
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 if (lane == 0 && t < ch.count)
-                    tbuf[((long long)pr * T + ch.rows[t]) * r_max + j] = s * ch.scale;
+                    tbuf[((long long)pr * T + row_of(ch.rows, t)) * r_max + j] = s * ch.scale;
             }
         }
         __syncthreads();   // xs is reused by the next item
@@ -177,12 +177,12 @@ __global__ void __launch_bounds__(kSxThreads) lora_expand_kernel(const __grid_co
             for (int e = threadIdx.x; e < r; e += blockDim.x) pg[e] = P.pt[bq + e];
         for (int e = threadIdx.x; e < kChunk * r; e += blockDim.x) {
             const int t = e / r, j = e % r;
-            ts[t][j] = t < ch.count ? tbuf[((long long)pr * T + ch.rows[t]) * r_max + j] : 0.f;
+            ts[t][j] = t < ch.count ? tbuf[((long long)pr * T + row_of(ch.rows, t)) * r_max + j] : 0.f;
         }
         uint4 yv[kChunk];
 #pragma unroll
         for (int t = 0; t < kChunk; ++t)
-            yv[t] = (g == 0 && v < w8 && t < ch.count) ? ld16(yq + (long long)ch.rows[t] * pd.ldy + v * 8)
+            yv[t] = (g == 0 && v < w8 && t < ch.count) ? ld16(yq + (long long)row_of(ch.rows, t) * pd.ldy + v * 8)
                                                        : make_uint4(0, 0, 0, 0);
         if (__syncthreads_or(bad)) {
             if (threadIdx.x == 0) set_error(&hdr->err, LORA_DERR_PAGE);
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kSxThreads) lora_expand_kernel(const __grid_co
 #pragma unroll
             for (int t = 0; t < kChunk; ++t) {
                 if (t >= ch.count) break;
-                __nv_bfloat16* yp = yq + (long long)ch.rows[t] * pd.ldy + v * 8;
+                __nv_bfloat16* yp = yq + (long long)row_of(ch.rows, t) * pd.ldy + v * 8;
                 float y8[8];
                 unpack8(yv[t], y8);
                 float s8[8];

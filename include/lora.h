@@ -156,7 +156,7 @@ typedef struct {
                                     4 or 8; 0 = 8 where three stages fit, else 4        */
     int32_t split_max_problems;  /* decode launches of at most this many projections run
                                     the cluster kernel (each chunk split over 8 CTAs);
-                                    0 = never, 1..8; -1 = default (2)                   */
+                                    0 = never, 1..8; -1 = default (1)                   */
     int32_t mma_min_rows;        /* prefill segments of at least this many rows take the
                                     tensor-core tiles; 0 = never, >= 2; -1 = default:
                                     by rank, 512 / r rows under rank 32, 16 from rank

@@ -137,7 +137,7 @@ def test_pool_tuning_defaults_overrides_and_checks(lib):
                 round(t.fused_ring_speed, 4))
 
     default = get()
-    assert default == (0, 2, -1, 3, 1.22)
+    assert default == (0, 1, -1, 3, 1.22)
 
     def set_(**kw):
         f = dict(ring_rows_per_stage=0, split_max_problems=-1, mma_min_rows=-1, mma_y_stages=0,

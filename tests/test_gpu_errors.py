@@ -20,8 +20,8 @@ def _wl(wide=False):
     return small_decode(71, 512, 1, 2, 6, [4, 8], 20)
 
 
-# the decode batches here have 2 projections: the cluster kernel by default, the ring
-# kernel when the cluster kernel is turned off
+# the decode batches here have 2 projections: the cluster kernel when its limit allows
+# them, the ring kernel when the cluster kernel is turned off
 PATHS = {"cluster": {"split_max_problems": 8}, "ring": {"split_max_problems": 0}}
 
 
