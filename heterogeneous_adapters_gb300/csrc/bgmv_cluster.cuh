@@ -26,7 +26,8 @@
 namespace lora {
 
 constexpr int kClusterCtas = 8;          // CTAs of one cluster (the portable maximum)
-constexpr int kClusterThreads = 256;
+constexpr int kClusterThreads = 256;      // three CTAs per SM (80 registers): 57 resident clusters,
+                                          // enough for a one-projection launch's chunks in one round
 constexpr int kClusterMaxProbs = 8;      // projections of one launch at most
 constexpr int kClusterDefaultProbs = 1;  // the default limit (measured against the ring kernel)
 constexpr int kClusterExpandVecs = 64;   // 16-byte column vectors per expand pass
@@ -120,7 +121,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 // W: the pool has projections whose widths differ from h (vectors over several pages);
 // W = false compiles the h x h case.
 template <bool W>
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterThreads)
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterThreads, 3)
     bgmv_cluster_kernel(const __grid_constant__ ClusterParams p) {
     extern __shared__ __align__(16) unsigned char cl_smem[];
     const ClusterSmem L = cluster_smem_layout(p.ni, p.pool.r_max, p.pv_max);
