@@ -309,7 +309,8 @@ lora_status lora_stage_pages(const lora_pool* pool, const void* host_rows, const
                              const int32_t* upd_page, int64_t nupd, void* stream);
 
 /* Adapter staging through the copy engines (the host link's DMA engines, no SM), on
- * `stream`.  host_rows: pinned host memory, row i = h bf16 values for pool page
+ * `stream`: the same prefetch as lora_stage_pages ("S-LoRA: Serving Thousands of
+ * Concurrent LoRA Adapters", "Host memory for adapters").  host_rows: pinned host memory, row i = h bf16 values for pool page
  * dst_pages[i], 16-byte aligned.  Destination pages that form runs of consecutive ids
  * (dst_pages[i + 1] = dst_pages[i] + 1) are copied straight into the pool, one
  * cudaMemcpyAsync per run, when the call has at most LORA_STAGE_MAX_RUNS runs; otherwise
