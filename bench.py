@@ -38,7 +38,9 @@ UNIT = "tokens/s"
 def workload_for(name: str):
     """A named workload of the workload module, or a small variant of one for profiler
     captures: "decode-small" (4 layers, 300 adapters, ~2.4 GB pool), "decode-l12" (12 layers,
-    100 adapters, ~2.4 GB: enough projections per launch for a sweep), "prefill-small" (2
+    100 adapters, ~2.4 GB: enough projections per launch for a sweep), "stress-distinct-small"
+    and "stress-zipf-small" (the unified-pool stress shape at 8 layers, 500 adapters, a 2^18-page
+    pool of one-layer slices), "prefill-small" (2
     layers x 2 projections, ~2 GB on the device), "mixed-small" (1 layer x 2 projections),
     "llama3-decode-small" and "llama3-prefill-small" (1 layer)."""
     from workloads import spec
@@ -48,6 +50,11 @@ def workload_for(name: str):
     if name == "decode-l12":
         return spec.decode_workload("llama7b-decode-bgmv-h4096-t64-a100-l12", 1001, 4096, 12, 4,
                                     100, [8, 16, 32, 64], 64, 1.0)
+    if name in ("stress-distinct-small", "stress-zipf-small"):
+        v = name.split("-")[1]
+        return spec.decode_workload(f"unified-pool-stress-{v}-h4096-t256-a500-l8", 1004 if v == "distinct" else 1014,
+                                    4096, 8, 4, 500, [8, 16, 32, 64], 256, 1.2 if v == "zipf" else None,
+                                    num_pages=1 << 18, distinct=(v == "distinct"), layer_slices=True)
     if name == "prefill-small":
         return spec.prefill_workload("llama7b-prefill-sgmv-h4096-s32-a1000-l2p2", 1002, 4096, 2, 2,
                                      1000, [8, 16, 32, 64], 32, 64, 1024, 1.0)
