@@ -18,12 +18,15 @@
 //                      rows of the chunk, then its A-row pages, then its B-column pages,
 //                      up to RP rows of 2h bytes per stage (RP = 4 or 8: the fewer,
 //                      larger stages the better a bulk-copy ring streams, as long as
-//                      three of them fit);
-//   warps 1..8         consume the stages in the same order: x into registers; each A
-//                      page -> fp32 partial dot products, reduced across the warp with a
-//                      transposing shuffle and across warps in shared memory (t, scaled);
-//                      each B page -> acc[row][col] += t[row][j] * B_j[col]; finally
-//                      y = bf16_rn(y + acc) with 16-byte stores.
+//                      three of them fit).  It prepares the next item while the current
+//                      one's x and A stages land;
+//   warps 1..CW        consume the stages in the same order: x into registers; the A
+//                      pages -> t (on the tensor cores with warp-level mma.sync where the
+//                      row splits into groups of four 16-byte vectors per warp, else fp32
+//                      partial dot products reduced with a transposing shuffle), summed
+//                      across warps in shared memory and scaled; each B page ->
+//                      acc[row][col] += t[row][j] * B_j[col]; finally y = bf16_rn(y + acc)
+//                      with 16-byte stores.
 // Bytes in flight are bounded by the ring (about 190 KB per SM), not by registers.
 // Every wait is bounded in time; a timeout sets LORA_DERR_TIMEOUT and unwinds.
 #pragma once
