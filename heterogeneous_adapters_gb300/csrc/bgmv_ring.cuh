@@ -193,7 +193,7 @@ __device__ __forceinline__ void ring_expand_stage(const unsigned char* stage, in
 #pragma unroll
                     for (int t = 0; t < NT; ++t)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[t][v][e] = fmaf(tv[t], b8[e], acc[t][v][e]);
+                        for (int e = 0; e < 8; e += 2) fma2_f32(acc[t][v][e], acc[t][v][e + 1], tv[t], b8[e], b8[e + 1]);
                 }
             }
         }

@@ -140,6 +140,18 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 // order with the mixed-precision FMA (bf16 inputs, fp32 addend and result): the products
 // are exact and each FMA rounds once, as fmaf on the widened values does, but the bf16
 // halves feed the FMA directly instead of being widened first.
+// Two fp32 FMAs in one instruction (packed f32x2, sm_100 and later): c0 += a * b0 and
+// c1 += a * b1, each rounded as fmaf would round it.  The expands multiply one fp32 t value
+// by the columns of a B vector, so pairs of neighbouring columns share the multiplier.
+__device__ __forceinline__ void fma2_f32(float& c0, float& c1, float a, float b0, float b1) {
+    unsigned long long c, av, bv;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "f"(a), "f"(a));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(bv) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(c0), "f"(c1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(av), "l"(bv));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(c));
+}
+
 __device__ __forceinline__ float fma_bf16x2(uint32_t x, uint32_t a, float s) {
     asm("{\n\t.reg .b16 xl, xh, al, ah;\n\t"
         "mov.b32 {xl, xh}, %1;\n\t"

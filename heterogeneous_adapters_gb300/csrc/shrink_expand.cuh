@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kSxThreads) lora_expand_kernel(const __grid_co
                 for (int t = 0; t < kChunk; ++t) {
                     const float tj = ts[t][j];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(tj, b8[e], acc[t][e]);
+                    for (int e = 0; e < 8; e += 2) fma2_f32(acc[t][e], acc[t][e + 1], tj, b8[e], b8[e + 1]);
                 }
             }
         }
