@@ -42,7 +42,7 @@ constexpr uint32_t kDerrTimeout = LORA_DERR_TIMEOUT;
 
 enum StageKind : int32_t { kStageX = 0, kStageA = 1, kStageB = 2, kStageStop = 3, kStageSkip = 4 };
 
-struct StageMeta {
+struct alignas(16) StageMeta {   // written and read as three 16-byte words
     int32_t kind;
     int32_t npages;   // rows carried by this stage
     int32_t j0;       // first page index (A/B stages)
@@ -84,6 +84,7 @@ __host__ __device__ inline RingSmem ring_smem_layout(int stages, int stage_bytes
     L.full = o;  o += stages * 8;
     L.empty = o; o += stages * 8;
     L.cbar = o;  o += 8;
+    o = (o + 15) & ~15u;
     L.meta = o;  o += stages * sizeof(StageMeta);
     o = (o + 15) & ~15u;
     L.red = o;   o += cwarps * rp * kChunk * 4;
@@ -435,7 +436,9 @@ __device__ __forceinline__ void ring_cta(const P& p, unsigned char* base, uint32
 #pragma unroll
             for (int k = 0; k < kPg; ++k) {
                 const int e = lane + 32 * k;
-                pg[k] = e < c.rank ? PV.pt[a0 + e] : (e < 2 * c.rank ? PV.pt[b0 + e - c.rank] : 0);
+                pg[k] = 0;
+                if (32 * k < 2 * c.rank)   // whole groups of 32 ids past the item's are skipped
+                    pg[k] = e < c.rank ? PV.pt[a0 + e] : (e < 2 * c.rank ? PV.pt[b0 + e - c.rank] : 0);
             }
         };
         struct Cur {
