@@ -234,8 +234,9 @@ __device__ __forceinline__ bool ring_consume_item(const P& p, unsigned char* bas
     // waited by the caller), then page kb of the A rows; partial sums add up over blocks
     const int pv_in = W ? vec_pages(pd.d_in, h) : 1, pv_out = W ? vec_pages(pd.d_out, h) : 1;
     // tensor-core shrink: one vector per thread (NV = 1), h x h pages, and the row's vectors
-    // split into groups of four per warp (h = 1024, 2048, 4096 with 8 or 16 warps)
-    constexpr bool kMmaShape = (NV == 1 && !W && RP == 8);
+    // split into groups of four per warp (h = 1024, 2048, 4096 with 8 or 16 warps); a 4-row
+    // stage fills half of the MMA's 8 page columns, the rest read as zeros
+    constexpr bool kMmaShape = (NV == 1 && !W && (RP == 8 || RP == 4));
     const int warp_vecs = h8 / CW;
     const int xgroups = warp_vecs / 4;   // k-step pairs of a warp: 1, 2, 4 or 8
     if (kMmaShape && h8 % (CW * 4) == 0 && (xgroups == 1 || xgroups == 2 || xgroups == 4 || xgroups == 8)) {
