@@ -14,7 +14,7 @@ from .harness import GpuCase, full_check
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("path", ["mapped", "copy_engine", "copy_engine_staged"])
+@pytest.mark.parametrize("path", ["mapped", "copy_engine", "copy_engine_runs", "copy_engine_staged"])
 def test_stage_moves_adapters_to_free_pages(path):
     import torch
 
@@ -34,6 +34,10 @@ def test_stage_moves_adapters_to_free_pages(path):
                                             pool.num_proj * 2 * pool.ranks[a]) for a in movers])
         old_pages = pool.pt[entries].astype(np.int64)
         new_pages = (pool.num_pages - extra + np.arange(entries.size)).astype(np.int32)
+        if path == "copy_engine_runs":   # a few runs of consecutive pages, separated by gaps
+            new_pages = (new_pages + 3 * (np.arange(new_pages.size) // 37)).astype(np.int32)
+            runs = 1 + int(np.count_nonzero(np.diff(new_pages) != 1))
+            assert 1 < runs <= lora.LORA_STAGE_MAX_RUNS
         if path == "copy_engine_staged":   # scattered destinations: more runs than direct copies take
             new_pages = np.random.default_rng(5).permutation(new_pages).astype(np.int32)
             runs = 1 + int(np.count_nonzero(np.diff(new_pages) != 1))
@@ -50,7 +54,7 @@ def test_stage_moves_adapters_to_free_pages(path):
             if path == "mapped":
                 lora.stage_pages(case.pool, host_rows, dst, entries.size, dev.pt, upd_index, upd_page,
                                  entries.size, side.cuda_stream)
-            elif path == "copy_engine":   # one run of consecutive pages: no staging buffer needed
+            elif path in ("copy_engine", "copy_engine_runs"):   # runs of consecutive pages: no staging buffer
                 lora.stage_pages_ce(case.pool, host_rows, None, 0, dst, entries.size, dev.pt,
                                     upd_index, upd_page, entries.size, side.cuda_stream)
             else:
