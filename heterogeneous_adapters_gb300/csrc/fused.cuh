@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) delta_fused_kernel(const __gri
     if (blockIdx.x < gf)
         ring_cta<NV, CW, RP, W>(p.ring, fused_smem_raw, blockIdx.x, gf);
     else
-        mma_cta<W>(p.mma, fused_smem_raw, blockIdx.x - gf, gridDim.x - gf);
+        mma_cta<W>(p.mma, fused_smem_raw, gridDim.x - gf);
 }
 
 }  // namespace lora

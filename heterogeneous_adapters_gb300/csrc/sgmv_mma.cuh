@@ -19,11 +19,16 @@
 //           the B-column pages' slices as an MN-major operand (TMA, 128-byte swizzle),
 //           double-buffered in TMEM so the epilogue of one slice overlaps the MMA of the
 //           next; the epilogue adds D2 to y (fp32) and stores bf16 rows of the tile.
-// Roles (one persistent CTA per SM, items dealt round-robin): warp 0 streams the shrink
-// operands (x and A chunks), warp 2 the B^T slices, warp 3 the y tiles, warp 1 owns TMEM
+// Roles (one persistent CTA per SM): warp 0 takes items from a queue shared by the
+// launch's CTAs (an atomic counter in the workspace), checks their pages, hands them to
+// the other roles through a small queue in shared memory and streams the shrink operands
+// (x and A chunks); warp 2 streams the B^T slices, warp 3 the y tiles, warp 1 owns TMEM
 // and issues the MMAs -- while it expands tile k it also issues tile k+1's shrink chunks
 // as they land, so the x stream of the next tile overlaps the y stream of this one -- and
-// warps 4-11 convert D1 and run the epilogue.  T lives in TMEM.
+// warps 4-11 convert D1 and run the epilogue.  T lives in TMEM.  Items differ in cost by
+// up to 10x (rank 8 to 64, projection widths 1024 to 14336); taken from a queue, the
+// CTAs of a launch end within about one item of each other, which a fixed round-robin
+// deal does not give.
 // All waits are bounded; a timeout sets an error bit and the CTA unwinds.
 #pragma once
 #include <cuda.h>
@@ -47,6 +52,8 @@ constexpr int kMmaKChunk = 64;              // elements per shrink K chunk (128 
 constexpr int kMmaNTile = 128;              // y columns per expand slice
 constexpr int kMmaRowBlock = 32;            // rows per x / y TMA box
 constexpr int kMmaMaxStages = 8;
+constexpr int kMmaQueue = 8;                // item slots of the CTA's item queue
+constexpr int kMmaQueueReaders = 3 + kMmaEpiWarps;   // warps 1, 2, 3 and the epilogue warps
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: D1 (shrink, fp32) 0..127, D2 (expand, fp32, two buffers) 128..383,
 // T_hi and T_lo (bf16 pairs, K / 2 columns each) 384..447 and 448..511.
@@ -76,7 +83,7 @@ struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
 
 struct MmaSmem {
     uint32_t ring1, ring2, ring3, full1, empty1, full2, empty2, full3, empty3, d1_full, t_ready, d2_full,
-        d2_empty, final_bar, tmem_slot, total;
+        d2_empty, final_bar, tmem_slot, qfull, qempty, qitem, total;
 };
 
 __host__ __device__ inline MmaSmem mma_smem_layout(int s1, int s1_bytes, int s2, int s2_bytes, int s3) {
@@ -97,14 +104,17 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int s1, int s1_bytes, int s2,
     L.d2_empty = o;  o += 16;
     L.final_bar = o; o += 8;
     L.tmem_slot = o; o += 8;
+    L.qfull = o;     o += kMmaQueue * 8;
+    L.qempty = o;    o += kMmaQueue * 8;
+    L.qitem = o;     o += kMmaQueue * 4;
     L.total = o;
     return L;
 }
 
 __host__ __device__ inline int mma_rpad(int r) { return r <= 16 ? 16 : (r + 15) / 16 * 16; }
 
-// All roles walk the same items; this reads one and checks its pages (every role gets
-// the same answer, so a bad item is skipped by all of them without communication).
+// One work item as every role reads it; warp 0 alone checks the pages (Check) and passes
+// on only the items that pass.
 struct MmaItem {
     Tile tile;
     int pr;
@@ -123,7 +133,7 @@ struct MmaItem {
 // tiles of one segment (which read the same adapter pages) run side by side.
 // W: the launch has projections whose widths differ from h; W = false compiles the h x h
 // case (one page block per vector, h / 64 chunks and h / 128 slices per item).
-template <bool W>
+template <bool W, bool Check>
 __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tiles, int n_tiles, uint32_t item,
                                             int lane) {
     MmaItem it;
@@ -138,26 +148,17 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
     it.n_kc = W ? p.n_kc[it.pr] : p.pool.h / kMmaKChunk;
     it.n_nt = W ? p.n_nt[it.pr] : p.pool.h / kMmaNTile;
     it.pv_in = W ? p.pv_in[it.pr] : 1;
-    bool bad = false;
-    const int n_ent = W ? (it.pv_in + p.pv_out[it.pr]) * r : 2 * r;   // every page of the item
-    for (int e = lane; e < n_ent; e += 32) {
-        const int page = p.pool.pt[it.blk + e];
-        bad |= (page < 0 || page >= p.pool.num_pages);
+    it.ok = true;
+    if (Check) {
+        bool bad = false;
+        const int n_ent = W ? (it.pv_in + p.pv_out[it.pr]) * r : 2 * r;   // every page of the item
+        for (int e = lane; e < n_ent; e += 32) {
+            const int page = p.pool.pt[it.blk + e];
+            bad |= (page < 0 || page >= p.pool.num_pages);
+        }
+        it.ok = !__any_sync(0xffffffffu, bad);
     }
-    it.ok = !__any_sync(0xffffffffu, bad);
     return it;
-}
-
-// The next processable item at or after `item` (skipping items with bad pages), or total.
-template <bool W>
-__device__ __forceinline__ uint32_t mma_next_ok(const MmaParams& p, const Tile* tiles, int n_tiles,
-                                                uint32_t item, uint32_t total, uint32_t ncta, int lane,
-                                                MmaItem& mi) {
-    for (; item < total; item += ncta) {
-        mi = mma_item<W>(p, tiles, n_tiles, item, lane);
-        if (mi.ok) return item;
-    }
-    return total;
 }
 
 // Issue the four shrink MMAs of one K chunk (stage at shared address st) into D1.
@@ -170,9 +171,10 @@ __device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t st, uin
     }
 }
 
-// One CTA of the tensor-core kernel: CTA `cta` of `ncta` taking part (all kMmaThreads threads).
+// One CTA of the tensor-core kernel (all kMmaThreads threads); `ncta` CTAs of the launch
+// run this body and share its item queue (the last of them to end resets the queue).
 template <bool W>
-__device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_raw, uint32_t cta, uint32_t ncta) {
+__device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_raw, uint32_t ncta) {
     // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -210,6 +212,10 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             mbar_init(bar(L.d2_empty + b * 8), kMmaEpiWarps);
         }
         mbar_init(bar(L.final_bar), 1);
+        for (int s = 0; s < kMmaQueue; ++s) {
+            mbar_init(bar(L.qfull + s * 8), 1);
+            mbar_init(bar(L.qempty + s * 8), kMmaQueueReaders);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -221,17 +227,57 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L.tmem_slot);
     bool ok = true;
+    // The CTA's item queue: warp 0 writes the ids of the items it has taken (an id >= total
+    // ends the queue), every other role reads each slot once.  False on a timeout.
+    auto take = [&](uint32_t& qk, uint32_t& item) -> bool {
+        const uint32_t s = qk % kMmaQueue;
+        if (!mbar_wait(bar(L.qfull + s * 8), (qk / kMmaQueue) & 1, kWaitLimitNs)) return false;
+        item = *reinterpret_cast<volatile const uint32_t*>(base + L.qitem + s * 4);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L.qempty + s * 8));
+        ++qk;
+        return true;
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ shrink producer
+        // ------------------------------------------------------------------ item queue + shrink producer
         if (lane == 0) prefetch_tmap(&p.pool_map);
-        uint32_t it = 0;
-        for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
-            if (!mi.ok) {
+        uint32_t it = 0, qp = 0;
+        unsigned int* const counter = &hdr->work_counter2;
+        // the launch's queue hands out item ids in order; the id after the one in use is
+        // fetched ahead (lane 0), so the atomic's round trip hides under a stream
+        uint32_t ahead = 0;
+        if (lane == 0) ahead = atomicAdd(counter, 1u);
+        // the next item whose pages are all in the pool, or total once the queue is empty
+        auto fetch = [&](MmaItem& mi) -> uint32_t {
+            for (;;) {
+                const uint32_t id = __shfl_sync(0xffffffffu, ahead, 0);
+                if (id >= total) return total;
+                if (lane == 0) ahead = atomicAdd(counter, 1u);
+                mi = mma_item<W, true>(p, tiles, n_tiles, id, lane);
+                if (mi.ok) return id;
                 if (lane == 0) set_error(&hdr->err, LORA_DERR_PAGE);
-                continue;
             }
+        };
+        auto publish = [&](uint32_t id) -> bool {
+            const uint32_t s = qp % kMmaQueue;
+            if (!mbar_wait(bar(L.qempty + s * 8), ((qp / kMmaQueue) & 1) ^ 1, kWaitLimitNs)) return false;
+            if (lane == 0) {
+                *reinterpret_cast<volatile uint32_t*>(base + L.qitem + s * 4) = id;
+                mbar_arrive(bar(L.qfull + s * 8));
+            }
+            __syncwarp();
+            ++qp;
+            return true;
+        };
+        MmaItem mi, mn;
+        uint32_t item = fetch(mi);
+        ok = publish(item);
+        while (item < total && ok) {
+            // the next item goes out before this one streams: the MMA issuer reads it when
+            // it starts this item's expand
+            const uint32_t next = fetch(mn);
+            if (!publish(next)) { ok = false; break; }
             const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
             const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
             const void* xmap = &p.x_map[mi.pr];
@@ -276,6 +322,8 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                 }
                 ++it;
             }
+            item = next;
+            mi = mn;
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
         if (lane == 0) {   // let every stage this warp filled land before the CTA can exit
@@ -284,10 +332,11 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------------ B^T producer
-        uint32_t it2 = 0;
-        for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
-            if (!mi.ok) continue;
+        uint32_t it2 = 0, qk = 0, item = 0;
+        while (ok) {
+            if (!take(qk, item)) { ok = false; break; }
+            if (item >= total) break;
+            const MmaItem mi = mma_item<W, false>(p, tiles, n_tiles, item, lane);
             const int r = mi.tile.rank, rp = mi.rp;
             int pgb[4];
             for (int nt = 0; nt < mi.n_nt; ++nt, ++it2) {
@@ -336,10 +385,11 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         }
     } else if (warp == 3) {
         // ------------------------------------------------------------------ y producer
-        uint32_t it3 = 0;
-        for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
-            if (!mi.ok) continue;
+        uint32_t it3 = 0, qk = 0, item = 0;
+        while (ok) {
+            if (!take(qk, item)) { ok = false; break; }
+            if (item >= total) break;
+            const MmaItem mi = mma_item<W, false>(p, tiles, n_tiles, item, lane);
             const int row0 = mi.tile.row0;
             const int nblk = (mi.tile.rows + kMmaRowBlock - 1) / kMmaRowBlock;
             const void* ymap = &p.y_map[mi.pr];
@@ -364,12 +414,14 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0;
+        uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0, qk = 0;
         MmaItem cur, nxt;
-        uint32_t item = mma_next_ok<W>(p, tiles, n_tiles, cta, total, ncta, lane, cur);
+        uint32_t item = total;
+        if (!take(qk, item)) ok = false;
         int kc_next = 0;   // shrink chunks of `nxt` already issued
         // shrink of the first tile
-        if (item < total) {
+        if (ok && item < total) {
+            cur = mma_item<W, false>(p, tiles, n_tiles, item, lane);
             const uint32_t id_shrink = idesc_bf16(128, cur.rp, 0, 0);
             for (int kc = 0; kc < cur.n_kc && ok; ++kc, ++it1) {
                 const uint32_t s = it1 % S1;
@@ -385,8 +437,10 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             __syncwarp();
         }
         while (item < total && ok) {
-            const uint32_t next_item = mma_next_ok<W>(p, tiles, n_tiles, item + ncta, total, ncta, lane, nxt);
+            uint32_t next_item = total;
+            if (!take(qk, next_item)) { ok = false; break; }
             const bool has_next = next_item < total;
+            if (has_next) nxt = mma_item<W, false>(p, tiles, n_tiles, next_item, lane);
             const uint32_t id_next = has_next ? idesc_bf16(128, nxt.rp, 0, 0) : 0;
             kc_next = 0;
             // D1 is free once this tile's convert has read it
@@ -460,11 +514,12 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         const int half = e >> 2;                // column half of each slice
         const int m = quad * 32 + lane;         // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        uint32_t tcount = 0, g = 0;
+        uint32_t tcount = 0, g = 0, qk = 0, item = 0;
         bool stored = false;
-        for (uint32_t item = cta; item < total && ok; item += ncta) {
-            const MmaItem mi = mma_item<W>(p, tiles, n_tiles, item, lane);
-            if (!mi.ok) continue;
+        while (ok) {
+            if (!take(qk, item)) { ok = false; break; }
+            if (item >= total) break;
+            const MmaItem mi = mma_item<W, false>(p, tiles, n_tiles, item, lane);
             const int rp = mi.rp, rows = mi.tile.rows, row0 = mi.tile.row0;
             const float scale = p.pool.scales[mi.tile.adapter];
             const bool live = m < rows;
@@ -561,12 +616,21 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    // the last of the launch's CTAs to end resets the queue for the next launch (every CTA
+    // has taken its last id by now; the next launch on the stream starts after this one)
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&hdr->done_counter, 1u) == ncta - 1) {
+            atomicExch(&hdr->work_counter2, 0u);
+            atomicExch(&hdr->done_counter, 0u);
+        }
+    }
 }
 
 template <bool W>
 __global__ void __launch_bounds__(kMmaThreads, 1) sgmv_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) unsigned char mma_smem_raw[];
-    mma_cta<W>(p, mma_smem_raw, blockIdx.x, gridDim.x);
+    mma_cta<W>(p, mma_smem_raw, gridDim.x);
 }
 
 }  // namespace lora
