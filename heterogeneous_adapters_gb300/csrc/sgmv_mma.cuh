@@ -55,9 +55,11 @@ constexpr int kMmaMaxStages = 8;
 constexpr int kMmaQueue = 8;                // item slots of the CTA's item queue
 constexpr int kMmaQueueReaders = 3 + kMmaEpiWarps;   // warps 1, 2, 3 and the epilogue warps
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D1 (shrink, fp32) 0..127, D2 (expand, fp32, two buffers) 128..383,
-// T_hi and T_lo (bf16 pairs, K / 2 columns each) 384..447 and 448..511.
+// TMEM columns: D1 (shrink, fp32) 0..127 -- two buffers of 64 columns when every rank of
+// the launch is <= 64 --, D2 (expand, fp32, two buffers) 128..383, T_hi and T_lo (bf16
+// pairs, K / 2 columns each) 384..447 and 448..511.
 constexpr uint32_t kD1Col = 0, kD2Col = 128, kThiCol = 384, kTloCol = 448;
+constexpr int kMmaD1Half = 64;
 constexpr uint32_t kDerrTimeoutMma = LORA_DERR_TIMEOUT;
 
 struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
@@ -98,7 +100,7 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int s1, int s1_bytes, int s2,
     L.empty2 = o;    o += kMmaMaxStages * 8;
     L.full3 = o;     o += kMmaMaxStages * 8;
     L.empty3 = o;    o += kMmaMaxStages * 8;
-    L.d1_full = o;   o += 8;
+    L.d1_full = o;   o += 16;
     L.t_ready = o;   o += 8;
     L.d2_full = o;   o += 16;
     L.d2_empty = o;  o += 16;
@@ -162,12 +164,12 @@ __device__ __forceinline__ MmaItem mma_item(const MmaParams& p, const Tile* tile
 }
 
 // Issue the four shrink MMAs of one K chunk (stage at shared address st) into D1.
-__device__ __forceinline__ void mma_shrink_chunk(uint32_t tmem, uint32_t st, uint32_t idesc, int kc) {
+__device__ __forceinline__ void mma_shrink_chunk(uint32_t d1, uint32_t st, uint32_t idesc, int kc) {
 #pragma unroll
     for (int kk = 0; kk < kMmaKChunk / 16; ++kk) {
         const uint64_t da = smem_desc(st + kk * 32, 16, 1024, 2);
         const uint64_t db = smem_desc(st + 16384 + kk * 32, 16, 1024, 2);
-        tc_mma_f16(tmem + kD1Col, da, db, idesc, (kc | kk) != 0);
+        tc_mma_f16(d1, da, db, idesc, (kc | kk) != 0);
     }
 }
 
@@ -206,6 +208,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             mbar_init(bar(L.empty3 + s * 8), kMmaEpiWarps);
         }
         mbar_init(bar(L.d1_full), 1);
+        mbar_init(bar(L.d1_full + 8), 1);
         mbar_init(bar(L.t_ready), kMmaEpiWarps);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L.d2_full + b * 8), 1);
@@ -414,42 +417,83 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
+        // Two cursors over the CTA's items, which the shrink side reads from the queue in
+        // order.  The shrink side issues an item's K chunks into a D1 buffer as they land;
+        // the expand side follows, starting an item once its shrink is issued and its t
+        // converted (which frees that D1 buffer).  With two D1 buffers (every rank <= 64)
+        // the shrink runs up to two items ahead of the expand, so the x stream of items with
+        // a short expand (k and v of grouped-query attention, down) goes on under a long
+        // one (gate, up); with one buffer, one item ahead.
+        const uint32_t nbuf = p.rp_max <= kMmaD1Half ? 2u : 1u;
         uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0, qk = 0;
-        MmaItem cur, nxt;
-        uint32_t item = total;
-        if (!take(qk, item)) ok = false;
-        int kc_next = 0;   // shrink chunks of `nxt` already issued
-        // shrink of the first tile
-        if (ok && item < total) {
-            cur = mma_item<W, false>(p, tiles, n_tiles, item, lane);
-            const uint32_t id_shrink = idesc_bf16(128, cur.rp, 0, 0);
-            for (int kc = 0; kc < cur.n_kc && ok; ++kc, ++it1) {
-                const uint32_t s = it1 % S1;
-                if (!mbar_wait(bar(L.full1 + s * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    mma_shrink_chunk(tmem, bar(L.ring1 + s * p.s1_bytes), id_shrink, kc);
-                    tc_commit(bar(L.empty1 + s * 8));
+        uint32_t s_seq = 0;      // items whose shrink is issued (and committed to d1_full)
+        uint32_t e_seq = 0;      // items whose expand has started
+        bool s_busy = false;     // item s_seq's shrink is under way
+        bool q_end = false;      // the queue's end has been read
+        MmaItem sh;              // item s_seq
+        int s_kc = 0;            // its chunks issued
+        uint32_t s_idesc = 0;
+        uint32_t f0 = 0, f1 = 0; // items e_seq and e_seq + 1 (shrunk or under way): n_nt << 8 | rp
+        // Advances the shrink side: starts the next item while a D1 buffer is free and
+        // issues the chunks that have landed; `block` waits for every chunk of one item.
+        // False on a timeout.
+        auto shrink_step = [&](bool block) -> bool {
+            for (;;) {
+                if (!s_busy) {
+                    if (q_end || s_seq >= e_seq + nbuf) return true;
+                    uint32_t id = total;
+                    if (!take(qk, id)) return false;
+                    if (id >= total) {
+                        q_end = true;
+                        return true;
+                    }
+                    sh = mma_item<W, false>(p, tiles, n_tiles, id, lane);
+                    s_idesc = idesc_bf16(128, sh.rp, 0, 0);
+                    s_kc = 0;
+                    s_busy = true;
+                    const uint32_t packed = (uint32_t)sh.n_nt << 8 | (uint32_t)sh.rp;
+                    if (s_seq == e_seq) f0 = packed;
+                    else f1 = packed;
                 }
+                const uint32_t b1 = s_seq % nbuf;
+                while (s_kc < sh.n_kc) {
+                    const uint32_t s1 = it1 % S1;
+                    if (block) {
+                        if (!mbar_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1, kWaitLimitNs)) return false;
+                    } else if (!mbar_test_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) {
+                        return true;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        mma_shrink_chunk(tmem + kD1Col + b1 * kMmaD1Half, bar(L.ring1 + s1 * p.s1_bytes), s_idesc,
+                                         s_kc);
+                        tc_commit(bar(L.empty1 + s1 * 8));
+                    }
+                    __syncwarp();
+                    ++s_kc;
+                    ++it1;
+                }
+                if (lane == 0) tc_commit(bar(L.d1_full + b1 * 8));
                 __syncwarp();
+                s_busy = false;
+                ++s_seq;
+                if (block) return true;
             }
-            if (lane == 0) tc_commit(bar(L.d1_full));
-            __syncwarp();
-        }
-        while (item < total && ok) {
-            uint32_t next_item = total;
-            if (!take(qk, next_item)) { ok = false; break; }
-            const bool has_next = next_item < total;
-            if (has_next) nxt = mma_item<W, false>(p, tiles, n_tiles, next_item, lane);
-            const uint32_t id_next = has_next ? idesc_bf16(128, nxt.rp, 0, 0) : 0;
-            kc_next = 0;
-            // D1 is free once this tile's convert has read it
+        };
+        while (ok) {
+            // the next item's shrink, completed (a wait) if still under way
+            while (ok && e_seq >= s_seq && (s_busy || !q_end))
+                if (!shrink_step(true)) ok = false;
+            if (!ok || e_seq >= s_seq) break;   // a timeout, or no item left
+            // its t is in TMEM once the convert has read its D1 buffer
             if (!mbar_wait(bar(L.t_ready), tcount & 1, kWaitLimitNs)) { ok = false; break; }
             ++tcount;
+            const int rp = (int)(f0 & 0xffu), n_nt = (int)(f0 >> 8);
+            f0 = f1;
+            ++e_seq;
             tc_fence_after();
-            const int rp = cur.rp;
             const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
-            for (int nt = 0; nt < cur.n_nt && ok; ++nt, ++g, ++it2) {
+            for (int nt = 0; nt < n_nt && ok; ++nt, ++g, ++it2) {
                 const uint32_t s = it2 % S2;
                 const uint32_t b = g & 1;
                 if (!mbar_wait(bar(L.full2 + s * 8), (it2 / S2) & 1, kWaitLimitNs)) { ok = false; break; }
@@ -467,38 +511,10 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     tc_commit(bar(L.d2_full + b * 8));
                 }
                 __syncwarp();
-                // the next tile's shrink chunks that have already landed (a test, not a
-                // wait: a suspending wait here would hold the expand back for the whole shrink)
-                while (has_next && kc_next < nxt.n_kc) {
-                    const uint32_t s1 = it1 % S1;
-                    if (!mbar_test_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1)) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
-                        tc_commit(bar(L.empty1 + s1 * 8));
-                    }
-                    __syncwarp();
-                    ++kc_next;
-                    ++it1;
-                }
+                // shrink chunks that have already landed (a test, not a wait: a suspending
+                // wait here would hold the expand back for a whole shrink)
+                if (!shrink_step(false)) ok = false;
             }
-            if (!ok || !has_next) break;
-            // the rest of the next tile's shrink
-            for (; kc_next < nxt.n_kc && ok; ++kc_next, ++it1) {
-                const uint32_t s1 = it1 % S1;
-                if (!mbar_wait(bar(L.full1 + s1 * 8), (it1 / S1) & 1, kWaitLimitNs)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    mma_shrink_chunk(tmem, bar(L.ring1 + s1 * p.s1_bytes), id_next, kc_next);
-                    tc_commit(bar(L.empty1 + s1 * 8));
-                }
-                __syncwarp();
-            }
-            if (!ok) break;
-            if (lane == 0) tc_commit(bar(L.d1_full));
-            __syncwarp();
-            cur = nxt;
-            item = next_item;
         }
         if (!ok && lane == 0) set_error(&hdr->err, kDerrTimeoutMma);
         // every MMA issued by this thread must be complete before TMEM is freed
@@ -514,6 +530,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         const int half = e >> 2;                // column half of each slice
         const int m = quad * 32 + lane;         // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const uint32_t nbuf = p.rp_max <= kMmaD1Half ? 2u : 1u;   // D1 buffers, as the MMA issuer
         uint32_t tcount = 0, g = 0, qk = 0, item = 0;
         bool stored = false;
         while (ok) {
@@ -526,14 +543,15 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             const bool block_full = quad * kMmaRowBlock + kMmaRowBlock <= rows;
             const bool block_part = !block_full && quad * kMmaRowBlock < rows;
             // ---- convert D1 -> T_hi, T_lo in TMEM (bf16 pairs, column c / 2 holds k = c, c + 1)
-            if (!mbar_wait(bar(L.d1_full), tcount & 1, kWaitLimitNs)) { ok = false; break; }
+            const uint32_t b1 = tcount % nbuf;
+            if (!mbar_wait(bar(L.d1_full + b1 * 8), (tcount / nbuf) & 1, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             // the rp / 16 column chunks of D1 are split between the two warpgroups
             const int nck = rp / 16;
             const int ck_begin = half ? (nck + 1) / 2 : 0, ck_end = half ? nck : (nck + 1) / 2;
             for (int c0 = ck_begin * 16; c0 < ck_end * 16; c0 += 16) {
                 float v[16];
-                tmem_ld16(tmem + lane_base + kD1Col + c0, v);
+                tmem_ld16(tmem + lane_base + kD1Col + b1 * kMmaD1Half + c0, v);
                 tmem_ld_wait();
                 uint32_t hi[8], lo[8];
 #pragma unroll
