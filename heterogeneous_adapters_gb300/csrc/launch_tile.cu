@@ -193,10 +193,11 @@ lora_status run_mma(const lora_pool* pool, const lora_problem* probs, int32_t np
 // measured on the 13B mixed step (ring CTAs split by bytes alone ended 18% before the
 // tensor-core ones; 1.0 / 1.1 / 1.22 / 1.35 / 1.5: 11.67 / 11.29 / 11.18 / 11.42 / 12.95 ms).
 // Pools with projections of other widths: the ring body streams multi-page vectors (an x
-// block and an A page per input page block), a slower byte rate per CTA; measured on the
-// Llama-3-8B mixed step (0.6 / 0.75 / 0.9 / 1.0 / 1.22 / 1.4: 1.96 / 1.84 / 1.82 / 1.95 /
-// 2.11 / 2.37 ms).
-float default_fused_ring_speed(bool square) { return square ? 1.22f : 0.85f; }
+// block and an A page per input page block), and the tensor-core body's wide shapes (gate,
+// up, down) run at their own rate; measured on the Llama-3-8B mixed step with the tile
+// items taken from a queue and three D1 buffers (0.85 / 1.0 / 1.15: 1.904 / 1.869 / 1.879
+// ms on one box; 0.85 / 1.0: 1.902 / 1.855 and 1.864 / 1.852 ms on two others).
+float default_fused_ring_speed(bool square) { return square ? 1.22f : 1.0f; }
 
 // Both work classes in one launch per batch of projections (h <= 5120, h % 128 == 0); the
 // ring body takes the stage shape the stand-alone ring kernel would take.

@@ -55,11 +55,16 @@ constexpr int kMmaMaxStages = 8;
 constexpr int kMmaQueue = 8;                // item slots of the CTA's item queue
 constexpr int kMmaQueueReaders = 3 + kMmaEpiWarps;   // warps 1, 2, 3 and the epilogue warps
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D1 (shrink, fp32) 0..127 -- two buffers of 64 columns when every rank of
-// the launch is <= 64 --, D2 (expand, fp32, two buffers) 128..383, T_hi and T_lo (bf16
-// pairs, K / 2 columns each) 384..447 and 448..511.
+// TMEM columns: D1 (shrink, fp32) 0..127, D2 (expand, fp32, two buffers) 128..383, T_hi
+// and T_lo (bf16 pairs, K / 2 columns each) 384..447 and 448..511.  When every rank of the
+// launch is <= 64, t takes 32 columns per half (T_lo at 416) and D1 has three buffers of
+// 64 columns: 0, 64 and 448.
 constexpr uint32_t kD1Col = 0, kD2Col = 128, kThiCol = 384, kTloCol = 448;
 constexpr int kMmaD1Half = 64;
+constexpr uint32_t kTloColSmall = 416, kD1ThirdCol = 448;
+__device__ __forceinline__ uint32_t mma_nbuf(int rp_max) { return rp_max <= kMmaD1Half ? 3u : 1u; }
+__device__ __forceinline__ uint32_t mma_d1_col(uint32_t b) { return b < 2 ? kD1Col + b * kMmaD1Half : kD1ThirdCol; }
+__device__ __forceinline__ uint32_t mma_tlo_col(int rp_max) { return rp_max <= kMmaD1Half ? kTloColSmall : kTloCol; }
 constexpr uint32_t kDerrTimeoutMma = LORA_DERR_TIMEOUT;
 
 struct MmaParams {   // about 25 KB: kernel parameters may hold up to 32 KB
@@ -100,7 +105,7 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int s1, int s1_bytes, int s2,
     L.empty2 = o;    o += kMmaMaxStages * 8;
     L.full3 = o;     o += kMmaMaxStages * 8;
     L.empty3 = o;    o += kMmaMaxStages * 8;
-    L.d1_full = o;   o += 16;
+    L.d1_full = o;   o += 24;
     L.t_ready = o;   o += 8;
     L.d2_full = o;   o += 16;
     L.d2_empty = o;  o += 16;
@@ -209,6 +214,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         }
         mbar_init(bar(L.d1_full), 1);
         mbar_init(bar(L.d1_full + 8), 1);
+        mbar_init(bar(L.d1_full + 16), 1);
         mbar_init(bar(L.t_ready), kMmaEpiWarps);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L.d2_full + b * 8), 1);
@@ -420,11 +426,12 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         // Two cursors over the CTA's items, which the shrink side reads from the queue in
         // order.  The shrink side issues an item's K chunks into a D1 buffer as they land;
         // the expand side follows, starting an item once its shrink is issued and its t
-        // converted (which frees that D1 buffer).  With two D1 buffers (every rank <= 64)
-        // the shrink runs up to two items ahead of the expand, so the x stream of items with
-        // a short expand (k and v of grouped-query attention, down) goes on under a long
-        // one (gate, up); with one buffer, one item ahead.
-        const uint32_t nbuf = p.rp_max <= kMmaD1Half ? 2u : 1u;
+        // converted (which frees that D1 buffer).  With three D1 buffers (every rank <= 64)
+        // the shrink runs up to three items ahead of the expand, so the x stream of items
+        // with a short expand (k and v of grouped-query attention, down) goes on under a
+        // long one (gate, up); with one buffer, one item ahead.
+        const uint32_t nbuf = mma_nbuf(p.rp_max);
+        const uint32_t tlo = mma_tlo_col(p.rp_max);
         uint32_t it1 = 0, it2 = 0, tcount = 0, g = 0, qk = 0;
         uint32_t s_seq = 0;      // items whose shrink is issued (and committed to d1_full)
         uint32_t e_seq = 0;      // items whose expand has started
@@ -433,7 +440,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         MmaItem sh;              // item s_seq
         int s_kc = 0;            // its chunks issued
         uint32_t s_idesc = 0;
-        uint32_t f0 = 0, f1 = 0; // items e_seq and e_seq + 1 (shrunk or under way): n_nt << 8 | rp
+        uint32_t f0 = 0, f1 = 0, f2 = 0;   // items e_seq .. e_seq + 2 (shrunk or under way): n_nt << 8 | rp
         // Advances the shrink side: starts the next item while a D1 buffer is free and
         // issues the chunks that have landed; `block` waits for every chunk of one item.
         // False on a timeout.
@@ -452,8 +459,10 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     s_kc = 0;
                     s_busy = true;
                     const uint32_t packed = (uint32_t)sh.n_nt << 8 | (uint32_t)sh.rp;
-                    if (s_seq == e_seq) f0 = packed;
-                    else f1 = packed;
+                    const uint32_t fi = s_seq - e_seq;
+                    if (fi == 0) f0 = packed;
+                    else if (fi == 1) f1 = packed;
+                    else f2 = packed;
                 }
                 const uint32_t b1 = s_seq % nbuf;
                 while (s_kc < sh.n_kc) {
@@ -465,8 +474,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        mma_shrink_chunk(tmem + kD1Col + b1 * kMmaD1Half, bar(L.ring1 + s1 * p.s1_bytes), s_idesc,
-                                         s_kc);
+                        mma_shrink_chunk(tmem + mma_d1_col(b1), bar(L.ring1 + s1 * p.s1_bytes), s_idesc, s_kc);
                         tc_commit(bar(L.empty1 + s1 * 8));
                     }
                     __syncwarp();
@@ -490,6 +498,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             ++tcount;
             const int rp = (int)(f0 & 0xffu), n_nt = (int)(f0 >> 8);
             f0 = f1;
+            f1 = f2;
             ++e_seq;
             tc_fence_after();
             const uint32_t id_expand = idesc_bf16(128, kMmaNTile, 0, 1);
@@ -505,7 +514,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     for (int ks = 0; ks < rp / 16; ++ks) {
                         const uint64_t dbt = smem_desc(st + ks * 4096, 1024, 2048, 2);
                         tc_mma_f16_ts(d2, tmem + kThiCol + ks * 8, dbt, id_expand, ks != 0);
-                        tc_mma_f16_ts(d2, tmem + kTloCol + ks * 8, dbt, id_expand, 1);
+                        tc_mma_f16_ts(d2, tmem + tlo + ks * 8, dbt, id_expand, 1);
                     }
                     tc_commit(bar(L.empty2 + s * 8));
                     tc_commit(bar(L.d2_full + b * 8));
@@ -530,7 +539,8 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         const int half = e >> 2;                // column half of each slice
         const int m = quad * 32 + lane;         // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const uint32_t nbuf = p.rp_max <= kMmaD1Half ? 2u : 1u;   // D1 buffers, as the MMA issuer
+        const uint32_t nbuf = mma_nbuf(p.rp_max);   // D1 buffers and T_lo column, as the MMA issuer
+        const uint32_t tlo = mma_tlo_col(p.rp_max);
         uint32_t tcount = 0, g = 0, qk = 0, item = 0;
         bool stored = false;
         while (ok) {
@@ -551,7 +561,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
             const int ck_begin = half ? (nck + 1) / 2 : 0, ck_end = half ? nck : (nck + 1) / 2;
             for (int c0 = ck_begin * 16; c0 < ck_end * 16; c0 += 16) {
                 float v[16];
-                tmem_ld16(tmem + lane_base + kD1Col + b1 * kMmaD1Half + c0, v);
+                tmem_ld16(tmem + lane_base + mma_d1_col(b1) + c0, v);
                 tmem_ld_wait();
                 uint32_t hi[8], lo[8];
 #pragma unroll
@@ -564,7 +574,7 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
                     lo[i] = *reinterpret_cast<const uint32_t*>(&l2);
                 }
                 tmem_st8(tmem + lane_base + kThiCol + c0 / 2, hi);
-                tmem_st8(tmem + lane_base + kTloCol + c0 / 2, lo);
+                tmem_st8(tmem + lane_base + tlo + c0 / 2, lo);
             }
             tmem_st_wait();
             tc_fence_before();
