@@ -157,6 +157,31 @@ def test_pool_tuning_defaults_overrides_and_checks(lib):
     lib.lora_pool_destroy(h)
 
 
+def test_mixed_width_pool_ring_speed_default(lib):
+    """A pool whose projections differ from h x h defaults the mixed launch's ring-body
+    speed to 1.0 (1.22 for h x h pools): the CTA split of the mixed launch as measured on
+    the Llama-3-8B step.  An explicit value overrides it and NULL restores it."""
+    from heterogeneous_adapters_gb300._binding import lora_tuning, lora_pool_desc
+    dims = (ctypes.c_int32 * 4)(256, 256, 256, 128)
+    h = ctypes.c_void_p()
+    d = lora_pool_desc(1 << 20, 16, 256, 2, 1, 2, 8, 0, 1 << 20, 64, 1 << 20, 1 << 20, 1 << 20,
+                       ctypes.cast(dims, ctypes.c_void_p))
+    assert lib.lora_pool_create(ctypes.byref(h), ctypes.byref(d)) == 0
+
+    def speed():
+        t = lora_tuning()
+        assert lib.lora_pool_get_tuning(h, ctypes.byref(t)) == 0
+        return round(t.fused_ring_speed, 4)
+
+    assert speed() == 1.0
+    t = lora_tuning(0, -1, -1, 0, 0.85)
+    assert lib.lora_pool_set_tuning(h, ctypes.byref(t)) == 0
+    assert speed() == 0.85
+    assert lib.lora_pool_set_tuning(h, None) == 0
+    assert speed() == 1.0
+    lib.lora_pool_destroy(h)
+
+
 def test_stage_pages_ce_host_checks(lib):
     """The copy-engine staging validates its index arrays and its staging buffer before
     launching or copying anything (a staging buffer is needed only when the destination
