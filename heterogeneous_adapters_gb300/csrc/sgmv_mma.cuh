@@ -283,8 +283,9 @@ __device__ __forceinline__ void mma_cta(const MmaParams& p, unsigned char* smem_
         uint32_t item = fetch(mi);
         ok = publish(item);
         while (item < total && ok) {
-            // the next item goes out before this one streams: the MMA issuer reads it when
-            // it starts this item's expand
+            // the next item goes out before this one streams, so a role that reads ids ahead
+            // of this stream (the MMA issuer's shrink side as soon as this item's chunks are
+            // issued, the B^T and y producers) finds it published
             const uint32_t next = fetch(mn);
             if (!publish(next)) { ok = false; break; }
             const int r = mi.tile.rank, rp = mi.rp, row0 = mi.tile.row0;
